@@ -1,0 +1,162 @@
+// ssa_api.cu -- the C ABI declared in include/ssa.h: argument validation,
+// workspace sizing and dispatch to the kernels.  Nothing here throws; every
+// failure is a status code.
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+using namespace ssa;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_params(const ssa_params* p, Problem* pr) {
+  if (!p) return SSA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->S < 1 || p->topk < 1 || p->L < 0 || p->L_cap < 0)
+    return SSA_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return SSA_ERR_INVALID_ARG;
+  if (p->dtype != SSA_F32 && p->dtype != SSA_BF16 && p->dtype != SSA_F16) return SSA_ERR_INVALID_ARG;
+  if (!(p->scale >= 0.f) || isinf(p->scale)) return SSA_ERR_INVALID_ARG;  // NaN, negative, inf
+  const int64_t L_cap = p->L_cap ? p->L_cap : p->L;
+  if (L_cap < p->L) return SSA_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SSA_ERR_UNSUPPORTED;
+  if (p->topk > 64) return SSA_ERR_UNSUPPORTED;
+  if (p->Hq / p->Hkv > 16) return SSA_ERR_UNSUPPORTED;
+  if (p->B > 65535 || p->Hkv > 65535) return SSA_ERR_UNSUPPORTED;
+  // element counts of K/V and summ must fit int64 comfortably
+  const double kv = (double)p->B * p->Hkv * (double)L_cap * p->d;
+  if (kv > 4.0e18) return SSA_ERR_UNSUPPORTED;
+  pr->B = p->B;
+  pr->Hq = p->Hq;
+  pr->Hkv = p->Hkv;
+  pr->d = p->d;
+  pr->g = p->Hq / p->Hkv;
+  pr->L = p->L;
+  pr->L_cap = L_cap;
+  pr->S = p->S;
+  pr->topk = p->topk;
+  pr->scale = p->scale > 0.f ? p->scale : 1.f / sqrtf((float)p->d);
+  pr->dtype = p->dtype;
+  pr->ns_cap = (L_cap + p->S - 1) / p->S;
+  return SSA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA; }
+
+size_t ws_need(const Problem& pr, int64_t n_q, int op) {
+  if (op == SSA_OP_ROUTE) return 0;
+  if (op == SSA_OP_DECODE)
+    return kWsHeader + (decode_fast_supported(pr) ? decode_ws_bytes(pr) : 0);
+  if (op == SSA_OP_PREFILL)
+    return kWsHeader + (prefill_fast_supported(pr) ? prefill_ws_bytes(pr, n_q) : 0);
+  return 0;
+}
+
+int check_ws(const Problem& pr, int64_t n_q, int op, const void* ws, size_t ws_bytes) {
+  const size_t need = ws_need(pr, n_q, op);
+  if (need == 0) return SSA_OK;
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return SSA_ERR_WORKSPACE;
+  return SSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssa_version(void) { return kVersion; }
+
+const char* ssa_status_string(int status) {
+  switch (status) {
+    case SSA_OK: return "ok";
+    case SSA_ERR_INVALID_ARG: return "invalid argument";
+    case SSA_ERR_UNSUPPORTED: return "unsupported parameters";
+    case SSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSA_ERR_CUDA: return "CUDA error";
+    case SSA_ERR_DEVICE: return "device-detected error (see the workspace error bits)";
+    default: return "unknown status";
+  }
+}
+
+size_t ssa_workspace_size(const ssa_params* p, int64_t n_q, int op) {
+  Problem pr;
+  if (check_params(p, &pr) != SSA_OK || n_q < 0) return 0;
+  return ws_need(pr, n_q, op);
+}
+
+int ssa_build_summaries(const ssa_params* p, const void* K, int64_t span_begin, int64_t span_end,
+                        float* summ, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (!K || !summ || !aligned16(K) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
+  const int64_t ns_valid = (pr.L + pr.S - 1) / pr.S;
+  if (span_begin < 0 || span_end < span_begin || span_end > ns_valid) return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_summaries(pr, K, span_begin, span_end, summ,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0, const float* summ,
+              int32_t* sel, float* sel_score, void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (n_q < 0 || q_pos0 < 0 || q_pos0 + n_q > pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !summ || !sel || !aligned16(Q) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, n_q, SSA_OP_ROUTE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  return cuda_status(launch_route(pr, Q, n_q, q_pos0, summ, sel, sel_score,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, const void* K, const void* V,
+                      const int32_t* sel, void* O, float* lse, void* ws, size_t ws_bytes,
+                      void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (decode_fast_supported(pr))
+    return cuda_status(launch_attend_decode(pr, Q, pos, K, V, sel, O, lse, ws, st));
+  return cuda_status(launch_attend_rows(pr, Q, 1, pos, K, V, sel, O, lse, ws_error(ws), st));
+}
+
+int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
+                       const void* K, const void* V, const int32_t* sel, void* O, float* lse,
+                       void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (n_q < 0 || q_pos0 < 0 || q_pos0 + n_q > pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, n_q, SSA_OP_PREFILL, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  if (n_q == 0) return SSA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (prefill_fast_supported(pr))
+    return cuda_status(launch_attend_prefill(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st));
+  return cuda_status(launch_attend_rows(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws_error(ws), st));
+}
+
+int ssa_workspace_error(void* ws, uint32_t* bits, void* stream) {
+  if (!ws) return SSA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSA_ERR_CUDA;
+  if (cudaMemcpy(&host, ws, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess) return SSA_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof host) != cudaSuccess) return SSA_ERR_CUDA;
+  if (bits) *bits = host;
+  return host ? SSA_ERR_DEVICE : SSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,180 @@
+/*
+ * ssa.h -- C ABI of the content-routed sparse attention library (libssa.so).
+ *
+ * The method (superlinear release post, geeks.co.kr/post/2077, key-idea
+ * section; SubQ SSA pages, stork.ai "SubQ AI: 1000x compute"): the context
+ * is cut into spans of about sqrt(L) tokens; each query scores the span
+ * summaries, keeps its top-k spans, and runs exact softmax attention over
+ * the tokens of those spans.  The pages leave the router open ("learned
+ * routing"); this library fixes it as follows:
+ *   summary_j = mean of the keys of span j             (fp32)
+ *   score_j   = q . summary_j, unscaled                (fp32)
+ *   candidates of a query at position t: the complete spans 0 .. l-1,
+ *     l = floor(t / S) being the query's own (local) span
+ *   selection = the k best candidates under (score desc, index asc)
+ *   attended tokens = the selected spans plus [l*S, t] (causal local span)
+ *   O = softmax(scale * q K^T) V over the attended tokens, lse = log-sum-exp
+ *
+ * Conventions shared by every entry point
+ *   Layouts (row-major, contiguous, element type = params.dtype):
+ *     Q prefill [B, Hq, n_q, d]      query i sits at position q_pos0 + i
+ *     Q decode  [B, Hq, d]           one query per head at position `pos`
+ *     K, V      [B, Hkv, L_cap, d]   the cache; rows 0 .. L-1 are valid
+ *     summ      [B, Hkv, ns_cap, d]  fp32, ns_cap = ceil(L_cap / S)
+ *     sel       [B, Hq, n_q, topk]   int32 span indices, ascending, padded
+ *                                    with -1 (decode: n_q = 1)
+ *     O         like Q; lse [B, Hq, n_q] fp32 (natural log)
+ *   Query head h reads kv-head h / (Hq / Hkv) (contiguous GQA groups).
+ *   Pointers: every tensor argument is a device pointer owned by the
+ *   caller; the library allocates no memory and keeps no state between
+ *   calls other than per-device attributes read once.
+ *   Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *   default stream).  Every call only enqueues work on it and returns
+ *   without synchronising the host.
+ *   Errors: argument errors are detected on the host and returned before
+ *   anything is enqueued; a failed launch returns SSA_ERR_CUDA.  Errors the
+ *   GPU detects (a sel entry that is not a candidate of its query, a wait
+ *   that exceeded its bound) are OR-ed into the first 4 bytes of the
+ *   workspace; read them with ssa_workspace_error after the stream is done.
+ *   No kernel traps or asserts.
+ *   Workspace: `ws` is caller-owned device memory of at least
+ *   ssa_workspace_size(...) bytes, 256-byte aligned, zeroed once before its
+ *   first use.  Its first 16 bytes are the sticky error record; the rest is
+ *   scratch that one call may overwrite, so calls that share a workspace
+ *   must be ordered on one stream.
+ *   Supported: d in {64, 128}; S >= 1; 1 <= topk <= 64; Hq a multiple of
+ *   Hkv with Hq / Hkv <= 16; dtype fp32, bf16 or fp16.  Other values return
+ *   SSA_ERR_UNSUPPORTED.
+ */
+#ifndef SSA_H
+#define SSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSA_API __attribute__((visibility("default")))
+#else
+#define SSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSA_OK = 0,
+  SSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, range outside the cache, ... */
+  SSA_ERR_UNSUPPORTED = 2, /* valid but not implemented (d, topk, group size, dtype) */
+  SSA_ERR_WORKSPACE = 3,   /* ws is NULL, misaligned or smaller than required */
+  SSA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  SSA_ERR_DEVICE = 5       /* the GPU flagged an error in the workspace record */
+} ssa_status;
+
+typedef enum { SSA_F32 = 0, SSA_BF16 = 1, SSA_F16 = 2 } ssa_dtype;
+
+/* Operation selector of ssa_workspace_size. */
+typedef enum { SSA_OP_ROUTE = 0, SSA_OP_DECODE = 1, SSA_OP_PREFILL = 2 } ssa_op;
+
+/* Bits of the device error record (first uint32 of a workspace). */
+#define SSA_DEVERR_BAD_SELECTION 0x1u /* sel entry not in -1 .. l-1, not ascending, or repeated */
+#define SSA_DEVERR_WAIT_TIMEOUT 0x2u  /* a bounded wait on a barrier gave up */
+#define SSA_DEVERR_OVERFLOW 0x4u      /* a work list outgrew the space sized for it */
+
+typedef struct {
+  int32_t B;      /* batch */
+  int32_t Hq;     /* query heads */
+  int32_t Hkv;    /* key/value heads; Hq % Hkv == 0 */
+  int32_t d;      /* head dimension */
+  int64_t L;      /* valid cache length: rows 0 .. L-1 of K and V hold data */
+  int64_t L_cap;  /* rows per (b, kv-head) in K and V (head stride L_cap * d); 0 means L */
+  int32_t S;      /* span length */
+  int32_t topk;   /* spans kept per query (besides the local span) */
+  float scale;    /* attention scale; 0 means 1 / sqrt(d) */
+  int32_t dtype;  /* ssa_dtype of Q, K, V and O */
+} ssa_params;
+
+/*
+ * Span summaries (superlinear post, key-idea section: the spans that get
+ * scored; the summary itself is fixed by the specification as the mean).
+ * Writes summ[b, kvh, j, :] = (1 / n_j) * sum of K[b, kvh, t, :] over the
+ * n_j = min(S, L - j*S) valid tokens t of span j, for every span j in
+ * [span_begin, span_end) (fp32 accumulation, fp32 result).  Other rows of
+ * summ are left untouched, so a chunked prefill calls this once per chunk
+ * for the spans the chunk completed.
+ * Requires 0 <= span_begin <= span_end <= ceil(L / S).
+ */
+SSA_API int ssa_build_summaries(const ssa_params* p, const void* K, int64_t span_begin,
+                        int64_t span_end, float* summ, void* stream);
+
+/*
+ * Routing: span scores and top-k selection (superlinear post, key-idea
+ * section: score the O(L^0.5) candidate spans and keep the top k).
+ * For each query row (b, h, i) at position t = q_pos0 + i with local span
+ * l = floor(t / S): scores q . summ[b, h / g, j, :] (fp32) for j < l and
+ * writes the min(l, topk) best under (score desc, j asc) to sel[b, h, i, :]
+ * in ascending j, then -1 up to topk.  sel_score (nullable, [B, Hq, n_q,
+ * topk] fp32) receives the score of each written span (NaN beside a -1).
+ * Summaries of spans 0 .. floor((q_pos0 + n_q - 1) / S) - 1 must be built.
+ * Requires n_q >= 0, q_pos0 >= 0, q_pos0 + n_q <= L.
+ * ws may be NULL when ssa_workspace_size(p, n_q, SSA_OP_ROUTE) is 0.
+ */
+SSA_API int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
+              const float* summ, int32_t* sel, float* sel_score, void* ws, size_t ws_bytes,
+              void* stream);
+
+/*
+ * Decode attention for one query per head at position `pos` (superlinear
+ * post, key-idea section: token-level attention inside the chosen spans;
+ * SubQ SSA page: exact attention over the content-selected subset).
+ * sel is [B, Hq, topk] as written by ssa_route with n_q = 1, q_pos0 = pos.
+ * Each query group of one kv-head streams the union of its heads' selected
+ * spans once, split across the GPU, and a log-sum-exp merge combines the
+ * pieces in ascending span order.  Writes O [B, Hq, d] (params.dtype) and,
+ * if lse is not NULL, lse [B, Hq] (fp32).
+ * Requires 0 <= pos < L.
+ */
+SSA_API int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, const void* K,
+                      const void* V, const int32_t* sel, void* O, float* lse, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * Chunked-prefill attention for n_q queries at positions q_pos0 .. q_pos0 +
+ * n_q - 1 (superlinear post: chunked prefill against the kept cache; the
+ * attention itself as for ssa_attend_decode).  Work is dispatched span-major:
+ * the (query, head) pairs that chose a span are gathered into tiles that
+ * stream the span's keys and values once per tile.  Writes O [B, Hq, n_q, d]
+ * (params.dtype) and, if lse is not NULL, lse [B, Hq, n_q] (fp32).
+ * Requires n_q >= 0, q_pos0 >= 0, q_pos0 + n_q <= L.
+ */
+SSA_API int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
+                       const void* K, const void* V, const int32_t* sel, void* O, float* lse,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of workspace the operation needs for n_q queries (n_q is ignored
+ * for SSA_OP_DECODE), or 0 when the parameters are invalid or unsupported
+ * and no workspace is needed (SSA_OP_ROUTE may legitimately return 0).
+ * Never fails loudly: validate with the entry point itself.
+ */
+SSA_API size_t ssa_workspace_size(const ssa_params* p, int64_t n_q, int op);
+
+/*
+ * Reads and clears the device error record at the start of ws: waits for
+ * `stream`, copies the record to the host, zeroes it, and returns SSA_OK or
+ * SSA_ERR_DEVICE; *bits (nullable) receives the SSA_DEVERR_* bits.  This is
+ * the one entry point that synchronises the host.
+ */
+SSA_API int ssa_workspace_error(void* ws, uint32_t* bits, void* stream);
+
+/* Static text for a status code (never NULL). */
+SSA_API const char* ssa_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+SSA_API int ssa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSA_H */

@@ -1,0 +1,97 @@
+"""The C ABI: the library loads, exports every symbol include/*.h declares,
+and rejects bad arguments on the host before anything reaches a GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import content_routed_sparse_build_b300 as ssa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"SSA_API\s+[\w\s\*]+?\b(ssa_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert {"ssa_build_summaries", "ssa_route", "ssa_attend_decode", "ssa_attend_prefill",
+            "ssa_workspace_size", "ssa_status_string"} <= set(names)
+    lib = ctypes.CDLL(ssa.library_path() if os.path.exists(ssa.library_path()) else ssa.lib()._name)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    for s in range(6):
+        assert ssa.ssa_status_string(s) and ssa.ssa_status_string(s) != "unknown status"
+    assert ssa.ssa_status_string(99) == "unknown status"
+    assert ssa.ssa_version() >= 100
+
+
+def test_workspace_sizes():
+    p = ssa.params(1, 32, 4, 128, 1 << 20, 1024, 16, torch.bfloat16)
+    assert ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_ROUTE) == 0
+    assert ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE) >= 256
+    assert ssa.ssa_workspace_size(p, 8192, ssa.SSA_OP_PREFILL) >= 256
+    bad = ssa.params(1, 32, 4, 96, 1 << 20, 1024, 16, torch.bfloat16)
+    assert ssa.ssa_workspace_size(bad, 1, ssa.SSA_OP_DECODE) == 0
+
+
+# The calls below pass pointer values that are never dereferenced: each one
+# is rejected by host validation.  They are kept off machines with a GPU.
+needs_no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-validation only")
+FAKE = ctypes.c_void_p(4096)
+
+
+def _call_route(p, Q=FAKE, n_q=1, pos=0, summ=FAKE, sel=FAKE):
+    return ssa.lib().ssa_route(ctypes.byref(p), Q, n_q, pos, summ, sel, None, None, 0, None)
+
+
+@needs_no_gpu
+def test_route_validation():
+    ok = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
+    assert _call_route(ok, Q=None) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ok, sel=None) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ok, Q=ctypes.c_void_p(4098)) == ssa.SSA_ERR_INVALID_ARG   # misaligned
+    assert _call_route(ok, pos=4096) == ssa.SSA_ERR_INVALID_ARG                  # beyond L
+    assert _call_route(ok, n_q=-1) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 3, 128, 4096, 64, 8, 1)) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 2, 96, 4096, 64, 8, 1)) == ssa.SSA_ERR_UNSUPPORTED
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 64, 65, 1)) == ssa.SSA_ERR_UNSUPPORTED
+    assert _call_route(ssa.params(1, 64, 2, 128, 4096, 64, 8, 1)) == ssa.SSA_ERR_UNSUPPORTED
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 0, 8, 1)) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 64, 8, 7)) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 64, 8, 1, L_cap=100)) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 64, 8, 1, scale=-1.0)) == ssa.SSA_ERR_INVALID_ARG
+    assert _call_route(ssa.params(1, 8, 2, 128, 4096, 64, 8, 1, scale=float("nan"))) == ssa.SSA_ERR_INVALID_ARG
+    assert ssa.lib().ssa_route(None, FAKE, 1, 0, FAKE, FAKE, None, None, 0, None) == ssa.SSA_ERR_INVALID_ARG
+
+
+@needs_no_gpu
+def test_attend_and_summary_validation():
+    p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
+    L = ssa.lib()
+    need = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE)
+    args = lambda pos, ws, n: (ctypes.byref(p), FAKE, pos, FAKE, FAKE, FAKE, FAKE, None, ws, n, None)
+    assert L.ssa_attend_decode(*args(4096, FAKE, need)) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_attend_decode(*args(-1, FAKE, need)) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_attend_decode(*args(10, None, 0)) == ssa.SSA_ERR_WORKSPACE
+    assert L.ssa_attend_decode(*args(10, FAKE, need - 1)) == ssa.SSA_ERR_WORKSPACE
+    assert L.ssa_attend_decode(*args(10, ctypes.c_void_p(4096 + 16), need)) == ssa.SSA_ERR_WORKSPACE
+    need_p = ssa.ssa_workspace_size(p, 100, ssa.SSA_OP_PREFILL)
+    pre = lambda n_q, q0, ws, n: (ctypes.byref(p), FAKE, n_q, q0, FAKE, FAKE, FAKE, FAKE, None, ws, n, None)
+    assert L.ssa_attend_prefill(*pre(100, 4000, FAKE, need_p)) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_attend_prefill(*pre(100, 0, None, 0)) == ssa.SSA_ERR_WORKSPACE
+    assert L.ssa_build_summaries(ctypes.byref(p), FAKE, 0, 65, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_build_summaries(ctypes.byref(p), FAKE, 5, 4, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_build_summaries(ctypes.byref(p), None, 0, 4, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
+    assert L.ssa_workspace_error(None, None, None) == ssa.SSA_ERR_WORKSPACE
