@@ -1,0 +1,502 @@
+"""Benchmark of content-routed sparse attention on B300.
+
+Headline (``value``): decode tok/s per attention layer at a 1M-token cache
+(B=1, Hq=32, Hkv=4, d=128, S=1024, k=16, bf16): one step = route one new
+query token per head (scores over 1023 span summaries + top-16) and attend
+its selected spans plus its local span.  The ``prefill`` object reports the
+chunked prefill of 8192 queries against the same-shaped 1M cache (summaries
+of the chunk's spans, route, attend).  Both run through the C ABI on inputs
+already resident in HBM; ``e2e`` repeats the decode through the same calls
+with the query copied in from pinned host memory and the output copied back
+every step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun, one process per GPU): every rank runs an independent
+replica of the workload; value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import content_routed_sparse_build_b300 as ssa  # noqa: E402
+from synth import workloads as W  # noqa: E402
+
+METRIC = "routed-attention decode tok/s and prefill tok/s per layer at 1M ctx; % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+
+
+# --------------------------------------------------------------------- helpers
+def peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        self.rows = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = ["-i", str(device)]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 3 + i and r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+# --------------------------------------------------------------------- decode
+class DecodeBench:
+    def __init__(self, w: W.Workload, dev):
+        self.w = w
+        self.dev = dev
+        self.inp = W.Inputs(w)
+        self.K = self.inp.k(dev)
+        self.V = self.inp.v(dev)
+        self.Q = self.inp.q(dev)                               # [steps, B, Hq, d]
+        self.p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+        self.summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+        self.ws = ssa.workspace(self.p, 1, ssa.SSA_OP_DECODE, dev)
+        self.sel = torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
+        self.O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=dev)
+        self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        self.qs = [self.Q[s].contiguous() for s in range(w.n_q)]
+        self.stream = torch.cuda.current_stream(dev)
+
+    def build_summaries(self):
+        ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
+
+    def step(self, s, ev=None):
+        w = self.w
+        i = s % w.n_q
+        pos = w.q_pos0 + i
+        q = self.qs[i]
+        ssa.ssa_route(self.p, q, 1, pos, self.summ, self.sel, None, None, self.stream)
+        if ev is not None:
+            ev[0].record(self.stream)
+        ssa.ssa_attend_decode(self.p, q, pos, self.K, self.V, self.sel, self.O, self.lse, self.ws,
+                              self.stream)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def algorithmic_bytes(self):
+        """Per query index: (attend bytes, route bytes), from the actual selections."""
+        w = self.w
+        el = 2 if w.dtype != torch.float32 else 4
+        out = []
+        for i in range(w.n_q):
+            pos = w.q_pos0 + i
+            ell = pos // w.S
+            ssa.ssa_route(self.p, self.qs[i], 1, pos, self.summ, self.sel)
+            sel = self.sel.reshape(w.B, w.Hkv, w.g * w.topk).cpu().numpy()
+            kv_rows = 0
+            for b in range(w.B):
+                for g in range(w.Hkv):
+                    u = np.unique(sel[b, g][sel[b, g] >= 0])
+                    kv_rows += len(u) * w.S + (pos - ell * w.S + 1)
+            attend = kv_rows * w.d * el * 2 + 2 * w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
+            route = w.B * w.Hkv * ell * w.d * 4 + w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
+            out.append((attend, route))
+        return out
+
+
+def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
+    db = DecodeBench(w, dev)
+    st = db.stream
+    # summaries of the whole cache (the decode steps read them), timed on its own
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    db.build_summaries()
+    torch.cuda.synchronize()
+    e0.record(st)
+    db.build_summaries()
+    e1.record(st)
+    torch.cuda.synchronize()
+    summ_ms = e0.elapsed_time(e1)
+    summ_bytes = w.B * w.Hkv * w.L * w.d * 2 + w.B * w.Hkv * w.n_spans * w.d * 4
+    per_q = db.algorithmic_bytes()
+
+    for s in range(warmup):
+        db.step(s)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier(ws_n)
+        torch.cuda.synchronize()
+        start.record(st)
+        for s in range(steps):
+            db.step(s, evs[s])
+        stop.record(st)
+        torch.cuda.synchronize()
+        barrier(ws_n)
+    total_ms = start.elapsed_time(stop)
+    attend_ms = sum(a.elapsed_time(b) for a, b in evs)
+    err = ssa.ssa_workspace_error(db.ws)
+    total_ms_max = max_over_ranks(total_ms, ws_n)
+
+    attend_bytes = sum(per_q[s % w.n_q][0] for s in range(steps))
+    route_bytes = sum(per_q[s % w.n_q][1] for s in range(steps))
+    pk = peaks()
+    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
+    res = {
+        "tok_s": steps * ws_n / (total_ms_max * 1e-3),
+        "ms_per_step": total_ms_max / steps,
+        "attend_ms_per_step": attend_ms / steps,
+        "route_plus_gaps_ms_per_step": (total_ms - attend_ms) / steps,
+        "attend_bytes_per_step": attend_bytes / steps,
+        "route_bytes_per_step": route_bytes / steps,
+        "step_bytes_gbs": (attend_bytes + route_bytes) / (total_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "attend_decode (gathered K/V of the union of selected spans + local span)",
+                     "peak_source": pk["source"]},
+        "summaries": {"ms": summ_ms, "gbs": summ_bytes / (summ_ms * 1e-3) / 1e9,
+                      "frac": summ_bytes / (summ_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "clocks": clk.summary(),
+        "device_error_bits": err,
+        "launches_per_step": None,
+    }
+    res["e2e"] = bench_decode_e2e(db, min(steps, 2048))
+    if cpu_leg:
+        res["cpu_baseline"] = cpu_baseline_decode(db)
+    return res, db
+
+
+def bench_decode_e2e(db: DecodeBench, steps: int):
+    """Same decode through the C ABI with host buffers: H2D query, D2H output, every step."""
+    w = db.w
+    st = db.stream
+    el = db.Q.element_size()
+    q_host = db.Q.cpu().pin_memory()
+    o_host = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype).pin_memory()
+    q_dev = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=db.dev)
+    for s in range(8):
+        i = s % w.n_q
+        q_dev.copy_(q_host[i], non_blocking=True)
+        ssa.ssa_route(db.p, q_dev, 1, w.q_pos0 + i, db.summ, db.sel, None, None, st)
+        ssa.ssa_attend_decode(db.p, q_dev, w.q_pos0 + i, db.K, db.V, db.sel, db.O, None, db.ws, st)
+        o_host.copy_(db.O, non_blocking=True)
+        st.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        i = s % w.n_q
+        q_dev.copy_(q_host[i], non_blocking=True)
+        ssa.ssa_route(db.p, q_dev, 1, w.q_pos0 + i, db.summ, db.sel, None, None, st)
+        ssa.ssa_attend_decode(db.p, q_dev, w.q_pos0 + i, db.K, db.V, db.sel, db.O, None, db.ws, st)
+        o_host.copy_(db.O, non_blocking=True)
+        st.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": "tok/s", "h2d_bytes_per_step": w.B * w.Hq * w.d * el,
+            "d2h_bytes_per_step": w.B * w.Hq * w.d * el, "steps": steps}
+
+
+def cpu_baseline_decode(db: DecodeBench, budget_s: float = 15.0):
+    """The oracle (as it stands) on the host cores, on a bounded sample of decode steps."""
+    import oracle
+    w = db.w
+    inp = db.inp
+    K = inp.k("cpu")
+    V = inp.v("cpu")
+    Q = inp.q("cpu")
+    summ = oracle.summaries(K, w.L, w.S)
+    n = 0
+    t0 = time.perf_counter()
+    while n < w.n_q:
+        q = Q[n].reshape(w.B, w.Hq, 1, w.d).contiguous()
+        sel, _ = oracle.route(q, w.q_pos0 + n, summ, w.Hkv, w.S, w.topk)
+        oracle.attend(q, K, V, w.q_pos0 + n, w.S, sel)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    del K, V
+    return {"value": n / dt, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": "%d of the %d decode steps (route + attend per step; summaries of the 1M "
+                      "cache built beforehand, untimed)" % (n, w.n_q)}
+
+
+# --------------------------------------------------------------------- prefill
+class PrefillBench:
+    """One chunk of queries against an existing cache (summaries of the chunk's
+    spans, route, attend)."""
+
+    def __init__(self, w: W.Workload, dev):
+        self.w = w
+        self.dev = dev
+        self.inp = W.Inputs(w)
+        self.K = self.inp.k(dev)
+        self.V = self.inp.v(dev)
+        self.Q = self.inp.q(dev)                               # [B, Hq, n_q, d]
+        self.p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+        self.summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+        self.sel = torch.empty((w.B, w.Hq, w.n_q, w.topk), dtype=torch.int32, device=dev)
+        self.O = torch.empty_like(self.Q)
+        self.lse = torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
+        self.ws = ssa.workspace(self.p, w.n_q, ssa.SSA_OP_PREFILL, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.j0 = w.q_pos0 // w.S
+        self.j1 = w.n_spans
+        pre = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.q_pos0, w.S, w.topk, w.dtype, L_cap=w.L)
+        if self.j0 > 0:
+            ssa.ssa_build_summaries(pre, self.K, 0, self.j0, self.summ)
+
+    def step(self, ev=None):
+        w = self.w
+        ssa.ssa_build_summaries(self.p, self.K, self.j0, self.j1, self.summ, self.stream)
+        ssa.ssa_route(self.p, self.Q, w.n_q, w.q_pos0, self.summ, self.sel, None, None, self.stream)
+        if ev is not None:
+            ev[0].record(self.stream)
+        ssa.ssa_attend_prefill(self.p, self.Q, w.n_q, w.q_pos0, self.K, self.V, self.sel, self.O,
+                               self.lse, self.ws, self.stream)
+        if ev is not None:
+            ev[1].record(self.stream)
+
+    def flops(self):
+        w = self.w
+        self.step()
+        sel = self.sel.cpu().numpy()
+        nsel = (sel >= 0).sum(axis=-1)                         # [B, Hq, n_q]
+        pos = w.q_pos0 + np.arange(w.n_q)
+        local = pos - (pos // w.S) * w.S + 1
+        tokens = nsel * w.S + local[None, None, :]
+        return float(4 * w.d * tokens.sum())
+
+
+def bench_prefill(w, dev, steps, warmup, ws_n, flush):
+    pb = PrefillBench(w, dev)
+    st = pb.stream
+    fl = pb.flops()
+    for _ in range(warmup):
+        pb.step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    tot = 0.0
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        pb.step(evs[s])
+        b.record(st)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    barrier(ws_n)
+    attend_ms = sum(x.elapsed_time(y) for x, y in evs) / steps
+    ms = max_over_ranks(tot / steps, ws_n)
+    err = ssa.ssa_workspace_error(pb.ws)
+    pk = peaks()
+    achieved = fl / (attend_ms * 1e-3) / 1e12
+    return {
+        "workload": w.name, "value": w.n_q * ws_n / (ms * 1e-3), "unit": "tok/s",
+        "ms_per_step": ms, "attend_ms": attend_ms, "steps": steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                     "kernel": "attend_prefill (4*d FLOP per attended token per query head)",
+                     "peak_source": pk["source"] + " sustained bf16"},
+        "selected_span_tflop_per_step": fl / 1e12,
+        "device_error_bits": err,
+    }
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args, ws_n, rank):
+    """The oracle timed on the host cores on the decode workload (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    w = W.DECODE_1M
+    inp = W.Inputs(w)
+    K, V, Q = inp.k("cpu"), inp.v("cpu"), inp.q("cpu")
+    summ = oracle.summaries(K, w.L, w.S)
+
+    def one(s):
+        i = s % w.n_q
+        q = Q[i].reshape(w.B, w.Hq, 1, w.d).contiguous()
+        sel, _ = oracle.route(q, w.q_pos0 + i, summ, w.Hkv, w.S, w.topk)
+        oracle.attend(q, K, V, w.q_pos0 + i, w.S, sel)
+
+    for s in range(args.warmup):
+        one(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        one(s)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    line = {"metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "L": w.L, "S": w.S, "topk": w.topk},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": oracle.threads(),
+                             "kind": "oracle",
+                             "sample": "%d decode steps of the 1M-cache workload" % args.steps},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws_n, rank, local = dist_setup()
+    if args.impl == "reference":
+        args.steps = args.steps if args.steps is not None else 3
+        args.warmup = args.warmup if args.warmup is not None else 1
+        run_reference(args, ws_n, rank)
+        return
+    steps = args.steps if args.steps is not None else 8192
+    warmup = max(3, args.warmup if args.warmup is not None else 256)
+    dev = torch.device("cuda", local)
+    ssa.lib()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
+
+    w = W.DECODE_1M
+    dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg=(rank == 0 and ws_n == 1
+                                                                 and not args.no_cpu_baseline))
+    del db
+    torch.cuda.empty_cache()
+    pre = None
+    if not args.no_prefill:
+        pre = bench_prefill(W.PREFILL_1M, dev, args.prefill_steps, 2, ws_n, flush)
+    line = {
+        "metric": METRIC, "value": dec["tok_s"], "unit": "tok/s", "n_gpus": ws_n, "steps": steps,
+        "warmup": warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
+                   "S": w.S, "topk": w.topk, "queries": "%d distinct decode queries at positions "
+                   "%d..%d, cycled" % (w.n_q, w.q_pos0, w.last_pos),
+                   "l2": "inputs larger than L2: 2 GiB K/V cache, ~250 MB gathered per step",
+                   "parallelism": "replicas" if ws_n > 1 else "single GPU"},
+        "roofline": dec["roofline"],
+        "e2e": dec["e2e"],
+        "clocks": dec["clocks"],
+        "gpu_launches": None,
+        "decode_detail": {k: dec[k] for k in ("attend_ms_per_step", "route_plus_gaps_ms_per_step",
+                                               "attend_bytes_per_step", "route_bytes_per_step",
+                                               "step_bytes_gbs", "summaries", "device_error_bits")},
+    }
+    line["gpu_launches"] = steps * launches_per_decode_step(w)
+    if pre is not None:
+        line["prefill"] = pre
+    if "cpu_baseline" in dec:
+        line["cpu_baseline"] = dec["cpu_baseline"]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def launches_per_decode_step(w) -> int:
+    """Kernels one decode step launches: route (1) + attend (1 row kernel, or
+    plan + split + merge on the fast path)."""
+    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+    fast = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE) > 256
+    return 1 + (3 if fast else 1)
+
+
+if __name__ == "__main__":
+    main()
