@@ -440,6 +440,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-L", type=int, default=None,
+                    help="shrink the decode cache (profiling runs on a smaller case)")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
@@ -454,6 +456,8 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
 
     w = W.DECODE_1M
+    if args.decode_L:
+        w = w.with_(name="decode_%d" % args.decode_L, L=args.decode_L, q_pos0=args.decode_L - w.n_q)
     dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg=(rank == 0 and ws_n == 1
                                                                  and not args.no_cpu_baseline))
     del db

@@ -112,23 +112,16 @@ __global__ void __launch_bounds__(256) attend_rows_kernel(
   st.m = -INFINITY;
   st.l = 0.f;
 
-  // Selected spans: ascending, each a complete span before the local one,
-  // -1 only as trailing padding.  Anything else is flagged and skipped.
+  // Selected spans: the row's leading strictly ascending run of complete
+  // spans before the local one; anything after it other than -1 is flagged.
   const int32_t* srow = sel + row * topk;
-  int64_t prev = -1;
-  bool padded = false;
-  for (int s = 0; s < topk; ++s) {
-    const int64_t j = srow[s];
-    if (j < 0) {
-      if (j != -1 && lane == 0) flag_error(err, SSA_DEVERR_BAD_SELECTION);
-      padded = true;
-      continue;
-    }
-    if (padded || j <= prev || j >= ell) {
-      if (lane == 0) flag_error(err, SSA_DEVERR_BAD_SELECTION);
-      continue;
-    }
-    prev = j;
+  const int j0 = lane < topk ? srow[lane] : -1;
+  const int j1 = lane + 32 < topk ? srow[lane + 32] : -1;
+  bool bad;
+  const int used = warp_sel_prefix(j0, j1, lane, topk, ell, &bad);
+  if (bad && lane == 0) flag_error(err, SSA_DEVERR_BAD_SELECTION);
+  for (int s = 0; s < used; ++s) {
+    const int64_t j = __shfl_sync(0xffffffffu, s < 32 ? j0 : j1, s & 31);
     attend_range<DT, D>(st, K, V, kvrow0, j * S, (j + 1) * S, lane);
   }
   attend_range<DT, D>(st, K, V, kvrow0, ell * S, t + 1, lane);

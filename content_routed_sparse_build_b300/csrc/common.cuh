@@ -95,4 +95,27 @@ __device__ __forceinline__ bool better(float s, int j, float s2, int j2) {
 
 constexpr int kNoSpan = 0x7fffffff;
 
+// Which entries of a sel row are used, computed by one warp (topk <= 64;
+// lane r holds entries r and r + 32).  The used entries are the row's
+// leading run of candidate spans (0 <= j < ell) in strictly ascending
+// order; the row is well formed when everything after that run is -1.
+// Returns the number of used entries; *bad is set for a malformed row.
+__device__ __forceinline__ int warp_sel_prefix(int j0, int j1, int lane, int topk, int64_t ell,
+                                               bool* bad) {
+  const int p0 = __shfl_up_sync(0xffffffffu, j0, 1);
+  const int last0 = __shfl_sync(0xffffffffu, j0, 31);
+  const int p1 = __shfl_up_sync(0xffffffffu, j1, 1);
+  const bool in0 = lane < topk, in1 = lane + 32 < topk;
+  const bool ok0 = in0 && j0 >= 0 && j0 < ell && (lane == 0 || p0 < j0);
+  const bool ok1 = in1 && j1 >= 0 && j1 < ell && (lane == 0 ? last0 < j1 : p1 < j1);
+  const uint64_t okm = (uint64_t)__ballot_sync(0xffffffffu, ok0) |
+                      ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
+  const int n = __ffsll((long long)~okm) - 1;  // first entry that is not used
+  const int used = n < 0 || n > topk ? topk : n;
+  const bool junk0 = in0 && lane >= used && j0 != -1;
+  const bool junk1 = in1 && lane + 32 >= used && j1 != -1;
+  *bad = __any_sync(0xffffffffu, junk0 || junk1);
+  return used;
+}
+
 }  // namespace ssa

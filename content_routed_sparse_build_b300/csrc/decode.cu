@@ -1,13 +1,733 @@
-// decode.cu -- decode attention fast path (split spans + merge).
+// decode.cu -- decode attention: one query per head, split over the spans,
+// log-sum-exp merge (16-bit K / V).
+//
+// Superlinear release post (geeks.co.kr/post/2077), key-idea section:
+// token-level attention inside each query's chosen spans; SubQ SSA page
+// (stork.ai): exact attention over the content-selected subset.  The local
+// span [l*S, pos] is always attended.
+//
+// Three kernels:
+//  plan    one CTA per (b, kv-head): validates the g heads' selections and
+//          builds their union U (ascending, local span last) with, per span,
+//          the mask of heads that chose it and each head's rank for it.
+//  attend  persistent, one CTA per SM, four independent warps.  Work items
+//          are (group, span of U, chunk of CH tokens), handed out by an
+//          atomic counter.  Each warp runs its own ring of 32-token K / V
+//          tiles loaded by TMA (128-byte swizzle, mbarrier completion),
+//          issuing STAGES tiles ahead of the one it computes.  The MMAs are
+//          transposed so that the query group fits the n8 side of
+//          mma.sync: S^T = K Q^T (tokens x heads) and O^T += V^T P^T
+//          (d x heads), P^T turned into the B operand by movmatrix.  An
+//          online softmax runs per head (column); at the end of an item the
+//          warp writes one partial (m, l, o) per head that chose the span.
+//          Every K / V byte of the union is read once.
+//  merge   one CTA per (b, q-head): combines the head's partials (span
+//          order, then chunk order) into O and lse.
+// Softmax runs in base 2: scores are scaled by scale * log2(e).
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ssa {
+namespace {
 
-bool decode_fast_supported(const Problem&) { return false; }
-size_t decode_ws_bytes(const Problem&) { return 0; }
-cudaError_t launch_attend_decode(const Problem&, const void*, int64_t, const void*, const void*,
-                                 const int32_t*, void*, float*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kTile = 16;     // tokens per ring stage
+constexpr int kWarps = 8;     // independent warps per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxG = 16;
+constexpr int kMaxK = 64;
+constexpr int kMaxGroups = 1024;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Plan {
+  int* n_union;     // [n_grp]   |U| including the local span
+  int* n_items;     // [n_grp]   work items of the group
+  int* span;        // [n_grp][umax]
+  uint32_t* mask;   // [n_grp][umax] heads (bit r = head kvh*g + r) that attend the span
+  uint8_t* rank;    // [n_grp][umax][16] position of the span in each head's sel row (topk = local)
+  int* counter;     // work-item counter of the attend kernel
+  float* ml;        // [B*Hq][topk+1][C][2]  (m, l) per partial, base-2 m
+  float* po;        // [B*Hq][topk+1][C][D]  unnormalised partial outputs
+};
+
+struct Geo {
+  int Hq, Hkv, g, topk, S, C, CH, umax, n_grp;
+  int64_t pos, ell;
+  float scale_log2e;
+  int tables_in_smem;  // plan tables and Q copied to shared memory
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;            // 128-byte boxes per row
+  static constexpr int kBox = kTile * 128;         // bytes per box
+  static constexpr int kHalf = kBoxes * kBox;      // K (or V) bytes per stage
+  static constexpr int kStage = 2 * kHalf;
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kQStride = D + 8;           // 16-bit elements per Q row in shared memory
+  static constexpr size_t kRing = (size_t)kWarps * kStages * kStage;
+  static constexpr size_t kBars = (size_t)kWarps * kStages * 8;
+  static constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
+  static constexpr size_t kFixed = 1024 + kRing + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Tokens per work item: aim at about two items per warp of the GPU for the
+// largest possible union, between 64 and 1024 tokens (a power of two).
+int chunk_tokens(const Problem& pr, int n_warps_total) {
+  const double work = (double)pr.B * pr.Hkv * (pr.g * pr.topk + 1) * (double)pr.S;
+  double ch = work / (2.0 * n_warps_total);
+  int c = 64;
+  while (c < 1024 && 2.0 * c <= ch) c *= 2;
+  return c;
+}
+
+struct Layout {
+  size_t n_union, n_items, span, mask, rank, counter, ml, po, total;
+  int C, CH;
+};
+
+Layout layout(const Problem& pr) {
+  Layout l;
+  l.CH = chunk_tokens(pr, device_sm_count() * kWarps);
+  l.C = (pr.S + l.CH - 1) / l.CH;
+  const size_t n_grp = (size_t)pr.B * pr.Hkv;
+  const size_t umax = (size_t)pr.g * pr.topk + 1;
+  const size_t parts = (size_t)pr.B * pr.Hq * (pr.topk + 1) * l.C;
+  size_t off = kWsHeader;
+  l.n_union = off; off = align256(off + n_grp * 4);
+  l.n_items = off; off = align256(off + n_grp * 4);
+  l.span = off; off = align256(off + n_grp * umax * 4);
+  l.mask = off; off = align256(off + n_grp * umax * 4);
+  l.rank = off; off = align256(off + n_grp * umax * 16);
+  l.counter = off; off = align256(off + 4);
+  l.ml = off; off = align256(off + parts * 2 * 4);
+  l.po = off; off = align256(off + parts * (size_t)pr.d * 4);
+  l.total = off;
+  return l;
+}
+
+// ---------------------------------------------------------------- plan
+// One CTA per (b, kv-head), one warp per query head of the group.  Also
+// empties the (m, l) slots of the group's partials: a slot that no item
+// writes keeps m = -inf and the merge skips it.
+constexpr int kPlanThreads = kMaxG * 32;
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t* __restrict__ sel,
+                                                                   Plan plan, Geo geo,
+                                                                   uint32_t* __restrict__ err) {
+  __shared__ int sj[kMaxG][kMaxK];         // used spans of each head, ascending
+  __shared__ int nv[kMaxG];
+  __shared__ int cpref[kMaxG][kMaxK + 1];  // prefix counts of canonical entries
+  __shared__ uint8_t canon[kMaxG][kMaxK];
+  __shared__ uint32_t smask[kMaxG * kMaxK + 1];
+
+  const int grp = blockIdx.x;
+  const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
+  const int g = geo.g, k = geo.topk, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int umax = geo.umax;
+  const uint32_t lt = (1u << lane) - 1u;
+
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  if (grp == 0 && tid == 0) *plan.counter = 0;
+  {
+    const int nparts = g * (k + 1) * geo.C;
+    float2* ml = reinterpret_cast<float2*>(plan.ml) + (int64_t)(b * geo.Hq + kvh * g) * (k + 1) * geo.C;
+    for (int x = tid; x < nparts; x += kPlanThreads) ml[x] = make_float2(-INFINITY, 0.f);
+  }
+  for (int x = tid; x < kMaxG * kMaxK + 1; x += kPlanThreads) smask[x] = 0u;
+  if (warp < g) {
+    const int32_t* row = sel + (int64_t)(b * geo.Hq + kvh * g + warp) * k;
+    const int j0 = lane < k ? __ldg(row + lane) : -1;
+    const int j1 = lane + 32 < k ? __ldg(row + lane + 32) : -1;
+    bool bad;
+    const int used = warp_sel_prefix(j0, j1, lane, k, geo.ell, &bad);
+    if (bad && lane == 0) flag_error(err, SSA_DEVERR_BAD_SELECTION);
+    if (lane < used) sj[warp][lane] = j0;
+    if (lane + 32 < used) sj[warp][lane + 32] = j1;
+    if (lane == 0) nv[warp] = used;
+  }
+  __syncthreads();
+  // canonical entry: no lower head of the group holds the same span
+  if (warp < g) {
+    uint32_t bal[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = lane + 32 * hh;
+      bool c = false;
+      if (r < nv[warp]) {
+        const int j = sj[warp][r];
+        bool dup = false;
+#pragma unroll
+        for (int h2 = 0; h2 < kMaxG; ++h2) {
+          if (h2 < warp) {
+            int lo = 0, hi = nv[h2];
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
+            }
+            dup |= lo < nv[h2] && sj[h2][lo] == j;
+          }
+        }
+        c = !dup;
+        canon[warp][r] = c ? 1 : 0;
+      }
+      bal[hh] = __ballot_sync(0xffffffffu, c);
+    }
+    cpref[warp][lane] = __popc(bal[0] & lt);
+    cpref[warp][lane + 32] = __popc(bal[0]) + __popc(bal[1] & lt);
+    if (lane == 0) cpref[warp][64] = __popc(bal[0]) + __popc(bal[1]);
+  }
+  __syncthreads();
+  // position of span j in U = number of distinct spans below j
+  const int gbase = grp * umax;
+  if (warp < g) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = lane + 32 * hh;
+      if (r >= nv[warp]) continue;
+      const int j = sj[warp][r];
+      int p = 0;
+#pragma unroll
+      for (int h2 = 0; h2 < kMaxG; ++h2) {
+        if (h2 < g) {
+          int lo = 0, hi = nv[h2];
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
+          }
+          p += cpref[h2][lo];
+        }
+      }
+      if (canon[warp][r]) plan.span[gbase + p] = j;
+      atomicOr(&smask[p], 1u << warp);
+      plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
+    }
+  }
+  __syncthreads();
+  int nu = 0;
+  for (int h = 0; h < g; ++h) nu += cpref[h][nv[h]];
+  for (int p = tid; p < nu; p += kPlanThreads) plan.mask[gbase + p] = smask[p];
+  if (tid < g) plan.rank[(size_t)(gbase + nu) * 16 + tid] = (uint8_t)k;
+  if (tid == 0) {
+    plan.span[gbase + nu] = (int)geo.ell;
+    plan.mask[gbase + nu] = (1u << g) - 1u;
+    plan.n_union[grp] = nu + 1;
+    const int64_t n_local = geo.pos - geo.ell * geo.S + 1;
+    plan.n_items[grp] = nu * geo.C + (int)((n_local + geo.CH - 1) / geo.CH);
+  }
+}
+
+// ---------------------------------------------------------------- attend
+// Where each warp reads the plan: shared-memory copies when they fit.
+struct Tables {
+  const int* gpref;       // [n_grp + 1] item prefix over groups
+  const int* n_union;     // [n_grp]
+  const int* span;        // [n_grp * umax]
+  const uint32_t* mask;   // [n_grp * umax]
+  const uint8_t* rank;    // [n_grp * umax * 16]
+  const uint16_t* q;      // [B * Hq] rows of q_stride elements
+  int q_stride;
+};
+
+struct Item {
+  int grp, u, c, ntiles;
+  int64_t t0, t1;
+};
+
+__device__ __forceinline__ void decode_item(int it, const Tables& tb, const Geo& geo, Item& x) {
+  int lo = 0, hi = geo.n_grp - 1;  // last group with gpref[g] <= it
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb.gpref[mid] <= it) lo = mid; else hi = mid - 1;
+  }
+  x.grp = lo;
+  const int li = it - tb.gpref[lo];
+  const int nu = tb.n_union[lo];
+  if (li < (nu - 1) * geo.C) {
+    x.u = li / geo.C;
+    x.c = li - x.u * geo.C;
+    const int64_t j = tb.span[lo * geo.umax + x.u];
+    x.t0 = j * geo.S + (int64_t)x.c * geo.CH;
+    x.t1 = min(x.t0 + geo.CH, (j + 1) * geo.S);
+  } else {
+    x.u = nu - 1;
+    x.c = li - (nu - 1) * geo.C;
+    x.t0 = geo.ell * geo.S + (int64_t)x.c * geo.CH;
+    x.t1 = min(x.t0 + geo.CH, geo.pos + 1);
+  }
+  x.ntiles = (int)((x.t1 - x.t0 + kTile - 1) / kTile);
+}
+
+template <int DT, int D, int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing);
+  int4* metas = reinterpret_cast<int4*>(bars + kWarps * C::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metas + kWarps * C::kStages);
+  uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_gpref + kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int n_slots = geo.n_grp * geo.umax;
+
+  // ---- shared set-up: barriers, group prefix, plan tables
+  if (tid == 0) {
+    for (int s = 0; s < kWarps * C::kStages; ++s) ptx::mbar_init(&bars[s], 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  Tables tb;
+  tb.gpref = s_gpref;
+  if (geo.tables_in_smem) {
+    int* nu_s = reinterpret_cast<int*>(s_tab);
+    int* sp_s = nu_s + geo.n_grp;
+    uint32_t* mk_s = reinterpret_cast<uint32_t*>(sp_s + n_slots);
+    uint16_t* q_s = reinterpret_cast<uint16_t*>(mk_s + n_slots);
+    const int nq_rows = geo.n_grp * geo.g;  // B * Hq
+    uint8_t* rk_s = reinterpret_cast<uint8_t*>(q_s + nq_rows * C::kQStride);
+    for (int x = tid; x < geo.n_grp; x += kThreads) nu_s[x] = plan.n_union[x];
+    for (int x = tid; x < n_slots; x += kThreads) {
+      sp_s[x] = plan.span[x];
+      mk_s[x] = plan.mask[x];
+    }
+    for (int x = tid; x < n_slots * 4; x += kThreads)
+      reinterpret_cast<uint32_t*>(rk_s)[x] = reinterpret_cast<const uint32_t*>(plan.rank)[x];
+    for (int x = tid; x < nq_rows * (D / 2); x += kThreads) {
+      const int r = x / (D / 2), c = x - r * (D / 2);
+      reinterpret_cast<uint32_t*>(q_s + r * C::kQStride)[c] = reinterpret_cast<const uint32_t*>(Q)[x];
+    }
+    tb.n_union = nu_s;
+    tb.span = sp_s;
+    tb.mask = mk_s;
+    tb.rank = rk_s;
+    tb.q = q_s;
+    tb.q_stride = C::kQStride;
+  } else {
+    tb.n_union = plan.n_union;
+    tb.span = plan.span;
+    tb.mask = plan.mask;
+    tb.rank = plan.rank;
+    tb.q = static_cast<const uint16_t*>(Q);
+    tb.q_stride = D;
+  }
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < geo.n_grp; base += 32) {
+      const int gi = base + lane;
+      int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (gi < geo.n_grp) s_gpref[gi + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_gpref[0] = 0;
+  }
+  __syncthreads();
+  const int total = s_gpref[geo.n_grp];
+
+  // ---- per-warp ring
+  uint8_t* wring = ring + (size_t)warp * C::kStages * C::kStage;
+  uint64_t* fb = bars + warp * C::kStages;
+  int4* meta = metas + warp * C::kStages;
+
+  // issue side (lane 0 drives, state kept warp-uniform)
+  Item iss;
+  iss.ntiles = 0;
+  iss.grp = iss.u = iss.c = 0;
+  iss.t0 = iss.t1 = 0;
+  int iss_tile = 0;
+  int next_it = 0;
+  if (lane == 0) next_it = atomicAdd(plan.counter, 1);
+  next_it = __shfl_sync(0xffffffffu, next_it, 0);
+  bool exhausted = false;
+
+  // Loads the next tile into `stage`; returns false when no work is left.
+  auto issue = [&](int stage) -> bool {
+    if (iss_tile == iss.ntiles) {
+      if (next_it >= total) {
+        exhausted = true;
+        return false;
+      }
+      decode_item(next_it, tb, geo, iss);
+      iss_tile = 0;
+      int nx = 0;
+      if (lane == 0) nx = atomicAdd(plan.counter, 1);
+      next_it = __shfl_sync(0xffffffffu, nx, 0);
+    }
+    if (lane == 0) {
+      meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ptx::mbar_arrive_expect_tx(&fb[stage], C::kStage);
+      uint8_t* dK = wring + (size_t)stage * C::kStage;
+      uint8_t* dV = dK + C::kHalf;
+      const int y = (int)(iss.t0 + (int64_t)iss_tile * kTile);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        ptx::tma_load_3d(dK + bx * C::kBox, &tmK, &fb[stage], bx * 64, y, iss.grp);
+        ptx::tma_load_3d(dV + bx * C::kBox, &tmV, &fb[stage], bx * 64, y, iss.grp);
+      }
+    }
+    ++iss_tile;
+    return true;
+  };
+
+  int inflight = 0;
+#pragma unroll 1
+  for (int s = 0; s < C::kStages; ++s) {
+    if (exhausted || !issue(s)) break;
+    ++inflight;
+  }
+
+  // Consumer state.  NG groups of 8 heads; lane holds, per group, heads
+  // 2*q4 and 2*q4+1 of the group (columns of S^T and O^T) and tokens / d
+  // rows r8 and r8 + 8 of each 16-row fragment.
+  const int q4 = lane & 3, r8 = lane >> 2;
+  const int mi = lane >> 3, rr = lane & 7;
+  uint32_t qb[NG][D / 16][2];
+  float o[NG][D / 16][4];
+  float m[NG][2], l[NG][2];
+  Item cur;
+  cur.grp = cur.u = cur.c = cur.ntiles = 0;
+  cur.t0 = cur.t1 = 0;
+  int stage = 0;
+  uint32_t phase = 0;
+#pragma unroll 1
+  while (inflight > 0) {
+    if (!ptx::mbar_wait(&fb[stage], phase)) {
+      if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    const int4 mt = meta[stage];
+    if (mt.w == 0) {
+      cur.grp = mt.x;
+      cur.u = mt.y;
+      cur.c = mt.z;
+      {
+        const int nu = tb.n_union[cur.grp];
+        if (cur.u < nu - 1) {
+          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
+          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
+        } else {
+          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
+        }
+        cur.ntiles = (int)((cur.t1 - cur.t0 + kTile - 1) / kTile);
+      }
+      // B operand of S^T = K Q^T: thread holds Q[head r8][d pair] per k-step
+      const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        const int h = ng * 8 + r8;
+        const bool ok = h < geo.g;
+        const uint32_t* qr =
+            reinterpret_cast<const uint32_t*>(tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          qb[ng][kk][0] = ok ? qr[kk * 8 + q4] : 0u;
+          qb[ng][kk][1] = ok ? qr[kk * 8 + 4 + q4] : 0u;
+        }
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) o[ng][mt2][0] = o[ng][mt2][1] = o[ng][mt2][2] = o[ng][mt2][3] = 0.f;
+        m[ng][0] = m[ng][1] = -INFINITY;
+        l[ng][0] = l[ng][1] = 0.f;
+      }
+    }
+    const uint32_t aK = ptx::smem_u32(wring + (size_t)stage * C::kStage);
+    const uint32_t aV = aK + C::kHalf;
+
+    // S^T (16 tokens x 8 heads per group): A = K tile rows, B = Q^T
+    float s[NG][4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) s[ng][0] = s[ng][1] = s[ng][2] = s[ng][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int row = (mi & 1) * 8 + rr;
+      const int chunk = 2 * (kk & 3) + (mi >> 1);
+      uint32_t a[4];
+      ptx::ldsm_x4(aK + (kk >> 2) * C::kBox + ptx::sw128(row, chunk), a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(s[ng], a, qb[ng][kk][0], qb[ng][kk][1]);
+    }
+    // mask tokens outside the item (partial tiles only)
+    const int64_t tbase = cur.t0 + (int64_t)mt.w * kTile;
+    if (tbase + kTile > cur.t1) {
+      const bool v0 = tbase + r8 < cur.t1, v1 = tbase + r8 + 8 < cur.t1;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        if (!v0) s[ng][0] = s[ng][1] = -INFINITY;
+        if (!v1) s[ng][2] = s[ng][3] = -INFINITY;
+      }
+    }
+    // online softmax per head (column): reduce over the 16 tokens = the
+    // lane's two rows and the eight lanes sharing q4
+    const float c = geo.scale_log2e;
+    uint32_t pb[NG][2];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      float mx[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float v = fmaxf(s[ng][i], s[ng][i + 2]) * c;
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        mx[i] = fmaxf(m[ng][i], v);
+      }
+      float nb[2], alpha[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float bse = mx[i] == -INFINITY ? 0.f : mx[i];
+        nb[i] = -bse;
+        alpha[i] = exp2f(m[ng][i] - bse);
+        m[ng][i] = mx[i];
+      }
+      const float p0 = exp2f(fmaf(s[ng][0], c, nb[0]));
+      const float p1 = exp2f(fmaf(s[ng][1], c, nb[1]));
+      const float p2 = exp2f(fmaf(s[ng][2], c, nb[0]));
+      const float p3 = exp2f(fmaf(s[ng][3], c, nb[1]));
+      l[ng][0] = l[ng][0] * alpha[0] + (p0 + p2);
+      l[ng][1] = l[ng][1] * alpha[1] + (p1 + p3);
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          o[ng][mt2][0] *= alpha[0];
+          o[ng][mt2][1] *= alpha[1];
+          o[ng][mt2][2] *= alpha[0];
+          o[ng][mt2][3] *= alpha[1];
+        }
+      }
+      // P^T rows (tokens) -> P rows (heads): the B operand of O^T += V^T P^T
+      pb[ng][0] = ptx::movmatrix_trans(ptx::pack2<DT>(p0, p1));
+      pb[ng][1] = ptx::movmatrix_trans(ptx::pack2<DT>(p2, p3));
+    }
+    // O^T (d x heads) += V^T (d x 16 tokens) P^T
+#pragma unroll
+    for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+      const int row = (mi >> 1) * 8 + rr;
+      const int chunk = 2 * mt2 + (mi & 1);
+      uint32_t a[4];
+      ptx::ldsm_x4_t(aV + (chunk >> 3) * C::kBox + ptx::sw128(row, chunk & 7), a[0], a[1], a[2], a[3]);
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(o[ng][mt2], a, pb[ng][0], pb[ng][1]);
+    }
+    __syncwarp();
+    --inflight;
+    const bool last = mt.w == cur.ntiles - 1;
+    if (!exhausted && issue(stage)) ++inflight;
+    if (++stage == C::kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (!last) continue;
+
+    // ---- item epilogue: one partial per head that attends this span
+    const int slot_idx = cur.grp * geo.umax + cur.u;
+    const uint32_t hmask = tb.mask[slot_idx];
+    const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float lt = l[ng][i];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int r = ng * 8 + 2 * q4 + i;  // head within the group
+        if (r >= geo.g || !((hmask >> r) & 1u)) continue;
+        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
+        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        float* dst = plan.po + slot * D + r8;
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          dst[mt2 * 16] = o[ng][mt2][i];
+          dst[mt2 * 16 + 8] = o[ng][mt2][i + 2];
+        }
+        if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- merge
+// One CTA per (b, q-head): its (topk + 1) * C partial slots, in (span rank,
+// chunk) order, split into 8 contiguous runs, one per warp; empty slots
+// (m = -inf) are skipped.  The warps' results are then combined in order.
+constexpr int kMergeWarps = 8;
+constexpr int kBatch = 8;
+
+template <int DT, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    decode_merge_kernel(Plan plan, Geo geo, void* __restrict__ O, float* __restrict__ lse) {
+  constexpr int E = D / 32;  // columns per lane
+  __shared__ float wm[kMergeWarps], wl[kMergeWarps];
+  __shared__ float wo[kMergeWarps][D];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int nslots = (geo.topk + 1) * geo.C;
+  const int per = (nslots + kMergeWarps - 1) / kMergeWarps;
+  const int s0 = warp * per, s1 = min(s0 + per, nslots);
+  const int64_t base = (int64_t)row * nslots;
+  const float2* ml = reinterpret_cast<const float2*>(plan.ml);
+  float M = -INFINITY, Ls = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int sb = s0; sb < s1; sb += 32) {
+    const int sl = sb + lane;
+    const float2 mlv = sl < s1 ? ml[base + sl] : make_float2(-INFINITY, 0.f);
+    uint32_t nz = __ballot_sync(0xffffffffu, mlv.x != -INFINITY);
+    while (nz) {
+      int ids[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        ids[i] = nz ? __ffs(nz) - 1 : -1;
+        nz &= nz ? nz - 1u : 0u;
+      }
+      float po[kBatch][E];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (ids[i] >= 0) {
+          const float* src = plan.po + (base + sb + ids[i]) * D + lane * E;
+          if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            po[i][0] = v.x; po[i][1] = v.y; po[i][2] = v.z; po[i][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            po[i][0] = v.x; po[i][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (ids[i] < 0) continue;
+        const float pm = __shfl_sync(0xffffffffu, mlv.x, ids[i]);
+        const float pl = __shfl_sync(0xffffffffu, mlv.y, ids[i]);
+        const float Mn = fmaxf(M, pm);
+        const float a = exp2f(M - Mn), bb = exp2f(pm - Mn);
+        Ls = Ls * a + pl * bb;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + po[i][e] * bb;
+        M = Mn;
+      }
+    }
+  }
+  if (lane == 0) {
+    wm[warp] = M;
+    wl[warp] = Ls;
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) wo[warp][lane * E + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int col = threadIdx.x;
+    float Mt = -INFINITY;
+    for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, wm[w]);
+    float Lt = 0.f, ot = 0.f;
+    for (int w = 0; w < kMergeWarps; ++w) {
+      if (wm[w] == -INFINITY) continue;
+      const float f = exp2f(wm[w] - Mt);
+      Lt += wl[w] * f;
+      ot += wo[w][col] * f;
+    }
+    store_elem<DT>(O, (int64_t)row * D + col, ot / Lt);
+    if (lse && col == 0) lse[row] = Mt * kLn2 + logf(Lt);
+  }
+}
+
+size_t tables_bytes(const Problem& pr) {
+  const size_t n_grp = (size_t)pr.B * pr.Hkv;
+  const size_t slots = n_grp * ((size_t)pr.g * pr.topk + 1);
+  return n_grp * 4 + slots * (4 + 4 + 16) + (size_t)pr.B * pr.Hq * (pr.d + 8) * 2;
+}
+
+template <int DT, int D>
+cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const void* K, const void* V,
+                         const int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
+  using Cf = Cfg<D>;
+  const Layout lay = layout(pr);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  Plan plan;
+  plan.n_union = reinterpret_cast<int*>(w8 + lay.n_union);
+  plan.n_items = reinterpret_cast<int*>(w8 + lay.n_items);
+  plan.span = reinterpret_cast<int*>(w8 + lay.span);
+  plan.mask = reinterpret_cast<uint32_t*>(w8 + lay.mask);
+  plan.rank = w8 + lay.rank;
+  plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
+  plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
+  plan.po = reinterpret_cast<float*>(w8 + lay.po);
+  Geo geo;
+  geo.Hq = pr.Hq;
+  geo.Hkv = pr.Hkv;
+  geo.g = pr.g;
+  geo.topk = pr.topk;
+  geo.S = pr.S;
+  geo.C = lay.C;
+  geo.CH = lay.CH;
+  geo.umax = pr.g * pr.topk + 1;
+  geo.n_grp = pr.B * pr.Hkv;
+  geo.pos = pos;
+  geo.ell = pos / pr.S;
+  geo.scale_log2e = pr.scale * kLog2e;
+  const size_t tb = tables_bytes(pr);
+  geo.tables_in_smem = Cf::kFixed + tb <= (size_t)kSmemLimit;
+  const size_t smem = Cf::kFixed + (geo.tables_in_smem ? tb : 0);
+  uint32_t* err = ws_error(ws);
+
+  CUtensorMap tmK, tmV;
+  cudaError_t e = make_kv_tmap(&tmK, K, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
+  if (e != cudaSuccess) return e;
+  e = make_kv_tmap(&tmV, V, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
+  if (e != cudaSuccess) return e;
+
+  auto attend = pr.g <= 8 ? decode_attend_kernel<DT, D, 1> : decode_attend_kernel<DT, D, 2>;
+  static bool attr_done[2][kMaxDevices] = {};
+  e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), smem, st, tmK, tmV, Q, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st,
+                    plan, geo, O, lse);
+}
+
+}  // namespace
+
+bool decode_fast_supported(const Problem& pr) {
+  return (pr.dtype == DT_BF16 || pr.dtype == DT_F16) && (pr.d == 64 || pr.d == 128) &&
+         pr.g <= kMaxG && pr.topk <= kMaxK && (int64_t)pr.B * pr.Hkv <= kMaxGroups && pr.L > 0;
+}
+
+size_t decode_ws_bytes(const Problem& pr) { return layout(pr).total - kWsHeader; }
+
+cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, const void* K,
+                                 const void* V, const int32_t* sel, void* O, float* lse, void* ws,
+                                 cudaStream_t st) {
+  if (pr.d == 128) {
+    if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 128>(pr, Q, pos, K, V, sel, O, lse, ws, st);
+    return launch_typed<DT_F16, 128>(pr, Q, pos, K, V, sel, O, lse, ws, st);
+  }
+  if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 64>(pr, Q, pos, K, V, sel, O, lse, ws, st);
+  return launch_typed<DT_F16, 64>(pr, Q, pos, K, V, sel, O, lse, ws, st);
 }
 
 }  // namespace ssa

@@ -1,9 +1,12 @@
 // internal.h -- validated problem description and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "common.cuh"
 
@@ -22,6 +25,44 @@ struct Problem {
 // Workspace layout shared by the attention entry points.
 constexpr size_t kWsHeader = 256;  // error record + counters, keeps what follows aligned
 inline uint32_t* ws_error(void* ws) { return static_cast<uint32_t*>(ws); }
+
+// TMA descriptor of a [B, Hkv, L_cap, d] cache as {d, L, B*Hkv}, 64 x box_rows
+// boxes with 128-byte swizzling (16-bit types only).
+cudaError_t make_kv_tmap(CUtensorMap* map, const void* base, int dtype, int d, int64_t L,
+                         int64_t L_cap, int64_t BH, int box_rows);
+int device_sm_count();
+
+// Launches a kernel with programmatic dependent launch enabled: it may begin
+// before the previous kernel on the stream ends and must call pdl_wait()
+// (ptx.cuh) before its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device.
+constexpr int kMaxDevices = 64;
+template <typename F>
+cudaError_t ensure_smem_attr(F* func, size_t bytes, bool* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return e;
+}
 
 cudaError_t launch_summaries(const Problem& pr, const void* K, int64_t j0, int64_t j1, float* summ,
                              cudaStream_t st);

@@ -6,14 +6,15 @@
 // the lower span index.  Candidates of a query at position t are the complete
 // spans j < l = floor(t / S) (its own span l is always attended anyway).
 //
-// Both kernels compute a score as one fp32 FMA chain over c = 0 .. d-1,
-// acc = fma(q[c], summary[c], acc), so a (query, span) pair gets the same
-// bits in decode and in prefill, and identical spans tie exactly.  Scores
-// never leave the chip: each kernel keeps, per query row, a running list of
-// its best k (score, span) pairs in shared memory.
+// Each kernel computes a score in an order that depends only on the index
+// of the dimension, never on the span's position in a tile, so spans with
+// identical summaries get identical scores and tie exactly.  Scores never
+// leave the chip: each kernel keeps, per query row, a running list of its
+// best k (score, span) pairs in shared memory.
 #include <cooperative_groups.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -24,112 +25,122 @@ constexpr int kMaxG = 16;   // query heads per kv-head
 constexpr int kMaxK = 64;   // topk limit
 constexpr int kCluster = 8; // CTAs splitting one kv-head's candidates in decode
 
-// Warp-wide arg-max under `better`; every lane returns the winner.
-__device__ __forceinline__ void warp_best(float& s, int& j) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float os = __shfl_xor_sync(0xffffffffu, s, off);
-    int oj = __shfl_xor_sync(0xffffffffu, j, off);
-    if (better(os, oj, s, j)) {
-      s = os;
-      j = oj;
-    }
-  }
+// Order-preserving 32-bit key of a finite score: a higher score has a
+// higher key; 0 is reserved for "no candidate".
+__device__ __forceinline__ uint32_t score_key(float s) {
+  const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Writes the (at most topk) valid entries a warp holds, ascending by span,
-// then -1.  Lane r holds the r-th best in slot A and the (r+32)-th best in
-// slot B, as (score, span) or (-inf, kNoSpan).
-__device__ __forceinline__ void warp_emit_sorted(float sa, int ja, float sb, int jb, int lane,
-                                                 int topk, int32_t* sel_row, float* score_row) {
-  int pa = 0, pb = 0, nvalid = 0;
-  for (int src = 0; src < 32; ++src) {
-    int oa = __shfl_sync(0xffffffffu, ja, src);
-    int ob = __shfl_sync(0xffffffffu, jb, src);
-    if (src < topk && oa != kNoSpan) {
-      ++nvalid;
-      pa += oa < ja;
-      pb += oa < jb;
-    }
-    if (src + 32 < topk && ob != kNoSpan) {
-      ++nvalid;
-      pa += ob < ja;
-      pb += ob < jb;
-    }
-  }
-  const float nan = __int_as_float(0x7fc00000);
-  if (lane < topk) {
-    if (ja != kNoSpan) {
-      sel_row[pa] = ja;
-      if (score_row) score_row[pa] = sa;
-    }
-    if (lane >= nvalid) {
-      sel_row[lane] = -1;
-      if (score_row) score_row[lane] = nan;
-    }
-  }
-  if (lane + 32 < topk) {
-    if (jb != kNoSpan) {
-      sel_row[pb] = jb;
-      if (score_row) score_row[pb] = sb;
-    }
-    if (lane + 32 >= nvalid) {
-      sel_row[lane + 32] = -1;
-      if (score_row) score_row[lane + 32] = nan;
-    }
-  }
-}
-
-// Extracts the topk best of NV entries per lane (warp-wide) into slots A/B.
+// Marks the k best of the warp's entries.  Entry (i, lane) is the i-th
+// register of the lane; the entries' order (i major, lane minor) must be
+// ascending span index, so that among equal keys the earlier entry is the
+// lower span.  Finds the k-th largest key T by a bitwise search on the
+// key's bits (one warp-wide count per bit), takes every key above T and the
+// first entries equal to T.  Returns the lane's bitmask of chosen entries.
 template <int NV>
-__device__ __forceinline__ void warp_topk(float (&v)[NV], int (&vj)[NV], int lane, int topk,
-                                          float& sa, int& ja, float& sb, int& jb) {
-  sa = -INFINITY;
-  ja = kNoSpan;
-  sb = -INFINITY;
-  jb = kNoSpan;
-  for (int r = 0; r < topk; ++r) {
-    float bs = -INFINITY;
-    int bj = kNoSpan;
+__device__ __forceinline__ uint32_t warp_select(const uint32_t (&key)[NV], int k, int lane) {
+  int nv = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) nv += key[i] != 0u;
+  nv = __reduce_add_sync(0xffffffffu, nv);
+  uint32_t chosen = 0u;
+  if (nv <= k) {
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (better(v[i], vj[i], bs, bj)) {
-        bs = v[i];
-        bj = vj[i];
-      }
-    warp_best(bs, bj);
-    if (bj == kNoSpan) break;
+      if (key[i] != 0u) chosen |= 1u << i;
+    return chosen;
+  }
+  uint32_t T = 0u;
+#pragma unroll 1
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    int c = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (vj[i] == bj) {
-        v[i] = -INFINITY;
-        vj[i] = kNoSpan;
-      }
-    if (lane == r) {
-      sa = bs;
-      ja = bj;
-    } else if (lane + 32 == r) {
-      sb = bs;
-      jb = bj;
+    for (int i = 0; i < NV; ++i) c += key[i] >= cand;
+    if (__reduce_add_sync(0xffffffffu, c) >= k) T = cand;
+  }
+  int gt = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) gt += key[i] > T;
+  int need = k - __reduce_add_sync(0xffffffffu, gt);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const uint32_t eq = __ballot_sync(0xffffffffu, key[i] == T);
+    const bool take = key[i] > T || (key[i] == T && __popc(eq & lt_mask) < need);
+    need -= min(need, __popc(eq));
+    if (take) chosen |= 1u << i;
+  }
+  return chosen;
+}
+
+// Replaces a head's list (topk entries, ascending spans, invalid = kNoSpan)
+// by the topk best of the list and one block of 128 scores (spans jb ..);
+// NL = 0 when the list is still empty.
+template <int NL>
+__device__ __forceinline__ void fold_block(float* lsv, int* lsj, const float* sc, int64_t jb,
+                                           int64_t hi, int lane, int topk) {
+  constexpr int NV = NL + 4;
+  float v[NV];
+  int vj[NV];
+  uint32_t key[NV];
+#pragma unroll
+  for (int i = 0; i < NL; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < topk ? lsv[e] : -INFINITY;
+    vj[i] = e < topk ? lsj[e] : kNoSpan;
+    key[i] = vj[i] == kNoSpan ? 0u : score_key(v[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t jj = jb + lane + 32 * i;
+    const bool ok = jj < hi;
+    v[NL + i] = ok ? sc[lane + 32 * i] : -INFINITY;
+    vj[NL + i] = ok ? (int)jj : kNoSpan;
+    key[NL + i] = ok ? score_key(v[NL + i]) : 0u;
+  }
+  const uint32_t chosen = warp_select<NV>(key, topk, lane);
+  __syncwarp();
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const bool c = (chosen >> i) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, c);
+    if (c) {
+      const int p = base + __popc(bal & ((1u << lane) - 1u));
+      lsv[p] = v[i];
+      lsj[p] = vj[i];
     }
+    base += __popc(bal);
+  }
+  for (int e = base + lane; e < topk; e += 32) {
+    lsv[e] = -INFINITY;
+    lsj[e] = kNoSpan;
   }
 }
 
 // ---------------------------------------------------------------- decode
 // grid (kCluster, Hkv, B), one cluster per (b, kv-head).  CTA `rank` scores
-// candidates [rank*chunk, (rank+1)*chunk) for all g heads of the group,
-// 256 candidates at a time (one per thread), and folds each batch into
-// per-head lists; then CTA `rank` merges head rank (+8) over the cluster's
-// lists through distributed shared memory.
-template <int DT, int D>
+// candidates [rank*chunk, (rank+1)*chunk) for all g heads of the group in
+// blocks of 256: two lanes per candidate, each summing one half of d with
+// all of its summary loads in flight at once, the two halves then added.
+// Each block is folded into per-head lists; finally CTA `rank` merges head
+// rank (+8) over the cluster's lists through distributed shared memory.
+constexpr int kBlk = 128;
+
+template <int DT, int D, int G, int NE>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
     route_decode_kernel(const void* __restrict__ Q, const float* __restrict__ summ,
                         int32_t* __restrict__ sel, float* __restrict__ sel_score, int Hq, int Hkv,
                         int64_t pos, int S, int topk, int64_t ns_cap) {
-  __shared__ __align__(16) float q_s[kMaxG][D];
-  __shared__ float sc_s[kMaxG][256];
-  __shared__ float lsv_s[kMaxG][kMaxK];
-  __shared__ int lsj_s[kMaxG][kMaxK];
+  constexpr int HD = D / 2;          // dims per lane
+  constexpr int HPAD = HD + 4;       // padded half stride, keeps the two halves in other banks
+  constexpr int NL = HD / 4;         // float4 loads per lane
+  __shared__ __align__(16) float q_s[G][2 * HPAD];
+  __shared__ float sc_s[G][kBlk];
+  __shared__ float lsv_s[G][kMaxK];
+  __shared__ int lsj_s[G][kMaxK];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -141,99 +152,106 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
   const int64_t lo = min(ell, (int64_t)rank * chunk);
   const int64_t hi = min(ell, lo + chunk);
 
-  for (int x = tid; x < g * D; x += 256) {
-    int hl = x / D, c = x - hl * D;
-    q_s[hl][c] = load_elem<DT>(Q, (int64_t)(b * Hq + kvh * g + hl) * D + c);
-  }
-  for (int x = tid; x < kMaxG * kMaxK; x += 256) {
+  for (int x = tid; x < G * kMaxK; x += 256) {
     lsv_s[x / kMaxK][x % kMaxK] = -INFINITY;
     lsj_s[x / kMaxK][x % kMaxK] = kNoSpan;
+  }
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  for (int x = tid; x < g * D; x += 256) {
+    const int hl = x / D, c = x - hl * D;
+    q_s[hl][(c / HD) * HPAD + (c % HD)] = load_elem<DT>(Q, (int64_t)(b * Hq + kvh * g + hl) * D + c);
   }
   __syncthreads();
 
   const float* sbase = summ + (int64_t)(b * Hkv + kvh) * ns_cap * D;
-  for (int64_t jb = lo; jb < hi; jb += 256) {
-    const int64_t j = jb + tid;
-    float acc[kMaxG];
+  const int half = tid & 1;
+  for (int64_t jb = lo; jb < hi; jb += kBlk) {
+    {
+      const int jj = tid >> 1;
+      const int64_t j = jb + jj;
+      float acc[G];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) acc[h] = 0.f;
-    if (j < hi) {
-      const float4* srow = reinterpret_cast<const float4*>(sbase + j * D);
-#pragma unroll 4
-      for (int c4 = 0; c4 < D / 4; ++c4) {
-        float4 s = __ldg(srow + c4);
+      for (int h = 0; h < G; ++h) acc[h] = 0.f;
+      if (j < hi) {
+        const float4* src = reinterpret_cast<const float4*>(sbase + j * D + half * HD);
+        float4 sv[NL];
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-          if (h < g) {
-            float4 qv = *reinterpret_cast<const float4*>(&q_s[h][c4 * 4]);
-            acc[h] = fmaf(qv.x, s.x, acc[h]);
-            acc[h] = fmaf(qv.y, s.y, acc[h]);
-            acc[h] = fmaf(qv.z, s.z, acc[h]);
-            acc[h] = fmaf(qv.w, s.w, acc[h]);
+        for (int i = 0; i < NL; ++i) sv[i] = __ldg(src + i);
+#pragma unroll
+        for (int i = 0; i < NL; ++i) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (h < g) {
+              const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][half * HPAD + 4 * i]);
+              acc[h] = fmaf(qv.x, sv[i].x, acc[h]);
+              acc[h] = fmaf(qv.y, sv[i].y, acc[h]);
+              acc[h] = fmaf(qv.z, sv[i].z, acc[h]);
+              acc[h] = fmaf(qv.w, sv[i].w, acc[h]);
+            }
           }
         }
       }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (h < g) {
+          const float other = __shfl_xor_sync(0xffffffffu, acc[h], 1);
+          if (half == 0) sc_s[h][jj] = j < hi ? acc[h] + other : -INFINITY;
+        }
+      }
     }
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-      if (h < g) sc_s[h][tid] = j < hi ? acc[h] : -INFINITY;
     __syncthreads();
-    // fold this batch into the head's list: topk rounds of warp arg-max
+    // fold this block into the head's list (list entries come first: their
+    // spans are below every span of the block; the first block has no list)
     for (int h = warp; h < g; h += 8) {
-      float v[10];
-      int vj[10];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        int64_t jj = jb + lane + 32 * i;
-        bool ok = jj < hi;
-        v[i] = ok ? sc_s[h][lane + 32 * i] : -INFINITY;
-        vj[i] = ok ? (int)jj : kNoSpan;
-      }
-      v[8] = lane < topk ? lsv_s[h][lane] : -INFINITY;
-      vj[8] = lane < topk ? lsj_s[h][lane] : kNoSpan;
-      v[9] = lane + 32 < topk ? lsv_s[h][lane + 32] : -INFINITY;
-      vj[9] = lane + 32 < topk ? lsj_s[h][lane + 32] : kNoSpan;
-      float sa, sb;
-      int ja, jb2;
-      warp_topk<10>(v, vj, lane, topk, sa, ja, sb, jb2);
-      __syncwarp();
-      if (lane < topk) {
-        lsv_s[h][lane] = sa;
-        lsj_s[h][lane] = ja;
-      }
-      if (lane + 32 < topk) {
-        lsv_s[h][lane + 32] = sb;
-        lsj_s[h][lane + 32] = jb2;
-      }
+      if (jb == lo)
+        fold_block<0>(lsv_s[h], lsj_s[h], sc_s[h], jb, hi, lane, topk);
+      else
+        fold_block<2>(lsv_s[h], lsj_s[h], sc_s[h], jb, hi, lane, topk);
     }
     __syncthreads();
   }
 
   cluster.sync();
+  // final: CTA `rank` selects head rank (+8) from the cluster's lists, which
+  // concatenated in rank order are ascending in span index
   if (warp == 0) {
-    constexpr int NE = kCluster * kMaxK / 32;  // entries per lane
     for (int h = rank; h < g; h += kCluster) {
       float v[NE];
       int vj[NE];
+      uint32_t key[NE];
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
-        int e = lane + 32 * i;  // entry e of the concatenated lists
-        int src = e / kMaxK, s = e % kMaxK;
+        const int e = i * 32 + lane;  // entry e = src * topk + s
+        const int src = e / topk, s = e - src * topk;
         v[i] = -INFINITY;
         vj[i] = kNoSpan;
-        if (s < topk) {
-          const float* rv = cluster.map_shared_rank(&lsv_s[h][0], src);
-          const int* rj = cluster.map_shared_rank(&lsj_s[h][0], src);
-          v[i] = rv[s];
-          vj[i] = rj[s];
+        if (src < kCluster) {
+          v[i] = cluster.map_shared_rank(&lsv_s[h][0], src)[s];
+          vj[i] = cluster.map_shared_rank(&lsj_s[h][0], src)[s];
         }
+        key[i] = vj[i] == kNoSpan ? 0u : score_key(v[i]);
       }
-      float sa, sb;
-      int ja, jb2;
-      warp_topk<NE>(v, vj, lane, topk, sa, ja, sb, jb2);
+      const uint32_t chosen = warp_select<NE>(key, topk, lane);
       const int64_t row = (int64_t)b * Hq + kvh * g + h;
-      warp_emit_sorted(sa, ja, sb, jb2, lane, topk, sel + row * topk,
-                       sel_score ? sel_score + row * topk : nullptr);
+      int32_t* out = sel + row * topk;
+      float* osc = sel_score ? sel_score + row * topk : nullptr;
+      int base = 0;
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
+        const bool c = (chosen >> i) & 1u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, c);
+        if (c) {
+          const int p = base + __popc(bal & ((1u << lane) - 1u));
+          out[p] = vj[i];
+          if (osc) osc[p] = v[i];
+        }
+        base += __popc(bal);
+      }
+      for (int e = base + lane; e < topk; e += 32) {
+        out[e] = -1;
+        if (osc) osc[e] = __int_as_float(0x7fc00000);
+      }
     }
   }
   cluster.sync();
@@ -377,24 +395,34 @@ __global__ void __launch_bounds__(256) route_prefill_kernel(
   }
 }
 
+template <int DT, int D, int G, int NE>
+cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
+                                int32_t* sel, float* sel_score, cudaStream_t st) {
+  dim3 grid(kCluster, pr.Hkv, pr.B);
+  return launch_pdl(route_decode_kernel<DT, D, G, NE>, grid, dim3(256), 0, st, Q, summ, sel,
+                    sel_score, pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap);
+}
+
+template <int DT, int D, int G>
+cudaError_t decode_route_ne(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
+                            int32_t* sel, float* sel_score, cudaStream_t st) {
+  // entries per lane of the final cluster merge: kCluster * topk / 32
+  if (pr.topk <= 16) return launch_decode_route<DT, D, G, 4>(pr, Q, q_pos0, summ, sel, sel_score, st);
+  return launch_decode_route<DT, D, G, 16>(pr, Q, q_pos0, summ, sel, sel_score, st);
+}
+
 template <int DT, int D>
 cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st) {
   if (n_q == 1) {
-    dim3 grid(kCluster, pr.Hkv, pr.B);
-    route_decode_kernel<DT, D><<<grid, 256, 0, st>>>(Q, summ, sel, sel_score, pr.Hq, pr.Hkv,
-                                                     q_pos0, pr.S, pr.topk, pr.ns_cap);
-    return cudaGetLastError();
+    if (pr.g <= 4) return decode_route_ne<DT, D, 4>(pr, Q, q_pos0, summ, sel, sel_score, st);
+    if (pr.g <= 8) return decode_route_ne<DT, D, 8>(pr, Q, q_pos0, summ, sel, sel_score, st);
+    return decode_route_ne<DT, D, 16>(pr, Q, q_pos0, summ, sel, sel_score, st);
   }
   const size_t smem = prefill_smem_bytes<D>(pr.topk);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(route_prefill_kernel<DT, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)prefill_smem_bytes<D>(kMaxK));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_attr(route_prefill_kernel<DT, D>, prefill_smem_bytes<D>(kMaxK), attr_done);
+  if (e != cudaSuccess) return e;
   int64_t tiles = (n_q * pr.g + kRows - 1) / kRows;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)tiles, pr.Hkv, pr.B);

@@ -1,0 +1,64 @@
+// tmap.cu -- host-side TMA descriptors for the key / value cache.
+//
+// The cache [B, Hkv, L_cap, d] is described as a 3-D tensor {d, L, B*Hkv}
+// with row stride d elements and head stride L_cap*d elements, so that a
+// load of rows >= L (the valid length) is zero-filled by the hardware
+// instead of reading whatever a not-yet-written part of the cache holds.
+// The box is 64 elements (128 bytes) wide with 128-byte swizzling.
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace ssa {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t make_kv_tmap(CUtensorMap* map, const void* base, int dtype, int d, int64_t L,
+                         int64_t L_cap, int64_t BH, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const int esz = dtype == DT_F32 ? 4 : 2;
+  if (dtype == DT_F32) return cudaErrorNotSupported;
+  CUtensorMapDataType t =
+      dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(L > 0 ? L : 1), (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)L_cap * d * esz};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace ssa
