@@ -140,6 +140,10 @@ def flush_l2(buf):
 
 # --------------------------------------------------------------------- decode
 class DecodeBench:
+    """The decode workload: 256 distinct queries at the last 256 positions of
+    the cache.  A step routes one query token per head and attends it; the
+    256 steps are captured once in a CUDA graph and replayed."""
+
     def __init__(self, w: W.Workload, dev):
         self.w = w
         self.dev = dev
@@ -150,27 +154,40 @@ class DecodeBench:
         self.p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
         self.summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
         self.ws = ssa.workspace(self.p, 1, ssa.SSA_OP_DECODE, dev)
-        self.sel = torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
+        self.sels = [torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
+                     for _ in range(w.n_q)]
+        self.sel = self.sels[0]
         self.O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=dev)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         self.qs = [self.Q[s].contiguous() for s in range(w.n_q)]
-        self.stream = torch.cuda.current_stream(dev)
 
     def build_summaries(self):
         ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
 
-    def step(self, s, ev=None):
-        w = self.w
-        i = s % w.n_q
-        pos = w.q_pos0 + i
-        q = self.qs[i]
-        ssa.ssa_route(self.p, q, 1, pos, self.summ, self.sel, None, None, self.stream)
-        if ev is not None:
-            ev[0].record(self.stream)
-        ssa.ssa_attend_decode(self.p, q, pos, self.K, self.V, self.sel, self.O, self.lse, self.ws,
-                              self.stream)
-        if ev is not None:
-            ev[1].record(self.stream)
+    def route(self, i):
+        ssa.ssa_route(self.p, self.qs[i], 1, self.w.q_pos0 + i, self.summ, self.sels[i])
+
+    def attend(self, i):
+        ssa.ssa_attend_decode(self.p, self.qs[i], self.w.q_pos0 + i, self.K, self.V, self.sels[i],
+                              self.O, self.lse, self.ws)
+
+    def step(self, i):
+        self.route(i)
+        self.attend(i)
+
+    def graph(self, fn, n):
+        """A CUDA graph of fn(0 .. n-1) (query index modulo the 256 queries)."""
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            for i in range(min(n, 3)):
+                fn(i % self.w.n_q)
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fn(i % self.w.n_q)
+        return g
 
     def algorithmic_bytes(self):
         """Per query index: (attend bytes, route bytes), from the actual selections."""
@@ -178,10 +195,12 @@ class DecodeBench:
         el = 2 if w.dtype != torch.float32 else 4
         out = []
         for i in range(w.n_q):
+            self.route(i)
+        torch.cuda.synchronize()
+        for i in range(w.n_q):
             pos = w.q_pos0 + i
             ell = pos // w.S
-            ssa.ssa_route(self.p, self.qs[i], 1, pos, self.summ, self.sel)
-            sel = self.sel.reshape(w.B, w.Hkv, w.g * w.topk).cpu().numpy()
+            sel = self.sels[i].reshape(w.B, w.Hkv, w.g * w.topk).cpu().numpy()
             kv_rows = 0
             for b in range(w.B):
                 for g in range(w.Hkv):
@@ -193,9 +212,19 @@ class DecodeBench:
         return out
 
 
+def replay_ms(g, reps, stream):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
 def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     db = DecodeBench(w, dev)
-    st = db.stream
+    st = torch.cuda.current_stream(dev)
     # summaries of the whole cache (the decode steps read them), timed on its own
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     db.build_summaries()
@@ -208,27 +237,35 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     summ_bytes = w.B * w.Hkv * w.L * w.d * 2 + w.B * w.Hkv * w.n_spans * w.d * 4
     per_q = db.algorithmic_bytes()
 
-    for s in range(warmup):
-        db.step(s)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = w.n_q
+    reps, rem = divmod(steps, n)
+    g_step = db.graph(db.step, n)
+    g_rem = db.graph(db.step, rem) if rem else None
+    g_att = db.graph(db.attend, n)          # attend only, on the selections routed above
+    for _ in range(max(1, -(-warmup // n))):
+        g_step.replay()
+    g_att.replay()
+    torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         barrier(ws_n)
         torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(st)
-        for s in range(steps):
-            db.step(s, evs[s])
+        for _ in range(reps):
+            g_step.replay()
+        if g_rem is not None:
+            g_rem.replay()
         stop.record(st)
         torch.cuda.synchronize()
         barrier(ws_n)
     total_ms = start.elapsed_time(stop)
-    attend_ms = sum(a.elapsed_time(b) for a, b in evs)
+    att_reps = max(1, reps)
+    attend_ms = replay_ms(g_att, att_reps, st) / (att_reps * n) * steps
     err = ssa.ssa_workspace_error(db.ws)
     total_ms_max = max_over_ranks(total_ms, ws_n)
 
-    attend_bytes = sum(per_q[s % w.n_q][0] for s in range(steps))
-    route_bytes = sum(per_q[s % w.n_q][1] for s in range(steps))
+    attend_bytes = sum(per_q[s % n][0] for s in range(steps))
+    route_bytes = sum(per_q[s % n][1] for s in range(steps))
     pk = peaks()
     achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
     res = {
@@ -241,13 +278,15 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
         "step_bytes_gbs": (attend_bytes + route_bytes) / (total_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "attend_decode (gathered K/V of the union of selected spans + local span)",
+                     "kernel": "ssa_attend_decode (plan + gathered K/V attend + merge), timed as "
+                               "one CUDA-graph node group",
                      "peak_source": pk["source"]},
         "summaries": {"ms": summ_ms, "gbs": summ_bytes / (summ_ms * 1e-3) / 1e9,
                       "frac": summ_bytes / (summ_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "clocks": clk.summary(),
         "device_error_bits": err,
-        "launches_per_step": None,
+        "timing": "CUDA graph of %d decode steps replayed %d times%s" % (
+            n, reps, " + %d-step remainder" % rem if rem else ""),
     }
     res["e2e"] = bench_decode_e2e(db, min(steps, 2048))
     if cpu_leg:
@@ -256,28 +295,28 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
 
 
 def bench_decode_e2e(db: DecodeBench, steps: int):
-    """Same decode through the C ABI with host buffers: H2D query, D2H output, every step."""
+    """Same decode through the C ABI with host buffers: every step copies its
+    query in from pinned host memory and the output back, then waits for it."""
     w = db.w
-    st = db.stream
+    st = torch.cuda.current_stream(db.dev)
     el = db.Q.element_size()
     q_host = db.Q.cpu().pin_memory()
     o_host = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype).pin_memory()
     q_dev = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=db.dev)
-    for s in range(8):
+
+    def one(s):
         i = s % w.n_q
         q_dev.copy_(q_host[i], non_blocking=True)
         ssa.ssa_route(db.p, q_dev, 1, w.q_pos0 + i, db.summ, db.sel, None, None, st)
         ssa.ssa_attend_decode(db.p, q_dev, w.q_pos0 + i, db.K, db.V, db.sel, db.O, None, db.ws, st)
         o_host.copy_(db.O, non_blocking=True)
         st.synchronize()
+
+    for s in range(8):
+        one(s)
     t0 = time.perf_counter()
     for s in range(steps):
-        i = s % w.n_q
-        q_dev.copy_(q_host[i], non_blocking=True)
-        ssa.ssa_route(db.p, q_dev, 1, w.q_pos0 + i, db.summ, db.sel, None, None, st)
-        ssa.ssa_attend_decode(db.p, q_dev, w.q_pos0 + i, db.K, db.V, db.sel, db.O, None, db.ws, st)
-        o_host.copy_(db.O, non_blocking=True)
-        st.synchronize()
+        one(s)
     dt = time.perf_counter() - t0
     return {"value": steps / dt, "unit": "tok/s", "h2d_bytes_per_step": w.B * w.Hq * w.d * el,
             "d2h_bytes_per_step": w.B * w.Hq * w.d * el, "steps": steps}
@@ -450,7 +489,7 @@ def main():
         run_reference(args, ws_n, rank)
         return
     steps = args.steps if args.steps is not None else 8192
-    warmup = max(3, args.warmup if args.warmup is not None else 256)
+    warmup = max(3, args.warmup if args.warmup is not None else 512)
     dev = torch.device("cuda", local)
     ssa.lib()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
@@ -480,7 +519,8 @@ def main():
         "gpu_launches": None,
         "decode_detail": {k: dec[k] for k in ("attend_ms_per_step", "route_plus_gaps_ms_per_step",
                                                "attend_bytes_per_step", "route_bytes_per_step",
-                                               "step_bytes_gbs", "summaries", "device_error_bits")},
+                                               "step_bytes_gbs", "summaries", "device_error_bits",
+                                               "timing")},
     }
     line["gpu_launches"] = steps * launches_per_decode_step(w)
     if pre is not None:
@@ -495,8 +535,8 @@ def main():
 
 
 def launches_per_decode_step(w) -> int:
-    """Kernels one decode step launches: route (1) + attend (1 row kernel, or
-    plan + split + merge on the fast path)."""
+    """Kernels one decode step launches: route (1) + attend (plan, split
+    attention and merge on the 16-bit path; one row kernel otherwise)."""
     p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
     fast = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE) > 256
     return 1 + (3 if fast else 1)

@@ -1,13 +1,799 @@
-// prefill.cu -- prefill attention fast path (span-major tiles + merge).
+// prefill.cu -- chunked-prefill attention on the 5th-generation tensor cores.
+//
+// Superlinear release post (geeks.co.kr/post/2077): chunked prefill against
+// the kept cache, and, in its key-idea section, token-level attention inside
+// each query's chosen spans; SubQ SSA page (stork.ai): exact attention over
+// the content-selected subset.
+//
+// The queries of a chunk choose different spans, so the work is dispatched
+// span-major: the (query, head) rows that chose span j of kv-head h form a
+// bucket, and a bucket is cut into tiles of 128 rows that share the span's
+// keys and values.  Each query's own span (causal) is a second kind of tile:
+// 128 / g consecutive queries times the g heads of a kv-head.
+//
+//  count    per (b, query head, 128 queries): validates sel rows and counts
+//           each bucket's rows (shared-memory histogram, one global atomic
+//           per non-empty bucket)
+//  scan     one CTA: bucket offsets, the tile table (span tiles, then local
+//           tiles)
+//  scatter  writes each row's id and its rank in the sel row into its
+//           bucket
+//  attend   persistent, one CTA per SM.  Per tile: the 128 query rows are
+//           gathered into shared memory (128-byte swizzled K-major operand),
+//           key / value blocks of 128 tokens stream through a 2-stage TMA
+//           ring, one thread issues tcgen05.mma: S = Q K^T into tensor
+//           memory (double buffered), four warps run the softmax (one row
+//           per thread, lazy rescaling of O when the running maximum grows
+//           by more than 2^8), write P as bf16 / fp16 to shared memory, and
+//           O += P V accumulates in tensor memory.  The tile ends by writing
+//           one partial (m, l, normalised o) per row.
+//  merge    per (b, head, query): combines the row's partials (its spans in
+//           sel order, then the local span) into O and lse.
 #include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
 
 namespace ssa {
+namespace {
 
-bool prefill_fast_supported(const Problem&) { return false; }
-size_t prefill_ws_bytes(const Problem&, int64_t) { return 0; }
-cudaError_t launch_attend_prefill(const Problem&, const void*, int64_t, int64_t, const void*,
-                                  const void*, const int32_t*, void*, float*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kTileRows = 128;
+constexpr int kKeyBlk = 128;
+constexpr int kMaxK = 64;
+constexpr int kMaxG = 16;
+constexpr int kHistMax = 12288;  // spans per kv-head the shared histogram covers
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct PrefLayout {
+  size_t counts, offsets, cursors, tiles, ntiles, rows, pml, po, total;
+  int64_t n_buckets, max_entries, max_tiles;
+};
+
+// Workspace of a chunk of n_q queries (the bucket index space covers every
+// span slot of the cache, so the layout needs no query positions).
+PrefLayout pref_layout(const Problem& pr, int64_t n_q) {
+  PrefLayout l;
+  const int64_t bh = (int64_t)pr.B * pr.Hkv;
+  l.n_buckets = bh * pr.ns_cap;
+  l.max_entries = (int64_t)pr.B * pr.Hq * n_q * pr.topk;
+  const int64_t mq = kTileRows / pr.g;  // queries per local tile
+  const int64_t local_tiles = bh * ((n_q + mq - 1) / mq + n_q / pr.S + 2);
+  l.max_tiles = l.max_entries / kTileRows + l.n_buckets + local_tiles;
+  const int64_t parts = (int64_t)pr.B * pr.Hq * n_q * (pr.topk + 1);
+  size_t off = kWsHeader;
+  l.counts = off; off = align256(off + l.n_buckets * 4);
+  l.offsets = off; off = align256(off + l.n_buckets * 4);
+  l.cursors = off; off = align256(off + l.n_buckets * 4);
+  l.ntiles = off; off = align256(off + 16);
+  l.tiles = off; off = align256(off + l.max_tiles * 16);
+  l.rows = off; off = align256(off + l.max_entries * 4);
+  l.pml = off; off = align256(off + parts * 8);
+  l.po = off; off = align256(off + parts * (size_t)pr.d * 2);
+  l.total = off;
+  return l;
+}
+
+struct PrefArgs {
+  int* counts;
+  int* offsets;
+  int* cursors;
+  int* ntiles;     // [0] tiles in the table
+  int4* tiles;     // {bucket or -1 - bh, row0 or first query, rows or queries, 0}
+  int* rows;       // bucket entries: row id << 6 | rank
+  float2* pml;     // [rows of Q][topk + 1] (m base 2, l)
+  uint16_t* po;    // [rows of Q][topk + 1][d] normalised partial output (Q's type)
+  int B, Hq, Hkv, g, d, S, topk;
+  int64_t n_q, q_pos0, ns_cap, n_buckets;
+  float scale_log2e;
+};
+
+// The used entries of a sel row (the leading strictly ascending run of
+// candidate spans; anything else but -1 after it is an error), one thread.
+__device__ __forceinline__ int row_used(const int32_t* row, int topk, int64_t ell, int* js, bool* bad) {
+  int n = 0;
+  int64_t prev = -1;
+  bool stop = false;
+  *bad = false;
+  for (int r = 0; r < topk; ++r) {
+    const int j = row[r];
+    if (!stop && j >= 0 && j < ell && j > prev) {
+      js[n++] = j;
+      prev = j;
+    } else {
+      stop = true;
+      if (j != -1) *bad = true;
+    }
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------- count
+// grid (ceil(n_q / 256), B * Hq), one thread per query of one query head.
+__global__ void __launch_bounds__(256) prefill_count_kernel(const int32_t* __restrict__ sel, PrefArgs a,
+                                                            uint32_t* __restrict__ err) {
+  extern __shared__ int hist[];
+  const int bhq = blockIdx.y;
+  const int b = bhq / a.Hq, h = bhq - b * a.Hq;
+  const int kvh = h / a.g;
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t ns = a.ns_cap;
+  const bool use_hist = ns <= kHistMax;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  if (use_hist)
+    for (int x = threadIdx.x; x < ns; x += 256) hist[x] = 0;
+  __syncthreads();
+  int* gcount = a.counts + (int64_t)(b * a.Hkv + kvh) * ns;
+  if (i < a.n_q) {
+    const int64_t row = (int64_t)bhq * a.n_q + i;
+    const int64_t ell = (a.q_pos0 + i) / a.S;
+    int js[kMaxK];
+    bool bad;
+    const int n = row_used(sel + row * a.topk, a.topk, ell, js, &bad);
+    if (bad) flag_error(err, SSA_DEVERR_BAD_SELECTION);
+    for (int r = 0; r < n; ++r) {
+      if (use_hist) atomicAdd(&hist[js[r]], 1);
+      else atomicAdd(&gcount[js[r]], 1);
+    }
+  }
+  __syncthreads();
+  if (use_hist)
+    for (int x = threadIdx.x; x < ns; x += 256)
+      if (hist[x]) atomicAdd(&gcount[x], hist[x]);
+}
+
+// ---------------------------------------------------------------- scan
+// One CTA of 1024 threads: exclusive scan of the bucket counts, the span
+// tiles, then the local tiles (queries of one local span, 128 / g at a time).
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tmp, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < (int)(blockDim.x >> 5) ? tmp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    tmp[lane] = w;
+  }
+  __syncthreads();
+  const int64_t before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
+  *total = tmp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kScanThreads) prefill_scan_kernel(PrefArgs a) {
+  __shared__ int64_t tmp[32];
+  __shared__ int64_t carry_e, carry_t;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  if (threadIdx.x == 0) carry_e = carry_t = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < a.n_buckets; base += kScanThreads) {
+    const int64_t bk = base + threadIdx.x;
+    const int c = bk < a.n_buckets ? a.counts[bk] : 0;
+    const int nt = (c + kTileRows - 1) / kTileRows;
+    int64_t tot_e, tot_t;
+    const int64_t pe = block_exclusive_scan(c, tmp, &tot_e) + carry_e;
+    const int64_t pt = block_exclusive_scan(nt, tmp, &tot_t) + carry_t;
+    if (bk < a.n_buckets) {
+      a.offsets[bk] = (int)pe;
+      a.cursors[bk] = (int)pe;
+      for (int t = 0; t < nt; ++t)
+        a.tiles[pt + t] = make_int4((int)bk, t * kTileRows, min(kTileRows, c - t * kTileRows), 0);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry_e += tot_e;
+      carry_t += tot_t;
+    }
+    __syncthreads();
+  }
+  // local tiles: for every (b, kv-head) and every span the chunk's queries touch
+  const int64_t mq = kTileRows / a.g;
+  const int64_t l0 = a.q_pos0 / a.S, l1 = (a.q_pos0 + a.n_q - 1) / a.S;
+  const int64_t nspan = l1 - l0 + 1;
+  const int64_t bh_n = (int64_t)a.B * a.Hkv;
+  for (int64_t base = 0; base < bh_n * nspan; base += kScanThreads) {
+    const int64_t e = base + threadIdx.x;
+    int64_t qa = 0, qn = 0;
+    if (e < bh_n * nspan) {
+      const int64_t ell = l0 + e % nspan;
+      const int64_t pa = max(a.q_pos0, ell * a.S), pb = min(a.q_pos0 + a.n_q, (ell + 1) * a.S);
+      qa = pa - a.q_pos0;
+      qn = pb - pa;
+    }
+    const int64_t nt = qn > 0 ? (qn + mq - 1) / mq : 0;
+    int64_t tot;
+    const int64_t pt = block_exclusive_scan(nt, tmp, &tot) + carry_t;
+    if (e < bh_n * nspan) {
+      const int bh = (int)(e / nspan);
+      for (int64_t t = 0; t < nt; ++t)
+        a.tiles[pt + t] = make_int4(-1 - bh, (int)(qa + t * mq), (int)min(mq, qn - t * mq), 0);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry_t += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.ntiles[0] = (int)carry_t;
+}
+
+// ---------------------------------------------------------------- scatter
+__global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __restrict__ sel, PrefArgs a) {
+  extern __shared__ int sh[];
+  const int bhq = blockIdx.y;
+  const int b = bhq / a.Hq, h = bhq - b * a.Hq;
+  const int kvh = h / a.g;
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t ns = a.ns_cap;
+  const bool use_hist = ns <= kHistMax;
+  int* hist = sh;
+  int* base = sh + (use_hist ? ns : 0);
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  if (use_hist)
+    for (int x = threadIdx.x; x < ns; x += 256) hist[x] = 0;
+  __syncthreads();
+  const int64_t bkt0 = (int64_t)(b * a.Hkv + kvh) * ns;
+  int js[kMaxK];
+  int n = 0;
+  const int64_t row = (int64_t)bhq * a.n_q + i;
+  if (i < a.n_q) {
+    bool bad;
+    n = row_used(sel + row * a.topk, a.topk, (a.q_pos0 + i) / a.S, js, &bad);
+    if (use_hist)
+      for (int r = 0; r < n; ++r) atomicAdd(&hist[js[r]], 1);
+  }
+  __syncthreads();
+  if (use_hist) {
+    for (int x = threadIdx.x; x < ns; x += 256) {
+      const int c = hist[x];
+      base[x] = c ? atomicAdd(&a.cursors[bkt0 + x], c) : 0;
+      hist[x] = 0;
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < n; ++r) {
+    const int j = js[r];
+    const int pos = use_hist ? base[j] + atomicAdd(&hist[j], 1) : atomicAdd(&a.cursors[bkt0 + j], 1);
+    a.rows[pos] = (int)((row << 6) | r);
+  }
+}
+
+// ---------------------------------------------------------------- attend
+template <int D>
+struct ACfg {
+  static constexpr int kRegion = kTileRows * 128;      // 128 rows x 128 bytes
+  static constexpr int kQBytes = (D / 64) * kRegion;    // Q tile, D/64 regions
+  static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block
+  static constexpr int kStage = 2 * kKVBytes;
+  static constexpr int kPBytes = 2 * kRegion;           // P tile: 128 keys = 2 regions
+  static constexpr int kStages = 2;
+  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + kStages * kStage + kPBytes + 256;
+  static constexpr uint32_t kTmemCols = 512;            // S0, S1, O
+};
+
+constexpr int kAttThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+
+struct Tile {
+  int kind_bh;  // bucket (>= 0) or -1 - bh
+  int row0, nrows;
+  int bh;
+  int64_t key0, key_end;  // keys [key0, key_end)
+  int nkb;
+  int64_t i0;              // local tiles: first query index
+};
+
+__device__ __forceinline__ Tile load_tile(const PrefArgs& a, int t) {
+  const int4 v = a.tiles[t];
+  Tile x;
+  x.kind_bh = v.x;
+  if (v.x >= 0) {
+    const int64_t bk = v.x;
+    x.bh = (int)(bk / a.ns_cap);
+    const int64_t j = bk - (int64_t)x.bh * a.ns_cap;
+    x.row0 = v.y;
+    x.nrows = v.z;
+    x.key0 = j * a.S;
+    x.key_end = x.key0 + a.S;
+    x.i0 = 0;
+  } else {
+    x.bh = -1 - v.x;
+    x.i0 = v.y;
+    x.row0 = 0;
+    x.nrows = v.z * a.g;
+    const int64_t t0 = a.q_pos0 + v.y;
+    x.key0 = (t0 / a.S) * a.S;
+    x.key_end = t0 + v.z;  // up to the last query's own position
+  }
+  x.nkb = (int)((x.key_end - x.key0 + kKeyBlk - 1) / kKeyBlk);
+  return x;
+}
+
+template <int DT, int D>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    prefill_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const void* __restrict__ Q, PrefArgs a, uint32_t* __restrict__ err) {
+  using C = ACfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = sQ + C::kQBytes;
+  uint8_t* sP = sKV + C::kStages * C::kStage;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + C::kPBytes);
+  uint64_t* q_full = bar + 0;
+  uint64_t* kv_full = bar + 1;   // [2]
+  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* s_full = bar + 5;    // [2]
+  uint64_t* s_free = bar + 7;    // [2]
+  uint64_t* p_full = bar + 9;
+  uint64_t* pv_done = bar + 10;
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 12);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 13);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    ptx::mbar_init(q_full, 128);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+      ptx::mbar_init(&s_full[s], 1);
+      ptx::mbar_init(&s_free[s], 4);
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(pv_done, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) tc::alloc(tmem_base, C::kTmemCols);
+  if (warp == 4 && lane == 0) {
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_base;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO = tmem + 256;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int ntiles = a.ntiles[0];
+
+  auto fail = [&](uint32_t bit) {
+    flag_error(err, bit);
+    *abort = 1;
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int64_t gb = 0;
+      for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+        const Tile x = load_tile(a, t);
+        for (int kb = 0; kb < x.nkb; ++kb) {
+          const int64_t g = gb + kb;
+          const int st = (int)(g & 1);
+          if (g >= 2 && !ptx::mbar_wait(&kv_empty[st], (uint32_t)(((g - 2) >> 1) & 1))) {
+            fail(SSA_DEVERR_WAIT_TIMEOUT);
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&kv_full[st], C::kStage);
+          uint8_t* dK = sKV + st * C::kStage;
+          uint8_t* dV = dK + C::kKVBytes;
+          const int y = (int)(x.key0 + (int64_t)kb * kKeyBlk);
+#pragma unroll
+          for (int r = 0; r < D / 64; ++r) {
+            ptx::tma_load_3d(dK + r * C::kRegion, &tmK, &kv_full[st], r * 64, y, x.bh);
+            ptx::tma_load_3d(dV + r * C::kRegion, &tmV, &kv_full[st], r * 64, y, x.bh);
+          }
+        }
+        gb += x.nkb;
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const int ab16 = DT == DT_BF16 ? 1 : 0;
+      const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
+      const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
+      const uint32_t aQ = ptx::smem_u32(sQ), aKV = ptx::smem_u32(sKV), aP = ptx::smem_u32(sP);
+      int64_t gb = 0;
+      int tcount = 0;
+      auto issue_pv = [&](int64_t g, int kb) -> bool {
+        if (!ptx::mbar_wait(p_full, (uint32_t)(g & 1))) return false;
+        tc::fence_after();
+        const int st = (int)(g & 1);
+        const uint32_t vbase = aKV + st * C::kStage + C::kKVBytes;
+#pragma unroll
+        for (int k = 0; k < kKeyBlk / 16; ++k) {
+          const uint64_t pd = tc::sdesc_sw128(aP + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
+          const uint64_t vd = tc::sdesc_sw128(vbase + k * 2048, C::kRegion, 1024);
+          tc::mma(tO, pd, vd, id_pv, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::commit(pv_done);
+        tc::commit(&kv_empty[st]);
+        return true;
+      };
+      for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
+        const Tile x = load_tile(a, t);
+        if (!ptx::mbar_wait(q_full, (uint32_t)(tcount & 1))) {
+          fail(SSA_DEVERR_WAIT_TIMEOUT);
+          break;
+        }
+        tc::fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < x.nkb && ok; ++kb) {
+          const int64_t g = gb + kb;
+          const int st = (int)(g & 1);
+          ok = ptx::mbar_wait(&kv_full[st], (uint32_t)((g >> 1) & 1));
+          if (ok && g >= 2) ok = ptx::mbar_wait(&s_free[st], (uint32_t)(((g - 2) >> 1) & 1));
+          if (!ok) break;
+          tc::fence_after();
+          const uint32_t kbase = aKV + st * C::kStage;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
+            const uint64_t kd = tc::sdesc_sw128(kbase + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
+            tc::mma(tS[st], qd, kd, id_qk, k > 0 ? 1u : 0u);
+          }
+          tc::commit(&s_full[st]);
+          if (kb >= 1) ok = issue_pv(g - 1, kb - 1);
+        }
+        if (ok) ok = issue_pv(gb + x.nkb - 1, x.nkb - 1);
+        if (!ok) {
+          fail(SSA_DEVERR_WAIT_TIMEOUT);
+          break;
+        }
+        gb += x.nkb;
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax warps: row r = tid
+    const int r = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float c = a.scale_log2e;
+    const uint32_t qrow_sw = (uint32_t)(r & 7);
+    int64_t gb = 0;
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
+      const Tile x = load_tile(a, t);
+      // row identity
+      int64_t qrow = -1;  // row of Q / sel / partials
+      int rank = a.topk;
+      int64_t tpos = 0;   // query position (local tiles)
+      if (x.kind_bh >= 0) {
+        if (r < x.nrows) {
+          const int v = a.rows[(int64_t)a.offsets[x.kind_bh] + x.row0 + r];
+          qrow = (int64_t)(v >> 6);
+          rank = v & 63;
+          if (qrow < 0 || qrow >= (int64_t)a.B * a.Hq * a.n_q || rank >= a.topk) {
+            flag_error(err, SSA_DEVERR_OVERFLOW);
+            qrow = -1;
+          }
+        }
+      } else if (r < x.nrows) {
+        const int b = x.bh / a.Hkv, kvh = x.bh - b * a.Hkv;
+        const int64_t i = x.i0 + r / a.g;
+        const int h = kvh * a.g + r % a.g;
+        qrow = (int64_t)(b * a.Hq + h) * a.n_q + i;
+        tpos = a.q_pos0 + i;
+      }
+      // gather this row of Q into the swizzled K-major tile
+      {
+        const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow < 0 ? 0 : qrow) * (int64_t)D * 2;
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch) {
+          uint8_t* dst = sQ + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
+          const uint32_t n = qrow < 0 ? 0u : 16u;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
+                       "l"(src + ch * 16), "r"(n)
+                       : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        tc::fence_proxy_async_smem();
+        ptx::mbar_arrive(q_full);
+      }
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int kb = 0; kb < x.nkb && ok; ++kb) {
+        const int64_t g = gb + kb;
+        const int st = (int)(g & 1);
+        if (!ptx::mbar_wait(&s_full[st], (uint32_t)((g >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        float sv[kKeyBlk];
+#pragma unroll
+        for (int q = 0; q < kKeyBlk / 32; ++q) {
+          uint32_t rr[32];
+          tc::ld32(tS[st] + lane_off + q * 32, rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[q * 32 + j] = __uint_as_float(rr[j]);
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s_free[st]);
+        // valid keys of this block
+        const int64_t kstart = x.key0 + (int64_t)kb * kKeyBlk;
+        int64_t klim = x.key_end - kstart;  // keys [0, klim) of the block exist
+        if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kKeyBlk; ++j) {
+          if (j >= klim) sv[j] = -INFINITY;
+          mx = fmaxf(mx, sv[j]);
+        }
+        mx *= c;
+        // rescale O only when the max grows by more than 2^8 (warp-uniform)
+        float m_new = m;
+        if (kb == 0) {
+          m_new = mx;
+        } else if (mx > m + kRescaleLog2) {
+          m_new = mx;
+        }
+        const bool need = kb > 0 && m_new != m;
+        bool waited = false;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!ptx::mbar_wait(pv_done, (uint32_t)((g - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          waited = true;
+          tc::fence_after();
+          const float f = need ? exp2f(m - m_new) : 1.f;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t rr[32];
+            tc::ld32(tO + lane_off + q * 32, rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
+            tc::st32(tO + lane_off + q * 32, rr);
+          }
+          l *= f;
+        }
+        m = m_new;
+        const float nb = m == -INFINITY ? 0.f : -m;
+        // P = exp2(s * c - m), packed to 16 bits
+        uint32_t pk[kKeyBlk / 2];
+#pragma unroll
+        for (int j = 0; j < kKeyBlk; j += 2) {
+          const float p0 = exp2f(fmaf(sv[j], c, nb));
+          const float p1 = exp2f(fmaf(sv[j + 1], c, nb));
+          l += p0 + p1;
+          pk[j / 2] = ptx::pack2<DT>(p0, p1);
+        }
+        if (kb >= 1 && !waited) {
+          if (!ptx::mbar_wait(pv_done, (uint32_t)((g - 1) & 1))) {
+            ok = false;
+            break;
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < kKeyBlk / 8; ++ch) {
+          uint8_t* dst = sP + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_full);
+      }
+      if (!ok) {
+        fail(SSA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      // epilogue: O / l to this row's partial slot
+      const int64_t glast = gb + x.nkb - 1;
+      if (!ptx::mbar_wait(pv_done, (uint32_t)(glast & 1))) {
+        fail(SSA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      tc::fence_after();
+      const float inv = 1.f / l;
+      const int64_t slot = qrow * (a.topk + 1) + rank;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t rr[32];
+        tc::ld32(tO + lane_off + q * 32, rr);
+        if (qrow >= 0) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = ptx::pack2<DT>(__uint_as_float(rr[2 * j]) * inv, __uint_as_float(rr[2 * j + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + q * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (qrow >= 0) a.pml[slot] = make_float2(m, l);
+      tc::fence_before();
+      gb += x.nkb;
+    }
+  }
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 5) tc::dealloc(tmem, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- merge
+// One warp per row of Q: its used spans (sel order) then its local span.
+template <int DT, int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
+                                                            void* __restrict__ O, float* __restrict__ lse) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int64_t n_rows = (int64_t)a.B * a.Hq * a.n_q;
+  if (row >= n_rows) return;
+  const int64_t i = row % a.n_q;
+  const int64_t ell = (a.q_pos0 + i) / a.S;
+  const int32_t* srow = sel + row * a.topk;
+  const int j0 = lane < a.topk ? srow[lane] : -1;
+  const int j1 = lane + 32 < a.topk ? srow[lane + 32] : -1;
+  bool bad;
+  const int used = warp_sel_prefix(j0, j1, lane, a.topk, ell, &bad);
+  const int nslot = used + 1;
+  float M = -INFINITY, Ls = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const int64_t base = row * (a.topk + 1);
+  for (int s0 = 0; s0 < nslot; s0 += 8) {
+    float2 ml[8];
+    float v[8][E];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      if (s < nslot) {
+        const int rk = s < used ? s : a.topk;
+        ml[u] = a.pml[base + rk];
+        const uint16_t* src = a.po + (base + rk) * D + lane * E;
+        if constexpr (E == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(src);
+          const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if constexpr (DT == DT_BF16) {
+              v[u][2 * k] = bf16_bits_to_f32(ww[k] & 0xffffu);
+              v[u][2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
+            } else {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+              v[u][2 * k] = f.x;
+              v[u][2 * k + 1] = f.y;
+            }
+          }
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+          if constexpr (DT == DT_BF16) {
+            v[u][0] = bf16_bits_to_f32(w & 0xffffu);
+            v[u][1] = __uint_as_float(w & 0xffff0000u);
+          } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+            v[u][0] = f.x;
+            v[u][1] = f.y;
+          }
+        }
+      } else {
+        ml[u] = make_float2(-INFINITY, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (s0 + u >= nslot) continue;
+      const float Mn = fmaxf(M, ml[u].x);
+      const float fa = exp2f(M - Mn), fb = exp2f(ml[u].x - Mn) * ml[u].y;
+      Ls = Ls * fa + fb;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = acc[e] * fa + v[u][e] * fb;
+      M = Mn;
+    }
+  }
+  const float inv = 1.f / Ls;
+#pragma unroll
+  for (int e = 0; e < E; ++e) store_elem<DT>(O, row * D + lane * E + e, acc[e] * inv);
+  if (lse && lane == 0) lse[row] = M * kLn2 + logf(Ls);
+}
+
+PrefArgs make_args(const Problem& pr, int64_t n_q, int64_t q_pos0, void* ws, const PrefLayout& lay) {
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  PrefArgs a;
+  a.counts = reinterpret_cast<int*>(w8 + lay.counts);
+  a.offsets = reinterpret_cast<int*>(w8 + lay.offsets);
+  a.cursors = reinterpret_cast<int*>(w8 + lay.cursors);
+  a.ntiles = reinterpret_cast<int*>(w8 + lay.ntiles);
+  a.tiles = reinterpret_cast<int4*>(w8 + lay.tiles);
+  a.rows = reinterpret_cast<int*>(w8 + lay.rows);
+  a.pml = reinterpret_cast<float2*>(w8 + lay.pml);
+  a.po = reinterpret_cast<uint16_t*>(w8 + lay.po);
+  a.B = pr.B;
+  a.Hq = pr.Hq;
+  a.Hkv = pr.Hkv;
+  a.g = pr.g;
+  a.d = pr.d;
+  a.S = pr.S;
+  a.topk = pr.topk;
+  a.n_q = n_q;
+  a.q_pos0 = q_pos0;
+  a.ns_cap = pr.ns_cap;
+  a.n_buckets = lay.n_buckets;
+  a.scale_log2e = pr.scale * kLog2e;
+  return a;
+}
+
+template <int DT, int D>
+cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0, const void* K,
+                         const void* V, const int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
+  using C = ACfg<D>;
+  const PrefLayout lay = pref_layout(pr, n_q);
+  const PrefArgs a = make_args(pr, n_q, q_pos0, ws, lay);
+  uint32_t* err = ws_error(ws);
+  cudaError_t e = cudaMemsetAsync(a.counts, 0, lay.n_buckets * 4, st);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tmK, tmV;
+  e = make_kv_tmap(&tmK, K, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kKeyBlk);
+  if (e != cudaSuccess) return e;
+  e = make_kv_tmap(&tmV, V, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kKeyBlk);
+  if (e != cudaSuccess) return e;
+  const size_t hist_bytes = pr.ns_cap <= kHistMax ? (size_t)pr.ns_cap * 4 : 0;
+  const dim3 grid_rows((unsigned)((n_q + 255) / 256), (unsigned)(pr.B * pr.Hq));
+  e = launch_pdl(prefill_count_kernel, grid_rows, dim3(256), hist_bytes, st, sel, a, err);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(prefill_scan_kernel, dim3(1), dim3(kScanThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(prefill_scatter_kernel, grid_rows, dim3(256), 2 * hist_bytes, st, sel, a);
+  if (e != cudaSuccess) return e;
+  static bool attr_done[kMaxDevices] = {};
+  e = ensure_smem_attr(prefill_attend_kernel<DT, D>, C::kSmem, attr_done);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(prefill_attend_kernel<DT, D>, dim3(device_sm_count()), dim3(kAttThreads), C::kSmem, st,
+                 tmK, tmV, Q, a, err);
+  if (e != cudaSuccess) return e;
+  const int64_t n_rows = (int64_t)pr.B * pr.Hq * n_q;
+  return launch_pdl(prefill_merge_kernel<DT, D>, dim3((unsigned)((n_rows + 7) / 8)), dim3(256), 0, st, sel,
+                    a, O, lse);
+}
+
+}  // namespace
+
+bool prefill_fast_supported(const Problem& pr) {
+  return (pr.dtype == DT_BF16 || pr.dtype == DT_F16) && (pr.d == 64 || pr.d == 128) && pr.g <= kMaxG &&
+         (kTileRows % pr.g) == 0 && pr.topk <= kMaxK && pr.L > 0;
+}
+
+size_t prefill_ws_bytes(const Problem& pr, int64_t n_q) {
+  // row ids are packed with the rank into 32 bits
+  if ((int64_t)pr.B * pr.Hq * n_q >= (1ll << 25)) return 0;
+  return pref_layout(pr, n_q).total - kWsHeader;
+}
+
+cudaError_t launch_attend_prefill(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
+                                  const void* K, const void* V, const int32_t* sel, void* O, float* lse,
+                                  void* ws, cudaStream_t st) {
+  if (pr.d == 128) {
+    if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 128>(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st);
+    return launch_typed<DT_F16, 128>(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st);
+  }
+  if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 64>(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st);
+  return launch_typed<DT_F16, 64>(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st);
 }
 
 }  // namespace ssa

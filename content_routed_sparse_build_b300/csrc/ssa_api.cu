@@ -47,12 +47,17 @@ int check_params(const ssa_params* p, Problem* pr) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA; }
 
+// The tensor-core prefill path takes 16-bit inputs whose row ids fit its
+// 32-bit bucket entries; everything else runs the row kernel.
+bool prefill_fast(const Problem& pr, int64_t n_q) {
+  return prefill_fast_supported(pr) && prefill_ws_bytes(pr, n_q) > 0;
+}
+
 size_t ws_need(const Problem& pr, int64_t n_q, int op) {
   if (op == SSA_OP_ROUTE) return 0;
   if (op == SSA_OP_DECODE)
     return kWsHeader + (decode_fast_supported(pr) ? decode_ws_bytes(pr) : 0);
-  if (op == SSA_OP_PREFILL)
-    return kWsHeader + (prefill_fast_supported(pr) ? prefill_ws_bytes(pr, n_q) : 0);
+  if (op == SSA_OP_PREFILL) return kWsHeader + (prefill_fast(pr, n_q) ? prefill_ws_bytes(pr, n_q) : 0);
   return 0;
 }
 
@@ -143,7 +148,7 @@ int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, int64_t 
   if (rc != SSA_OK) return rc;
   if (n_q == 0) return SSA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (prefill_fast_supported(pr))
+  if (prefill_fast(pr, n_q))
     return cuda_status(launch_attend_prefill(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st));
   return cuda_status(launch_attend_rows(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws_error(ws), st));
 }
