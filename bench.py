@@ -365,6 +365,7 @@ class PrefillBench:
         self.O = torch.empty_like(self.Q)
         self.lse = torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
         self.ws = ssa.workspace(self.p, w.n_q, ssa.SSA_OP_PREFILL, dev)
+        self.ws_route = ssa.workspace(self.p, w.n_q, ssa.SSA_OP_ROUTE, dev)
         self.stream = torch.cuda.current_stream(dev)
         self.j0 = w.q_pos0 // w.S
         self.j1 = w.n_spans
@@ -375,7 +376,8 @@ class PrefillBench:
     def step(self, ev=None):
         w = self.w
         ssa.ssa_build_summaries(self.p, self.K, self.j0, self.j1, self.summ, self.stream)
-        ssa.ssa_route(self.p, self.Q, w.n_q, w.q_pos0, self.summ, self.sel, None, None, self.stream)
+        ssa.ssa_route(self.p, self.Q, w.n_q, w.q_pos0, self.summ, self.sel, None, self.ws_route,
+                      self.stream)
         if ev is not None:
             ev[0].record(self.stream)
         ssa.ssa_attend_prefill(self.p, self.Q, w.n_q, w.q_pos0, self.K, self.V, self.sel, self.O,
@@ -481,6 +483,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-L", type=int, default=None,
                     help="shrink the decode cache (profiling runs on a smaller case)")
+    ap.add_argument("--prefill-L", type=int, default=None,
+                    help="shrink the prefill cache (profiling runs on a smaller case)")
+    ap.add_argument("--prefill-chunk", type=int, default=None,
+                    help="queries of the prefill chunk (profiling runs on a smaller case)")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
@@ -497,13 +504,24 @@ def main():
     w = W.DECODE_1M
     if args.decode_L:
         w = w.with_(name="decode_%d" % args.decode_L, L=args.decode_L, q_pos0=args.decode_L - w.n_q)
-    dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg=(rank == 0 and ws_n == 1
-                                                                 and not args.no_cpu_baseline))
-    del db
+    if args.no_decode:
+        dec = {"tok_s": None, "ms_per_step": None, "roofline": None, "e2e": None, "clocks": None,
+               "attend_ms_per_step": None, "route_plus_gaps_ms_per_step": None,
+               "attend_bytes_per_step": None, "route_bytes_per_step": None, "step_bytes_gbs": None,
+               "summaries": None, "device_error_bits": None, "timing": None}
+    else:
+        dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg=(rank == 0 and ws_n == 1
+                                                                     and not args.no_cpu_baseline))
+        del db
     torch.cuda.empty_cache()
     pre = None
     if not args.no_prefill:
-        pre = bench_prefill(W.PREFILL_1M, dev, args.prefill_steps, 2, ws_n, flush)
+        wp = W.PREFILL_1M
+        if args.prefill_L or args.prefill_chunk:
+            L = args.prefill_L or wp.L
+            n = args.prefill_chunk or wp.n_q
+            wp = wp.with_(name="prefill_%d_vs_%d" % (n, L), L=L, n_q=n, chunk=n, q_pos0=L - n)
+        pre = bench_prefill(wp, dev, args.prefill_steps, 2, ws_n, flush)
     line = {
         "metric": METRIC, "value": dec["tok_s"], "unit": "tok/s", "n_gpus": ws_n, "steps": steps,
         "warmup": warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,

@@ -68,9 +68,16 @@ cudaError_t launch_summaries(const Problem& pr, const void* K, int64_t j0, int64
                              cudaStream_t st);
 
 // Routing.  Decode (n_q == 1) uses a cluster kernel that splits the
-// candidates over 8 CTAs per kv-head; prefill uses query tiles.
+// candidates over 8 CTAs per kv-head; a chunk of 16-bit queries uses the
+// tensor-core router (its workspace holds split summaries); anything else
+// uses fp32 query tiles.
 cudaError_t launch_route(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st);
+bool route_tc_supported(const Problem& pr, int64_t n_q);
+size_t route_tc_ws_bytes(const Problem& pr);
+cudaError_t launch_route_tc(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
+                            const float* summ, int32_t* sel, float* sel_score, void* ws,
+                            cudaStream_t st);
 
 // Reference-quality attention: one warp per query row, any dtype.
 cudaError_t launch_attend_rows(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,

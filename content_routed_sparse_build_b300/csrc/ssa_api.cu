@@ -54,7 +54,7 @@ bool prefill_fast(const Problem& pr, int64_t n_q) {
 }
 
 size_t ws_need(const Problem& pr, int64_t n_q, int op) {
-  if (op == SSA_OP_ROUTE) return 0;
+  if (op == SSA_OP_ROUTE) return route_tc_supported(pr, n_q) ? kWsHeader + route_tc_ws_bytes(pr) : 0;
   if (op == SSA_OP_DECODE)
     return kWsHeader + (decode_fast_supported(pr) ? decode_ws_bytes(pr) : 0);
   if (op == SSA_OP_PREFILL) return kWsHeader + (prefill_fast(pr, n_q) ? prefill_ws_bytes(pr, n_q) : 0);
@@ -114,8 +114,10 @@ int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0, c
   if (!Q || !summ || !sel || !aligned16(Q) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
   rc = check_ws(pr, n_q, SSA_OP_ROUTE, ws, ws_bytes);
   if (rc != SSA_OK) return rc;
-  return cuda_status(launch_route(pr, Q, n_q, q_pos0, summ, sel, sel_score,
-                                  static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (route_tc_supported(pr, n_q))
+    return cuda_status(launch_route_tc(pr, Q, n_q, q_pos0, summ, sel, sel_score, ws, st));
+  return cuda_status(launch_route(pr, Q, n_q, q_pos0, summ, sel, sel_score, st));
 }
 
 int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, const void* K, const void* V,

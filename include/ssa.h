@@ -117,7 +117,9 @@ SSA_API int ssa_build_summaries(const ssa_params* p, const void* K, int64_t span
  * topk] fp32) receives the score of each written span (NaN beside a -1).
  * Summaries of spans 0 .. floor((q_pos0 + n_q - 1) / S) - 1 must be built.
  * Requires n_q >= 0, q_pos0 >= 0, q_pos0 + n_q <= L.
- * ws may be NULL when ssa_workspace_size(p, n_q, SSA_OP_ROUTE) is 0.
+ * A chunk (n_q > 1) of bf16 / fp16 queries is scored on the tensor cores
+ * against a three-way 16-bit split of the fp32 summaries kept in ws; ws may
+ * be NULL when ssa_workspace_size(p, n_q, SSA_OP_ROUTE) is 0 (decode, fp32).
  */
 SSA_API int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
               const float* summ, int32_t* sel, float* sel_score, void* ws, size_t ws_bytes,

@@ -166,9 +166,12 @@ class GpuRun:
             oc = torch.empty((w.B, w.Hq, n, w.d), dtype=w.dtype, device=self.dev)
             lc = torch.empty((w.B, w.Hq, n), dtype=torch.float32, device=self.dev)
             ws = ssa.workspace(p, n, ssa.SSA_OP_PREFILL, self.dev)
-            ssa.ssa_route(p, qc, n, pos0, self.summ, sc)
+            wsr = ssa.workspace(p, n, ssa.SSA_OP_ROUTE, self.dev)
+            ssa.ssa_route(p, qc, n, pos0, self.summ, sc, None, wsr)
             ssa.ssa_attend_prefill(p, qc, n, pos0, self.K, self.V, sc, oc, lc, ws)
             errs |= ssa.ssa_workspace_error(ws)
+            if wsr is not None:
+                errs |= ssa.ssa_workspace_error(wsr)
             sel[:, :, c0: c0 + n] = sc
             O[:, :, c0: c0 + n] = oc
             lse[:, :, c0: c0 + n] = lc
