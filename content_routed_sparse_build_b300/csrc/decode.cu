@@ -499,10 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha[i] = exp2f(m[ng][i] - bse);
         m[ng][i] = mx[i];
       }
-      const float p0 = exp2f(fmaf(s[ng][0], c, nb[0]));
-      const float p1 = exp2f(fmaf(s[ng][1], c, nb[1]));
-      const float p2 = exp2f(fmaf(s[ng][2], c, nb[0]));
-      const float p3 = exp2f(fmaf(s[ng][3], c, nb[1]));
+      const float p0 = ptx::ex2(fmaf(s[ng][0], c, nb[0]));
+      const float p1 = ptx::ex2(fmaf(s[ng][1], c, nb[1]));
+      const float p2 = ptx::ex2(fmaf(s[ng][2], c, nb[0]));
+      const float p3 = ptx::ex2(fmaf(s[ng][3], c, nb[1]));
       l[ng][0] = l[ng][0] * alpha[0] + (p0 + p2);
       l[ng][1] = l[ng][1] * alpha[1] + (p1 + p3);
       if (alpha[0] != 1.f || alpha[1] != 1.f) {

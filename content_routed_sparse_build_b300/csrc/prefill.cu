@@ -280,14 +280,17 @@ struct ACfg {
   static constexpr int kRegion = kTileRows * 128;      // 128 rows x 128 bytes
   static constexpr int kQBytes = (D / 64) * kRegion;    // Q tile, D/64 regions
   static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block
-  static constexpr int kStage = 2 * kKVBytes;
   static constexpr int kPBytes = 2 * kRegion;           // P tile: 128 keys = 2 regions
-  static constexpr int kStages = 2;
-  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + kStages * kStage + kPBytes + 256;
+  static constexpr int kKStages = 3;                    // K slots free once S = Q K^T is done
+  static constexpr int kVStages = 2;                    // V slots free once O += P V is done
+  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes +
+                                  kPBytes + 256 + 2 * 128 * 4;
   static constexpr uint32_t kTmemCols = 512;            // S0, S1, O
 };
 
-constexpr int kAttThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kSoftWarps = 8;      // two warps per tensor-memory lane quarter
+constexpr int kAttThreads = (kSoftWarps + 2) * 32;  // + TMA warp + MMA warp
+constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 
 struct Tile {
   int kind_bh;  // bucket (>= 0) or -1 - bh
@@ -333,36 +336,44 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + C::kQBytes;
-  uint8_t* sP = sKV + C::kStages * C::kStage;
+  uint8_t* sK = sQ + C::kQBytes;
+  uint8_t* sV = sK + C::kKStages * C::kKVBytes;
+  uint8_t* sP = sV + C::kVStages * C::kKVBytes;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sP + C::kPBytes);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* s_free = bar + 7;    // [2]
-  uint64_t* p_full = bar + 9;
-  uint64_t* pv_done = bar + 10;
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 12);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 13);
+  uint64_t* k_full = bar + 1;    // [3]
+  uint64_t* k_empty = bar + 4;   // [3]
+  uint64_t* v_full = bar + 7;    // [2]
+  uint64_t* v_empty = bar + 9;   // [2]
+  uint64_t* s_full = bar + 11;   // [2]
+  uint64_t* s_free = bar + 13;   // [2]
+  uint64_t* p_full = bar + 15;
+  uint64_t* pv_done = bar + 16;
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 17);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 18);
+  float* xchg = reinterpret_cast<float*>(bar + 32);  // [2 halves][128 rows] row values exchanged by warp pairs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    ptx::mbar_init(q_full, 128);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&kv_full[s], 1);
-      ptx::mbar_init(&kv_empty[s], 1);
-      ptx::mbar_init(&s_full[s], 1);
-      ptx::mbar_init(&s_free[s], 4);
+    ptx::mbar_init(q_full, kSoftWarps * 32);
+    for (int s = 0; s < C::kKStages; ++s) {
+      ptx::mbar_init(&k_full[s], 1);
+      ptx::mbar_init(&k_empty[s], 1);
     }
-    ptx::mbar_init(p_full, 4);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&v_full[s], 1);
+      ptx::mbar_init(&v_empty[s], 1);
+      ptx::mbar_init(&s_full[s], 1);
+      ptx::mbar_init(&s_free[s], kSoftWarps);
+    }
+    ptx::mbar_init(p_full, kSoftWarps);
     ptx::mbar_init(pv_done, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) tc::alloc(tmem_base, C::kTmemCols);
-  if (warp == 4 && lane == 0) {
+  if (warp == kMmaWarp) tc::alloc(tmem_base, C::kTmemCols);
+  if (warp == kTmaWarp && lane == 0) {
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
   }
@@ -381,46 +392,66 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     *abort = 1;
   };
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------ TMA producer
+    // Loads in the order the MMAs consume them: K(g), then V(g - 1).
     if (lane == 0) {
-      int64_t gb = 0;
-      for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x) {
+      int64_t g = 0;
+      int prev_bh = 0, prev_y = 0;
+      bool have_prev = false, ok = true;
+      auto load_v = [&](int64_t gv, int bh, int y) -> bool {
+        const int st = (int)(gv % C::kVStages);
+        if (gv >= C::kVStages &&
+            !ptx::mbar_wait(&v_empty[st], (uint32_t)(((gv - C::kVStages) / C::kVStages) & 1)))
+          return false;
+        ptx::mbar_arrive_expect_tx(&v_full[st], C::kKVBytes);
+#pragma unroll
+        for (int r = 0; r < D / 64; ++r)
+          ptx::tma_load_3d(sV + st * C::kKVBytes + r * C::kRegion, &tmV, &v_full[st], r * 64, y, bh);
+        return true;
+      };
+      for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x) {
         const Tile x = load_tile(a, t);
-        for (int kb = 0; kb < x.nkb; ++kb) {
-          const int64_t g = gb + kb;
-          const int st = (int)(g & 1);
-          if (g >= 2 && !ptx::mbar_wait(&kv_empty[st], (uint32_t)(((g - 2) >> 1) & 1))) {
-            fail(SSA_DEVERR_WAIT_TIMEOUT);
+        for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
+          const int st = (int)(g % C::kKStages);
+          if (g >= C::kKStages &&
+              !ptx::mbar_wait(&k_empty[st], (uint32_t)(((g - C::kKStages) / C::kKStages) & 1))) {
+            ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&kv_full[st], C::kStage);
-          uint8_t* dK = sKV + st * C::kStage;
-          uint8_t* dV = dK + C::kKVBytes;
           const int y = (int)(x.key0 + (int64_t)kb * kKeyBlk);
+          ptx::mbar_arrive_expect_tx(&k_full[st], C::kKVBytes);
 #pragma unroll
-          for (int r = 0; r < D / 64; ++r) {
-            ptx::tma_load_3d(dK + r * C::kRegion, &tmK, &kv_full[st], r * 64, y, x.bh);
-            ptx::tma_load_3d(dV + r * C::kRegion, &tmV, &kv_full[st], r * 64, y, x.bh);
+          for (int r = 0; r < D / 64; ++r)
+            ptx::tma_load_3d(sK + st * C::kKVBytes + r * C::kRegion, &tmK, &k_full[st], r * 64, y, x.bh);
+          if (have_prev && !load_v(g - 1, prev_bh, prev_y)) {
+            ok = false;
+            break;
           }
+          prev_bh = x.bh;
+          prev_y = y;
+          have_prev = true;
         }
-        gb += x.nkb;
       }
+      if (ok && have_prev) ok = load_v(g - 1, prev_bh, prev_y);
+      if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const int ab16 = DT == DT_BF16 ? 1 : 0;
       const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
       const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
-      const uint32_t aQ = ptx::smem_u32(sQ), aKV = ptx::smem_u32(sKV), aP = ptx::smem_u32(sP);
+      const uint32_t aQ = ptx::smem_u32(sQ), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV),
+                     aP = ptx::smem_u32(sP);
       int64_t gb = 0;
       int tcount = 0;
       auto issue_pv = [&](int64_t g, int kb) -> bool {
+        const int sv = (int)(g % C::kVStages);
         if (!ptx::mbar_wait(p_full, (uint32_t)(g & 1))) return false;
+        if (!ptx::mbar_wait(&v_full[sv], (uint32_t)((g / C::kVStages) & 1))) return false;
         tc::fence_after();
-        const int st = (int)(g & 1);
-        const uint32_t vbase = aKV + st * C::kStage + C::kKVBytes;
+        const uint32_t vbase = aV + sv * C::kKVBytes;
 #pragma unroll
         for (int k = 0; k < kKeyBlk / 16; ++k) {
           const uint64_t pd = tc::sdesc_sw128(aP + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
@@ -428,7 +459,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           tc::mma(tO, pd, vd, id_pv, (kb > 0 || k > 0) ? 1u : 0u);
         }
         tc::commit(pv_done);
-        tc::commit(&kv_empty[st]);
+        tc::commit(&v_empty[sv]);
         return true;
       };
       for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
@@ -441,19 +472,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         bool ok = true;
         for (int kb = 0; kb < x.nkb && ok; ++kb) {
           const int64_t g = gb + kb;
-          const int st = (int)(g & 1);
-          ok = ptx::mbar_wait(&kv_full[st], (uint32_t)((g >> 1) & 1));
-          if (ok && g >= 2) ok = ptx::mbar_wait(&s_free[st], (uint32_t)(((g - 2) >> 1) & 1));
+          const int sb = (int)(g & 1);
+          const int sk = (int)(g % C::kKStages);
+          ok = ptx::mbar_wait(&k_full[sk], (uint32_t)((g / C::kKStages) & 1));
+          if (ok && g >= 2) ok = ptx::mbar_wait(&s_free[sb], (uint32_t)(((g - 2) >> 1) & 1));
           if (!ok) break;
           tc::fence_after();
-          const uint32_t kbase = aKV + st * C::kStage;
+          const uint32_t kbase = aK + sk * C::kKVBytes;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
             const uint64_t kd = tc::sdesc_sw128(kbase + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
-            tc::mma(tS[st], qd, kd, id_qk, k > 0 ? 1u : 0u);
+            tc::mma(tS[sb], qd, kd, id_qk, k > 0 ? 1u : 0u);
           }
-          tc::commit(&s_full[st]);
+          tc::commit(&s_full[sb]);
+          tc::commit(&k_empty[sk]);
           if (kb >= 1) ok = issue_pv(g - 1, kb - 1);
         }
         if (ok) ok = issue_pv(gb + x.nkb - 1, x.nkb - 1);
@@ -465,14 +498,25 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ softmax warps: row r = tid
-    const int r = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------ softmax warps
+    // Warps w and w + 4 read the same tensor-memory lanes (rows r = 32 (w % 4)
+    // + lane); warp w takes key / output columns of half 0, warp w + 4 half 1,
+    // and the pair exchanges row maxima and sums through shared memory.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int pair_bar = 1 + quarter;  // named barrier of the warp pair
     const float c = a.scale_log2e;
     const uint32_t qrow_sw = (uint32_t)(r & 7);
+    constexpr int KH = kKeyBlk / 2;    // key columns per half
+    constexpr int OH = D / 2;          // output columns per half
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     int64_t gb = 0;
     int tcount = 0;
-    for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
+    // No abort check here: both warps of a pair must walk the same tiles
+    // (they meet at named barriers); they leave only through bounded waits,
+    // which time out together.
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const Tile x = load_tile(a, t);
       // row identity
       int64_t qrow = -1;  // row of Q / sel / partials
@@ -495,11 +539,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         qrow = (int64_t)(b * a.Hq + h) * a.n_q + i;
         tpos = a.q_pos0 + i;
       }
-      // gather this row of Q into the swizzled K-major tile
+      // gather this half of the row of Q into the swizzled K-major tile
       {
         const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow < 0 ? 0 : qrow) * (int64_t)D * 2;
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) {
+        for (int cc = 0; cc < D / 16; ++cc) {
+          const int ch = half * (D / 16) + cc;
           uint8_t* dst = sQ + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
           const uint32_t n = qrow < 0 ? 0u : 16u;
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
@@ -520,28 +565,33 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           break;
         }
         tc::fence_after();
-        float sv[kKeyBlk];
-#pragma unroll
-        for (int q = 0; q < kKeyBlk / 32; ++q) {
-          uint32_t rr[32];
-          tc::ld32(tS[st] + lane_off + q * 32, rr);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sv[q * 32 + j] = __uint_as_float(rr[j]);
-        }
+        // valid keys of this block: [0, klim)
+        const int64_t kstart = x.key0 + (int64_t)kb * kKeyBlk;
+        int64_t klim = x.key_end - kstart;
+        if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
+        const int64_t hlim = klim - half * KH;  // valid keys of this half
+        const bool partial = hlim < KH;
+        const uint32_t tsrow = tS[st] + lane_off + half * KH;
+        // this half of the row of S, then the S buffer is free for the next MMA
+        static_assert(KH == 64, "one 64-column load per half row");
+        uint32_t sr[64];
+        tc::ld64(tsrow, sr);
         tc::fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&s_free[st]);
-        // valid keys of this block
-        const int64_t kstart = x.key0 + (int64_t)kb * kKeyBlk;
-        int64_t klim = x.key_end - kstart;  // keys [0, klim) of the block exist
-        if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
         float mx = -INFINITY;
+        if (partial) {
 #pragma unroll
-        for (int j = 0; j < kKeyBlk; ++j) {
-          if (j >= klim) sv[j] = -INFINITY;
-          mx = fmaxf(mx, sv[j]);
+          for (int j = 0; j < KH; ++j)
+            if (j < hlim) mx = fmaxf(mx, __uint_as_float(sr[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < KH; ++j) mx = fmaxf(mx, __uint_as_float(sr[j]));
         }
-        mx *= c;
+        xchg[half * 128 + r] = mx;
+        pair_sync();
+        mx = fmaxf(mx, xchg[(half ^ 1) * 128 + r]) * c;
+        pair_sync();
         // rescale O only when the max grows by more than 2^8 (warp-uniform)
         float m_new = m;
         if (kb == 0) {
@@ -558,38 +608,46 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
           waited = true;
           tc::fence_after();
-          const float f = need ? exp2f(m - m_new) : 1.f;
+          const float f = need ? ptx::ex2(m - m_new) : 1.f;
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
+          for (int q = 0; q < OH / 32; ++q) {
             uint32_t rr[32];
-            tc::ld32(tO + lane_off + q * 32, rr);
+            tc::ld32(tO + lane_off + half * OH + q * 32, rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tc::st32(tO + lane_off + q * 32, rr);
+            tc::st32(tO + lane_off + half * OH + q * 32, rr);
           }
           l *= f;
         }
         m = m_new;
         const float nb = m == -INFINITY ? 0.f : -m;
-        // P = exp2(s * c - m), packed to 16 bits
-        uint32_t pk[kKeyBlk / 2];
-#pragma unroll
-        for (int j = 0; j < kKeyBlk; j += 2) {
-          const float p0 = exp2f(fmaf(sv[j], c, nb));
-          const float p1 = exp2f(fmaf(sv[j + 1], c, nb));
-          l += p0 + p1;
-          pk[j / 2] = ptx::pack2<DT>(p0, p1);
-        }
         if (kb >= 1 && !waited) {
           if (!ptx::mbar_wait(pv_done, (uint32_t)((g - 1) & 1))) {
             ok = false;
             break;
           }
         }
+        // P = 2^(s * c - m) as 16-bit pairs
 #pragma unroll
-        for (int ch = 0; ch < kKeyBlk / 8; ++ch) {
-          uint8_t* dst = sP + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
+        for (int q = 0; q < KH / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float p0 = ptx::ex2(fmaf(__uint_as_float(sr[q * 32 + j]), c, nb));
+            float p1 = ptx::ex2(fmaf(__uint_as_float(sr[q * 32 + j + 1]), c, nb));
+            if (partial) {
+              if (q * 32 + j >= hlim) p0 = 0.f;
+              if (q * 32 + j + 1 >= hlim) p1 = 0.f;
+            }
+            l += p0 + p1;
+            pk[j / 2] = ptx::pack2<DT>(p0, p1);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int ch = half * (KH / 8) + q * 4 + i;
+            uint8_t* dst = sP + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
         }
         tc::fence_proxy_async_smem();
         tc::fence_before();
@@ -600,51 +658,49 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
-      // epilogue: O / l to this row's partial slot
+      // epilogue: O / l (both halves' sums) to this row's partial slot
       const int64_t glast = gb + x.nkb - 1;
       if (!ptx::mbar_wait(pv_done, (uint32_t)(glast & 1))) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
       tc::fence_after();
-      const float inv = 1.f / l;
+      xchg[half * 128 + r] = l;
+      pair_sync();
+      const float lt = l + xchg[(half ^ 1) * 128 + r];
+      pair_sync();
+      const float inv = 1.f / lt;
       const int64_t slot = qrow * (a.topk + 1) + rank;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int q = 0; q < OH / 32; ++q) {
         uint32_t rr[32];
-        tc::ld32(tO + lane_off + q * 32, rr);
+        tc::ld32(tO + lane_off + half * OH + q * 32, rr);
         if (qrow >= 0) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             pk[j] = ptx::pack2<DT>(__uint_as_float(rr[2 * j]) * inv, __uint_as_float(rr[2 * j + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + q * 32);
+          uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + half * OH + q * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      if (qrow >= 0) a.pml[slot] = make_float2(m, l);
+      if (qrow >= 0 && half == 0) a.pml[slot] = make_float2(m, lt);
       tc::fence_before();
       gb += x.nkb;
     }
   }
   __syncthreads();
   tc::fence_after();
-  if (warp == 5) tc::dealloc(tmem, C::kTmemCols);
+  if (warp == kMmaWarp) tc::dealloc(tmem, C::kTmemCols);
 }
 
 // ---------------------------------------------------------------- merge
 // One warp per row of Q: its used spans (sel order) then its local span.
 template <int DT, int D>
-__global__ void __launch_bounds__(256) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
-                                                            void* __restrict__ O, float* __restrict__ lse) {
+__device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const PrefArgs& a, void* __restrict__ O,
+                                          float* __restrict__ lse, int64_t row, int lane) {
   constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  ptx::pdl_wait();
-  ptx::pdl_launch_dependents();
-  const int64_t n_rows = (int64_t)a.B * a.Hq * a.n_q;
-  if (row >= n_rows) return;
   const int64_t i = row % a.n_q;
   const int64_t ell = (a.q_pos0 + i) / a.S;
   const int32_t* srow = sel + row * a.topk;
@@ -713,6 +769,17 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const int32_t* __res
   if (lse && lane == 0) lse[row] = M * kLn2 + logf(Ls);
 }
 
+template <int DT, int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
+                                                            void* __restrict__ O, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int64_t n_rows = (int64_t)a.B * a.Hq * a.n_q;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < n_rows; row += (int64_t)gridDim.x * 8)
+    merge_row<DT, D>(sel, a, O, lse, row, lane);
+}
+
 PrefArgs make_args(const Problem& pr, int64_t n_q, int64_t q_pos0, void* ws, const PrefLayout& lay) {
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   PrefArgs a;
@@ -768,8 +835,8 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t 
                  tmK, tmV, Q, a, err);
   if (e != cudaSuccess) return e;
   const int64_t n_rows = (int64_t)pr.B * pr.Hq * n_q;
-  return launch_pdl(prefill_merge_kernel<DT, D>, dim3((unsigned)((n_rows + 7) / 8)), dim3(256), 0, st, sel,
-                    a, O, lse);
+  const int64_t merge_ctas = min((n_rows + 7) / 8, (int64_t)device_sm_count() * 8);
+  return launch_pdl(prefill_merge_kernel<DT, D>, dim3((unsigned)merge_ctas), dim3(256), 0, st, sel, a, O, lse);
 }
 
 }  // namespace

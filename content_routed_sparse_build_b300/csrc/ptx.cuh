@@ -133,6 +133,15 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
+// 2^x by the special-function unit's approximation (PTX ex2.approx.ftz,
+// relative error below 2^-22; -inf gives +0).  Used where the result is
+// rounded to 16 bits or only weights an fp32 sum.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two floats -> packed 16-bit pair (lo in the low half), round to nearest.
 template <int DT>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
