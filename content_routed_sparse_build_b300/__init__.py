@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   ssa_route            span scores + top-k selection
   ssa_attend_decode    one query per head, split over spans, LSE merge
   ssa_attend_prefill   a chunk of queries, span-major tiles, LSE merge
+  ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
   ssa_workspace_size / ssa_workspace_error / ssa_status_string
 """
 from __future__ import annotations
@@ -166,6 +167,34 @@ def ssa_attend_prefill(p: ssa_params, Q: torch.Tensor, n_q: int, q_pos0: int, K:
     rc = lib().ssa_attend_prefill(ctypes.byref(p), _ptr(Q), int(n_q), int(q_pos0), _ptr(K),
                                   _ptr(V), _ptr(sel), _ptr(O), _ptr(lse), wp, wn, _stream(stream))
     _check(rc, "ssa_attend_prefill")
+
+
+class ScratchBlock:
+    """The library-owned decode scratch of one device, as returned by
+    ssa_attend_decode_noalloc; pass it to ssa_workspace_error."""
+
+    def __init__(self, address: int):
+        self.address = address
+
+    def data_ptr(self) -> int:
+        return self.address
+
+
+SSA_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def ssa_attend_decode_noalloc(p: ssa_params, Q: torch.Tensor, pos: int, K: torch.Tensor,
+                              V: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
+                              lse: torch.Tensor | None, stream=None) -> ScratchBlock:
+    """ssa_attend_decode on the library's own scratch block; returns the block."""
+    f = lib().ssa_attend_decode_noalloc
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, ctypes.POINTER(_P), _P]
+    f.restype = ctypes.c_int
+    scratch = _P(0)
+    rc = f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(K), _ptr(V), _ptr(sel), _ptr(O), _ptr(lse),
+           ctypes.byref(scratch), _stream(stream))
+    _check(rc, "ssa_attend_decode_noalloc")
+    return ScratchBlock(int(scratch.value))
 
 
 def ssa_workspace_error(ws: torch.Tensor, stream=None) -> int:

@@ -153,6 +153,40 @@ SSA_API int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, 
                        const void* K, const void* V, const int32_t* sel, void* O, float* lse,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the library's own decode scratch block, one per device (8 MiB). */
+#define SSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * ssa_attend_decode without a caller-supplied workspace.  The method's
+ * pages have no counterpart to this call: it is an interface convenience,
+ * and the attention it computes is exactly that of ssa_attend_decode.
+ *
+ * It serves callers that cannot allocate device memory at the point of the
+ * call, such as a plugin whose host runtime owns every device allocation,
+ * or a decode loop that must never reach an allocator.  The scratch is a
+ * block of SSA_NOALLOC_SCRATCH_BYTES that the library defines as static
+ * device memory; it exists once per device from the moment the library's
+ * device code is loaded.  No call allocates or frees anything.
+ *
+ * Arguments, layouts and the returned status are those of
+ * ssa_attend_decode, plus:
+ *   scratch  nullable; receives the device address of the block, whose
+ *            first 16 bytes are the sticky device error record.  Read it with
+ *            ssa_workspace_error(*scratch, ...).  The library keeps ownership.
+ * Limit: if ssa_workspace_size(p, 1, SSA_OP_DECODE) exceeds
+ *   SSA_NOALLOC_SCRATCH_BYTES, returns SSA_ERR_WORKSPACE and enqueues
+ *   nothing; use ssa_attend_decode with a workspace of that size instead.
+ * Set-up: the first call on a device (the current one) looks up the block's
+ *   address and enqueues a clear of its error record on `stream`.  Make
+ *   that first call before any stream capture begins.
+ * Races: every call on one device shares the block.  Calls that can overlap
+ *   in time (two streams, two host threads) corrupt each other's results and
+ *   error record; keep them on one stream.
+ */
+SSA_API int ssa_attend_decode_noalloc(const ssa_params* p, const void* Q, int64_t pos,
+                                      const void* K, const void* V, const int32_t* sel, void* O,
+                                      float* lse, void** scratch, void* stream);
+
 /*
  * Bytes of workspace the operation needs for n_q queries (n_q is ignored
  * for SSA_OP_DECODE), or 0 when the parameters are invalid or unsupported
