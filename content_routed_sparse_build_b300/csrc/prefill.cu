@@ -18,15 +18,17 @@
 //           tiles)
 //  scatter  writes each row's id and its rank in the sel row into its
 //           bucket
-//  attend   persistent, one CTA per SM.  Per tile: the 128 query rows are
-//           gathered into shared memory (128-byte swizzled K-major operand),
-//           key / value blocks of 128 tokens stream through a 2-stage TMA
-//           ring, one thread issues tcgen05.mma: S = Q K^T into tensor
-//           memory (double buffered), four warps run the softmax (one row
-//           per thread, lazy rescaling of O when the running maximum grows
-//           by more than 2^8), write P as bf16 / fp16 to shared memory, and
-//           O += P V accumulates in tensor memory.  The tile ends by writing
-//           one partial (m, l, normalised o) per row.
+//  attend   persistent, one CTA per SM, eleven warps.  A loader warp
+//           gathers each tile's 128 query rows into one of two Q buffers
+//           (128-byte swizzled K-major operand) ahead of use; a TMA warp
+//           streams key / value blocks of 128 tokens through their own
+//           rings; one thread issues tcgen05.mma: S = Q K^T into tensor
+//           memory (double buffered), then O += P V with P read from tensor
+//           memory.  Eight softmax warps (two per row quarter, one row per
+//           thread, each warp half of the keys) turn S into P = 2^(S c - m)
+//           (16-bit, double buffered in tensor memory), rescale O only when
+//           the running maximum grows by more than 2^8, and end each tile
+//           by writing one partial (m, l, normalised o) per row.
 //  merge    per (b, head, query): combines the row's partials (its spans in
 //           sel order, then the local span) into O and lse.
 #include "internal.h"
@@ -279,18 +281,25 @@ template <int D>
 struct ACfg {
   static constexpr int kRegion = kTileRows * 128;      // 128 rows x 128 bytes
   static constexpr int kQBytes = (D / 64) * kRegion;    // Q tile, D/64 regions
-  static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block
-  static constexpr int kPBytes = 2 * kRegion;           // P tile: 128 keys = 2 regions
-  static constexpr int kKStages = 3;                    // K slots free once S = Q K^T is done
-  static constexpr int kVStages = 2;                    // V slots free once O += P V is done
-  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes +
-                                  kPBytes + 256 + 2 * 128 * 4;
-  static constexpr uint32_t kTmemCols = 512;            // S0, S1, O
+  static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block of 128 tokens
+  static constexpr int kKStages = D == 128 ? 2 : 3;
+  static constexpr int kVStages = 2;
+  // small state first (barriers, pair exchange, tile metadata), then the
+  // 1024-byte aligned operand buffers: Q[2], K[kKStages], V[kVStages]
+  static constexpr int kBarBytes = 256;
+  static constexpr int kXchgBytes = 2 * kTileRows * 4;
+  static constexpr int kMetaBytes = 2 * 16 + 2 * kTileRows * 4;
+  static constexpr int kSmallBytes = ((kBarBytes + kXchgBytes + kMetaBytes + 1023) / 1024) * 1024;
+  static constexpr size_t kSmem =
+      1024 + kSmallBytes + 2 * (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes;
+  // tensor memory: S0 [0, 128), S1 [128, 256), O [256, 256 + D), P0, P1 (64 columns each)
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256, kColP = 256 + D;
 };
 
 constexpr int kSoftWarps = 8;      // two warps per tensor-memory lane quarter
-constexpr int kAttThreads = (kSoftWarps + 2) * 32;  // + TMA warp + MMA warp
-constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
+constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1, kQWarp = kSoftWarps + 2;
+constexpr int kAttThreads = (kSoftWarps + 3) * 32;
 
 struct Tile {
   int kind_bh;  // bucket (>= 0) or -1 - bh
@@ -301,8 +310,7 @@ struct Tile {
   int64_t i0;              // local tiles: first query index
 };
 
-__device__ __forceinline__ Tile load_tile(const PrefArgs& a, int t) {
-  const int4 v = a.tiles[t];
+__device__ __forceinline__ Tile decode_tile(const PrefArgs& a, int4 v) {
   Tile x;
   x.kind_bh = v.x;
   if (v.x >= 0) {
@@ -327,48 +335,75 @@ __device__ __forceinline__ Tile load_tile(const PrefArgs& a, int t) {
   return x;
 }
 
+// Row r of a local tile: query i0 + r / g of head kvh * g + r % g.
+__device__ __forceinline__ int64_t local_row(const PrefArgs& a, const Tile& x, int r, int64_t* i_out) {
+  const int b = x.bh / a.Hkv, kvh = x.bh - b * a.Hkv;
+  const int64_t i = x.i0 + r / a.g;
+  const int h = kvh * a.g + r % a.g;
+  *i_out = i;
+  return (int64_t)(b * a.Hq + h) * a.n_q + i;
+}
+
+// Warp roles: 0-7 softmax (warps w and w + 4 share the tensor-memory lanes
+// of quarter w % 4 and split the key / output columns), 8 TMA producer of
+// the K / V blocks, 9 MMA issuer, 10 Q loader.
+//
+// Block g (a global count of key blocks over this CTA's tiles):
+//   S(g) = Q K(g)^T       -> tensor memory S[g % 2]
+//   P(g) = 2^(S c - m)    -> tensor memory P[g % 2] (16-bit, written by the softmax warps)
+//   O   += P(g) V(g)      A operand read from tensor memory
+// The softmax of block g waits only for O += P(g - 2) V (its P buffer), or
+// for O += P(g - 1) V when it must rescale O.  The Q loader fills the other
+// Q buffer while a tile runs, so the next tile's first S can start while
+// the softmax warps write the previous tile's partials.
 template <int DT, int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
     prefill_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const void* __restrict__ Q, PrefArgs a, uint32_t* __restrict__ err) {
   using C = ACfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
+  uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::kQBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base);
+  uint64_t* q_full = bar + 0;    // [2] Q tile and its metadata loaded
+  uint64_t* q_empty = bar + 2;   // [2] last S of the tile done + partials written
+  uint64_t* k_full = bar + 4;    // [3]
+  uint64_t* k_empty = bar + 7;   // [3]
+  uint64_t* v_full = bar + 10;   // [2]
+  uint64_t* v_empty = bar + 12;  // [2]
+  uint64_t* s_full = bar + 14;   // [2]
+  uint64_t* s_free = bar + 16;   // [2]
+  uint64_t* p_full = bar + 18;   // [2]
+  uint64_t* p_free = bar + 20;   // [2] O += P V done for the buffer's last block
+  uint64_t* o_free = bar + 22;   // O read out by the epilogue
+  uint64_t* drain = bar + 23;    // every MMA issued has completed
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 24);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 25);
+  float* xchg = reinterpret_cast<float*>(base + C::kBarBytes);   // [2 halves][128 rows]
+  int4* tinfo = reinterpret_cast<int4*>(base + C::kBarBytes + C::kXchgBytes);  // [2] tile entries
+  int* meta = reinterpret_cast<int*>(tinfo + 2);                  // [2][128] bucket entries or -1
+  uint8_t* sQ = base + C::kSmallBytes;
+  uint8_t* sK = sQ + 2 * C::kQBytes;
   uint8_t* sV = sK + C::kKStages * C::kKVBytes;
-  uint8_t* sP = sV + C::kVStages * C::kKVBytes;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + C::kPBytes);
-  uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;    // [3]
-  uint64_t* k_empty = bar + 4;   // [3]
-  uint64_t* v_full = bar + 7;    // [2]
-  uint64_t* v_empty = bar + 9;   // [2]
-  uint64_t* s_full = bar + 11;   // [2]
-  uint64_t* s_free = bar + 13;   // [2]
-  uint64_t* p_full = bar + 15;
-  uint64_t* pv_done = bar + 16;
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 17);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 18);
-  float* xchg = reinterpret_cast<float*>(bar + 32);  // [2 halves][128 rows] row values exchanged by warp pairs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    ptx::mbar_init(q_full, kSoftWarps * 32);
-    for (int s = 0; s < C::kKStages; ++s) {
-      ptx::mbar_init(&k_full[s], 1);
-      ptx::mbar_init(&k_empty[s], 1);
-    }
+  if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&q_full[s], 1);
+      ptx::mbar_init(&q_empty[s], 1 + kSoftWarps);
       ptx::mbar_init(&v_full[s], 1);
       ptx::mbar_init(&v_empty[s], 1);
       ptx::mbar_init(&s_full[s], 1);
       ptx::mbar_init(&s_free[s], kSoftWarps);
+      ptx::mbar_init(&p_full[s], kSoftWarps);
+      ptx::mbar_init(&p_free[s], 1);
     }
-    ptx::mbar_init(p_full, kSoftWarps);
-    ptx::mbar_init(pv_done, 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      ptx::mbar_init(&k_full[s], 1);
+      ptx::mbar_init(&k_empty[s], 1);
+    }
+    ptx::mbar_init(o_free, kSoftWarps);
+    ptx::mbar_init(drain, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -381,8 +416,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_base;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
   const int ntiles = a.ntiles[0];
@@ -393,7 +426,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   };
 
   if (warp == kTmaWarp) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ K / V producer
     // Loads in the order the MMAs consume them: K(g), then V(g - 1).
     if (lane == 0) {
       int64_t g = 0;
@@ -411,7 +444,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         return true;
       };
       for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x) {
-        const Tile x = load_tile(a, t);
+        const Tile x = decode_tile(a, a.tiles[t]);
         for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
           const int st = (int)(g % C::kKStages);
           if (g >= C::kKStages &&
@@ -435,43 +468,114 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       if (ok && have_prev) ok = load_v(g - 1, prev_bh, prev_y);
       if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
+      // let every load this thread issued land before the CTA can exit
+      const int64_t nk = g, nv = have_prev ? g : 0;
+      for (int s = 0; s < C::kKStages; ++s) {
+        if (nk <= s) break;
+        const int64_t last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
+        if (!ptx::mbar_wait(&k_full[s], (uint32_t)((last / C::kKStages) & 1))) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      }
+      for (int s = 0; s < C::kVStages; ++s) {
+        if (nv <= s) break;
+        const int64_t last = s + ((nv - 1 - s) / C::kVStages) * C::kVStages;
+        if (!ptx::mbar_wait(&v_full[s], (uint32_t)((last / C::kVStages) & 1))) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      }
     }
+  } else if (warp == kQWarp) {
+    // ------------------------------------------------ Q loader
+    // Gathers the tile's 128 query rows into the swizzled K-major Q buffer
+    // and publishes the tile entry and the rows' bucket entries.
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
+      const int qb = tcount & 1;
+      if (tcount >= 2 && !ptx::mbar_wait(&q_empty[qb], (uint32_t)(((tcount - 2) >> 1) & 1))) {
+        fail(SSA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      const int4 v = a.tiles[t];
+      const Tile x = decode_tile(a, v);
+      if (lane == 0) tinfo[qb] = v;
+      const int64_t off0 = x.kind_bh >= 0 ? (int64_t)a.offsets[x.kind_bh] + x.row0 : 0;
+      uint8_t* q = sQ + qb * C::kQBytes;
+#pragma unroll 1
+      for (int rr = 0; rr < kTileRows / 32; ++rr) {
+        const int r = rr * 32 + lane;
+        int64_t qrow = -1;
+        int entry = -1;
+        if (r < x.nrows) {
+          if (x.kind_bh >= 0) {
+            const int e = a.rows[off0 + r];
+            const int64_t row = (int64_t)(e >> 6);
+            if (e < 0 || row >= (int64_t)a.B * a.Hq * a.n_q || (e & 63) >= a.topk) {
+              flag_error(err, SSA_DEVERR_OVERFLOW);
+            } else {
+              qrow = row;
+              entry = e;
+            }
+          } else {
+            int64_t i;
+            qrow = local_row(a, x, r, &i);
+          }
+        }
+        meta[qb * kTileRows + r] = entry;
+        const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow < 0 ? 0 : qrow) * (int64_t)D * 2;
+        const uint32_t n = qrow < 0 ? 0u : 16u;
+        const uint32_t rsw = (uint32_t)(r & 7);
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch) {
+          uint8_t* dst = q + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ rsw) << 4);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
+                       "l"(src + ch * 16), "r"(n)
+                       : "memory");
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&q_full[qb]);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const int ab16 = DT == DT_BF16 ? 1 : 0;
       const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
       const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
-      const uint32_t aQ = ptx::smem_u32(sQ), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV),
-                     aP = ptx::smem_u32(sP);
-      int64_t gb = 0;
-      int tcount = 0;
-      auto issue_pv = [&](int64_t g, int kb) -> bool {
-        const int sv = (int)(g % C::kVStages);
-        if (!ptx::mbar_wait(p_full, (uint32_t)(g & 1))) return false;
-        if (!ptx::mbar_wait(&v_full[sv], (uint32_t)((g / C::kVStages) & 1))) return false;
+      const uint32_t aQ0 = ptx::smem_u32(sQ), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
+      const uint32_t tO = tmem + C::kColO;
+      int64_t g = 0;
+      int64_t pend = -1;        // block whose O += P V is still to be issued
+      bool pend_first = false;  // ... first block of its tile (overwrites O)
+      int pend_tile = 0;
+      auto issue_pv = [&](int64_t gg, bool first, int tc_) -> bool {
+        if (first && tc_ > 0 && !ptx::mbar_wait(o_free, (uint32_t)((tc_ - 1) & 1))) return false;
+        const int pb = (int)(gg & 1), sv = (int)(gg % C::kVStages);
+        if (!ptx::mbar_wait(&p_full[pb], (uint32_t)((gg >> 1) & 1))) return false;
+        if (!ptx::mbar_wait(&v_full[sv], (uint32_t)((gg / C::kVStages) & 1))) return false;
         tc::fence_after();
         const uint32_t vbase = aV + sv * C::kKVBytes;
+        const uint32_t tP = tmem + C::kColP + pb * 64;
 #pragma unroll
         for (int k = 0; k < kKeyBlk / 16; ++k) {
-          const uint64_t pd = tc::sdesc_sw128(aP + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
           const uint64_t vd = tc::sdesc_sw128(vbase + k * 2048, C::kRegion, 1024);
-          tc::mma(tO, pd, vd, id_pv, (kb > 0 || k > 0) ? 1u : 0u);
+          tc::mma_ts(tO, tP + k * 8, vd, id_pv, (first && k == 0) ? 0u : 1u);
         }
-        tc::commit(pv_done);
+        tc::commit(&p_free[pb]);
         tc::commit(&v_empty[sv]);
         return true;
       };
-      for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
-        const Tile x = load_tile(a, t);
-        if (!ptx::mbar_wait(q_full, (uint32_t)(tcount & 1))) {
-          fail(SSA_DEVERR_WAIT_TIMEOUT);
+      bool ok = true;
+      int tcount = 0;
+      for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x, ++tcount) {
+        const int qb = tcount & 1;
+        if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((tcount >> 1) & 1))) {
+          ok = false;
           break;
         }
         tc::fence_after();
-        bool ok = true;
-        for (int kb = 0; kb < x.nkb && ok; ++kb) {
-          const int64_t g = gb + kb;
+        const Tile x = decode_tile(a, tinfo[qb]);
+        const uint32_t aQ = aQ0 + qb * C::kQBytes;
+        for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
           const int sb = (int)(g & 1);
           const int sk = (int)(g % C::kKStages);
           ok = ptx::mbar_wait(&k_full[sk], (uint32_t)((g / C::kKStages) & 1));
@@ -483,19 +587,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int k = 0; k < D / 16; ++k) {
             const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
             const uint64_t kd = tc::sdesc_sw128(kbase + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
-            tc::mma(tS[sb], qd, kd, id_qk, k > 0 ? 1u : 0u);
+            tc::mma(tmem + sb * 128, qd, kd, id_qk, k > 0 ? 1u : 0u);
           }
           tc::commit(&s_full[sb]);
           tc::commit(&k_empty[sk]);
-          if (kb >= 1) ok = issue_pv(g - 1, kb - 1);
+          if (kb == x.nkb - 1) tc::commit(&q_empty[qb]);
+          if (pend >= 0) ok = issue_pv(pend, pend_first, pend_tile);
+          pend = g;
+          pend_first = kb == 0;
+          pend_tile = tcount;
         }
-        if (ok) ok = issue_pv(gb + x.nkb - 1, x.nkb - 1);
-        if (!ok) {
-          fail(SSA_DEVERR_WAIT_TIMEOUT);
-          break;
-        }
-        gb += x.nkb;
       }
+      if (ok && pend >= 0 && !*abort) ok = issue_pv(pend, pend_first, pend_tile);
+      if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
+      // every MMA issued completes before the tensor memory is released
+      tc::commit(drain);
+      if (!ptx::mbar_wait(drain, 0)) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
     }
   } else {
     // ------------------------------------------------ softmax warps
@@ -507,9 +614,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int pair_bar = 1 + quarter;  // named barrier of the warp pair
     const float c = a.scale_log2e;
-    const uint32_t qrow_sw = (uint32_t)(r & 7);
     constexpr int KH = kKeyBlk / 2;    // key columns per half
     constexpr int OH = D / 2;          // output columns per half
+    const uint32_t tOh = tmem + C::kColO + lane_off + half * OH;
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     int64_t gb = 0;
     int tcount = 0;
@@ -517,43 +624,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // (they meet at named barriers); they leave only through bounded waits,
     // which time out together.
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-      const Tile x = load_tile(a, t);
+      const int qb = tcount & 1;
+      if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((tcount >> 1) & 1))) {
+        fail(SSA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      const Tile x = decode_tile(a, tinfo[qb]);
       // row identity
       int64_t qrow = -1;  // row of Q / sel / partials
       int rank = a.topk;
       int64_t tpos = 0;   // query position (local tiles)
       if (x.kind_bh >= 0) {
-        if (r < x.nrows) {
-          const int v = a.rows[(int64_t)a.offsets[x.kind_bh] + x.row0 + r];
-          qrow = (int64_t)(v >> 6);
-          rank = v & 63;
-          if (qrow < 0 || qrow >= (int64_t)a.B * a.Hq * a.n_q || rank >= a.topk) {
-            flag_error(err, SSA_DEVERR_OVERFLOW);
-            qrow = -1;
-          }
+        const int e = meta[qb * kTileRows + r];
+        if (e >= 0) {
+          qrow = (int64_t)(e >> 6);
+          rank = e & 63;
         }
       } else if (r < x.nrows) {
-        const int b = x.bh / a.Hkv, kvh = x.bh - b * a.Hkv;
-        const int64_t i = x.i0 + r / a.g;
-        const int h = kvh * a.g + r % a.g;
-        qrow = (int64_t)(b * a.Hq + h) * a.n_q + i;
+        int64_t i;
+        qrow = local_row(a, x, r, &i);
         tpos = a.q_pos0 + i;
-      }
-      // gather this half of the row of Q into the swizzled K-major tile
-      {
-        const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow < 0 ? 0 : qrow) * (int64_t)D * 2;
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) {
-          const int ch = half * (D / 16) + cc;
-          uint8_t* dst = sQ + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
-          const uint32_t n = qrow < 0 ? 0u : 16u;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
-                       "l"(src + ch * 16), "r"(n)
-                       : "memory");
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        tc::fence_proxy_async_smem();
-        ptx::mbar_arrive(q_full);
       }
       float m = -INFINITY, l = 0.f;
       bool ok = true;
@@ -571,11 +661,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
         const int64_t hlim = klim - half * KH;  // valid keys of this half
         const bool partial = hlim < KH;
-        const uint32_t tsrow = tS[st] + lane_off + half * KH;
         // this half of the row of S, then the S buffer is free for the next MMA
         static_assert(KH == 64, "one 64-column load per half row");
         uint32_t sr[64];
-        tc::ld64(tsrow, sr);
+        tc::ld64(tmem + st * 128 + lane_off + half * KH, sr);
         tc::fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&s_free[st]);
@@ -592,7 +681,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         pair_sync();
         mx = fmaxf(mx, xchg[(half ^ 1) * 128 + r]) * c;
         pair_sync();
-        // rescale O only when the max grows by more than 2^8 (warp-uniform)
+        // rescale O only when the max grows by more than 2^8 (identical
+        // decision in both warps of the pair)
         float m_new = m;
         if (kb == 0) {
           m_new = mx;
@@ -600,59 +690,50 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           m_new = mx;
         }
         const bool need = kb > 0 && m_new != m;
-        bool waited = false;
         if (__any_sync(0xffffffffu, need)) {
-          if (!ptx::mbar_wait(pv_done, (uint32_t)((g - 1) & 1))) {
+          // O += P(g - 1) V must be complete before O is rescaled
+          if (!ptx::mbar_wait(&p_free[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1))) {
             ok = false;
             break;
           }
-          waited = true;
           tc::fence_after();
           const float f = need ? ptx::ex2(m - m_new) : 1.f;
 #pragma unroll
           for (int q = 0; q < OH / 32; ++q) {
             uint32_t rr[32];
-            tc::ld32(tO + lane_off + half * OH + q * 32, rr);
+            tc::ld32(tOh + q * 32, rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tc::st32(tO + lane_off + half * OH + q * 32, rr);
+            tc::st32(tOh + q * 32, rr);
           }
           l *= f;
-        }
-        m = m_new;
-        const float nb = m == -INFINITY ? 0.f : -m;
-        if (kb >= 1 && !waited) {
-          if (!ptx::mbar_wait(pv_done, (uint32_t)((g - 1) & 1))) {
+        } else if (g >= 2) {
+          // P buffer st is free once O += P(g - 2) V is complete
+          if (!ptx::mbar_wait(&p_free[st], (uint32_t)(((g - 2) >> 1) & 1))) {
             ok = false;
             break;
           }
+          tc::fence_after();
         }
-        // P = 2^(s * c - m) as 16-bit pairs
+        m = m_new;
+        const float nb = m == -INFINITY ? 0.f : -m;
+        // P = 2^(s * c - m) as 16-bit pairs into tensor memory
+        uint32_t pk[32];
 #pragma unroll
-        for (int q = 0; q < KH / 32; ++q) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float p0 = ptx::ex2(fmaf(__uint_as_float(sr[q * 32 + j]), c, nb));
-            float p1 = ptx::ex2(fmaf(__uint_as_float(sr[q * 32 + j + 1]), c, nb));
-            if (partial) {
-              if (q * 32 + j >= hlim) p0 = 0.f;
-              if (q * 32 + j + 1 >= hlim) p1 = 0.f;
-            }
-            l += p0 + p1;
-            pk[j / 2] = ptx::pack2<DT>(p0, p1);
+        for (int j = 0; j < KH; j += 2) {
+          float p0 = ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb));
+          float p1 = ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb));
+          if (partial) {
+            if (j >= hlim) p0 = 0.f;
+            if (j + 1 >= hlim) p1 = 0.f;
           }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int ch = half * (KH / 8) + q * 4 + i;
-            uint8_t* dst = sP + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ qrow_sw) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
+          l += p0 + p1;
+          pk[j / 2] = ptx::pack2<DT>(p0, p1);
         }
-        tc::fence_proxy_async_smem();
+        tc::st32(tmem + C::kColP + st * 64 + lane_off + half * 32, pk);
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(p_full);
+        if (lane == 0) ptx::mbar_arrive(&p_full[st]);
       }
       if (!ok) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
@@ -660,33 +741,38 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       // epilogue: O / l (both halves' sums) to this row's partial slot
       const int64_t glast = gb + x.nkb - 1;
-      if (!ptx::mbar_wait(pv_done, (uint32_t)(glast & 1))) {
+      if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
       tc::fence_after();
+      uint32_t ov[OH];
+      if constexpr (OH == 64) {
+        tc::ld64(tOh, ov);
+      } else {
+        tc::ld32(tOh, ov);
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(o_free);
       xchg[half * 128 + r] = l;
       pair_sync();
       const float lt = l + xchg[(half ^ 1) * 128 + r];
       pair_sync();
       const float inv = 1.f / lt;
-      const int64_t slot = qrow * (a.topk + 1) + rank;
+      if (qrow >= 0) {
+        const int64_t slot = qrow * (a.topk + 1) + rank;
+        uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + half * OH);
 #pragma unroll
-      for (int q = 0; q < OH / 32; ++q) {
-        uint32_t rr[32];
-        tc::ld32(tO + lane_off + half * OH + q * 32, rr);
-        if (qrow >= 0) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = ptx::pack2<DT>(__uint_as_float(rr[2 * j]) * inv, __uint_as_float(rr[2 * j + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + half * OH + q * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        }
+        for (int j = 0; j < OH / 8; ++j)
+          dst[j] = make_uint4(ptx::pack2<DT>(__uint_as_float(ov[8 * j]) * inv, __uint_as_float(ov[8 * j + 1]) * inv),
+                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv),
+                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv),
+                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv));
+        if (half == 0) a.pml[slot] = make_float2(m, lt);
       }
-      if (qrow >= 0 && half == 0) a.pml[slot] = make_float2(m, lt);
-      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
       gb += x.nkb;
     }
   }
