@@ -762,13 +762,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const float inv = 1.f / lt;
       if (qrow >= 0) {
         const int64_t slot = qrow * (a.topk + 1) + rank;
-        uint4* dst = reinterpret_cast<uint4*>(a.po + slot * D + half * OH);
+        uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
+        uint32_t pk[OH / 2];
 #pragma unroll
-        for (int j = 0; j < OH / 8; ++j)
-          dst[j] = make_uint4(ptx::pack2<DT>(__uint_as_float(ov[8 * j]) * inv, __uint_as_float(ov[8 * j + 1]) * inv),
-                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 2]) * inv, __uint_as_float(ov[8 * j + 3]) * inv),
-                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 4]) * inv, __uint_as_float(ov[8 * j + 5]) * inv),
-                              ptx::pack2<DT>(__uint_as_float(ov[8 * j + 6]) * inv, __uint_as_float(ov[8 * j + 7]) * inv));
+        for (int j = 0; j < OH / 2; ++j)
+          pk[j] = ptx::pack2<DT>(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
+#pragma unroll
+        for (int j = 0; j < OH / 16; ++j)
+          ptx::st_global_v8(dst + 16 * j, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3], pk[8 * j + 4],
+                            pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
         if (half == 0) a.pml[slot] = make_float2(m, lt);
       }
       __syncwarp();
