@@ -106,16 +106,24 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
 
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """One process per GPU, launched by torchrun: (world size, rank, local rank).
+
+    The ranks run independent replicas of the workload (the path has no
+    exchange step); the process group only carries the barrier around the
+    timed region and the max over ranks of its duration.
+    """
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if backend == "nccl":
+        torch.cuda.set_device(local)
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return ws, rank, local
 
 
@@ -126,12 +134,19 @@ def barrier(ws):
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The largest of the ranks' values (the job's time is its slowest rank's)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
+    """Whole-job throughput: the units every rank processed over the max-over-ranks time."""
+    return units_per_rank * ws / seconds
 
 
 def flush_l2(buf):
@@ -269,7 +284,7 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     pk = peaks()
     achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
     res = {
-        "tok_s": steps * ws_n / (total_ms_max * 1e-3),
+        "tok_s": job_throughput(steps, total_ms_max * 1e-3, ws_n),
         "ms_per_step": total_ms_max / steps,
         "attend_ms_per_step": attend_ms / steps,
         "route_plus_gaps_ms_per_step": (total_ms - attend_ms) / steps,
@@ -422,7 +437,7 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush):
     pk = peaks()
     achieved = fl / (attend_ms * 1e-3) / 1e12
     return {
-        "workload": w.name, "value": w.n_q * ws_n / (ms * 1e-3), "unit": "tok/s",
+        "workload": w.name, "value": job_throughput(w.n_q, ms * 1e-3, ws_n), "unit": "tok/s",
         "ms_per_step": ms, "attend_ms": attend_ms, "steps": steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
