@@ -674,8 +674,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int j = 0; j < KH; ++j)
             if (j < hlim) mx = fmaxf(mx, __uint_as_float(sr[j]));
         } else {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < KH; ++j) mx = fmaxf(mx, __uint_as_float(sr[j]));
+          for (int j = 0; j < KH; j += 8)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              m4[u] = ptx::max3(m4[u], __uint_as_float(sr[j + 2 * u]), __uint_as_float(sr[j + 2 * u + 1]));
+          mx = ptx::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
         }
         xchg[half * 128 + r] = mx;
         pair_sync();
@@ -785,6 +790,40 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
 // ---------------------------------------------------------------- merge
 // One warp per row of Q: its used spans (sel order) then its local span.
+// The partials of a row are read in batches of kMergeBatch slots with all of
+// a batch's loads in flight at once (one memory round trip per batch; one
+// batch covers topk <= 23).
+constexpr int kMergeBatch = 24;
+
+template <int DT, int E>
+__device__ __forceinline__ void widen_partial(const uint16_t* src, float (&v)[E]) {
+  if constexpr (E == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if constexpr (DT == DT_BF16) {
+        v[2 * k] = bf16_bits_to_f32(ww[k] & 0xffffu);
+        v[2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
+      } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+        v[2 * k] = f.x;
+        v[2 * k + 1] = f.y;
+      }
+    }
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    if constexpr (DT == DT_BF16) {
+      v[0] = bf16_bits_to_f32(w & 0xffffu);
+      v[1] = __uint_as_float(w & 0xffff0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+      v[0] = f.x;
+      v[1] = f.y;
+    }
+  }
+}
+
 template <int DT, int D>
 __device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const PrefArgs& a, void* __restrict__ O,
                                           float* __restrict__ lse, int64_t row, int lane) {
@@ -801,53 +840,35 @@ __device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const int64_t base = row * (a.topk + 1);
-  for (int s0 = 0; s0 < nslot; s0 += 8) {
-    float2 ml[8];
-    float v[8][E];
+  for (int s0 = 0; s0 < nslot; s0 += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    uint2 raw[kMergeBatch];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kMergeBatch; ++u) {
       const int s = s0 + u;
       if (s < nslot) {
         const int rk = s < used ? s : a.topk;
         ml[u] = a.pml[base + rk];
         const uint16_t* src = a.po + (base + rk) * D + lane * E;
         if constexpr (E == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(src);
-          const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            if constexpr (DT == DT_BF16) {
-              v[u][2 * k] = bf16_bits_to_f32(ww[k] & 0xffffu);
-              v[u][2 * k + 1] = __uint_as_float(ww[k] & 0xffff0000u);
-            } else {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
-              v[u][2 * k] = f.x;
-              v[u][2 * k + 1] = f.y;
-            }
-          }
+          raw[u] = *reinterpret_cast<const uint2*>(src);
         } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-          if constexpr (DT == DT_BF16) {
-            v[u][0] = bf16_bits_to_f32(w & 0xffffu);
-            v[u][1] = __uint_as_float(w & 0xffff0000u);
-          } else {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
-            v[u][0] = f.x;
-            v[u][1] = f.y;
-          }
+          raw[u] = make_uint2(*reinterpret_cast<const uint32_t*>(src), 0u);
         }
       } else {
         ml[u] = make_float2(-INFINITY, 0.f);
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kMergeBatch; ++u) {
       if (s0 + u >= nslot) continue;
+      float v[E];
+      widen_partial<DT, E>(reinterpret_cast<const uint16_t*>(&raw[u]), v);
       const float Mn = fmaxf(M, ml[u].x);
       const float fa = exp2f(M - Mn), fb = exp2f(ml[u].x - Mn) * ml[u].y;
       Ls = Ls * fa + fb;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * fa + v[u][e] * fb;
+      for (int e = 0; e < E; ++e) acc[e] = acc[e] * fa + v[e] * fb;
       M = Mn;
     }
   }

@@ -142,6 +142,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two floats -> packed 16-bit pair (lo in the low half), round to nearest.
 template <int DT>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {

@@ -84,8 +84,12 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ su
 
 // A row's 16 best (score, span), sorted by score descending (the first k of
 // them are its k best for any k <= 16).  A candidate enters only when
-// strictly greater than the 16th, so among equal scores the earlier (lower)
-// span stays.  All indexing is static, so the list lives in registers.
+// strictly greater than the 16th, and behind every entry of equal score, so
+// among equal scores the earlier (lower) span stays ahead.  All indexing is
+// static, so the list lives in registers, and an insertion is one parallel
+// shift: since the list is sorted, ge[i] = (v[i] >= s) is true on a prefix,
+// and entry i becomes v[i] (inside the prefix), s (first slot after it) or
+// v[i - 1] (further down).
 struct Top16 {
   float v[16];
   int j[16];
@@ -99,21 +103,33 @@ struct Top16 {
   __device__ __forceinline__ float thr() const { return v[15]; }
   __device__ __forceinline__ void push(float s, int span) {
     if (!(s > v[15])) return;
-    v[15] = s;
-    j[15] = span;
+    bool ge[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ge[i] = v[i] >= s;
 #pragma unroll
     for (int i = 15; i > 0; --i) {
-      if (v[i] > v[i - 1]) {
-        const float tv = v[i];
-        v[i] = v[i - 1];
-        v[i - 1] = tv;
-        const int tj = j[i];
-        j[i] = j[i - 1];
-        j[i - 1] = tj;
-      }
+      v[i] = ge[i] ? v[i] : (ge[i - 1] ? s : v[i - 1]);
+      j[i] = ge[i] ? j[i] : (ge[i - 1] ? span : j[i - 1]);
     }
+    v[0] = ge[0] ? v[0] : s;
+    j[0] = ge[0] ? j[0] : span;
   }
 };
+
+// r[p] for a runtime p in [0, 32): a 5-level select tree over the static
+// register array.
+__device__ __forceinline__ float pick32(const uint32_t (&r)[32], int p) {
+  float t16[16], t8[8], t4[4], t2[2];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t16[i] = __uint_as_float((p & 1) ? r[2 * i + 1] : r[2 * i]);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t8[i] = (p & 2) ? t16[2 * i + 1] : t16[2 * i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t4[i] = (p & 4) ? t8[2 * i + 1] : t8[2 * i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) t2[i] = (p & 8) ? t4[2 * i + 1] : t4[2 * i];
+  return (p & 16) ? t2[1] : t2[0];
+}
 
 template <int DT, int D>
 __global__ void __launch_bounds__(kRouteThreads, 1)
@@ -271,10 +287,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
           if (pass) {
             const int p = __ffs(pass) - 1;
             pass &= pass - 1u;
-            float val = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) val = c == p ? __uint_as_float(rr[c]) : val;
-            best.push(val, j0 + p);
+            best.push(pick32(rr, p), j0 + p);
           }
         }
       }
