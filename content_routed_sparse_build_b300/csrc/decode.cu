@@ -353,23 +353,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   iss.grp = iss.u = iss.c = 0;
   iss.t0 = iss.t1 = 0;
   int iss_tile = 0;
-  int next_it = 0;
-  if (lane == 0) next_it = atomicAdd(plan.counter, 1);
-  next_it = __shfl_sync(0xffffffffu, next_it, 0);
+  // Work items come from an atomic counter.  The claim for the next item is
+  // made when two tiles of the current one remain to be issued, so that the
+  // atomic's round trip is hidden without reserving work for long (which
+  // would unbalance the tail).
+  int it_next = 0, it_claim = 0;
+  bool have_next = true, claim_issued = false;
+  if (lane == 0) it_next = atomicAdd(plan.counter, 1);
+  it_next = __shfl_sync(0xffffffffu, it_next, 0);
   bool exhausted = false;
 
   // Loads the next tile into `stage`; returns false when no work is left.
   auto issue = [&](int stage) -> bool {
     if (iss_tile == iss.ntiles) {
-      if (next_it >= total) {
+      if (!have_next) it_next = __shfl_sync(0xffffffffu, it_claim, 0);
+      if (it_next >= total) {
         exhausted = true;
         return false;
       }
-      decode_item(next_it, tb, geo, iss);
+      decode_item(it_next, tb, geo, iss);
       iss_tile = 0;
-      int nx = 0;
-      if (lane == 0) nx = atomicAdd(plan.counter, 1);
-      next_it = __shfl_sync(0xffffffffu, nx, 0);
+      have_next = false;
+      claim_issued = false;
     }
     if (lane == 0) {
       meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
@@ -385,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     ++iss_tile;
+    if (!claim_issued && iss.ntiles - iss_tile <= 2) {
+      if (lane == 0) it_claim = atomicAdd(plan.counter, 1);
+      claim_issued = true;
+    }
     return true;
   };
 
