@@ -149,6 +149,22 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
     return units_per_rank * ws / seconds
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that
+# ncu measured for the dominant kernels of the two default workloads, as the
+# kernels stand in this tree; each figure names the profile summary it comes
+# from.  They are reported as the roofline's "traffic" only for the workload
+# they were measured on.
+NCU_TRAFFIC = {
+    "decode_1m": (2.204e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
+    "prefill_chunk_vs_1m": (3.838e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
+}
+
+
+def traffic_of(workload: str):
+    t = NCU_TRAFFIC.get(workload)
+    return (t[0], t[1]) if t else (None, None)
+
+
 def flush_l2(buf):
     buf.zero_()
 
@@ -292,7 +308,8 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
         "route_bytes_per_step": route_bytes / steps,
         "step_bytes_gbs": (attend_bytes + route_bytes) / (total_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": traffic_of(w.name)[0], "traffic_source": traffic_of(w.name)[1],
                      "kernel": "ssa_attend_decode (plan + gathered K/V attend + merge), timed as "
                                "one CUDA-graph node group",
                      "peak_source": pk["source"]},
@@ -441,7 +458,8 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush):
         "ms_per_step": ms, "attend_ms": attend_ms, "steps": steps,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4), "traffic": None,
+                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
+                     "traffic": traffic_of(w.name)[0], "traffic_source": traffic_of(w.name)[1],
                      "kernel": "attend_prefill (4*d FLOP per attended token per query head)",
                      "peak_source": pk["source"] + " sustained bf16"},
         "selected_span_tflop_per_step": fl / 1e12,
