@@ -17,13 +17,10 @@
 //          (128 / g queries x g heads): Q rows gathered into a swizzled
 //          K-major tile, 128-span blocks of the three planes stream through
 //          a 2-stage TMA ring, one thread issues S = sum_p Q S_p^T into
-//          tensor memory (double buffered), and eight warps fold each block
-//          into register lists of the rows' k best: warps w and w + 4 share
-//          the rows of lane quarter w % 4, each taking one half of every
-//          block's columns (strictly greater scores only, so among equal
-//          scores the earlier, lower span stays).  At the end the two lists
-//          of a row are merged under (score desc, span asc) and written in
-//          ascending span order.
+//          tensor memory (double buffered), and four warps (one row per
+//          thread) fold each block into a register list of the row's k best
+//          (strictly greater scores only, so among equal scores the earlier,
+//          lower span stays).  The list is written in ascending span order.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -33,9 +30,7 @@ namespace {
 
 constexpr int kRows = 128;    // (query, head) rows per tile
 constexpr int kBlk = 128;     // candidate spans per block
-constexpr int kSelWarps = 8;       // two per tensor-memory lane quarter, one per column half
-constexpr int kTmaWarp = kSelWarps, kMmaWarp = kSelWarps + 1;
-constexpr int kRouteThreads = (kSelWarps + 2) * 32;
+constexpr int kRouteThreads = 192;  // warps 0-3 select, 4 TMA, 5 MMA
 constexpr int kMaxTopK = 16;  // register list size; larger k uses the fp32 tile router
 
 template <int D>
@@ -106,21 +101,6 @@ struct Top16 {
     }
   }
   __device__ __forceinline__ float thr() const { return v[15]; }
-  // Inserts (s, span) under the order (score desc, span asc) whatever the
-  // spans already held (used to merge two lists).
-  __device__ __forceinline__ void push_ordered(float s, int span) {
-    if (!(s > v[15] || (s == v[15] && span < j[15]))) return;
-    bool ge[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ge[i] = v[i] > s || (v[i] == s && j[i] < span);
-#pragma unroll
-    for (int i = 15; i > 0; --i) {
-      v[i] = ge[i] ? v[i] : (ge[i - 1] ? s : v[i - 1]);
-      j[i] = ge[i] ? j[i] : (ge[i - 1] ? span : j[i - 1]);
-    }
-    v[0] = ge[0] ? v[0] : s;
-    j[0] = ge[0] ? j[0] : span;
-  }
   __device__ __forceinline__ void push(float s, int span) {
     if (!(s > v[15])) return;
     bool ge[16];
@@ -181,18 +161,18 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   const int nblk = (int)((ell_max + kBlk - 1) / kBlk);
 
   if (tid == 0) {
-    ptx::mbar_init(q_full, kSelWarps * 32);
+    ptx::mbar_init(q_full, 128);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&b_full[s], 1);
       ptx::mbar_init(&b_empty[s], 1);
       ptx::mbar_init(&s_full[s], 1);
-      ptx::mbar_init(&s_free[s], kSelWarps);
+      ptx::mbar_init(&s_free[s], 4);
     }
     *abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == kMmaWarp) tc::alloc(tmem_base, 256);
-  if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tmP);
+  if (warp == 5) tc::alloc(tmem_base, 256);
+  if (warp == 4 && lane == 0) ptx::prefetch_tmap(&tmP);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -201,7 +181,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   ptx::pdl_launch_dependents();
   const int bh = b * Hkv + kvh;
 
-  if (warp == kTmaWarp) {
+  if (warp == 4) {
     if (lane == 0) {
       for (int blk = 0; blk < nblk && !*abort; ++blk) {
         const int st = blk & 1;
@@ -220,7 +200,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                              bh * 3 + p);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == 5) {
     if (lane == 0) {
       const uint32_t id = tc::idesc_f16(kRows, kBlk, DT == DT_BF16 ? 1 : 0, 0, 0);
       const uint32_t aQ = ptx::smem_u32(sQ), aB = ptx::smem_u32(sB);
@@ -252,21 +232,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ selection
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;   // row of the tile (tensor-memory lane)
+    // ------------------------------------------------ selection: row r = tid
+    const int r = tid;
     const int64_t grow = row0 + r;
     const bool valid = grow < rows_total;
     const int64_t i = valid ? grow / g : 0;
     const int h = kvh * g + (int)(valid ? grow % g : 0);
     const int64_t qrow = (int64_t)(b * Hq + h) * n_q + i;
     const int64_t ell = valid ? (q_pos0 + i) / S : 0;
-    // gather this half of the row of Q (zeros beyond the chunk)
+    // gather the row of Q (zeros beyond the chunk)
     {
       const uint8_t* src = static_cast<const uint8_t*>(Q) + (valid ? qrow : 0) * (int64_t)D * 2;
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        const int ch = half * (D / 16) + cc;
+      for (int ch = 0; ch < D / 8; ++ch) {
         uint8_t* dst = sQ + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ ((uint32_t)r & 7)) << 4);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
                      "l"(src + ch * 16), "r"(valid ? 16u : 0u)
@@ -278,7 +256,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
     Top16 best;
     best.init();
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     for (int blk = 0; blk < nblk; ++blk) {
       const int st = blk & 1;
       if (!ptx::mbar_wait(&s_full[st], (uint32_t)((blk >> 1) & 1))) {
@@ -287,12 +265,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         break;
       }
       tc::fence_after();
-      const int jb = blk * kBlk + half * (kBlk / 2);
+      const int jb = blk * kBlk;
 #pragma unroll 1
-      for (int q = 0; q < kBlk / 64; ++q) {
+      for (int q = 0; q < kBlk / 32; ++q) {
         uint32_t rr[32];
-        tc::ld32(tmem + st * 128 + lane_off + half * (kBlk / 2) + q * 32, rr);
-        if (q == kBlk / 64 - 1) {
+        tc::ld32(tmem + st * 128 + lane_off + q * 32, rr);
+        if (q == kBlk / 32 - 1) {
           tc::fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&s_free[st]);
@@ -314,25 +292,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         }
       }
     }
-    // merge the two halves' lists of each row through the Q tile's space,
-    // which is free once every gather into it has landed (q_full; a tile
-    // without candidates runs no MMA) and every MMA reading it completed
-    // (implied by the last block's s_full)
-    float* xv = reinterpret_cast<float*>(sQ);                 // [128 rows][16]
-    int* xj = reinterpret_cast<int*>(sQ) + kRows * 16;        // [128 rows][16]
-    const int pair_bar = 1 + quarter;
-    if (!ptx::mbar_wait(q_full, 0)) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
-    if (half == 1) {
-#pragma unroll
-      for (int a = 0; a < 16; ++a) {
-        xv[r * 16 + a] = best.v[a];
-        xj[r * 16 + a] = best.j[a];
-      }
-    }
-    asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-    if (half == 1) goto done;
-#pragma unroll
-    for (int a = 0; a < 16; ++a) best.push_ordered(xv[r * 16 + a], xj[r * 16 + a]);
     if (valid) {
       // the first topk entries, written in ascending span order
       int32_t* out = sel + qrow * topk;
@@ -354,12 +313,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         if (osc) osc[a] = __int_as_float(0x7fc00000);
       }
     }
-  done:;
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == kMmaWarp) tc::dealloc(tmem, 256);
+  if (warp == 5) tc::dealloc(tmem, 256);
 }
 
 template <int DT, int D>
