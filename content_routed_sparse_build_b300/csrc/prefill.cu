@@ -282,19 +282,24 @@ struct ACfg {
   static constexpr int kRegion = kTileRows * 128;      // 128 rows x 128 bytes
   static constexpr int kQBytes = (D / 64) * kRegion;    // Q tile, D/64 regions
   static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block of 128 tokens
-  static constexpr int kKStages = D == 128 ? 2 : 3;
+  // two stages each: a K slot is free once S of its block is done (s_full),
+  // a V slot once O += P V of its block is done (p_free); with two stages
+  // those barriers can never run two phases ahead of the producer's wait
+  static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   // small state first (barriers, pair exchange, tile metadata), then the
   // 1024-byte aligned operand buffers: Q[2], K[kKStages], V[kVStages]
   static constexpr int kBarBytes = 256;
-  static constexpr int kXchgBytes = 2 * kTileRows * 4;
+  static constexpr int kXchgBytes = 2 * 2 * kTileRows * 4;
   static constexpr int kMetaBytes = 2 * 16 + 2 * kTileRows * 4;
   static constexpr int kSmallBytes = ((kBarBytes + kXchgBytes + kMetaBytes + 1023) / 1024) * 1024;
   static constexpr size_t kSmem =
       1024 + kSmallBytes + 2 * (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes;
-  // tensor memory: S0 [0, 128), S1 [128, 256), O [256, 256 + D), P0, P1 (64 columns each)
+  // tensor memory: S0 [0, 128), S1 [128, 256) (P of a block is written over
+  // the S columns it came from), then the two key-half accumulators
+  // O0 [256, 256 + D) and O1 [256 + D, 256 + 2 D)
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256, kColP = 256 + D;
+  static constexpr uint32_t kColO = 256;
 };
 
 constexpr int kSoftWarps = 8;      // two warps per tensor-memory lane quarter
@@ -367,19 +372,16 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(base);
   uint64_t* q_full = bar + 0;    // [2] Q tile and its metadata loaded
   uint64_t* q_empty = bar + 2;   // [2] last S of the tile done + partials written
-  uint64_t* k_full = bar + 4;    // [3]
-  uint64_t* k_empty = bar + 7;   // [3]
-  uint64_t* v_full = bar + 10;   // [2]
-  uint64_t* v_empty = bar + 12;  // [2]
-  uint64_t* s_full = bar + 14;   // [2]
-  uint64_t* s_free = bar + 16;   // [2]
-  uint64_t* p_full = bar + 18;   // [2]
-  uint64_t* p_free = bar + 20;   // [2] O += P V done for the buffer's last block
-  uint64_t* o_free = bar + 22;   // O read out by the epilogue
-  uint64_t* drain = bar + 23;    // every MMA issued has completed
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 24);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 25);
-  float* xchg = reinterpret_cast<float*>(base + C::kBarBytes);   // [2 halves][128 rows]
+  uint64_t* k_full = bar + 4;    // [2]
+  uint64_t* v_full = bar + 6;    // [2]
+  uint64_t* s_full = bar + 8;    // [2] S of the buffer's last block done (its K slot is free)
+  uint64_t* p_full = bar + 10;   // [2 buffers][2 halves]
+  uint64_t* p_free = bar + 14;   // [2] O += P V of the buffer's last block done (its V slot is free)
+  uint64_t* o_free = bar + 24;   // O read out by the epilogue
+  uint64_t* drain = bar + 25;    // every MMA issued has completed
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 26);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 27);
+  float* xchg = reinterpret_cast<float*>(base + C::kBarBytes);   // [2 halves][m, l][128 rows]
   int4* tinfo = reinterpret_cast<int4*>(base + C::kBarBytes + C::kXchgBytes);  // [2] tile entries
   int* meta = reinterpret_cast<int*>(tinfo + 2);                  // [2][128] bucket entries or -1
   uint8_t* sQ = base + C::kSmallBytes;
@@ -391,16 +393,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&q_full[s], 1);
       ptx::mbar_init(&q_empty[s], 1 + kSoftWarps);
-      ptx::mbar_init(&v_full[s], 1);
-      ptx::mbar_init(&v_empty[s], 1);
-      ptx::mbar_init(&s_full[s], 1);
-      ptx::mbar_init(&s_free[s], kSoftWarps);
-      ptx::mbar_init(&p_full[s], kSoftWarps);
-      ptx::mbar_init(&p_free[s], 1);
-    }
-    for (int s = 0; s < C::kKStages; ++s) {
       ptx::mbar_init(&k_full[s], 1);
-      ptx::mbar_init(&k_empty[s], 1);
+      ptx::mbar_init(&v_full[s], 1);
+      ptx::mbar_init(&s_full[s], 1);
+      ptx::mbar_init(&p_free[s], 1);
+      for (int h = 0; h < 2; ++h) ptx::mbar_init(&p_full[2 * s + h], kSoftWarps / 2);
     }
     ptx::mbar_init(o_free, kSoftWarps);
     ptx::mbar_init(drain, 1);
@@ -434,9 +431,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       bool have_prev = false, ok = true;
       auto load_v = [&](int64_t gv, int bh, int y) -> bool {
         const int st = (int)(gv % C::kVStages);
-        if (gv >= C::kVStages &&
-            !ptx::mbar_wait(&v_empty[st], (uint32_t)(((gv - C::kVStages) / C::kVStages) & 1)))
-          return false;
+        if (gv >= 2 && !ptx::mbar_wait(&p_free[(gv - 2) & 1], (uint32_t)(((gv - 2) >> 1) & 1))) return false;
         ptx::mbar_arrive_expect_tx(&v_full[st], C::kKVBytes);
 #pragma unroll
         for (int r = 0; r < D / 64; ++r)
@@ -447,8 +442,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const Tile x = decode_tile(a, a.tiles[t]);
         for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
           const int st = (int)(g % C::kKStages);
-          if (g >= C::kKStages &&
-              !ptx::mbar_wait(&k_empty[st], (uint32_t)(((g - C::kKStages) / C::kKStages) & 1))) {
+          if (g >= 2 && !ptx::mbar_wait(&s_full[(g - 2) & 1], (uint32_t)(((g - 2) >> 1) & 1))) {
             ok = false;
             break;
           }
@@ -542,26 +536,32 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
       const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
       const uint32_t aQ0 = ptx::smem_u32(sQ), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
-      const uint32_t tO = tmem + C::kColO;
       int64_t g = 0;
       int64_t pend = -1;        // block whose O += P V is still to be issued
       bool pend_first = false;  // ... first block of its tile (overwrites O)
       int pend_tile = 0;
+      // O_h += P_h V_h for the two key halves h of block gg: P_h sits in
+      // tensor memory over the S columns of its half, V_h is rows
+      // [64 h, 64 h + 64) of the block's V tile.
       auto issue_pv = [&](int64_t gg, bool first, int tc_) -> bool {
         if (first && tc_ > 0 && !ptx::mbar_wait(o_free, (uint32_t)((tc_ - 1) & 1))) return false;
         const int pb = (int)(gg & 1), sv = (int)(gg % C::kVStages);
-        if (!ptx::mbar_wait(&p_full[pb], (uint32_t)((gg >> 1) & 1))) return false;
+        const uint32_t par = (uint32_t)((gg >> 1) & 1);
         if (!ptx::mbar_wait(&v_full[sv], (uint32_t)((gg / C::kVStages) & 1))) return false;
-        tc::fence_after();
         const uint32_t vbase = aV + sv * C::kKVBytes;
-        const uint32_t tP = tmem + C::kColP + pb * 64;
 #pragma unroll
-        for (int k = 0; k < kKeyBlk / 16; ++k) {
-          const uint64_t vd = tc::sdesc_sw128(vbase + k * 2048, C::kRegion, 1024);
-          tc::mma_ts(tO, tP + k * 8, vd, id_pv, (first && k == 0) ? 0u : 1u);
+        for (int h = 0; h < 2; ++h) {
+          if (!ptx::mbar_wait(&p_full[2 * pb + h], par)) return false;
+          tc::fence_after();
+          const uint32_t tP = tmem + pb * 128 + h * 64;
+          const uint32_t tOh = tmem + C::kColO + h * D;
+#pragma unroll
+          for (int k = 0; k < kKeyBlk / 32; ++k) {
+            const uint64_t vd = tc::sdesc_sw128(vbase + (h * (kKeyBlk / 32) + k) * 2048, C::kRegion, 1024);
+            tc::mma_ts(tOh, tP + k * 8, vd, id_pv, (first && k == 0) ? 0u : 1u);
+          }
         }
         tc::commit(&p_free[pb]);
-        tc::commit(&v_empty[sv]);
         return true;
       };
       bool ok = true;
@@ -578,8 +578,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
           const int sb = (int)(g & 1);
           const int sk = (int)(g % C::kKStages);
+          // S(g) overwrites S[g % 2], which holds P(g - 2): its O += P V was
+          // issued before, and the tensor pipe runs this thread's MMAs in order
           ok = ptx::mbar_wait(&k_full[sk], (uint32_t)((g / C::kKStages) & 1));
-          if (ok && g >= 2) ok = ptx::mbar_wait(&s_free[sb], (uint32_t)(((g - 2) >> 1) & 1));
           if (!ok) break;
           tc::fence_after();
           const uint32_t kbase = aK + sk * C::kKVBytes;
@@ -590,7 +591,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             tc::mma(tmem + sb * 128, qd, kd, id_qk, k > 0 ? 1u : 0u);
           }
           tc::commit(&s_full[sb]);
-          tc::commit(&k_empty[sk]);
           if (kb == x.nkb - 1) tc::commit(&q_empty[qb]);
           if (pend >= 0) ok = issue_pv(pend, pend_first, pend_tile);
           pend = g;
@@ -606,23 +606,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
   } else {
     // ------------------------------------------------ softmax warps
-    // Warps w and w + 4 read the same tensor-memory lanes (rows r = 32 (w % 4)
-    // + lane); warp w takes key / output columns of half 0, warp w + 4 half 1,
-    // and the pair exchanges row maxima and sums through shared memory.
+    // Warp (quarter, half) owns tensor-memory lanes 32 quarter .. + 31 (its
+    // rows) and the keys of one half of every block.  It keeps its own
+    // running max and sum for its half and writes P of its half over the S
+    // columns it read; O_half accumulates only that half's keys.  The two
+    // halves of a row meet once per tile, in the epilogue: with M = max(m0,
+    // m1), O = (2^(m0 - M) O0 + 2^(m1 - M) O1) / (2^(m0 - M) l0 + 2^(m1 - M) l1).
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int pair_bar = 1 + quarter;  // named barrier of the warp pair
     const float c = a.scale_log2e;
     constexpr int KH = kKeyBlk / 2;    // key columns per half
-    constexpr int OH = D / 2;          // output columns per half
-    const uint32_t tOh = tmem + C::kColO + lane_off + half * OH;
+    constexpr int OH = D / 2;          // output columns this warp writes
+    const uint32_t tOown = tmem + C::kColO + half * D + lane_off;   // this half's accumulator
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     int64_t gb = 0;
     int tcount = 0;
     // No abort check here: both warps of a pair must walk the same tiles
-    // (they meet at named barriers); they leave only through bounded waits,
-    // which time out together.
+    // (they meet at a named barrier per tile); they leave only through
+    // bounded waits, which time out together.
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const int qb = tcount & 1;
       if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((tcount >> 1) & 1))) {
@@ -661,13 +664,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
         const int64_t hlim = klim - half * KH;  // valid keys of this half
         const bool partial = hlim < KH;
-        // this half of the row of S, then the S buffer is free for the next MMA
         static_assert(KH == 64, "one 64-column load per half row");
+        const uint32_t tS = tmem + st * 128 + lane_off + half * KH;
         uint32_t sr[64];
-        tc::ld64(tmem + st * 128 + lane_off + half * KH, sr);
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&s_free[st]);
+        tc::ld64(tS, sr);
         float mx = -INFINITY;
         if (partial) {
 #pragma unroll
@@ -682,12 +682,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
               m4[u] = ptx::max3(m4[u], __uint_as_float(sr[j + 2 * u]), __uint_as_float(sr[j + 2 * u + 1]));
           mx = ptx::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
         }
-        xchg[half * 128 + r] = mx;
-        pair_sync();
-        mx = fmaxf(mx, xchg[(half ^ 1) * 128 + r]) * c;
-        pair_sync();
-        // rescale O only when the max grows by more than 2^8 (identical
-        // decision in both warps of the pair)
+        mx *= c;
+        // rescale O_half only when this half's max grows by more than 2^8
         float m_new = m;
         if (kb == 0) {
           m_new = mx;
@@ -696,7 +692,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         const bool need = kb > 0 && m_new != m;
         if (__any_sync(0xffffffffu, need)) {
-          // O += P(g - 1) V must be complete before O is rescaled
+          // O_half += P_half(g - 1) V must be complete before it is rescaled
           if (!ptx::mbar_wait(&p_free[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1))) {
             ok = false;
             break;
@@ -704,25 +700,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           tc::fence_after();
           const float f = need ? ptx::ex2(m - m_new) : 1.f;
 #pragma unroll
-          for (int q = 0; q < OH / 32; ++q) {
+          for (int q = 0; q < D / 32; ++q) {
             uint32_t rr[32];
-            tc::ld32(tOh + q * 32, rr);
+            tc::ld32(tOown + q * 32, rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tc::st32(tOh + q * 32, rr);
+            tc::st32(tOown + q * 32, rr);
           }
           l *= f;
-        } else if (g >= 2) {
-          // P buffer st is free once O += P(g - 2) V is complete
-          if (!ptx::mbar_wait(&p_free[st], (uint32_t)(((g - 2) >> 1) & 1))) {
-            ok = false;
-            break;
-          }
-          tc::fence_after();
         }
         m = m_new;
         const float nb = m == -INFINITY ? 0.f : -m;
-        // P = 2^(s * c - m) as 16-bit pairs into tensor memory
+        // P_half = 2^(s c - m) as 16-bit pairs, over the S columns just read
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < KH; j += 2) {
@@ -735,48 +724,61 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           l += p0 + p1;
           pk[j / 2] = ptx::pack2<DT>(p0, p1);
         }
-        tc::st32(tmem + C::kColP + st * 64 + lane_off + half * 32, pk);
+        tc::st32(tS, pk);
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&p_full[st]);
+        if (lane == 0) ptx::mbar_arrive(&p_full[2 * st + half]);
       }
       if (!ok) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
-      // epilogue: O / l (both halves' sums) to this row's partial slot
+      // epilogue: combine the halves' accumulators into this warp's output
+      // columns [half * D / 2, + D / 2), normalised, to the row's partial slot
       const int64_t glast = gb + x.nkb - 1;
       if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
       tc::fence_after();
-      uint32_t ov[OH];
-      if constexpr (OH == 64) {
-        tc::ld64(tOh, ov);
-      } else {
-        tc::ld32(tOh, ov);
+      xchg[half * 256 + r] = m;
+      xchg[half * 256 + 128 + r] = l;
+      pair_sync();
+      const float m_o = xchg[(half ^ 1) * 256 + r], l_o = xchg[(half ^ 1) * 256 + 128 + r];
+      pair_sync();
+      const float m0 = half == 0 ? m : m_o, m1 = half == 0 ? m_o : m;
+      const float l0 = half == 0 ? l : l_o, l1 = half == 0 ? l_o : l;
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
+      const float lt = l0 * w0 + l1 * w1;
+      const float inv = 1.f / lt;
+      const float s0 = w0 * inv, s1 = w1 * inv;
+      const uint32_t tO0 = tmem + C::kColO + lane_off + half * OH;
+      const uint32_t tO1 = tO0 + D;
+      uint32_t pk[OH / 2];
+#pragma unroll
+      for (int q = 0; q < OH / 32; ++q) {
+        uint32_t o0[32], o1[32];
+        tc::ld32(tO0 + q * 32, o0);
+        tc::ld32(tO1 + q * 32, o1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[q * 16 + j] = ptx::pack2<DT>(
+              __uint_as_float(o0[2 * j]) * s0 + __uint_as_float(o1[2 * j]) * s1,
+              __uint_as_float(o0[2 * j + 1]) * s0 + __uint_as_float(o1[2 * j + 1]) * s1);
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(o_free);
-      xchg[half * 128 + r] = l;
-      pair_sync();
-      const float lt = l + xchg[(half ^ 1) * 128 + r];
-      pair_sync();
-      const float inv = 1.f / lt;
       if (qrow >= 0) {
         const int64_t slot = qrow * (a.topk + 1) + rank;
         uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
-        uint32_t pk[OH / 2];
-#pragma unroll
-        for (int j = 0; j < OH / 2; ++j)
-          pk[j] = ptx::pack2<DT>(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
 #pragma unroll
         for (int j = 0; j < OH / 16; ++j)
           ptx::st_global_v8(dst + 16 * j, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3], pk[8 * j + 4],
                             pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
-        if (half == 0) a.pml[slot] = make_float2(m, lt);
+        if (half == 0) a.pml[slot] = make_float2(M, lt);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
