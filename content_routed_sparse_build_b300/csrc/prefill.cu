@@ -794,8 +794,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 // One warp per row of Q: its used spans (sel order) then its local span.
 // The partials of a row are read in batches of kMergeBatch slots with all of
 // a batch's loads in flight at once (one memory round trip per batch; one
-// batch covers topk <= 23).
-constexpr int kMergeBatch = 24;
+// batch covers topk <= 16).
+constexpr int kMergeBatch = 17;
 
 template <int DT, int E>
 __device__ __forceinline__ void widen_partial(const uint16_t* src, float (&v)[E]) {
@@ -833,15 +833,18 @@ __device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const
   const int64_t i = row % a.n_q;
   const int64_t ell = (a.q_pos0 + i) / a.S;
   const int32_t* srow = sel + row * a.topk;
+  // the sel row and the partials are loaded together: every slot of the row
+  // (ranks 0 .. topk, the local span last) is read whether used or not, and
+  // only the used ones (the sel row's valid prefix, then the local span) are
+  // combined, in rank order
   const int j0 = lane < a.topk ? srow[lane] : -1;
   const int j1 = lane + 32 < a.topk ? srow[lane + 32] : -1;
-  bool bad;
-  const int used = warp_sel_prefix(j0, j1, lane, a.topk, ell, &bad);
-  const int nslot = used + 1;
+  const int nslot = a.topk + 1;
+  const int64_t base = row * (a.topk + 1);
   float M = -INFINITY, Ls = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const int64_t base = row * (a.topk + 1);
+  int used = -1;
   for (int s0 = 0; s0 < nslot; s0 += kMergeBatch) {
     float2 ml[kMergeBatch];
     uint2 raw[kMergeBatch];
@@ -849,21 +852,23 @@ __device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const
     for (int u = 0; u < kMergeBatch; ++u) {
       const int s = s0 + u;
       if (s < nslot) {
-        const int rk = s < used ? s : a.topk;
-        ml[u] = a.pml[base + rk];
-        const uint16_t* src = a.po + (base + rk) * D + lane * E;
+        ml[u] = a.pml[base + s];
+        const uint16_t* src = a.po + (base + s) * D + lane * E;
         if constexpr (E == 4) {
           raw[u] = *reinterpret_cast<const uint2*>(src);
         } else {
           raw[u] = make_uint2(*reinterpret_cast<const uint32_t*>(src), 0u);
         }
-      } else {
-        ml[u] = make_float2(-INFINITY, 0.f);
       }
+    }
+    if (used < 0) {
+      bool bad;
+      used = warp_sel_prefix(j0, j1, lane, a.topk, ell, &bad);
     }
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      if (s0 + u >= nslot) continue;
+      const int s = s0 + u;
+      if (s >= nslot || (s < a.topk && s >= used)) continue;
       float v[E];
       widen_partial<DT, E>(reinterpret_cast<const uint16_t*>(&raw[u]), v);
       const float Mn = fmaxf(M, ml[u].x);
@@ -881,7 +886,7 @@ __device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const
 }
 
 template <int DT, int D>
-__global__ void __launch_bounds__(256) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
+__global__ void __launch_bounds__(256, 2) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
                                                             void* __restrict__ O, float* __restrict__ lse) {
   const int lane = threadIdx.x & 31;
   ptx::pdl_wait();

@@ -27,6 +27,9 @@ PREFILL_CASES = [
                n_q=1076, q_pos0=1024, chunk=512, lowrank=4, seed=12),
     W.Workload("case_prefill_bf16_g16", "prefill", 1, 16, 1, 128, 2048, 256, 3, BF16,
                n_q=600, q_pos0=1448, chunk=600, needles=2, seed=13),
+    # k above the tensor-core router's 16 and above one merge batch of slots
+    W.Workload("case_prefill_bf16_k20", "prefill", 1, 8, 2, 128, 4096, 64, 20, BF16,
+               n_q=1024, q_pos0=3072, chunk=512, needles=2, seed=14),
 ]
 
 DECODE_CASES = [
