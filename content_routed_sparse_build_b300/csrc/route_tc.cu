@@ -15,7 +15,7 @@
 //  split   one pass over the candidate summaries into the workspace
 //  route   one CTA per tile of 128 (query, head) rows of one kv-head
 //          (128 / g queries x g heads): Q rows gathered into a swizzled
-//          K-major tile, 128-span blocks of the three planes stream through
+//          K-major tile, 32-span blocks of the three planes stream through
 //          a 2-stage TMA ring, one thread issues S = sum_p Q S_p^T into
 //          tensor memory (double buffered), and four warps (one row per
 //          thread) fold each block into a register list of the row's k best
@@ -29,15 +29,16 @@ namespace ssa {
 namespace {
 
 constexpr int kRows = 128;    // (query, head) rows per tile
-constexpr int kBlk = 128;     // candidate spans per block
+constexpr int kBlk = 32;      // candidate spans per block (small, so that two CTAs fit an SM)
 constexpr int kRouteThreads = 192;  // warps 0-3 select, 4 TMA, 5 MMA
 constexpr int kMaxTopK = 16;  // register list size; larger k uses the fp32 tile router
 
 template <int D>
 struct RCfg {
-  static constexpr int kRegion = 128 * 128;           // 128 rows x 128 bytes
+  static constexpr int kRegion = 128 * 128;           // Q: 128 rows x 128 bytes
+  static constexpr int kRegionB = kBlk * 128;          // summaries: kBlk rows x 128 bytes
   static constexpr int kQBytes = (D / 64) * kRegion;
-  static constexpr int kPlane = (D / 64) * kRegion;    // one plane of a block
+  static constexpr int kPlane = (D / 64) * kRegionB;   // one plane of a block
   static constexpr int kStage = 3 * kPlane;
   static constexpr size_t kSmem = 1024 + (size_t)kQBytes + 2 * kStage + 256;
 };
@@ -132,7 +133,7 @@ __device__ __forceinline__ float pick32(const uint32_t (&r)[32], int p) {
 }
 
 template <int DT, int D>
-__global__ void __launch_bounds__(kRouteThreads, 1)
+__global__ void __launch_bounds__(kRouteThreads, 2)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmP, const void* __restrict__ Q, int32_t* __restrict__ sel,
                     float* __restrict__ sel_score, int Hq, int Hkv, int64_t n_q, int64_t q_pos0, int S, int topk,
                     uint32_t* __restrict__ err) {
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     *abort = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) tc::alloc(tmem_base, 256);
+  if (warp == 5) tc::alloc(tmem_base, 2 * kBlk);
   if (warp == 4 && lane == 0) ptx::prefetch_tmap(&tmP);
   tc::fence_before();
   __syncthreads();
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         for (int p = 0; p < 3; ++p)
 #pragma unroll
           for (int r = 0; r < D / 64; ++r)
-            ptx::tma_load_3d(dst + p * C::kPlane + r * C::kRegion, &tmP, &b_full[st], r * 64, blk * kBlk,
+            ptx::tma_load_3d(dst + p * C::kPlane + r * C::kRegionB, &tmP, &b_full[st], r * 64, blk * kBlk,
                              bh * 3 + p);
       }
     }
@@ -211,14 +212,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         if (ok && blk >= 2) ok = ptx::mbar_wait(&s_free[st], (uint32_t)(((blk - 2) >> 1) & 1));
         if (!ok) break;
         tc::fence_after();
-        const uint32_t dS = tmem + st * 128;
+        const uint32_t dS = tmem + st * kBlk;
         int step = 0;
 #pragma unroll
         for (int p = 0; p < 3; ++p)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k, ++step) {
             const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(aB + st * C::kStage + p * C::kPlane + (k >> 2) * C::kRegion +
+            const uint64_t bd = tc::sdesc_sw128(aB + st * C::kStage + p * C::kPlane + (k >> 2) * C::kRegionB +
                                                     (k & 3) * 32,
                                                 16, 1024);
             tc::mma(dS, qd, bd, id, step > 0 ? 1u : 0u);
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 #pragma unroll 1
       for (int q = 0; q < kBlk / 32; ++q) {
         uint32_t rr[32];
-        tc::ld32(tmem + st * 128 + lane_off + q * 32, rr);
+        tc::ld32(tmem + st * kBlk + lane_off + q * 32, rr);
         if (q == kBlk / 32 - 1) {
           tc::fence_before();
           __syncwarp();
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 5) tc::dealloc(tmem, 256);
+  if (warp == 5) tc::dealloc(tmem, 2 * kBlk);
 }
 
 template <int DT, int D>
