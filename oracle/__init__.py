@@ -56,6 +56,8 @@ def _load():
         lib.oracle_summaries.argtypes = [I, P, I, I, I64, I64, I, I, I64, I64, P, I64]
         lib.oracle_route.restype = I
         lib.oracle_route.argtypes = [I, P, I, I, I, I64, I64, I, I, I, P, I64, P, I64, P, P, P]
+        lib.oracle_route_group.restype = I
+        lib.oracle_route_group.argtypes = [I, P, I, I, I, I64, I64, I, I, I, P, I64, P, I64, P, P, P]
         lib.oracle_attend.restype = I
         lib.oracle_attend.argtypes = [I, P, P, P, I, I, I, I64, I64, I64, I, I, I, D, P, P, I64,
                                       P, P, P]
@@ -119,6 +121,31 @@ def route(Q: torch.Tensor, q_pos0: int, summ: np.ndarray, Hkv: int, S: int, topk
                               sc.ctypes.data if sc is not None else None)
     if rc != 0:
         raise ValueError("oracle_route: a candidate span has no summary")
+    return (sel, margin, sc) if want_scores else (sel, margin)
+
+
+def route_group(Q: torch.Tensor, q_pos0: int, summ: np.ndarray, Hkv: int, S: int, topk: int,
+                rows: np.ndarray | None = None, want_scores: bool = False):
+    """Group-shared selections for Q [B, Hq, n_q, d]: one per (b, kv-head,
+    query), scored by the sum of the group's heads' scores, repeated on every
+    head row of the group.  Returns as route()."""
+    _host(Q)
+    B, Hq, n_q, d = Q.shape
+    ns_cap = summ.shape[2]
+    summ = np.ascontiguousarray(summ, dtype=np.float64)
+    rp, nr = None, 0
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        rp, nr = rows.ctypes.data, len(rows)
+    n = nr if rows is not None else B * Hq * n_q
+    sel = np.zeros((n, topk), np.int32)
+    margin = np.zeros(n, np.float64)
+    sc = np.zeros((n, topk), np.float64) if want_scores else None
+    rc = _load().oracle_route_group(_DT[Q.dtype], Q.data_ptr(), B, Hq, Hkv, n_q, q_pos0, d, S, topk,
+                                    summ.ctypes.data, ns_cap, rp, nr, sel.ctypes.data,
+                                    margin.ctypes.data, sc.ctypes.data if sc is not None else None)
+    if rc != 0:
+        raise ValueError("oracle_route_group: a candidate span has no summary")
     return (sel, margin, sc) if want_scores else (sel, margin)
 
 

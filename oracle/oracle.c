@@ -173,6 +173,64 @@ int oracle_route(int dtype, const void* Q, int B, int Hq, int Hkv, int64_t n_q, 
 }
 
 /*
+ * Group-shared selection (GQA): one selection per (b, kv-head, query), which
+ * every query head of the group then uses.  The pages leave the router open;
+ * this variant scores span j by the sum of the group's query heads' scores,
+ *   score_j = sum over the g heads hh of kv-head h / g of q_hh . summary_j,
+ * and keeps the top k under the same order (score desc, j asc) over the
+ * same candidates as oracle_route.  Row convention and outputs as for
+ * oracle_route: every head row of a group gets the group's selection.
+ */
+int oracle_route_group(int dtype, const void* Q, int B, int Hq, int Hkv, int64_t n_q, int64_t q_pos0,
+                       int d, int S, int topk, const double* summ, int64_t ns_cap, const int64_t* rows,
+                       int64_t n_rows, int32_t* sel, double* margin, double* sel_score) {
+  int g = Hq / Hkv;
+  int64_t n = rows ? n_rows : (int64_t)B * Hq * n_q;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t o = 0; o < n; ++o) {
+    int64_t r = rows ? rows[o] : o;
+    int64_t b, h, i;
+    row_coords(r, Hq, n_q, &b, &h, &i);
+    int64_t t = q_pos0 + i;
+    int64_t l = t / S;
+    if (l > ns_cap) {
+      bad = 1;
+      continue;
+    }
+    int64_t grp = h / g;
+    int64_t kvh = b * Hkv + grp;
+    cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(l > 0 ? l : 1));
+    for (int64_t j = 0; j < l; ++j) {
+      double acc = 0.0;
+      for (int64_t hh = grp * g; hh < grp * g + g; ++hh) {
+        const int64_t qoff = ((b * Hq + hh) * n_q + i) * d;
+        for (int x = 0; x < d; ++x) acc += load_f64(dtype, Q, qoff + x) * summ[(kvh * ns_cap + j) * d + x];
+      }
+      c[j].score = acc;
+      c[j].j = (int32_t)j;
+    }
+    qsort(c, (size_t)l, sizeof(cand_t), cand_order);
+    int64_t nsel = l < topk ? l : topk;
+    int32_t* out = sel + o * topk;
+    for (int64_t s = 0; s < nsel; ++s) out[s] = c[s].j;
+    qsort(out, (size_t)nsel, sizeof(int32_t), int_ascending);
+    for (int64_t s = nsel; s < topk; ++s) out[s] = -1;
+    if (sel_score) {
+      for (int64_t s = 0; s < topk; ++s) {
+        double v = NAN;
+        for (int64_t u = 0; u < nsel; ++u)
+          if (c[u].j == out[s]) v = c[u].score;
+        sel_score[o * topk + s] = v;
+      }
+    }
+    if (margin) margin[o] = l > topk ? c[topk - 1].score - c[topk].score : INFINITY;
+    free(c);
+  }
+  return bad ? -1 : 0;
+}
+
+/*
  * Steps 6-7 for the rows of Q (same row convention as oracle_route).
  *   K, V [B, Hkv, L_cap, d]; sel [n, topk] as produced by step 5
  *   O    [n, d] double; lse [n] double; wsum [n] double (nullable): the sum

@@ -26,6 +26,8 @@ MUTANTS = {
     "own_token_dropped": ("for (int64_t tau = l * S; tau <= t; ++tau)", "for (int64_t tau = l * S; tau < t; ++tau)"),
     "scale_dropped": ("x[u] = scale * acc;", "x[u] = acc;"),
     "max_not_subtracted_in_lse": ("lse[o] = mx + log(denom);", "lse[o] = log(denom);"),
+    "group_sum_first_head_only": ("for (int64_t hh = grp * g; hh < grp * g + g; ++hh) {",
+                                  "for (int64_t hh = grp * g; hh < grp * g + 1; ++hh) {"),
     "values_from_keys": ("load_f64(dtype, V, (kvh * L_cap + tok[u]) * d + c)",
                          "load_f64(dtype, K, (kvh * L_cap + tok[u]) * d + c)"),
 }

@@ -139,6 +139,60 @@ def test_route_probe_selects_every_needle():
                 assert set(inp.needle_spans[bh].tolist()) <= got
 
 
+# ---------------------------------------------------------------- group-shared route
+@pytest.mark.parametrize("Hq,Hkv,S,topk", [(4, 2, 4, 3), (8, 2, 8, 2), (6, 3, 4, 5)])
+def test_route_group_equals_full_sort_of_summed_scores(Hq, Hkv, S, topk):
+    """Group selection = the first k of a full sort of the group's summed
+    scores (computed here from the summed queries, by linearity), and every
+    head of a group gets the same row."""
+    L, d = 64, 4
+    Q, K, _ = _int_inputs(2, Hq, Hkv, L, d, 11, lo=-2, hi=3)
+    summ = oracle.summaries(K, L, S)
+    sel, margin = oracle.route_group(Q, 0, summ, Hkv, S, topk)
+    g = Hq // Hkv
+    qsum = Q.double().numpy().reshape(2, Hkv, g, L, d).sum(axis=2)       # [B, Hkv, L, d]
+    sc = np.einsum("bhqc,bhjc->bhqj", qsum, summ)
+    ties_seen = 0
+    for b in range(2):
+        for h in range(Hq):
+            for t in range(L):
+                r = (b * Hq + h) * L + t
+                ell = t // S
+                s = sc[b, h // g, t, :ell]
+                order = np.lexsort((np.arange(ell), -s))
+                ref = sorted(order[: min(topk, ell)].tolist())
+                got = sel[r][sel[r] >= 0].tolist()
+                assert got == ref, (b, h, t)
+                h0 = (h // g) * g
+                assert (sel[r] == sel[(b * Hq + h0) * L + t]).all()
+                if ell > topk:
+                    ss = s[order]
+                    assert margin[r] == ss[topk - 1] - ss[topk]
+                    ties_seen += ss[topk - 1] == ss[topk]
+    assert ties_seen > 0
+
+
+def test_route_group_one_head_per_group_is_the_per_head_route():
+    L, d, S, topk = 96, 8, 8, 4
+    Q, K, _ = _int_inputs(1, 3, 3, L, d, 12)
+    summ = oracle.summaries(K, L, S)
+    a, ma = oracle.route_group(Q, 0, summ, 3, S, topk)
+    b, mb = oracle.route(Q, 0, summ, 3, S, topk)
+    assert np.array_equal(a, b) and np.array_equal(ma, mb)
+
+
+def test_route_group_probe_selects_every_needle():
+    w = W.TINY_PREFILL.with_(Hq=8, Hkv=2, needles=2)
+    inp = W.Inputs(w)
+    K = inp.k()
+    summ = oracle.summaries(K, w.L, w.S)
+    probe = inp.probe_q().reshape(w.B, w.Hq, 1, w.d).contiguous()
+    sel, _ = oracle.route_group(probe, w.last_pos, summ, w.Hkv, w.S, w.topk)
+    for h in range(w.Hq):
+        got = set(sel[h].tolist()) - {-1}
+        assert set(inp.needle_spans[h // w.g].tolist()) <= got
+
+
 def test_route_reports_missing_summary():
     Q = torch.zeros(1, 1, 1, 2)
     with pytest.raises(ValueError):
