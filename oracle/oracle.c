@@ -201,14 +201,14 @@ int oracle_route_group(int dtype, const void* Q, int B, int Hq, int Hkv, int64_t
     int64_t grp = h / g;
     int64_t kvh = b * Hkv + grp;
     cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(l > 0 ? l : 1));
-    for (int64_t j = 0; j < l; ++j) {
-      double acc = 0.0;
+    for (int64_t span = 0; span < l; ++span) {
+      double sum = 0.0;  /* over the group's heads and the dimensions */
       for (int64_t hh = grp * g; hh < grp * g + g; ++hh) {
         const int64_t qoff = ((b * Hq + hh) * n_q + i) * d;
-        for (int x = 0; x < d; ++x) acc += load_f64(dtype, Q, qoff + x) * summ[(kvh * ns_cap + j) * d + x];
+        for (int x = 0; x < d; ++x) sum += load_f64(dtype, Q, qoff + x) * summ[(kvh * ns_cap + span) * d + x];
       }
-      c[j].score = acc;
-      c[j].j = (int32_t)j;
+      c[span].score = sum;
+      c[span].j = (int32_t)span;
     }
     qsort(c, (size_t)l, sizeof(cand_t), cand_order);
     int64_t nsel = l < topk ? l : topk;

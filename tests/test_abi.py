@@ -95,3 +95,19 @@ def test_attend_and_summary_validation():
     assert L.ssa_build_summaries(ctypes.byref(p), FAKE, 5, 4, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
     assert L.ssa_build_summaries(ctypes.byref(p), None, 0, 4, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
     assert L.ssa_workspace_error(None, None, None) == ssa.SSA_ERR_WORKSPACE
+
+
+@needs_no_gpu
+def test_route_group_validation_and_workspace():
+    p = ssa.params(1, 32, 4, 128, 1 << 20, 1024, 16, torch.bfloat16)
+    n = ssa.ssa_workspace_size(p, 8192, ssa.SSA_OP_ROUTE_GROUP)
+    # header + the summed queries (fp32) + the group selections and scores
+    assert n >= 256 + 4 * 8192 * 128 * 4 + 2 * 4 * 8192 * 16 * 4
+    L = ssa.lib()
+    call = lambda p, ws=None, wsn=0, **kw: L.ssa_route_group(
+        ctypes.byref(p), kw.get("Q", FAKE), kw.get("n_q", 1), kw.get("pos", 0), FAKE, FAKE, None,
+        ws, wsn, None)
+    assert call(p) == ssa.SSA_ERR_WORKSPACE                       # missing workspace
+    assert call(p, ws=ctypes.c_void_p(4096), wsn=16) == ssa.SSA_ERR_WORKSPACE
+    assert call(p, Q=None) == ssa.SSA_ERR_INVALID_ARG
+    assert call(ssa.params(1, 8, 3, 128, 4096, 64, 8, 1)) == ssa.SSA_ERR_INVALID_ARG
