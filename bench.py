@@ -156,7 +156,7 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 # they were measured on.
 NCU_TRAFFIC = {
     "decode_1m": (2.204e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
-    "prefill_chunk_vs_1m": (3.838e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
+    "prefill_chunk_vs_1m": (3.835e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
 }
 
 
@@ -175,9 +175,10 @@ class DecodeBench:
     the cache.  A step routes one query token per head and attends it; the
     256 steps are captured once in a CUDA graph and replayed."""
 
-    def __init__(self, w: W.Workload, dev):
+    def __init__(self, w: W.Workload, dev, group: bool = False):
         self.w = w
         self.dev = dev
+        self.group = group                                     # group-shared selection
         self.inp = W.Inputs(w)
         self.K = self.inp.k(dev)
         self.V = self.inp.v(dev)
@@ -185,6 +186,7 @@ class DecodeBench:
         self.p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
         self.summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
         self.ws = ssa.workspace(self.p, 1, ssa.SSA_OP_DECODE, dev)
+        self.wsg = ssa.workspace(self.p, 1, ssa.SSA_OP_ROUTE_GROUP, dev) if group else None
         self.sels = [torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
                      for _ in range(w.n_q)]
         self.sel = self.sels[0]
@@ -196,7 +198,11 @@ class DecodeBench:
         ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
 
     def route(self, i):
-        ssa.ssa_route(self.p, self.qs[i], 1, self.w.q_pos0 + i, self.summ, self.sels[i])
+        if self.group:
+            ssa.ssa_route_group(self.p, self.qs[i], 1, self.w.q_pos0 + i, self.summ, self.sels[i], None,
+                                self.wsg)
+        else:
+            ssa.ssa_route(self.p, self.qs[i], 1, self.w.q_pos0 + i, self.summ, self.sels[i])
 
     def attend(self, i):
         ssa.ssa_attend_decode(self.p, self.qs[i], self.w.q_pos0 + i, self.K, self.V, self.sels[i],
@@ -324,6 +330,37 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     if cpu_leg:
         res["cpu_baseline"] = cpu_baseline_decode(db)
     return res, db
+
+
+def bench_decode_group(w, dev, steps, ws_n):
+    """The same decode workload with group-shared selection (one top-k per
+    kv-head group): each group's heads attend the same k spans, so a step
+    streams k spans plus the local span per kv-head."""
+    db = DecodeBench(w, dev, group=True)
+    st = torch.cuda.current_stream(dev)
+    db.build_summaries()
+    per_q = db.algorithmic_bytes()
+    n = w.n_q
+    reps = max(1, steps // n)
+    g_step = db.graph(db.step, n)
+    g_att = db.graph(db.attend, n)
+    g_step.replay()
+    g_att.replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
+    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
+    err = ssa.ssa_workspace_error(db.ws) | ssa.ssa_workspace_error(db.wsg)
+    attend_bytes = sum(a for a, _ in per_q) / n
+    pk = peaks()
+    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
+    return {"workload": w.name, "routing": "group-shared (one top-k per kv-head group)",
+            "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
+            "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": pk["source"]},
+            "device_error_bits": err}
 
 
 def bench_decode_e2e(db: DecodeBench, steps: int):
@@ -521,6 +558,8 @@ def main():
     ap.add_argument("--prefill-chunk", type=int, default=None,
                     help="queries of the prefill chunk (profiling runs on a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-group", action="store_true",
+                    help="skip the decode line with group-shared selection")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
@@ -548,6 +587,11 @@ def main():
         del db
     torch.cuda.empty_cache()
     pre = None
+    grp = None
+    if not args.no_decode and not args.no_group:
+        torch.cuda.empty_cache()
+        grp = bench_decode_group(w, dev, min(steps, 4096), ws_n)
+        torch.cuda.empty_cache()
     if not args.no_prefill:
         wp = W.PREFILL_1M
         if args.prefill_L or args.prefill_chunk:
@@ -574,6 +618,8 @@ def main():
                                                "timing")},
     }
     line["gpu_launches"] = steps * launches_per_decode_step(w)
+    if grp is not None:
+        line["decode_group_shared"] = grp
     if pre is not None:
         line["prefill"] = pre
     if "cpu_baseline" in dec:

@@ -9,6 +9,7 @@ the library cannot be built or loaded, importing it raises.
 Entry points (same names as the C ABI):
   ssa_build_summaries  span means of the keys
   ssa_route            span scores + top-k selection
+  ssa_route_group      one top-k per kv-head group (summed scores of its heads)
   ssa_attend_decode    one query per head, split over spans, LSE merge
   ssa_attend_prefill   a chunk of queries, span-major tiles, LSE merge
   ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
@@ -31,7 +32,7 @@ SSA_ERR_CUDA = 4
 SSA_ERR_DEVICE = 5
 
 SSA_F32, SSA_BF16, SSA_F16 = 0, 1, 2
-SSA_OP_ROUTE, SSA_OP_DECODE, SSA_OP_PREFILL = 0, 1, 2
+SSA_OP_ROUTE, SSA_OP_DECODE, SSA_OP_PREFILL, SSA_OP_ROUTE_GROUP = 0, 1, 2, 3
 SSA_DEVERR_BAD_SELECTION = 0x1
 SSA_DEVERR_WAIT_TIMEOUT = 0x2
 SSA_DEVERR_OVERFLOW = 0x4
@@ -73,6 +74,7 @@ def lib() -> ctypes.CDLL:
         PP = ctypes.POINTER(ssa_params)
         L.ssa_build_summaries.argtypes = [PP, _P, _I64, _I64, _P, _P]
         L.ssa_route.argtypes = [PP, _P, _I64, _I64, _P, _P, _P, _P, _SZ, _P]
+        L.ssa_route_group.argtypes = [PP, _P, _I64, _I64, _P, _P, _P, _P, _SZ, _P]
         L.ssa_attend_decode.argtypes = [PP, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.ssa_attend_prefill.argtypes = [PP, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.ssa_workspace_size.argtypes = [PP, _I64, ctypes.c_int]
@@ -81,8 +83,8 @@ def lib() -> ctypes.CDLL:
         L.ssa_status_string.argtypes = [ctypes.c_int]
         L.ssa_status_string.restype = ctypes.c_char_p
         L.ssa_version.restype = ctypes.c_int
-        for name in ("ssa_build_summaries", "ssa_route", "ssa_attend_decode", "ssa_attend_prefill",
-                     "ssa_workspace_error"):
+        for name in ("ssa_build_summaries", "ssa_route", "ssa_route_group", "ssa_attend_decode",
+                     "ssa_attend_prefill", "ssa_workspace_error"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -149,6 +151,15 @@ def ssa_route(p: ssa_params, Q: torch.Tensor, n_q: int, q_pos0: int, summ: torch
     rc = lib().ssa_route(ctypes.byref(p), _ptr(Q), int(n_q), int(q_pos0), _ptr(summ), _ptr(sel),
                          _ptr(sel_score), wp, wn, _stream(stream))
     _check(rc, "ssa_route")
+
+
+def ssa_route_group(p: ssa_params, Q: torch.Tensor, n_q: int, q_pos0: int, summ: torch.Tensor,
+                    sel: torch.Tensor, sel_score: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None, stream=None) -> None:
+    wp, wn = _ws_args(ws)
+    rc = lib().ssa_route_group(ctypes.byref(p), _ptr(Q), int(n_q), int(q_pos0), _ptr(summ), _ptr(sel),
+                               _ptr(sel_score), wp, wn, _stream(stream))
+    _check(rc, "ssa_route_group")
 
 
 def ssa_attend_decode(p: ssa_params, Q: torch.Tensor, pos: int, K: torch.Tensor, V: torch.Tensor,

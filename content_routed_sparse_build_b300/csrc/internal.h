@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include <utility>
 
 #include "common.cuh"
@@ -75,6 +77,9 @@ cudaError_t launch_route(const Problem& pr, const void* Q, int64_t n_q, int64_t 
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st);
 bool route_tc_supported(const Problem& pr, int64_t n_q);
 size_t route_tc_ws_bytes(const Problem& pr);
+size_t route_group_ws_bytes(const Problem& pr, int64_t n_q);
+cudaError_t launch_route_group(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0, const float* summ,
+                               int32_t* sel, float* sel_score, void* ws, cudaStream_t st);
 cudaError_t launch_route_tc(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                             const float* summ, int32_t* sel, float* sel_score, void* ws,
                             cudaStream_t st);

@@ -58,6 +58,7 @@ size_t ws_need(const Problem& pr, int64_t n_q, int op) {
   if (op == SSA_OP_DECODE)
     return kWsHeader + (decode_fast_supported(pr) ? decode_ws_bytes(pr) : 0);
   if (op == SSA_OP_PREFILL) return kWsHeader + (prefill_fast(pr, n_q) ? prefill_ws_bytes(pr, n_q) : 0);
+  if (op == SSA_OP_ROUTE_GROUP) return kWsHeader + route_group_ws_bytes(pr, n_q);
   return 0;
 }
 
@@ -118,6 +119,19 @@ int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0, c
   if (route_tc_supported(pr, n_q))
     return cuda_status(launch_route_tc(pr, Q, n_q, q_pos0, summ, sel, sel_score, ws, st));
   return cuda_status(launch_route(pr, Q, n_q, q_pos0, summ, sel, sel_score, st));
+}
+
+int ssa_route_group(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0, const float* summ,
+                    int32_t* sel, float* sel_score, void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (n_q < 0 || q_pos0 < 0 || q_pos0 + n_q > pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !summ || !sel || !aligned16(Q) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, n_q, SSA_OP_ROUTE_GROUP, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  return cuda_status(launch_route_group(pr, Q, n_q, q_pos0, summ, sel, sel_score, ws,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, const void* K, const void* V,

@@ -74,7 +74,7 @@ typedef enum {
 typedef enum { SSA_F32 = 0, SSA_BF16 = 1, SSA_F16 = 2 } ssa_dtype;
 
 /* Operation selector of ssa_workspace_size. */
-typedef enum { SSA_OP_ROUTE = 0, SSA_OP_DECODE = 1, SSA_OP_PREFILL = 2 } ssa_op;
+typedef enum { SSA_OP_ROUTE = 0, SSA_OP_DECODE = 1, SSA_OP_PREFILL = 2, SSA_OP_ROUTE_GROUP = 3 } ssa_op;
 
 /* Bits of the device error record (first uint32 of a workspace). */
 #define SSA_DEVERR_BAD_SELECTION 0x1u /* sel entry not in -1 .. l-1, not ascending, or repeated */
@@ -124,6 +124,26 @@ SSA_API int ssa_build_summaries(const ssa_params* p, const void* K, int64_t span
 SSA_API int ssa_route(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
               const float* summ, int32_t* sel, float* sel_score, void* ws, size_t ws_bytes,
               void* stream);
+
+/*
+ * Group-shared routing for grouped-query attention: one selection per
+ * (b, kv-head, query), used by all g = Hq / Hkv query heads of the group.
+ * The pages leave the router open (superlinear post, key-idea section: each
+ * query keeps the top k of the candidate spans); this variant scores span j
+ * of kv-head h for the group as score_j = sum over its query heads hq of
+ * q_hq . summ[b, h, j, :] (fp32), keeps the k best under (score desc, j asc)
+ * over the same candidates (the complete spans before the query's own), and
+ * writes that row to sel[b, hq, i, :] for every head hq of the group (and
+ * the scores to sel_score when not NULL).  Arguments, layouts and
+ * requirements as for ssa_route; ws must hold
+ * ssa_workspace_size(p, n_q, SSA_OP_ROUTE_GROUP) bytes.  The selections then
+ * go to ssa_attend_decode / ssa_attend_prefill unchanged; with all heads of
+ * a group on the same spans, decode streams k spans plus the local span per
+ * kv-head.
+ */
+SSA_API int ssa_route_group(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
+                            const float* summ, int32_t* sel, float* sel_score, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /*
  * Decode attention for one query per head at position `pos` (superlinear
