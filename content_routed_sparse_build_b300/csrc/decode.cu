@@ -10,11 +10,11 @@
 //  plan    one CTA per (b, kv-head): validates the g heads' selections and
 //          builds their union U (ascending, local span last) with, per span,
 //          the mask of heads that chose it and each head's rank for it.
-//  attend  persistent, one CTA per SM, four independent warps.  Work items
+//  attend  persistent, one CTA per SM, six independent warps.  Work items
 //          are (group, span of U, chunk of CH tokens), handed out by an
-//          atomic counter.  Each warp runs its own ring of 32-token K / V
-//          tiles loaded by TMA (128-byte swizzle, mbarrier completion),
-//          issuing STAGES tiles ahead of the one it computes.  The MMAs are
+//          atomic counter.  Each warp runs its own two-stage ring of 32-token
+//          K / V tiles loaded by TMA (128-byte swizzle, mbarrier completion),
+//          each tile computed as two 16-token fragments.  The MMAs are
 //          transposed so that the query group fits the n8 side of
 //          mma.sync: S^T = K Q^T (tokens x heads) and O^T += V^T P^T
 //          (d x heads), P^T turned into the B operand by movmatrix.  An
@@ -30,8 +30,9 @@
 namespace ssa {
 namespace {
 
-constexpr int kTile = 16;     // tokens per ring stage
-constexpr int kWarps = 8;     // independent warps per CTA
+constexpr int kTile = 32;     // tokens per ring stage
+constexpr int kSub = kTile / 16;  // m16 fragments per tile
+constexpr int kWarps = 6;     // independent warps per CTA (6 x 2 stages x 16 KB of K / V ring)
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxG = 16;
 constexpr int kMaxK = 64;
@@ -64,7 +65,7 @@ struct Cfg {
   static constexpr int kBox = kTile * 128;         // bytes per box
   static constexpr int kHalf = kBoxes * kBox;      // K (or V) bytes per stage
   static constexpr int kStage = 2 * kHalf;
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQStride = D + 8;           // 16-bit elements per Q row in shared memory
   static constexpr size_t kRing = (size_t)kWarps * kStages * kStage;
   static constexpr size_t kBars = (size_t)kWarps * kStages * 8;
@@ -462,39 +463,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aK = ptx::smem_u32(wring + (size_t)stage * C::kStage);
     const uint32_t aV = aK + C::kHalf;
 
-    // S^T (16 tokens x 8 heads per group): A = K tile rows, B = Q^T
-    float s[NG][4];
+    // S^T (kTile tokens x 8 heads per group), one m16 fragment per 16 tokens:
+    // A = K tile rows, B = Q^T
+    float s[NG][kSub][4];
 #pragma unroll
-    for (int ng = 0; ng < NG; ++ng) s[ng][0] = s[ng][1] = s[ng][2] = s[ng][3] = 0.f;
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) s[ng][t][0] = s[ng][t][1] = s[ng][t][2] = s[ng][t][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const int row = (mi & 1) * 8 + rr;
-      const int chunk = 2 * (kk & 3) + (mi >> 1);
-      uint32_t a[4];
-      ptx::ldsm_x4(aK + (kk >> 2) * C::kBox + ptx::sw128(row, chunk), a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(s[ng], a, qb[ng][kk][0], qb[ng][kk][1]);
+      for (int t = 0; t < kSub; ++t) {
+        const int row = t * 16 + (mi & 1) * 8 + rr;
+        const int chunk = 2 * (kk & 3) + (mi >> 1);
+        uint32_t a[4];
+        ptx::ldsm_x4(aK + (kk >> 2) * C::kBox + ptx::sw128(row, chunk), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(s[ng][t], a, qb[ng][kk][0], qb[ng][kk][1]);
+      }
     }
     // mask tokens outside the item (partial tiles only)
     const int64_t tbase = cur.t0 + (int64_t)mt.w * kTile;
     if (tbase + kTile > cur.t1) {
-      const bool v0 = tbase + r8 < cur.t1, v1 = tbase + r8 + 8 < cur.t1;
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) {
-        if (!v0) s[ng][0] = s[ng][1] = -INFINITY;
-        if (!v1) s[ng][2] = s[ng][3] = -INFINITY;
+      for (int t = 0; t < kSub; ++t) {
+        const bool v0 = tbase + t * 16 + r8 < cur.t1, v1 = tbase + t * 16 + r8 + 8 < cur.t1;
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          if (!v0) s[ng][t][0] = s[ng][t][1] = -INFINITY;
+          if (!v1) s[ng][t][2] = s[ng][t][3] = -INFINITY;
+        }
       }
     }
-    // online softmax per head (column): reduce over the 16 tokens = the
-    // lane's two rows and the eight lanes sharing q4
+    // online softmax per head (column): reduce over the tile's tokens = the
+    // lane's rows of every fragment and the eight lanes sharing q4
     const float c = geo.scale_log2e;
-    uint32_t pb[NG][2];
+    uint32_t pb[NG][kSub][2];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
       float mx[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        float v = fmaxf(s[ng][i], s[ng][i + 2]) * c;
+        float v = fmaxf(s[ng][0][i], s[ng][0][i + 2]);
+#pragma unroll
+        for (int t = 1; t < kSub; ++t) v = fmaxf(v, fmaxf(s[ng][t][i], s[ng][t][i + 2]));
+        v *= c;
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
@@ -508,12 +521,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha[i] = exp2f(m[ng][i] - bse);
         m[ng][i] = mx[i];
       }
-      const float p0 = ptx::ex2(fmaf(s[ng][0], c, nb[0]));
-      const float p1 = ptx::ex2(fmaf(s[ng][1], c, nb[1]));
-      const float p2 = ptx::ex2(fmaf(s[ng][2], c, nb[0]));
-      const float p3 = ptx::ex2(fmaf(s[ng][3], c, nb[1]));
-      l[ng][0] = l[ng][0] * alpha[0] + (p0 + p2);
-      l[ng][1] = l[ng][1] * alpha[1] + (p1 + p3);
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
+        const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
+        const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
+        const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
+        ls0 += p0 + p2;
+        ls1 += p1 + p3;
+        // P^T rows (tokens) -> P rows (heads): the B operand of O^T += V^T P^T
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT>(p0, p1));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT>(p2, p3));
+      }
+      l[ng][0] = l[ng][0] * alpha[0] + ls0;
+      l[ng][1] = l[ng][1] * alpha[1] + ls1;
       if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
@@ -523,19 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[ng][mt2][3] *= alpha[1];
         }
       }
-      // P^T rows (tokens) -> P rows (heads): the B operand of O^T += V^T P^T
-      pb[ng][0] = ptx::movmatrix_trans(ptx::pack2<DT>(p0, p1));
-      pb[ng][1] = ptx::movmatrix_trans(ptx::pack2<DT>(p2, p3));
     }
-    // O^T (d x heads) += V^T (d x 16 tokens) P^T
+    // O^T (d x heads) += V^T (d x kTile tokens) P^T, one k16 step per fragment
 #pragma unroll
     for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-      const int row = (mi >> 1) * 8 + rr;
-      const int chunk = 2 * mt2 + (mi & 1);
-      uint32_t a[4];
-      ptx::ldsm_x4_t(aV + (chunk >> 3) * C::kBox + ptx::sw128(row, chunk & 7), a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(o[ng][mt2], a, pb[ng][0], pb[ng][1]);
+      for (int t = 0; t < kSub; ++t) {
+        const int row = t * 16 + (mi >> 1) * 8 + rr;
+        const int chunk = 2 * mt2 + (mi & 1);
+        uint32_t a[4];
+        ptx::ldsm_x4_t(aV + (chunk >> 3) * C::kBox + ptx::sw128(row, chunk & 7), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) ptx::mma16816<DT>(o[ng][mt2], a, pb[ng][t][0], pb[ng][t][1]);
+      }
     }
     __syncwarp();
     --inflight;
