@@ -17,6 +17,7 @@ replica of the workload; value = tokens of all ranks / max time over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -155,7 +156,7 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 # from.  They are reported as the roofline's "traffic" only for the workload
 # they were measured on.
 NCU_TRAFFIC = {
-    "decode_1m": (2.204e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
+    "decode_1m": (2.189e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
     "prefill_chunk_vs_1m": (3.835e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
 }
 
@@ -365,30 +366,53 @@ def bench_decode_group(w, dev, steps, ws_n):
 
 def bench_decode_e2e(db: DecodeBench, steps: int):
     """Same decode through the C ABI with host buffers: every step copies its
-    query in from pinned host memory and the output back, then waits for it."""
+    query in from pinned host memory, routes and attends it, copies the
+    output back and waits for it.  The calls go straight to the C ABI and to
+    the CUDA runtime's cudaMemcpyAsync (ctypes, arguments prepared once), so
+    the loop measures the library and the copies, not Python tensor calls."""
     w = db.w
     st = torch.cuda.current_stream(db.dev)
     el = db.Q.element_size()
-    q_host = db.Q.cpu().pin_memory()
+    nbytes = w.B * w.Hq * w.d * el
+    q_host = db.Q.cpu().pin_memory()                       # [steps, B, Hq, d]
     o_host = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype).pin_memory()
     q_dev = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=db.dev)
+    rt = ctypes.CDLL("libcudart.so.13")
+    rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                   ctypes.c_void_p]
+    rt.cudaStreamSynchronize.argtypes = [ctypes.c_void_p]
+    L = ssa.lib()
+    sp = ctypes.c_void_p(st.cuda_stream)
+    pp = ctypes.byref(db.p)
+    qd, od = ctypes.c_void_p(q_dev.data_ptr()), ctypes.c_void_p(db.O.data_ptr())
+    oh = ctypes.c_void_p(o_host.data_ptr())
+    summ, sel = ctypes.c_void_p(db.summ.data_ptr()), ctypes.c_void_p(db.sel.data_ptr())
+    K, V = ctypes.c_void_p(db.K.data_ptr()), ctypes.c_void_p(db.V.data_ptr())
+    ws, wsn = ctypes.c_void_p(db.ws.data_ptr()), db.ws.numel()
+    qh = [ctypes.c_void_p(q_host.data_ptr() + i * nbytes) for i in range(w.n_q)]
 
     def one(s):
         i = s % w.n_q
-        q_dev.copy_(q_host[i], non_blocking=True)
-        ssa.ssa_route(db.p, q_dev, 1, w.q_pos0 + i, db.summ, db.sel, None, None, st)
-        ssa.ssa_attend_decode(db.p, q_dev, w.q_pos0 + i, db.K, db.V, db.sel, db.O, None, db.ws, st)
-        o_host.copy_(db.O, non_blocking=True)
-        st.synchronize()
+        pos = w.q_pos0 + i
+        rc = rt.cudaMemcpyAsync(qd, qh[i], nbytes, 1, sp)
+        rc |= L.ssa_route(pp, qd, 1, pos, summ, sel, None, None, 0, sp)
+        rc |= L.ssa_attend_decode(pp, qd, pos, K, V, sel, od, None, ws, wsn, sp)
+        rc |= rt.cudaMemcpyAsync(oh, od, nbytes, 2, sp)
+        rc |= rt.cudaStreamSynchronize(sp)
+        return rc
 
     for s in range(8):
-        one(s)
+        if one(s):
+            raise RuntimeError("e2e decode step failed")
     t0 = time.perf_counter()
+    bad = 0
     for s in range(steps):
-        one(s)
+        bad |= one(s)
     dt = time.perf_counter() - t0
-    return {"value": steps / dt, "unit": "tok/s", "h2d_bytes_per_step": w.B * w.Hq * w.d * el,
-            "d2h_bytes_per_step": w.B * w.Hq * w.d * el, "steps": steps}
+    if bad:
+        raise RuntimeError("e2e decode step failed")
+    return {"value": steps / dt, "unit": "tok/s", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+            "steps": steps}
 
 
 def cpu_baseline_decode(db: DecodeBench, budget_s: float = 15.0):
