@@ -23,7 +23,7 @@ namespace {
 
 constexpr int kMaxG = 16;   // query heads per kv-head
 constexpr int kMaxK = 64;   // topk limit
-constexpr int kCluster = 8; // CTAs splitting one kv-head's candidates in decode
+constexpr int kCluster = 16; // CTAs splitting one kv-head's candidates in decode
 
 // Order-preserving 32-bit key of a finite score: a higher score has a
 // higher key; 0 is reserved for "no candidate".
@@ -126,7 +126,7 @@ __device__ __forceinline__ void fold_block(float* lsv, int* lsj, const float* sc
 // blocks of 256: two lanes per candidate, each summing one half of d with
 // all of its summary loads in flight at once, the two halves then added.
 // Each block is folded into per-head lists; finally CTA `rank` merges head
-// rank (+8) over the cluster's lists through distributed shared memory.
+// rank (+16) over the cluster's lists through distributed shared memory.
 constexpr int kBlk = 128;
 
 template <int DT, int D, int G, int NE>
@@ -213,7 +213,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
   }
 
   cluster.sync();
-  // final: CTA `rank` selects head rank (+8) from the cluster's lists, which
+  // final: CTA `rank` selects head rank (+16) from the cluster's lists, which
   // concatenated in rank order are ascending in span index
   if (warp == 0) {
     for (int h = rank; h < g; h += kCluster) {
@@ -399,6 +399,16 @@ template <int DT, int D, int G, int NE>
 cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
                                 int32_t* sel, float* sel_score, cudaStream_t st) {
   dim3 grid(kCluster, pr.Hkv, pr.B);
+  // a cluster of 16 is above the portable size of 8: the kernel opts in once per device
+  static bool attr_done[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, NE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
   return launch_pdl(route_decode_kernel<DT, D, G, NE>, grid, dim3(256), 0, st, Q, summ, sel,
                     sel_score, pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap);
 }
@@ -407,8 +417,8 @@ template <int DT, int D, int G>
 cudaError_t decode_route_ne(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
                             int32_t* sel, float* sel_score, cudaStream_t st) {
   // entries per lane of the final cluster merge: kCluster * topk / 32
-  if (pr.topk <= 16) return launch_decode_route<DT, D, G, 4>(pr, Q, q_pos0, summ, sel, sel_score, st);
-  return launch_decode_route<DT, D, G, 16>(pr, Q, q_pos0, summ, sel, sel_score, st);
+  if (pr.topk <= 16) return launch_decode_route<DT, D, G, 8>(pr, Q, q_pos0, summ, sel, sel_score, st);
+  return launch_decode_route<DT, D, G, 32>(pr, Q, q_pos0, summ, sel, sel_score, st);
 }
 
 template <int DT, int D>
