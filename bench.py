@@ -489,6 +489,61 @@ class PrefillBench:
         return float(4 * w.d * tokens.sum())
 
 
+def time_ms(fn, reps, warmup, stream, flush=None):
+    """Mean CUDA-event time of fn() over reps calls (L2 flushed before each when given)."""
+    for _ in range(warmup):
+        fn()
+    tot = 0.0
+    for _ in range(reps):
+        if flush is not None:
+            flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / reps
+
+
+def bench_dense_comparison(dev, flush, decode_step_ms, prefill_1m_ms):
+    """The pages' comparison point: dense attention over the whole context,
+    here PyTorch's scaled_dot_product_attention (a library call, used for this
+    measurement only; GQA native, bf16), on the same shapes as the routed
+    lines.  The dense prefill chunk attends every query to the whole cache
+    without a mask, so it also counts the chunk's own causal triangle (0.4%
+    of its work at 1M); the dense decode step attends the whole cache."""
+    import torch.nn.functional as F
+    st = torch.cuda.current_stream(dev)
+    out = {"dense": "torch scaled_dot_product_attention, enable_gqa, bf16, no mask"}
+    # decode at 1M: one query per head
+    w = W.DECODE_1M
+    inp = W.Inputs(w)
+    K, V = inp.k(dev), inp.v(dev)
+    q = inp.q(dev)[0].reshape(w.B, w.Hq, 1, w.d)
+    dense_dec = time_ms(lambda: F.scaled_dot_product_attention(q, K, V, enable_gqa=True), 20, 3, st, flush)
+    out["decode_1m"] = {"routed_ms_per_step": decode_step_ms, "dense_ms_per_step": dense_dec,
+                        "speedup": dense_dec / decode_step_ms if decode_step_ms else None}
+    # prefill chunk of 8192 queries against 1M
+    wp = W.PREFILL_1M
+    Qp = W.Inputs(wp.with_(needles=0)).q(dev)
+    dense_pre = time_ms(lambda: F.scaled_dot_product_attention(Qp, K, V, enable_gqa=True), 3, 1, st, flush)
+    out["prefill_1m"] = {"routed_ms_per_chunk": prefill_1m_ms, "dense_ms_per_chunk": dense_pre,
+                         "speedup": dense_pre / prefill_1m_ms if prefill_1m_ms else None}
+    del K, V, q, Qp
+    torch.cuda.empty_cache()
+    # prefill: the last 8192-query chunk of the 128K workload, routed and dense
+    w1 = W.PREFILL_128K.with_(n_q=8192, chunk=8192, q_pos0=W.PREFILL_128K.L - 8192)
+    pb = PrefillBench(w1, dev)
+    routed = time_ms(pb.step, 5, 2, st, flush)
+    dense = time_ms(lambda: F.scaled_dot_product_attention(pb.Q, pb.K, pb.V, enable_gqa=True), 5, 2, st, flush)
+    out["prefill_128k_last_chunk"] = {"routed_ms_per_chunk": routed, "dense_ms_per_chunk": dense,
+                                      "speedup": dense / routed}
+    del pb
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_prefill(w, dev, steps, warmup, ws_n, flush):
     pb = PrefillBench(w, dev)
     st = pb.stream
@@ -582,6 +637,8 @@ def main():
     ap.add_argument("--prefill-chunk", type=int, default=None,
                     help="queries of the prefill chunk (profiling runs on a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense-attention comparison (PyTorch SDPA on the same shapes)")
     ap.add_argument("--no-group", action="store_true",
                     help="skip the decode line with group-shared selection")
     args = ap.parse_args()
@@ -644,6 +701,11 @@ def main():
     line["gpu_launches"] = steps * launches_per_decode_step(w)
     if grp is not None:
         line["decode_group_shared"] = grp
+    if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1
+            and not (args.decode_L or args.prefill_L or args.prefill_chunk)):
+        torch.cuda.empty_cache()
+        line["dense_comparison"] = bench_dense_comparison(dev, flush, dec["ms_per_step"],
+                                                          pre["ms_per_step"])
     if pre is not None:
         line["prefill"] = pre
     if "cpu_baseline" in dec:
