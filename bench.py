@@ -632,6 +632,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-L", type=int, default=None,
                     help="shrink the decode cache (profiling runs on a smaller case)")
+    ap.add_argument("--prefill-128k", action="store_true",
+                    help="time the last 8192-query chunk of the 128K prefill workload instead")
     ap.add_argument("--prefill-L", type=int, default=None,
                     help="shrink the prefill cache (profiling runs on a smaller case)")
     ap.add_argument("--prefill-chunk", type=int, default=None,
@@ -675,7 +677,10 @@ def main():
         torch.cuda.empty_cache()
     if not args.no_prefill:
         wp = W.PREFILL_1M
-        if args.prefill_L or args.prefill_chunk:
+        if args.prefill_128k:
+            wp = W.PREFILL_128K.with_(name="prefill_128k_last_chunk", n_q=8192, chunk=8192,
+                                      q_pos0=W.PREFILL_128K.L - 8192)
+        elif args.prefill_L or args.prefill_chunk:
             L = args.prefill_L or wp.L
             n = args.prefill_chunk or wp.n_q
             wp = wp.with_(name="prefill_%d_vs_%d" % (n, L), L=L, n_q=n, chunk=n, q_pos0=L - n)
@@ -702,7 +707,7 @@ def main():
     if grp is not None:
         line["decode_group_shared"] = grp
     if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1
-            and not (args.decode_L or args.prefill_L or args.prefill_chunk)):
+            and not (args.decode_L or args.prefill_L or args.prefill_chunk or args.prefill_128k)):
         torch.cuda.empty_cache()
         line["dense_comparison"] = bench_dense_comparison(dev, flush, dec["ms_per_step"],
                                                           pre["ms_per_step"])
