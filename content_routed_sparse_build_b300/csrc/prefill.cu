@@ -623,6 +623,60 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     int64_t gb = 0;
     int tcount = 0;
+    // the previous tile's epilogue, still to run
+    bool pend = false;
+    int64_t pend_glast = 0, pend_qrow = -1;
+    float pend_m = -INFINITY, pend_l = 0.f;
+    int pend_rank = 0;
+    // Epilogue of the pending tile: combine the halves' accumulators into
+    // this warp's output columns [half * D / 2, + D / 2), normalised, to the
+    // row's partial slot.  Returns false when a bounded wait gave up.
+    auto epilogue = [&]() -> bool {
+      pend = false;
+      const int64_t glast = pend_glast;
+      if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) return false;
+      tc::fence_after();
+      xchg[half * 256 + r] = pend_m;
+      xchg[half * 256 + 128 + r] = pend_l;
+      pair_sync();
+      const float m_o = xchg[(half ^ 1) * 256 + r], l_o = xchg[(half ^ 1) * 256 + 128 + r];
+      pair_sync();
+      const float m0 = half == 0 ? pend_m : m_o, m1 = half == 0 ? m_o : pend_m;
+      const float l0 = half == 0 ? pend_l : l_o, l1 = half == 0 ? l_o : pend_l;
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
+      const float lt = l0 * w0 + l1 * w1;
+      const float inv = 1.f / lt;
+      const float s0 = w0 * inv, s1 = w1 * inv;
+      const uint32_t tO0 = tmem + C::kColO + lane_off + half * OH;
+      const uint32_t tO1 = tO0 + D;
+      uint32_t pk[OH / 2];
+#pragma unroll
+      for (int q = 0; q < OH / 32; ++q) {
+        uint32_t o0[32], o1[32];
+        tc::ld32(tO0 + q * 32, o0);
+        tc::ld32(tO1 + q * 32, o1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[q * 16 + j] = ptx::pack2<DT>(
+              __uint_as_float(o0[2 * j]) * s0 + __uint_as_float(o1[2 * j]) * s1,
+              __uint_as_float(o0[2 * j + 1]) * s0 + __uint_as_float(o1[2 * j + 1]) * s1);
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(o_free);
+      if (pend_qrow >= 0) {
+        const int64_t slot = pend_qrow * (a.topk + 1) + pend_rank;
+        uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
+#pragma unroll
+        for (int j = 0; j < OH / 16; ++j)
+          ptx::st_global_v8(dst + 16 * j, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3], pk[8 * j + 4],
+                            pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
+        if (half == 0) a.pml[slot] = make_float2(M, lt);
+      }
+      return true;
+    };
     // No abort check here: both warps of a pair must walk the same tiles
     // (they meet at a named barrier per tile); they leave only through
     // bounded waits, which time out together.
@@ -648,11 +702,20 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         qrow = local_row(a, x, r, &i);
         tpos = a.q_pos0 + i;
       }
+      // the tile entry and row entries are in registers now: the loader may
+      // reuse them (with the Q buffer, once the tile's last S is done)
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int kb = 0; kb < x.nkb && ok; ++kb) {
         const int64_t g = gb + kb;
         const int st = (int)(g & 1);
+        // the previous tile's epilogue, once this tile's first P is out
+        if (kb == 1 && pend && !epilogue()) {
+          ok = false;
+          break;
+        }
         if (!ptx::mbar_wait(&s_full[st], (uint32_t)((g >> 1) & 1))) {
           ok = false;
           break;
@@ -733,57 +796,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
-      // epilogue: combine the halves' accumulators into this warp's output
-      // columns [half * D / 2, + D / 2), normalised, to the row's partial slot
-      const int64_t glast = gb + x.nkb - 1;
-      if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) {
+      // a one-block tile has not run the previous epilogue yet
+      if (ok && pend && !epilogue()) ok = false;
+      if (!ok) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
-      tc::fence_after();
-      xchg[half * 256 + r] = m;
-      xchg[half * 256 + 128 + r] = l;
-      pair_sync();
-      const float m_o = xchg[(half ^ 1) * 256 + r], l_o = xchg[(half ^ 1) * 256 + 128 + r];
-      pair_sync();
-      const float m0 = half == 0 ? m : m_o, m1 = half == 0 ? m_o : m;
-      const float l0 = half == 0 ? l : l_o, l1 = half == 0 ? l_o : l;
-      const float M = fmaxf(m0, m1);
-      const float w0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - M);
-      const float w1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
-      const float lt = l0 * w0 + l1 * w1;
-      const float inv = 1.f / lt;
-      const float s0 = w0 * inv, s1 = w1 * inv;
-      const uint32_t tO0 = tmem + C::kColO + lane_off + half * OH;
-      const uint32_t tO1 = tO0 + D;
-      uint32_t pk[OH / 2];
-#pragma unroll
-      for (int q = 0; q < OH / 32; ++q) {
-        uint32_t o0[32], o1[32];
-        tc::ld32(tO0 + q * 32, o0);
-        tc::ld32(tO1 + q * 32, o1);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[q * 16 + j] = ptx::pack2<DT>(
-              __uint_as_float(o0[2 * j]) * s0 + __uint_as_float(o1[2 * j]) * s1,
-              __uint_as_float(o0[2 * j + 1]) * s0 + __uint_as_float(o1[2 * j + 1]) * s1);
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(o_free);
-      if (qrow >= 0) {
-        const int64_t slot = qrow * (a.topk + 1) + rank;
-        uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
-#pragma unroll
-        for (int j = 0; j < OH / 16; ++j)
-          ptx::st_global_v8(dst + 16 * j, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3], pk[8 * j + 4],
-                            pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
-        if (half == 0) a.pml[slot] = make_float2(M, lt);
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
+      // this tile's epilogue runs after the next tile's first block (or
+      // after the last tile), so that waiting for its last O += P V overlaps
+      // the next tile's softmax
+      pend = true;
+      pend_glast = gb + x.nkb - 1;
+      pend_m = m;
+      pend_l = l;
+      pend_qrow = qrow;
+      pend_rank = rank;
       gb += x.nkb;
     }
+    if (pend && !epilogue()) fail(SSA_DEVERR_WAIT_TIMEOUT);
   }
   __syncthreads();
   tc::fence_after();
