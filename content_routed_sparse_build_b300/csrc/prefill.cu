@@ -292,7 +292,8 @@ struct ACfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kXchgBytes = 2 * 2 * kTileRows * 4;
   static constexpr int kMetaBytes = 2 * 16 + 2 * kTileRows * 4;
-  static constexpr int kSmallBytes = ((kBarBytes + kXchgBytes + kMetaBytes + 1023) / 1024) * 1024;
+  static constexpr int kSlotBytes = 2 * kTileRows * 8;  // pending tile: partial slot per softmax thread
+  static constexpr int kSmallBytes = ((kBarBytes + kXchgBytes + kMetaBytes + kSlotBytes + 1023) / 1024) * 1024;
   static constexpr size_t kSmem =
       1024 + kSmallBytes + 2 * (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes;
   // tensor memory: S0 [0, 128), S1 [128, 256) (P of a block is written over
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   float* xchg = reinterpret_cast<float*>(base + C::kBarBytes);   // [2 halves][m, l][128 rows]
   int4* tinfo = reinterpret_cast<int4*>(base + C::kBarBytes + C::kXchgBytes);  // [2] tile entries
   int* meta = reinterpret_cast<int*>(tinfo + 2);                  // [2][128] bucket entries or -1
+  int64_t* pslot = reinterpret_cast<int64_t*>(meta + 2 * kTileRows);  // [256] pending partial slot or -1
   uint8_t* sQ = base + C::kSmallBytes;
   uint8_t* sK = sQ + 2 * C::kQBytes;
   uint8_t* sV = sK + C::kKStages * C::kKVBytes;
@@ -624,25 +626,22 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     int64_t gb = 0;
     int tcount = 0;
     // the previous tile's epilogue, still to run
+    // (its rows' m and l wait in xchg, its partial slots in pslot: only the
+    // flag stays in registers while the next tile runs)
     bool pend = false;
-    int64_t pend_glast = 0, pend_qrow = -1;
-    float pend_m = -INFINITY, pend_l = 0.f;
-    int pend_rank = 0;
     // Epilogue of the pending tile: combine the halves' accumulators into
     // this warp's output columns [half * D / 2, + D / 2), normalised, to the
     // row's partial slot.  Returns false when a bounded wait gave up.
     auto epilogue = [&]() -> bool {
       pend = false;
-      const int64_t glast = pend_glast;
+      const int64_t glast = gb - 1;  // the pending tile's last block: every call site has gb one past it
       if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) return false;
       tc::fence_after();
-      xchg[half * 256 + r] = pend_m;
-      xchg[half * 256 + 128 + r] = pend_l;
       pair_sync();
-      const float m_o = xchg[(half ^ 1) * 256 + r], l_o = xchg[(half ^ 1) * 256 + 128 + r];
+      const float m0 = xchg[r], l0 = xchg[128 + r];
+      const float m1 = xchg[256 + r], l1 = xchg[256 + 128 + r];
+      const int64_t slot = pslot[threadIdx.x];
       pair_sync();
-      const float m0 = half == 0 ? pend_m : m_o, m1 = half == 0 ? m_o : pend_m;
-      const float l0 = half == 0 ? pend_l : l_o, l1 = half == 0 ? l_o : pend_l;
       const float M = fmaxf(m0, m1);
       const float w0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - M);
       const float w1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
@@ -651,30 +650,27 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const float s0 = w0 * inv, s1 = w1 * inv;
       const uint32_t tO0 = tmem + C::kColO + lane_off + half * OH;
       const uint32_t tO1 = tO0 + D;
-      uint32_t pk[OH / 2];
+      uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
+      // 32 columns at a time: read both accumulators, combine, store
 #pragma unroll
       for (int q = 0; q < OH / 32; ++q) {
-        uint32_t o0[32], o1[32];
+        uint32_t o0[32], o1[32], pk[16];
         tc::ld32(tO0 + q * 32, o0);
         tc::ld32(tO1 + q * 32, o1);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          pk[q * 16 + j] = ptx::pack2<DT>(
+          pk[j] = ptx::pack2<DT>(
               __uint_as_float(o0[2 * j]) * s0 + __uint_as_float(o1[2 * j]) * s1,
               __uint_as_float(o0[2 * j + 1]) * s0 + __uint_as_float(o1[2 * j + 1]) * s1);
+        if (slot >= 0) {
+          ptx::st_global_v8(dst + 32 * q, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          ptx::st_global_v8(dst + 32 * q + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+        }
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(o_free);
-      if (pend_qrow >= 0) {
-        const int64_t slot = pend_qrow * (a.topk + 1) + pend_rank;
-        uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
-#pragma unroll
-        for (int j = 0; j < OH / 16; ++j)
-          ptx::st_global_v8(dst + 16 * j, pk[8 * j], pk[8 * j + 1], pk[8 * j + 2], pk[8 * j + 3], pk[8 * j + 4],
-                            pk[8 * j + 5], pk[8 * j + 6], pk[8 * j + 7]);
-        if (half == 0) a.pml[slot] = make_float2(M, lt);
-      }
+      if (slot >= 0 && half == 0) a.pml[slot] = make_float2(M, lt);
       return true;
     };
     // No abort check here: both warps of a pair must walk the same tiles
@@ -776,16 +772,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const float nb = m == -INFINITY ? 0.f : -m;
         // P_half = 2^(s c - m) as 16-bit pairs, over the S columns just read
         uint32_t pk[32];
+        if (!partial) {
+          // two partial sums keep the adds off one dependency chain
+          float la = 0.f, lb = 0.f;
 #pragma unroll
-        for (int j = 0; j < KH; j += 2) {
-          float p0 = ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb));
-          if (partial) {
-            if (j >= hlim) p0 = 0.f;
-            if (j + 1 >= hlim) p1 = 0.f;
+          for (int j = 0; j < KH; j += 2) {
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb));
+            la += p0;
+            lb += p1;
+            pk[j / 2] = ptx::pack2<DT>(p0, p1);
           }
-          l += p0 + p1;
-          pk[j / 2] = ptx::pack2<DT>(p0, p1);
+          l += la + lb;
+        } else {
+#pragma unroll
+          for (int j = 0; j < KH; j += 2) {
+            const float p0 = j < hlim ? ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb)) : 0.f;
+            const float p1 = j + 1 < hlim ? ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb)) : 0.f;
+            l += p0 + p1;
+            pk[j / 2] = ptx::pack2<DT>(p0, p1);
+          }
         }
         tc::st32(tS, pk);
         tc::fence_before();
@@ -806,11 +812,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       // after the last tile), so that waiting for its last O += P V overlaps
       // the next tile's softmax
       pend = true;
-      pend_glast = gb + x.nkb - 1;
-      pend_m = m;
-      pend_l = l;
-      pend_qrow = qrow;
-      pend_rank = rank;
+      xchg[half * 256 + r] = m;
+      xchg[half * 256 + 128 + r] = l;
+      pslot[threadIdx.x] = qrow >= 0 ? qrow * (a.topk + 1) + rank : -1;
       gb += x.nkb;
     }
     if (pend && !epilogue()) fail(SSA_DEVERR_WAIT_TIMEOUT);
