@@ -13,6 +13,10 @@ Entry points (same names as the C ABI):
   ssa_attend_decode    one query per head, split over spans, LSE merge
   ssa_attend_prefill   a chunk of queries, span-major tiles, LSE merge
   ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
+  ssa_quantize_kv / ssa_build_summaries_q8 / ssa_attend_decode_q8
+                       the 8-bit cache: quantised rows, their summaries, decode over them
+  ssa_snapshot_save / ssa_snapshot_load / ssa_snapshot_read_header
+                       the cache rows and summaries of a session, to and from a file
   ssa_workspace_size / ssa_workspace_error / ssa_status_string
 """
 from __future__ import annotations
@@ -30,6 +34,7 @@ SSA_ERR_UNSUPPORTED = 2
 SSA_ERR_WORKSPACE = 3
 SSA_ERR_CUDA = 4
 SSA_ERR_DEVICE = 5
+SSA_ERR_IO = 6
 
 SSA_F32, SSA_BF16, SSA_F16 = 0, 1, 2
 SSA_OP_ROUTE, SSA_OP_DECODE, SSA_OP_PREFILL, SSA_OP_ROUTE_GROUP = 0, 1, 2, 3
@@ -206,6 +211,104 @@ def ssa_attend_decode_noalloc(p: ssa_params, Q: torch.Tensor, pos: int, K: torch
            ctypes.byref(scratch), _stream(stream))
     _check(rc, "ssa_attend_decode_noalloc")
     return ScratchBlock(int(scratch.value))
+
+
+def q8_cache(p: ssa_params, device=None):
+    """Empty 8-bit cache tensors (Kq, Ks, Vq, Vs) laid out for p (L_cap a
+    multiple of 32)."""
+    L_cap = p.L_cap or p.L
+    if L_cap % 32:
+        raise ValueError("the 8-bit cache needs L_cap % 32 == 0")
+    dev = device if device is not None else torch.device("cuda")
+    Kq = torch.empty((p.B, p.Hkv, L_cap, p.d), dtype=torch.int8, device=dev)
+    Vq = torch.empty((p.B, p.Hkv, L_cap // 32, p.d, 32), dtype=torch.int8, device=dev)
+    Ks = torch.empty((p.B, p.Hkv, L_cap), dtype=torch.float32, device=dev)
+    Vs = torch.empty((p.B, p.Hkv, L_cap), dtype=torch.float32, device=dev)
+    return Kq, Ks, Vq, Vs
+
+
+def ssa_quantize_kv(p: ssa_params, K: torch.Tensor, V: torch.Tensor, t_begin: int, t_end: int,
+                    Kq: torch.Tensor, Ks: torch.Tensor, Vq: torch.Tensor, Vs: torch.Tensor, stream=None) -> None:
+    f = lib().ssa_quantize_kv
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _P, _I64, _I64, _P, _P, _P, _P, _P]
+    f.restype = ctypes.c_int
+    _check(f(ctypes.byref(p), _ptr(K), _ptr(V), int(t_begin), int(t_end), _ptr(Kq), _ptr(Ks), _ptr(Vq),
+             _ptr(Vs), _stream(stream)), "ssa_quantize_kv")
+
+
+def ssa_build_summaries_q8(p: ssa_params, Kq: torch.Tensor, Ks: torch.Tensor, span_begin: int, span_end: int,
+                           summ: torch.Tensor, stream=None) -> None:
+    f = lib().ssa_build_summaries_q8
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _P, _I64, _I64, _P, _P]
+    f.restype = ctypes.c_int
+    _check(f(ctypes.byref(p), _ptr(Kq), _ptr(Ks), int(span_begin), int(span_end), _ptr(summ), _stream(stream)),
+           "ssa_build_summaries_q8")
+
+
+def ssa_attend_decode_q8(p: ssa_params, Q: torch.Tensor, pos: int, Kq: torch.Tensor, Ks: torch.Tensor,
+                         Vq: torch.Tensor, Vs: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
+                         lse: torch.Tensor | None, ws: torch.Tensor | None, stream=None) -> None:
+    f = lib().ssa_attend_decode_q8
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(Kq), _ptr(Ks), _ptr(Vq), _ptr(Vs), _ptr(sel), _ptr(O),
+             _ptr(lse), wp, wn, _stream(stream)), "ssa_attend_decode_q8")
+
+
+SSA_SNAPSHOT_MAGIC = b"SSAKVSN1"
+SSA_SNAPSHOT_VERSION = 1
+
+
+class ssa_snapshot_header(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_char * 8), ("version", ctypes.c_uint32), ("dtype", ctypes.c_int32),
+                ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("S", ctypes.c_int32),
+                ("n_tokens", ctypes.c_int64), ("n_summ", ctypes.c_int64), ("payload_bytes", ctypes.c_uint64),
+                ("reserved", ctypes.c_uint8 * 8)]
+
+
+def _staging(staging, nbytes: int):
+    """(pointer, bytes) of a staging buffer: the caller's host tensor, or a
+    fresh page-locked one of nbytes."""
+    if staging is None:
+        staging = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    return staging, _P(staging.data_ptr()), staging.numel() * staging.element_size()
+
+
+def ssa_snapshot_save(p: ssa_params, n_tokens: int, K: torch.Tensor, V: torch.Tensor, summ: torch.Tensor,
+                      path: str, staging: torch.Tensor | None = None, stream=None) -> None:
+    """Write rows 0 .. n_tokens-1 of K and V and the complete spans' summaries to path."""
+    f = lib().ssa_snapshot_save
+    f.argtypes = [ctypes.POINTER(ssa_params), _I64, _P, _P, _P, ctypes.c_char_p, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    buf, ptr, nb = _staging(staging, 64 << 20)
+    rc = f(ctypes.byref(p), int(n_tokens), _ptr(K), _ptr(V), _ptr(summ), os.fsencode(path), ptr, nb,
+           _stream(stream))
+    _check(rc, "ssa_snapshot_save")
+
+
+def ssa_snapshot_load(p: ssa_params, path: str, K: torch.Tensor, V: torch.Tensor, summ: torch.Tensor,
+                      staging: torch.Tensor | None = None, stream=None) -> int:
+    """Restore a snapshot into K, V and summ; returns its n_tokens."""
+    f = lib().ssa_snapshot_load
+    f.argtypes = [ctypes.POINTER(ssa_params), ctypes.c_char_p, _P, _P, _P, ctypes.POINTER(_I64), _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    buf, ptr, nb = _staging(staging, 64 << 20)
+    n = _I64(0)
+    rc = f(ctypes.byref(p), os.fsencode(path), _ptr(K), _ptr(V), _ptr(summ), ctypes.byref(n), ptr, nb,
+           _stream(stream))
+    _check(rc, "ssa_snapshot_load")
+    return int(n.value)
+
+
+def ssa_snapshot_read_header(path: str) -> ssa_snapshot_header:
+    """The checked header of a snapshot file (host only)."""
+    f = lib().ssa_snapshot_read_header
+    f.argtypes = [ctypes.c_char_p, ctypes.POINTER(ssa_snapshot_header)]
+    f.restype = ctypes.c_int
+    h = ssa_snapshot_header()
+    _check(f(os.fsencode(path), ctypes.byref(h)), "ssa_snapshot_read_header")
+    return h
 
 
 def ssa_workspace_error(ws: torch.Tensor, stream=None) -> int:

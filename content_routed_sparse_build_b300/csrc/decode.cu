@@ -597,6 +597,397 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- attend, 8-bit cache
+// The same work items, plan and merge as the 16-bit kernel, over the 8-bit
+// cache of quant.cu (d = 128).  Each ring stage holds one 32-token tile: the
+// K rows (TMA, 128-byte swizzle), the d-major V tile and the tile's K and V
+// scales (bulk copies).  Tiles are 32-token aligned; tokens of a tile
+// outside the item are masked.  The MMAs run in fp16: 8-bit values convert
+// to fp16 exactly, and Q is rounded to fp16 once per item.
+//   S^T = ks * (Kq Q^T)                       (tokens x heads)
+//   O^T += Vq^T (vs * P)^T,  l += sum of P    (d x heads)
+// The k order of the K fragments is permuted: thread quad c reads 8
+// consecutive bytes d = 32 J + 8 c .. + 7 of a row, bytes 0-3 feeding k-step
+// 2 J and bytes 4-7 k-step 2 J + 1; Q's fragments are built with the same
+// d-to-k map, so every product still pairs K[t][d] with Q[h][d].
+namespace q8 {
+constexpr int kStages = 3;
+constexpr int kKBytes = kTile * 128;   // 32 rows of 128 int8
+constexpr int kVBytes = kTile * 128;   // 128 d-rows of 32 tokens
+constexpr int kSBytes = 2 * kTile * 4; // ks then vs
+constexpr size_t kRingK = (size_t)kWarps * kStages * kKBytes;
+constexpr size_t kRingV = (size_t)kWarps * kStages * kVBytes;
+constexpr size_t kRingS = (size_t)kWarps * kStages * kSBytes;
+constexpr size_t kBars = (size_t)kWarps * kStages * 8;
+constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
+constexpr size_t kFixed = 1024 + kRingK + kRingV + kRingS + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+constexpr int kQStride = 128 + 8;
+
+// First 32-aligned tile start and tile count of tokens [t0, t1).
+__device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kTile - 1); }
+__device__ __forceinline__ int tiles(int64_t t0, int64_t t1) {
+  return (int)((t1 - tile_base(t0) + kTile - 1) / kTile);
+}
+}  // namespace q8
+
+template <int DT, int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_attend_q8_kernel(const __grid_constant__ CUtensorMap tmK, const int8_t* __restrict__ Vq,
+                            const float* __restrict__ Ks, const float* __restrict__ Vs, int64_t L_cap,
+                            const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ringK = smem;
+  uint8_t* ringV = ringK + q8::kRingK;
+  uint8_t* ringS = ringV + q8::kRingV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ringS + q8::kRingS);
+  int4* metas = reinterpret_cast<int4*>(bars + kWarps * q8::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metas + kWarps * q8::kStages);
+  uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_gpref + kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int n_slots = geo.n_grp * geo.umax;
+
+  if (tid == 0) {
+    for (int s = 0; s < kWarps * q8::kStages; ++s) ptx::mbar_init(&bars[s], 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmK);
+  }
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  Tables tb;
+  tb.gpref = s_gpref;
+  if (geo.tables_in_smem) {
+    int* nu_s = reinterpret_cast<int*>(s_tab);
+    int* sp_s = nu_s + geo.n_grp;
+    uint32_t* mk_s = reinterpret_cast<uint32_t*>(sp_s + n_slots);
+    uint16_t* q_s = reinterpret_cast<uint16_t*>(mk_s + n_slots);
+    const int nq_rows = geo.n_grp * geo.g;
+    uint8_t* rk_s = reinterpret_cast<uint8_t*>(q_s + nq_rows * q8::kQStride);
+    for (int x = tid; x < geo.n_grp; x += kThreads) nu_s[x] = plan.n_union[x];
+    for (int x = tid; x < n_slots; x += kThreads) {
+      sp_s[x] = plan.span[x];
+      mk_s[x] = plan.mask[x];
+    }
+    for (int x = tid; x < n_slots * 4; x += kThreads)
+      reinterpret_cast<uint32_t*>(rk_s)[x] = reinterpret_cast<const uint32_t*>(plan.rank)[x];
+    for (int x = tid; x < nq_rows * (D / 2); x += kThreads) {
+      const int r = x / (D / 2), c = x - r * (D / 2);
+      reinterpret_cast<uint32_t*>(q_s + r * q8::kQStride)[c] = reinterpret_cast<const uint32_t*>(Q)[x];
+    }
+    tb.n_union = nu_s;
+    tb.span = sp_s;
+    tb.mask = mk_s;
+    tb.rank = rk_s;
+    tb.q = q_s;
+    tb.q_stride = q8::kQStride;
+  } else {
+    tb.n_union = plan.n_union;
+    tb.span = plan.span;
+    tb.mask = plan.mask;
+    tb.rank = plan.rank;
+    tb.q = static_cast<const uint16_t*>(Q);
+    tb.q_stride = D;
+  }
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < geo.n_grp; base += 32) {
+      const int gi = base + lane;
+      int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (gi < geo.n_grp) s_gpref[gi + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_gpref[0] = 0;
+  }
+  __syncthreads();
+  const int total = s_gpref[geo.n_grp];
+
+  uint8_t* wK = ringK + (size_t)warp * q8::kStages * q8::kKBytes;
+  uint8_t* wV = ringV + (size_t)warp * q8::kStages * q8::kVBytes;
+  uint8_t* wS = ringS + (size_t)warp * q8::kStages * q8::kSBytes;
+  uint64_t* fb = bars + warp * q8::kStages;
+  int4* meta = metas + warp * q8::kStages;
+  const int64_t tiles_per_head = L_cap / kTile;
+
+  Item iss;
+  iss.ntiles = 0;
+  iss.grp = iss.u = iss.c = 0;
+  iss.t0 = iss.t1 = 0;
+  int iss_tile = 0;
+  int it_next = 0, it_claim = 0;
+  bool have_next = true, claim_issued = false;
+  if (lane == 0) it_next = atomicAdd(plan.counter, 1);
+  it_next = __shfl_sync(0xffffffffu, it_next, 0);
+  bool exhausted = false;
+
+  auto issue = [&](int stage) -> bool {
+    if (iss_tile == iss.ntiles) {
+      if (!have_next) it_next = __shfl_sync(0xffffffffu, it_claim, 0);
+      if (it_next >= total) {
+        exhausted = true;
+        return false;
+      }
+      decode_item(it_next, tb, geo, iss);
+      iss.ntiles = q8::tiles(iss.t0, iss.t1);
+      iss_tile = 0;
+      have_next = false;
+      claim_issued = false;
+    }
+    if (lane == 0) {
+      meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ptx::mbar_arrive_expect_tx(&fb[stage], q8::kKBytes + q8::kVBytes + q8::kSBytes);
+      const int64_t y = q8::tile_base(iss.t0) + (int64_t)iss_tile * kTile;
+      uint8_t* dS = wS + stage * q8::kSBytes;
+      ptx::tma_load_3d(wK + stage * q8::kKBytes, &tmK, &fb[stage], 0, (int)y, iss.grp);
+      ptx::bulk_load(wV + stage * q8::kVBytes, Vq + ((int64_t)iss.grp * tiles_per_head + y / kTile) * (D * kTile),
+                     q8::kVBytes, &fb[stage]);
+      ptx::bulk_load(dS, Ks + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
+      ptx::bulk_load(dS + kTile * 4, Vs + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
+    }
+    ++iss_tile;
+    if (!claim_issued && iss.ntiles - iss_tile <= 2) {
+      if (lane == 0) it_claim = atomicAdd(plan.counter, 1);
+      claim_issued = true;
+    }
+    return true;
+  };
+
+  int inflight = 0;
+#pragma unroll 1
+  for (int s = 0; s < q8::kStages; ++s) {
+    if (exhausted || !issue(s)) break;
+    ++inflight;
+  }
+
+  const int q4 = lane & 3, r8 = lane >> 2;
+  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+  float o[NG][D / 16][4];
+  float m[NG][2], l[NG][2];
+  Item cur;
+  cur.grp = cur.u = cur.c = cur.ntiles = 0;
+  cur.t0 = cur.t1 = 0;
+  int stage = 0;
+  uint32_t phase = 0;
+#pragma unroll 1
+  while (inflight > 0) {
+    if (!ptx::mbar_wait(&fb[stage], phase)) {
+      if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    const int4 mt = meta[stage];
+    if (mt.w == 0) {
+      cur.grp = mt.x;
+      cur.u = mt.y;
+      cur.c = mt.z;
+      {
+        const int nu = tb.n_union[cur.grp];
+        if (cur.u < nu - 1) {
+          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
+          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
+        } else {
+          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
+        }
+        cur.ntiles = q8::tiles(cur.t0, cur.t1);
+      }
+      const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        const int h = ng * 8 + r8;
+        const bool ok = h < geo.g;
+        const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
+#pragma unroll
+        for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            uint32_t v = 0u;
+            if (ok) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(qr + 32 * J + 8 * q4 + 2 * pr);
+              if constexpr (DT == DT_BF16) {
+                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+                v = ptx::pack2<DT_F16>(lo, hi);
+              } else {
+                v = w;
+              }
+            }
+            qf[ng][J][pr] = v;
+          }
+        }
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) o[ng][mt2][0] = o[ng][mt2][1] = o[ng][mt2][2] = o[ng][mt2][3] = 0.f;
+        m[ng][0] = m[ng][1] = -INFINITY;
+        l[ng][0] = l[ng][1] = 0.f;
+      }
+    }
+    const uint32_t aK = ptx::smem_u32(wK + stage * q8::kKBytes);
+    const uint32_t aV = ptx::smem_u32(wV + stage * q8::kVBytes);
+    const float* sks = reinterpret_cast<const float*>(wS + stage * q8::kSBytes);
+    const float* svs = sks + kTile;
+
+    // S^T = Kq Q^T per 16-token fragment t
+    float s[NG][kSub][4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) s[ng][t][0] = s[ng][t][1] = s[ng][t][2] = s[ng][t][3] = 0.f;
+#pragma unroll
+    for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        const int ra = t * 16 + r8, rb = ra + 8;
+        const int chunk = 2 * J + (q4 >> 1);
+        const uint2 wa = ptx::lds64(aK + ptx::sw128(ra, chunk) + 8 * (q4 & 1));
+        const uint2 wb = ptx::lds64(aK + ptx::sw128(rb, chunk) + 8 * (q4 & 1));
+        uint32_t a0[4], a1[4];
+        ptx::s8x4_to_f16x2(wa.x, a0[0], a0[2]);
+        ptx::s8x4_to_f16x2(wb.x, a0[1], a0[3]);
+        ptx::s8x4_to_f16x2(wa.y, a1[0], a1[2]);
+        ptx::s8x4_to_f16x2(wb.y, a1[1], a1[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          ptx::mma16816<DT_F16>(s[ng][t], a0, qf[ng][J][0], qf[ng][J][1]);
+          ptx::mma16816<DT_F16>(s[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
+        }
+      }
+    }
+    // rows (tokens) r8 and r8 + 8 of each fragment: K / V scales, validity
+    const int64_t tbase = q8::tile_base(cur.t0) + (int64_t)mt.w * kTile;
+    float ksc[kSub][2], vsc[kSub][2];
+    bool valid[kSub][2];
+#pragma unroll
+    for (int t = 0; t < kSub; ++t)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = t * 16 + r8 + 8 * i;
+        const int64_t tok = tbase + row;
+        valid[t][i] = tok >= cur.t0 && tok < cur.t1;
+        ksc[t][i] = sks[row];
+        vsc[t][i] = svs[row];
+      }
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        s[ng][t][0] = valid[t][0] ? s[ng][t][0] * ksc[t][0] : -INFINITY;
+        s[ng][t][1] = valid[t][0] ? s[ng][t][1] * ksc[t][0] : -INFINITY;
+        s[ng][t][2] = valid[t][1] ? s[ng][t][2] * ksc[t][1] : -INFINITY;
+        s[ng][t][3] = valid[t][1] ? s[ng][t][3] * ksc[t][1] : -INFINITY;
+      }
+    const float c = geo.scale_log2e;
+    uint32_t pb[NG][kSub][2];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      float mx[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float v = fmaxf(s[ng][0][i], s[ng][0][i + 2]);
+#pragma unroll
+        for (int t = 1; t < kSub; ++t) v = fmaxf(v, fmaxf(s[ng][t][i], s[ng][t][i + 2]));
+        v *= c;
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        mx[i] = fmaxf(m[ng][i], v);
+      }
+      float nb[2], alpha[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float bse = mx[i] == -INFINITY ? 0.f : mx[i];
+        nb[i] = -bse;
+        alpha[i] = exp2f(m[ng][i] - bse);
+        m[ng][i] = mx[i];
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
+        const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
+        const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
+        const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
+        ls0 += p0 + p2;
+        ls1 += p1 + p3;
+        // the V scale of each token weights its P (0 for masked tokens,
+        // whose scale slot may hold anything)
+        const float v0 = valid[t][0] ? vsc[t][0] : 0.f, v1 = valid[t][1] ? vsc[t][1] : 0.f;
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * v0, p1 * v0));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * v1, p3 * v1));
+      }
+      l[ng][0] = l[ng][0] * alpha[0] + ls0;
+      l[ng][1] = l[ng][1] * alpha[1] + ls1;
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          o[ng][mt2][0] *= alpha[0];
+          o[ng][mt2][1] *= alpha[1];
+          o[ng][mt2][2] *= alpha[0];
+          o[ng][mt2][3] *= alpha[1];
+        }
+      }
+    }
+    // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one
+    // 8-byte load per row covering both 16-token fragments
+#pragma unroll
+    for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+      const uint2 va = ptx::lds64(aV + (mt2 * 16 + r8) * 32 + 8 * q4);
+      const uint2 vb = ptx::lds64(aV + (mt2 * 16 + r8 + 8) * 32 + 8 * q4);
+      uint32_t a0[4], a1[4];
+      ptx::s8x4_to_f16x2(va.x, a0[0], a0[2]);
+      ptx::s8x4_to_f16x2(vb.x, a0[1], a0[3]);
+      ptx::s8x4_to_f16x2(va.y, a1[0], a1[2]);
+      ptx::s8x4_to_f16x2(vb.y, a1[1], a1[3]);
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        ptx::mma16816<DT_F16>(o[ng][mt2], a0, pb[ng][0][0], pb[ng][0][1]);
+        ptx::mma16816<DT_F16>(o[ng][mt2], a1, pb[ng][1][0], pb[ng][1][1]);
+      }
+    }
+    __syncwarp();
+    --inflight;
+    const bool last = mt.w == cur.ntiles - 1;
+    if (!exhausted && issue(stage)) ++inflight;
+    if (++stage == q8::kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (!last) continue;
+
+    const int slot_idx = cur.grp * geo.umax + cur.u;
+    const uint32_t hmask = tb.mask[slot_idx];
+    const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float lt = l[ng][i];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int r = ng * 8 + 2 * q4 + i;
+        if (r >= geo.g || !((hmask >> r) & 1u)) continue;
+        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
+        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        float* dst = plan.po + slot * D + r8;
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          dst[mt2 * 16] = o[ng][mt2][i];
+          dst[mt2 * 16 + 8] = o[ng][mt2][i + 2];
+        }
+        if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- merge
 // One CTA per (b, q-head): its (topk + 1) * C partial slots, in (span rank,
 // chunk) order, split into 8 contiguous runs, one per warp; empty slots
@@ -690,6 +1081,61 @@ size_t tables_bytes(const Problem& pr) {
   return n_grp * 4 + slots * (4 + 4 + 16) + (size_t)pr.B * pr.Hq * (pr.d + 8) * 2;
 }
 
+// The plan's workspace pointers and the geometry of a decode step.
+void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
+  const Layout lay = layout(pr);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  plan.n_union = reinterpret_cast<int*>(w8 + lay.n_union);
+  plan.n_items = reinterpret_cast<int*>(w8 + lay.n_items);
+  plan.span = reinterpret_cast<int*>(w8 + lay.span);
+  plan.mask = reinterpret_cast<uint32_t*>(w8 + lay.mask);
+  plan.rank = w8 + lay.rank;
+  plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
+  plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
+  plan.po = reinterpret_cast<float*>(w8 + lay.po);
+  geo.Hq = pr.Hq;
+  geo.Hkv = pr.Hkv;
+  geo.g = pr.g;
+  geo.topk = pr.topk;
+  geo.S = pr.S;
+  geo.C = lay.C;
+  geo.CH = lay.CH;
+  geo.umax = pr.g * pr.topk + 1;
+  geo.n_grp = pr.B * pr.Hkv;
+  geo.pos = pos;
+  geo.ell = pos / pr.S;
+  geo.scale_log2e = pr.scale * kLog2e;
+  geo.tables_in_smem = 0;
+}
+
+template <int DT>
+cudaError_t launch_typed_q8(const Problem& pr, const void* Q, int64_t pos, const int8_t* Kq, const float* Ks,
+                            const int8_t* Vq, const float* Vs, const int32_t* sel, void* O, float* lse, void* ws,
+                            cudaStream_t st) {
+  constexpr int D = 128;
+  Plan plan;
+  Geo geo;
+  plan_geo(pr, pos, ws, plan, geo);
+  const size_t tb = tables_bytes(pr);
+  geo.tables_in_smem = q8::kFixed + tb <= (size_t)kSmemLimit;
+  const size_t smem = q8::kFixed + (geo.tables_in_smem ? tb : 0);
+  uint32_t* err = ws_error(ws);
+  CUtensorMap tmK;
+  cudaError_t e = make_q8_tmap(&tmK, Kq, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
+  if (e != cudaSuccess) return e;
+  auto attend = pr.g <= 8 ? decode_attend_q8_kernel<DT, 1> : decode_attend_q8_kernel<DT, 2>;
+  static bool attr_done[2][kMaxDevices] = {};
+  e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), smem, st, tmK, Vq, Ks, Vs, pr.L_cap, Q, plan,
+                 geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st,
+                    plan, geo, O, lse);
+}
+
 template <int DT, int D>
 cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const void* K, const void* V,
                          const int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
@@ -742,6 +1188,13 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const vo
 }
 
 }  // namespace
+
+cudaError_t launch_attend_decode_q8(const Problem& pr, const void* Q, int64_t pos, const int8_t* Kq,
+                                    const float* Ks, const int8_t* Vq, const float* Vs, const int32_t* sel,
+                                    void* O, float* lse, void* ws, cudaStream_t st) {
+  if (pr.dtype == DT_BF16) return launch_typed_q8<DT_BF16>(pr, Q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws, st);
+  return launch_typed_q8<DT_F16>(pr, Q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws, st);
+}
 
 bool decode_fast_supported(const Problem& pr) {
   return (pr.dtype == DT_BF16 || pr.dtype == DT_F16) && (pr.d == 64 || pr.d == 128) &&

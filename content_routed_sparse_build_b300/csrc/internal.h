@@ -24,6 +24,9 @@ struct Problem {
   int64_t ns_cap;        // ceil(L_cap / S): span slots per (b, kv-head) in summ
 };
 
+// Validates the public parameters and resolves them (SSA_OK or a status).
+int check_params(const ssa_params* p, Problem* pr);
+
 // Workspace layout shared by the attention entry points.
 constexpr size_t kWsHeader = 256;  // error record + counters, keeps what follows aligned
 inline uint32_t* ws_error(void* ws) { return static_cast<uint32_t*>(ws); }
@@ -33,6 +36,10 @@ inline uint32_t* ws_error(void* ws) { return static_cast<uint32_t*>(ws); }
 cudaError_t make_kv_tmap(CUtensorMap* map, const void* base, int dtype, int d, int64_t L,
                          int64_t L_cap, int64_t BH, int box_rows);
 int device_sm_count();
+// TMA descriptor of an 8-bit [B, Hkv, L_cap, d] cache (d = 128: one
+// 128-byte box per row, 128-byte swizzling), box_rows rows per box.
+cudaError_t make_q8_tmap(CUtensorMap* map, const void* base, int d, int64_t L, int64_t L_cap, int64_t BH,
+                         int box_rows);
 
 // Launches a kernel with programmatic dependent launch enabled: it may begin
 // before the previous kernel on the stream ends and must call pdl_wait()
@@ -88,6 +95,16 @@ cudaError_t launch_route_tc(const Problem& pr, const void* Q, int64_t n_q, int64
 cudaError_t launch_attend_rows(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                                const void* K, const void* V, const int32_t* sel, void* O,
                                float* lse, uint32_t* err, cudaStream_t st);
+
+// The 8-bit cache (quant.cu): quantised rows and their span summaries.
+cudaError_t launch_quantize_kv(const Problem& pr, const void* K, const void* V, int64_t t0, int64_t t1,
+                               int8_t* Kq, float* Ks, int8_t* Vq, float* Vs, cudaStream_t st);
+cudaError_t launch_summaries_q8(const Problem& pr, const int8_t* Kq, const float* Ks, int64_t j0, int64_t j1,
+                                float* summ, cudaStream_t st);
+// Decode attention over the 8-bit cache (16-bit Q and O, d = 128).
+cudaError_t launch_attend_decode_q8(const Problem& pr, const void* Q, int64_t pos, const int8_t* Kq,
+                                    const float* Ks, const int8_t* Vq, const float* Vs, const int32_t* sel,
+                                    void* O, float* lse, void* ws, cudaStream_t st);
 
 // Decode attention fast path (16-bit types): plan, split spans, merge.
 size_t decode_ws_bytes(const Problem& pr);

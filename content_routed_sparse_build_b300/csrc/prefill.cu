@@ -655,8 +655,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
       for (int q = 0; q < OH / 32; ++q) {
         uint32_t o0[32], o1[32], pk[16];
-        tc::ld32(tO0 + q * 32, o0);
-        tc::ld32(tO1 + q * 32, o1);
+        tc::ld32x2(tO0 + q * 32, o0, tO1 + q * 32, o1);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           pk[j] = ptx::pack2<DT>(

@@ -8,13 +8,7 @@
 
 using namespace ssa;
 
-namespace {
-
-constexpr int kVersion = 100;  // 0.1.0
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int check_params(const ssa_params* p, Problem* pr) {
+int ssa::check_params(const ssa_params* p, Problem* pr) {
   if (!p) return SSA_ERR_INVALID_ARG;
   if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->S < 1 || p->topk < 1 || p->L < 0 || p->L_cap < 0)
     return SSA_ERR_INVALID_ARG;
@@ -44,6 +38,12 @@ int check_params(const ssa_params* p, Problem* pr) {
   pr->ns_cap = (L_cap + p->S - 1) / p->S;
   return SSA_OK;
 }
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA; }
 
@@ -84,6 +84,7 @@ const char* ssa_status_string(int status) {
     case SSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SSA_ERR_CUDA: return "CUDA error";
     case SSA_ERR_DEVICE: return "device-detected error (see the workspace error bits)";
+    case SSA_ERR_IO: return "snapshot file error (open, read, write or format)";
     default: return "unknown status";
   }
 }
@@ -167,6 +168,52 @@ int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, int64_t 
   if (prefill_fast(pr, n_q))
     return cuda_status(launch_attend_prefill(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws, st));
   return cuda_status(launch_attend_rows(pr, Q, n_q, q_pos0, K, V, sel, O, lse, ws_error(ws), st));
+}
+
+int ssa_quantize_kv(const ssa_params* p, const void* K, const void* V, int64_t t_begin, int64_t t_end,
+                    int8_t* Kq, float* Ks, int8_t* Vq, float* Vs, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.L_cap % 32 != 0) return SSA_ERR_UNSUPPORTED;
+  if (t_begin < 0 || t_end < t_begin || t_end > pr.L) return SSA_ERR_INVALID_ARG;
+  if (!K || !V || !Kq || !Ks || !Vq || !Vs) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(Kq) || !aligned16(Ks) || !aligned16(Vq) || !aligned16(Vs))
+    return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_kv(pr, K, V, t_begin, t_end, Kq, Ks, Vq, Vs,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_build_summaries_q8(const ssa_params* p, const int8_t* Kq, const float* Ks, int64_t span_begin,
+                           int64_t span_end, float* summ, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.L_cap % 32 != 0) return SSA_ERR_UNSUPPORTED;
+  if (!Kq || !Ks || !summ || !aligned16(Kq) || !aligned16(Ks) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
+  const int64_t ns_valid = (pr.L + pr.S - 1) / pr.S;
+  if (span_begin < 0 || span_end < span_begin || span_end > ns_valid) return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_summaries_q8(pr, Kq, Ks, span_begin, span_end, summ,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_attend_decode_q8(const ssa_params* p, const void* Q, int64_t pos, const int8_t* Kq, const float* Ks,
+                         const int8_t* Vq, const float* Vs, const int32_t* sel, void* O, float* lse, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.d != 128 || pr.L_cap % 32 != 0 || (pr.dtype != SSA_BF16 && pr.dtype != SSA_F16) ||
+      !decode_fast_supported(pr))
+    return SSA_ERR_UNSUPPORTED;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !Kq || !Ks || !Vq || !Vs || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(Kq) || !aligned16(Ks) || !aligned16(Vq) || !aligned16(Vs) || !aligned16(O))
+    return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  return cuda_status(launch_attend_decode_q8(pr, Q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int ssa_workspace_error(void* ws, uint32_t* bits, void* stream) {

@@ -47,6 +47,20 @@ cudaError_t make_kv_tmap(CUtensorMap* map, const void* base, int dtype, int d, i
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_q8_tmap(CUtensorMap* map, const void* base, int d, int64_t L, int64_t L_cap, int64_t BH,
+                         int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(L > 0 ? L : 1), (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)L_cap * d};
+  cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;

@@ -68,7 +68,8 @@ typedef enum {
   SSA_ERR_UNSUPPORTED = 2, /* valid but not implemented (d, topk, group size, dtype) */
   SSA_ERR_WORKSPACE = 3,   /* ws is NULL, misaligned or smaller than required */
   SSA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-  SSA_ERR_DEVICE = 5       /* the GPU flagged an error in the workspace record */
+  SSA_ERR_DEVICE = 5,      /* the GPU flagged an error in the workspace record */
+  SSA_ERR_IO = 6           /* a snapshot file could not be opened, read or written, or is not one */
 } ssa_status;
 
 typedef enum { SSA_F32 = 0, SSA_BF16 = 1, SSA_F16 = 2 } ssa_dtype;
@@ -206,6 +207,120 @@ SSA_API int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, 
 SSA_API int ssa_attend_decode_noalloc(const ssa_params* p, const void* Q, int64_t pos,
                                       const void* K, const void* V, const int32_t* sel, void* O,
                                       float* lse, void** scratch, void* stream);
+
+/*
+ * The 8-bit cache (SubQ release post, geeks.co.kr/post/2077, limitations
+ * and quantisation plan: fp16 only so far, 8-bit / 4-bit K / V coming so
+ * that a 1M-token cache fits a 24 GB card).  The pages fix no scheme; this
+ * library uses symmetric 8-bit rows, one fp32 scale per (b, kv-head, token):
+ *   s = max_i |x_i| / 127,  q_i = clamp(rint(x_i / s), -127, 127), 0 if s == 0
+ * in fp32 (IEEE division, round to nearest even); a row's dequantised value
+ * is q_i * s.  Summaries stay fp32 (the mean of the dequantised keys), so
+ * routing is ssa_route / ssa_route_group on them, unchanged.
+ * Layouts (params.L_cap must be a multiple of 32; d = 128 for attention):
+ *   Kq [B, Hkv, L_cap, d]            int8, row-major
+ *   Vq [B, Hkv, L_cap / 32, d, 32]   int8: each 32-token tile stored d-major;
+ *        in a tile's d-row of 32 bytes, byte 8 c + e (c = 0..3, e = 0..7)
+ *        holds token 16 * (e / 4) + (2c, 2c+1, 2c+8, 2c+9)[e % 4] of the tile
+ *   Ks, Vs [B, Hkv, L_cap]           fp32 scales
+ * Every pointer is 16-byte aligned device memory owned by the caller.
+ */
+
+/*
+ * Quantises rows [t_begin, t_end) of every (b, kv-head) of K and V (layouts
+ * of the conventions above, element type params.dtype) into Kq, Ks, Vq, Vs.
+ * Other rows are untouched, so a decode loop quantises each new token and a
+ * chunked prefill each chunk.  Requires 0 <= t_begin <= t_end <= L.
+ */
+SSA_API int ssa_quantize_kv(const ssa_params* p, const void* K, const void* V, int64_t t_begin,
+                            int64_t t_end, int8_t* Kq, float* Ks, int8_t* Vq, float* Vs, void* stream);
+
+/*
+ * ssa_build_summaries over the 8-bit keys: summ[b, kvh, j, :] = mean over
+ * span j's valid tokens of Kq * Ks (fp32), for spans [span_begin, span_end).
+ */
+SSA_API int ssa_build_summaries_q8(const ssa_params* p, const int8_t* Kq, const float* Ks,
+                                   int64_t span_begin, int64_t span_end, float* summ, void* stream);
+
+/*
+ * ssa_attend_decode over the 8-bit cache: the same selections, work split
+ * and merge, with K[t] = Kq[t] * Ks[t] and V[t] = Vq[t] * Vs[t].  Q and O are
+ * bf16 or fp16 (params.dtype), d = 128.  The products run in fp16 (8-bit
+ * values convert exactly; Q is rounded to fp16, so |q| must stay below
+ * 65504) with fp32 accumulation.  ws as for ssa_attend_decode
+ * (ssa_workspace_size(p, 1, SSA_OP_DECODE) bytes).  Requires 0 <= pos < L.
+ */
+SSA_API int ssa_attend_decode_q8(const ssa_params* p, const void* Q, int64_t pos, const int8_t* Kq,
+                                 const float* Ks, const int8_t* Vq, const float* Vs, const int32_t* sel,
+                                 void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Cache snapshots (superlinear release post, geeks.co.kr/post/2077, "why
+ * this matters": the cache is kept instead of re-processing the context, in
+ * memory for instant replies and saved to / restored from disk per session).
+ * A snapshot holds the first n_tokens rows of every (b, kv-head) of K and V
+ * and the summaries of the n_tokens / S complete spans, so that a restored
+ * session routes and attends exactly as the saved one did.
+ *
+ * File format (little-endian), the header below followed by the payload:
+ *   K rows   [B][Hkv][n_tokens][d]  element type dtype
+ *   V rows   [B][Hkv][n_tokens][d]  element type dtype
+ *   summ     [B][Hkv][n_summ][d]    fp32, n_summ = floor(n_tokens / S)
+ * There is no checksum; the file size must equal 64 + payload_bytes.
+ */
+#define SSA_SNAPSHOT_MAGIC "SSAKVSN1"
+#define SSA_SNAPSHOT_VERSION 1u
+
+typedef struct {
+  char magic[8];          /* SSA_SNAPSHOT_MAGIC, not NUL-terminated */
+  uint32_t version;       /* SSA_SNAPSHOT_VERSION */
+  int32_t dtype;          /* ssa_dtype of K and V */
+  int32_t B, Hkv, d, S;   /* as in ssa_params */
+  int64_t n_tokens;       /* cache rows per (b, kv-head) in the file */
+  int64_t n_summ;         /* summaries per (b, kv-head): n_tokens / S */
+  uint64_t payload_bytes; /* bytes after the header */
+  uint8_t reserved[8];    /* zero */
+} ssa_snapshot_header;    /* 64 bytes */
+
+/*
+ * Writes a snapshot of rows 0 .. n_tokens-1 of K and V (device, the layouts
+ * of the conventions above, head stride L_cap * d) and of summ rows
+ * 0 .. n_tokens / S - 1 (device) to the file `path`, replacing it.
+ * `staging` is caller-owned host memory of staging_bytes (page-locked for
+ * speed; at least 2 * d * 4 bytes, a few tens of MiB recommended): the copy
+ * runs in chunks of staging_bytes / 2, device-to-host on `stream` into one
+ * half while the other half is written to the file.  The copies follow
+ * whatever was enqueued on `stream` before.  Unlike every other entry
+ * point, this call returns only when the file is complete (or on error).
+ * Requires 0 <= n_tokens <= L (params.L).
+ * Returns SSA_ERR_INVALID_ARG for bad arguments (checked before anything
+ * touches the GPU or the file), SSA_ERR_IO when the file cannot be
+ * written, SSA_ERR_CUDA when a copy fails.
+ */
+SSA_API int ssa_snapshot_save(const ssa_params* p, int64_t n_tokens, const void* K, const void* V,
+                              const float* summ, const char* path, void* staging, size_t staging_bytes,
+                              void* stream);
+
+/*
+ * Restores a snapshot written by ssa_snapshot_save into K, V and summ
+ * (device, caller-owned, laid out by `p`): rows 0 .. n_tokens-1 of every
+ * (b, kv-head) of K and V and summ rows 0 .. n_tokens / S - 1.  Other rows
+ * are left untouched.  *n_tokens (nullable) receives the row count; the
+ * caller then decodes with params.L = n_tokens.  The file's B, Hkv, d, S
+ * and dtype must equal p's and n_tokens must fit L_cap (params.L_cap, or L
+ * when 0); otherwise returns SSA_ERR_IO and writes nothing to the device.
+ * `staging` and `stream` as for ssa_snapshot_save (host-to-device copies
+ * overlap the file reads); returns when the copies are complete.
+ */
+SSA_API int ssa_snapshot_load(const ssa_params* p, const char* path, void* K, void* V, float* summ,
+                              int64_t* n_tokens, void* staging, size_t staging_bytes, void* stream);
+
+/*
+ * Reads and checks the header of a snapshot file (host only, no GPU):
+ * SSA_OK when the magic, version, reserved bytes, payload size and file
+ * size agree, else SSA_ERR_IO.  *out (nullable) receives the header.
+ */
+SSA_API int ssa_snapshot_read_header(const char* path, ssa_snapshot_header* out);
 
 /*
  * Bytes of workspace the operation needs for n_q queries (n_q is ignored

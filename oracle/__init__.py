@@ -27,7 +27,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(HERE, "liboracle.so")
 SRC = os.path.join(HERE, "oracle.c")
 
-_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.float64: 3}
 _lib = None
 
 
@@ -61,6 +61,7 @@ def _load():
         lib.oracle_attend.restype = I
         lib.oracle_attend.argtypes = [I, P, P, P, I, I, I, I64, I64, I64, I, I, I, D, P, P, I64,
                                       P, P, P]
+        lib.oracle_quantize_rows.argtypes = [I, P, I64, I, P, P]
         _lib = lib
     return _lib
 
@@ -178,3 +179,22 @@ def attend(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, q_pos0: int, S: in
     if rc != 0:
         raise ValueError("oracle_attend: a selected span is not a complete span before the query")
     return O, lse, ws
+
+
+def quantize_rows(X: torch.Tensor):
+    """8-bit rows of X [..., d]: (q int8 [..., d], scale float32 [...]).
+
+    Symmetric, one fp32 scale per row: s = max|x| / 127, q = rint(x / s)
+    clamped to [-127, 127] (0 when s == 0), every step in fp32."""
+    _host(X)
+    d = X.shape[-1]
+    rows = X.numel() // d
+    q = np.zeros(X.shape, np.int8)
+    s = np.zeros(X.shape[:-1], np.float32)
+    _load().oracle_quantize_rows(_DT[X.dtype], X.data_ptr(), rows, d, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def dequantize_rows(q: np.ndarray, s: np.ndarray) -> torch.Tensor:
+    """q * s in float64 (exact), as a host tensor of q's shape."""
+    return torch.from_numpy(q.astype(np.float64) * s.astype(np.float64)[..., None])

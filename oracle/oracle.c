@@ -38,10 +38,11 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_F64 = 3 };
 
 /* Exact widening of one stored element to double. */
 static double load_f64(int dtype, const void* base, int64_t i) {
+  if (dtype == ORACLE_F64) return ((const double*)base)[i];
   if (dtype == ORACLE_F32) return (double)((const float*)base)[i];
   uint16_t h = ((const uint16_t*)base)[i];
   if (dtype == ORACLE_BF16) {
@@ -293,4 +294,40 @@ int oracle_attend(int dtype, const void* Q, const void* K, const void* V, int B,
     free(tok);
   }
   return bad ? -1 : 0;
+}
+
+/*
+ * 8-bit cache rows (the SubQ release post's quantisation plan: 8-bit / 4-bit
+ * K / V so that a 1M-token cache fits a 24 GB card; the summaries stay fp32).
+ * The pages fix no scheme; the plainest one is used: symmetric, one fp32
+ * scale per (b, kv-head, token) row, round to nearest even.  For each of the
+ * `rows` rows of d elements of X (dtype, widened exactly to fp32):
+ *   amax = max |x_i|,  s = amax / 127 (fp32 division)
+ *   q_i  = 0 if s == 0, else clamp(rint(x_i / s), -127, 127) (fp32 division)
+ * The row's dequantised value is q_i * s.  Every step is fp32, as the
+ * quantised code is an integer decided in floating point.
+ */
+void oracle_quantize_rows(int dtype, const void* X, int64_t rows, int d, int8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    float amax = 0.f;
+    for (int c = 0; c < d; ++c) {
+      const float x = (float)load_f64(dtype, X, r * d + c);
+      const float a = fabsf(x);
+      if (a > amax) amax = a;
+    }
+    const float s = amax / 127.0f;
+    scale[r] = s;
+    for (int c = 0; c < d; ++c) {
+      int v = 0;
+      if (s != 0.f) {
+        const float x = (float)load_f64(dtype, X, r * d + c);
+        float t = rintf(x / s);
+        if (t > 127.f) t = 127.f;
+        if (t < -127.f) t = -127.f;
+        v = (int)t;
+      }
+      q[r * d + c] = (int8_t)v;
+    }
+  }
 }
