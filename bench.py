@@ -176,10 +176,11 @@ class DecodeBench:
     the cache.  A step routes one query token per head and attends it; the
     256 steps are captured once in a CUDA graph and replayed."""
 
-    def __init__(self, w: W.Workload, dev, group: bool = False):
+    def __init__(self, w: W.Workload, dev, group: bool = False, q8: bool = False):
         self.w = w
         self.dev = dev
         self.group = group                                     # group-shared selection
+        self.q8 = q8                                           # attend over the 8-bit cache
         self.inp = W.Inputs(w)
         self.K = self.inp.k(dev)
         self.V = self.inp.v(dev)
@@ -194,9 +195,15 @@ class DecodeBench:
         self.O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=dev)
         self.lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         self.qs = [self.Q[s].contiguous() for s in range(w.n_q)]
+        if q8:
+            self.Kq, self.Ks, self.Vq, self.Vs = ssa.q8_cache(self.p, dev)
+            ssa.ssa_quantize_kv(self.p, self.K, self.V, 0, w.L, self.Kq, self.Ks, self.Vq, self.Vs)
 
     def build_summaries(self):
-        ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
+        if self.q8:
+            ssa.ssa_build_summaries_q8(self.p, self.Kq, self.Ks, 0, self.w.n_spans, self.summ)
+        else:
+            ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
 
     def route(self, i):
         if self.group:
@@ -206,8 +213,12 @@ class DecodeBench:
             ssa.ssa_route(self.p, self.qs[i], 1, self.w.q_pos0 + i, self.summ, self.sels[i])
 
     def attend(self, i):
-        ssa.ssa_attend_decode(self.p, self.qs[i], self.w.q_pos0 + i, self.K, self.V, self.sels[i],
-                              self.O, self.lse, self.ws)
+        if self.q8:
+            ssa.ssa_attend_decode_q8(self.p, self.qs[i], self.w.q_pos0 + i, self.Kq, self.Ks, self.Vq, self.Vs,
+                                     self.sels[i], self.O, self.lse, self.ws)
+        else:
+            ssa.ssa_attend_decode(self.p, self.qs[i], self.w.q_pos0 + i, self.K, self.V, self.sels[i],
+                                  self.O, self.lse, self.ws)
 
     def step(self, i):
         self.route(i)
@@ -244,7 +255,8 @@ class DecodeBench:
                 for g in range(w.Hkv):
                     u = np.unique(sel[b, g][sel[b, g] >= 0])
                     kv_rows += len(u) * w.S + (pos - ell * w.S + 1)
-            attend = kv_rows * w.d * el * 2 + 2 * w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
+            row_bytes = (2 * w.d + 8) if self.q8 else w.d * el * 2       # K + V (+ two fp32 scales)
+            attend = kv_rows * row_bytes + 2 * w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
             route = w.B * w.Hkv * ell * w.d * 4 + w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
             out.append((attend, route))
         return out
@@ -360,6 +372,38 @@ def bench_decode_group(w, dev, steps, ws_n):
             "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": pk["source"]},
+            "device_error_bits": err}
+
+
+def bench_decode_q8(w, dev, steps, ws_n):
+    """The same decode workload over the 8-bit cache (per-head selection on
+    the summaries of the dequantised keys): a step streams the same spans
+    at 2 d + 8 bytes per token instead of 4 d."""
+    db = DecodeBench(w, dev, q8=True)
+    st = torch.cuda.current_stream(dev)
+    db.build_summaries()
+    per_q = db.algorithmic_bytes()
+    n = w.n_q
+    reps = max(1, steps // n)
+    g_step = db.graph(db.step, n)
+    g_att = db.graph(db.attend, n)
+    g_step.replay()
+    g_att.replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
+    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
+    err = ssa.ssa_workspace_error(db.ws)
+    attend_bytes = sum(a for a, _ in per_q) / n
+    pk = peaks()
+    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
+    return {"workload": w.name, "cache": "8-bit K / V, one fp32 scale per token row; fp32 summaries",
+            "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
+            "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                         "kernel": "ssa_attend_decode_q8 (plan + gathered 8-bit K/V attend + merge)",
                          "peak_source": pk["source"]},
             "device_error_bits": err}
 
@@ -643,6 +687,8 @@ def main():
                     help="skip the dense-attention comparison (PyTorch SDPA on the same shapes)")
     ap.add_argument("--no-group", action="store_true",
                     help="skip the decode line with group-shared selection")
+    ap.add_argument("--no-q8", action="store_true",
+                    help="skip the decode line over the 8-bit cache")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
@@ -675,6 +721,10 @@ def main():
         torch.cuda.empty_cache()
         grp = bench_decode_group(w, dev, min(steps, 4096), ws_n)
         torch.cuda.empty_cache()
+    q8 = None
+    if not args.no_decode and not args.no_q8:
+        q8 = bench_decode_q8(w, dev, min(steps, 4096), ws_n)
+        torch.cuda.empty_cache()
     if not args.no_prefill:
         wp = W.PREFILL_1M
         if args.prefill_128k:
@@ -706,6 +756,8 @@ def main():
     line["gpu_launches"] = steps * launches_per_decode_step(w)
     if grp is not None:
         line["decode_group_shared"] = grp
+    if q8 is not None:
+        line["decode_q8"] = q8
     if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1
             and not (args.decode_L or args.prefill_L or args.prefill_chunk or args.prefill_128k)):
         torch.cuda.empty_cache()

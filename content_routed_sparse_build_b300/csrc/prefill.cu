@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(o_free);
+      if (lane == 0) ptx::mbar_arrive_relaxed(o_free);
       if (slot >= 0 && half == 0) a.pml[slot] = make_float2(M, lt);
       return true;
     };
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tc::st32(tS, pk);
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&p_full[2 * st + half]);
+        if (lane == 0) ptx::mbar_arrive_relaxed(&p_full[2 * st + half]);
       }
       if (!ok) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);

@@ -1,0 +1,197 @@
+"""The 8-bit cache against the oracle.
+
+* ssa_quantize_kv: codes and scales bit for bit equal to the oracle's fp32
+  quantiser (an integer decided in floating point: both sides divide in
+  IEEE fp32 and round to nearest even); the V tile layout is unpacked here
+  from its definition in the public header.
+* ssa_build_summaries_q8: the mean of the dequantised keys.
+* decode over the 8-bit cache: selections equal the oracle's on the
+  dequantised cache (margin-checked inputs), outputs within the 16-bit
+  tolerance of the oracle's exact attention over the dequantised K / V.
+
+SubQ release post (geeks.co.kr/post/2077), quantisation plan: 8-bit K / V
+with the summaries kept in fp32.
+"""
+import numpy as np
+import pytest
+import torch
+
+import content_routed_sparse_build_b300 as ssa
+import oracle
+from synth import workloads as W
+
+from harness import LSE_TOL, MARGIN, TOL, max_abs
+
+pytestmark = pytest.mark.gpu
+
+
+def vq_token_of_byte():
+    """Token (0..31) held by byte b of a tile's d-row, from the header's
+    definition: byte 8 c + e holds token 16 (e / 4) + (2c, 2c+1, 2c+8, 2c+9)[e % 4]."""
+    tok = np.zeros(32, np.int64)
+    for c in range(4):
+        for e in range(8):
+            tok[8 * c + e] = 16 * (e // 4) + (2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9)[e % 4]
+    assert sorted(tok.tolist()) == list(range(32))
+    return tok
+
+
+def unpack_vq(Vq: torch.Tensor) -> np.ndarray:
+    """[B, Hkv, L_cap / 32, d, 32] tile layout -> row-major [B, Hkv, L_cap, d]."""
+    a = Vq.cpu().numpy()
+    B, H, T, d, _ = a.shape
+    out = np.zeros((B, H, T, 32, d), np.int8)
+    tok = vq_token_of_byte()
+    out[:, :, :, tok, :] = np.transpose(a, (0, 1, 2, 4, 3))
+    return out.reshape(B, H, T * 32, d)
+
+
+QCASES = [
+    ("bf16_d128", 1, 2, 128, 320, 5, 300, torch.bfloat16),
+    ("f16_d64_b2", 2, 1, 64, 96, 0, 96, torch.float16),
+    ("f32_d128", 1, 3, 128, 64, 31, 33, torch.float32),
+]
+
+
+@pytest.mark.parametrize("name,B,Hkv,d,L,t0,t1,dt", QCASES, ids=[c[0] for c in QCASES])
+def test_quantize_matches_oracle_bit_for_bit(name, B, Hkv, d, L, t0, t1, dt):
+    g = torch.Generator().manual_seed(7)
+    K = (torch.randn((B, Hkv, L, d), generator=g) * 3).to(dt)
+    V = (torch.randn((B, Hkv, L, d), generator=g) * 0.7).to(dt)
+    K[0, 0, t0] = 0                                   # an all-zero row: scale 0, codes 0
+    if t1 - t0 > 1:
+        K[0, 0, t0 + 1, :4] = torch.tensor([127.0, 0.5, 1.5, -2.5]).to(dt)   # ties to even
+        K[0, 0, t0 + 1, 4:] = 0
+    p = ssa.params(B, 8 * Hkv, Hkv, d, L, 64, 4, dt)
+    Kq, Ks, Vq, Vs = ssa.q8_cache(p)
+    for t in (Kq, Vq):
+        t.fill_(99)
+    for t in (Ks, Vs):
+        t.fill_(-1.0)
+    ssa.ssa_quantize_kv(p, K.cuda(), V.cuda(), t0, t1, Kq, Ks, Vq, Vs)
+    torch.cuda.synchronize()
+    qk, sk = oracle.quantize_rows(K[:, :, t0:t1].contiguous())
+    qv, sv = oracle.quantize_rows(V[:, :, t0:t1].contiguous())
+    Kq_h, Ks_h, Vs_h = Kq.cpu().numpy(), Ks.cpu().numpy(), Vs.cpu().numpy()
+    Vq_h = unpack_vq(Vq)
+    assert np.array_equal(Kq_h[:, :, t0:t1], qk)
+    assert np.array_equal(Vq_h[:, :, t0:t1], qv)
+    assert np.array_equal(Ks_h[:, :, t0:t1].view(np.uint32), sk.view(np.uint32))
+    assert np.array_equal(Vs_h[:, :, t0:t1].view(np.uint32), sv.view(np.uint32))
+    for a in (Kq_h, Vq_h):
+        assert (a[:, :, :t0] == 99).all() and (a[:, :, t1:] == 99).all()
+    for a in (Ks_h, Vs_h):
+        assert (a[:, :, :t0] == -1).all() and (a[:, :, t1:] == -1).all()
+    if t1 - t0 > 1:
+        assert Kq_h[0, 0, t0].tolist() == [0] * d and Ks_h[0, 0, t0] == 0
+        assert Kq_h[0, 0, t0 + 1, :4].tolist() == [127, 0, 2, -2]
+
+
+def test_summaries_q8_are_means_of_the_dequantised_keys():
+    B, Hkv, d, L, S = 1, 2, 128, 1000 + 24, 100
+    g = torch.Generator().manual_seed(8)
+    K = torch.randn((B, Hkv, L, d), generator=g).to(torch.bfloat16)
+    p = ssa.params(B, 8, Hkv, d, 1000, S, 4, torch.bfloat16, L_cap=L)
+    Kq, Ks, Vq, Vs = ssa.q8_cache(p)
+    ssa.ssa_quantize_kv(p, K.cuda(), K.cuda(), 0, 1000, Kq, Ks, Vq, Vs)
+    ns_cap = (L + S - 1) // S
+    summ = torch.full((B, Hkv, ns_cap, d), float("nan"), dtype=torch.float32, device="cuda")
+    ssa.ssa_build_summaries_q8(p, Kq, Ks, 0, 10, summ)
+    q, s = oracle.quantize_rows(K.contiguous())
+    ref = oracle.summaries(oracle.dequantize_rows(q, s), 1000, S, 0, 10)
+    got = summ.cpu().double().numpy()
+    assert np.isnan(got[:, :, 10:]).all()
+    # fp32 sums of 100 products of magnitude below 5: well inside 2e-5
+    err = np.abs(got[:, :, :10] - ref[:, :, :10]).max()
+    assert err <= 2e-5, err
+
+
+DCASES = [
+    # ragged: the local span ends mid-tile; S a multiple of 32
+    W.Workload("q8_bf16_gqa8", "decode", 1, 32, 4, 128, 65536 + 100, 1024, 16, torch.bfloat16,
+               n_q=2, q_pos0=65536 + 98, chunk=1, needles=4, seed=81),
+    # S = 300 (not a multiple of 32 tokens): items start inside a tile
+    W.Workload("q8_f16_s300_b2", "decode", 2, 16, 2, 128, 20000 + 32, 300, 8, torch.float16,
+               n_q=2, q_pos0=19990, chunk=1, needles=2, seed=82),
+    # g = 16: two head groups per warp
+    W.Workload("q8_bf16_g16", "decode", 1, 32, 2, 128, 8192, 100, 12, torch.bfloat16,
+               n_q=2, q_pos0=8000, chunk=1, seed=83),
+]
+
+
+@pytest.mark.parametrize("w", DCASES, ids=lambda w: w.name)
+def test_decode_q8_matches_oracle_on_the_dequantised_cache(w):
+    n_rows = int(np.prod(w.q_shape[:-1]))
+    attempt = torch.zeros(n_rows, dtype=torch.int32)
+    inp = W.Inputs(w, attempt=attempt)
+    K, V = inp.k(), inp.v()
+    qk, sk = oracle.quantize_rows(K)
+    qv, sv = oracle.quantize_rows(V)
+    Kdq, Vdq = oracle.dequantize_rows(qk, sk), oracle.dequantize_rows(qv, sv)
+    summ_o = oracle.summaries(Kdq, w.L, w.S)
+    Q = inp.q()
+    for _ in range(32):
+        margins = []
+        for s in range(w.n_q):
+            _, m = oracle.route(Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous(), w.q_pos0 + s, summ_o,
+                                w.Hkv, w.S, w.topk)
+            margins.append(m)
+        bad = np.nonzero(np.stack(margins).reshape(-1) < MARGIN)[0]
+        if len(bad) == 0:
+            break
+        attempt[bad] += 1
+        Q = inp.q()
+    else:
+        raise RuntimeError("margins not reached")
+    L_cap = (w.L + 31) // 32 * 32
+    Kd = torch.zeros((w.B, w.Hkv, L_cap, w.d), dtype=w.dtype, device="cuda")
+    Vd = torch.zeros_like(Kd)
+    Kd[:, :, :w.L] = K.cuda()
+    Vd[:, :, :w.L] = V.cuda()
+    p_full = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype, L_cap=L_cap)
+    Kq, Ks, Vq, Vs = ssa.q8_cache(p_full)
+    Ks.fill_(float("nan"))                         # rows past L: masked, never read as numbers
+    Vs.fill_(float("nan"))
+    ssa.ssa_quantize_kv(p_full, Kd, Vd, 0, w.L, Kq, Ks, Vq, Vs)
+    ns_cap = (L_cap + w.S - 1) // w.S
+    summ = torch.zeros((w.B, w.Hkv, ns_cap, w.d), dtype=torch.float32, device="cuda")
+    ws = ssa.workspace(p_full, 1, ssa.SSA_OP_DECODE)
+    Qd = Q.cuda()
+    for s in range(w.n_q):
+        pos = w.q_pos0 + s
+        p = ssa.params(w.B, w.Hq, w.Hkv, w.d, pos + 1, w.S, w.topk, w.dtype, L_cap=L_cap)
+        ssa.ssa_build_summaries_q8(p, Kq, Ks, 0, pos // w.S, summ)
+        q = Qd[s].contiguous()
+        sel = torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device="cuda")
+        O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device="cuda")
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+        ssa.ssa_route(p, q, 1, pos, summ, sel)
+        ssa.ssa_attend_decode_q8(p, q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+        qh = Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous()
+        sel_o, _ = oracle.route(qh, pos, summ_o, w.Hkv, w.S, w.topk)
+        assert np.array_equal(sel.reshape(-1, w.topk).cpu().numpy(), sel_o), pos
+        O_o, lse_o, _ = oracle.attend(qh.double(), Kdq, Vdq, pos, w.S, sel_o)
+        assert max_abs(O.reshape(-1, w.d).cpu(), O_o) <= TOL[w.dtype]
+        assert max_abs(lse.reshape(-1).cpu(), lse_o) <= LSE_TOL[w.dtype]
+    assert ssa.ssa_workspace_error(ws) == 0
+
+
+def test_q8_entry_points_reject_what_they_do_not_take():
+    t = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    i8 = torch.zeros(64, dtype=torch.int8, device="cuda")
+    f = torch.zeros(64, dtype=torch.float32, device="cuda")
+    sel = torch.zeros(64, dtype=torch.int32, device="cuda")
+    p = ssa.params(1, 8, 2, 128, 100, 64, 4, torch.bfloat16, L_cap=100)     # L_cap not a multiple of 32
+    for call in (lambda: ssa.ssa_quantize_kv(p, t, t, 0, 10, i8, f, i8, f),
+                 lambda: ssa.ssa_attend_decode_q8(p, t, 5, i8, f, i8, f, sel, t, None, None)):
+        with pytest.raises(ssa.SSAError) as e:
+            call()
+        assert e.value.status == ssa.SSA_ERR_UNSUPPORTED
+    p64 = ssa.params(1, 8, 2, 64, 128, 64, 4, torch.bfloat16)               # d = 64: no 8-bit attention
+    with pytest.raises(ssa.SSAError) as e:
+        ssa.ssa_attend_decode_q8(p64, t, 5, i8, f, i8, f, sel, t, None, None)
+    assert e.value.status == ssa.SSA_ERR_UNSUPPORTED
+    p = ssa.params(1, 8, 2, 128, 128, 64, 4, torch.bfloat16)
+    with pytest.raises(ssa.SSAError) as e:
+        ssa.ssa_quantize_kv(p, t, t, 0, 129, i8, f, i8, f)                 # t_end > L
+    assert e.value.status == ssa.SSA_ERR_INVALID_ARG

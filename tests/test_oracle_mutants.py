@@ -28,6 +28,8 @@ MUTANTS = {
     "max_not_subtracted_in_lse": ("lse[o] = mx + log(denom);", "lse[o] = log(denom);"),
     "group_sum_first_head_only": ("for (int64_t hh = grp * g; hh < grp * g + g; ++hh) {",
                                   "for (int64_t hh = grp * g; hh < grp * g + 1; ++hh) {"),
+    "quantize_ties_away_from_zero": ("float t = rintf(x / s);", "float t = roundf(x / s);"),
+    "quantize_scale_over_128": ("const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
     "values_from_keys": ("load_f64(dtype, V, (kvh * L_cap + tok[u]) * d + c)",
                          "load_f64(dtype, K, (kvh * L_cap + tok[u]) * d + c)"),
 }

@@ -352,3 +352,60 @@ def test_needles_raise_selection_rate():
         nd = inp.needle_spans[h]
         other = np.setdiff1d(np.arange(32), nd)
         assert counts[nd].mean() > counts[other].mean()
+
+
+# ---------------------------------------------------------------- 8-bit rows
+# The quantiser (SubQ release post, quantisation plan; scheme fixed by the
+# library: symmetric rows, s = max|x| / 127, q = rint(x / s) in fp32).
+
+
+def test_quantize_hand_examples():
+    # s = 127 / 127 = 1 exactly: codes are the nearest integers, ties to even
+    x = torch.tensor([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.49, -126.6]], dtype=torch.float32)
+    q, s = oracle.quantize_rows(x)
+    assert s.tolist() == [1.0]
+    assert q.tolist() == [[127, 0, 2, 2, 0, -2, 3, -127]]
+    # all-zero row: scale 0, codes 0; negative extreme maps to -127
+    x = torch.tensor([[0.0, 0.0], [-4.0, 1.0]], dtype=torch.float32)
+    q, s = oracle.quantize_rows(x)
+    assert q.tolist() == [[0, 0], [-127, 32]]      # 1 / (4 / 127) = 31.75 -> 32
+    assert s[0] == 0.0 and s[1] == np.float32(4.0) / np.float32(127.0)
+
+
+def test_quantize_invariants_on_random_rows():
+    g = torch.Generator().manual_seed(3)
+    for dt in (torch.float32, torch.bfloat16, torch.float16):
+        x = (torch.randn((64, 128), generator=g) * torch.rand((64, 1), generator=g) * 10).to(dt)
+        q, s = oracle.quantize_rows(x)
+        xf = x.float().numpy().astype(np.float64)
+        amax = np.abs(xf).max(axis=1)
+        # the largest element of every row maps to +-127
+        assert (np.abs(q).max(axis=1) == 127).all()
+        assert np.allclose(s, amax / 127.0, rtol=2 ** -23, atol=0)
+        # reconstruction within half a step, plus the fp32 rounding of s and
+        # of x / s (relative 2^-24 each, times at most 127 steps)
+        err = np.abs(xf - q.astype(np.float64) * s.astype(np.float64)[:, None])
+        assert (err <= (0.5 + 127 * 2.0 ** -22) * s[:, None]).all()
+        # signs agree or the code is 0
+        assert ((np.sign(q) == np.sign(xf)) | (q == 0)).all()
+
+
+def test_quantize_is_equivariant_under_powers_of_two():
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn((16, 64), generator=g)
+    q1, s1 = oracle.quantize_rows(x)
+    for k in (-3, 5):
+        q2, s2 = oracle.quantize_rows(x * 2.0 ** k)
+        assert np.array_equal(q1, q2)
+        assert np.array_equal(s2, s1 * np.float32(2.0 ** k))
+
+
+def test_dequantized_summaries_and_attention_accept_f64():
+    g = torch.Generator().manual_seed(5)
+    K = torch.randn((1, 1, 32, 4), generator=g)
+    q, s = oracle.quantize_rows(K)
+    Kd = oracle.dequantize_rows(q, s)
+    assert Kd.dtype == torch.float64
+    assert np.array_equal(Kd.numpy(), q.astype(np.float64) * s.astype(np.float64)[..., None])
+    summ = oracle.summaries(Kd, 32, 8)
+    assert np.allclose(summ[0, 0], Kd.numpy()[0, 0].reshape(4, 8, 4).mean(axis=1), rtol=0, atol=1e-15)
