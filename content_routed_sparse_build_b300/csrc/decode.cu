@@ -56,7 +56,6 @@ struct Geo {
   int Hq, Hkv, g, topk, S, C, CH, umax, n_grp;
   int64_t pos, ell;
   float scale_log2e;
-  int tables_in_smem;  // plan tables and Q copied to shared memory
 };
 
 template <int D>
@@ -66,7 +65,6 @@ struct Cfg {
   static constexpr int kHalf = kBoxes * kBox;      // K (or V) bytes per stage
   static constexpr int kStage = 2 * kHalf;
   static constexpr int kStages = D == 128 ? 2 : 4;
-  static constexpr int kQStride = D + 8;           // 16-bit elements per Q row in shared memory
   static constexpr size_t kRing = (size_t)kWarps * kStages * kStage;
   static constexpr size_t kBars = (size_t)kWarps * kStages * 8;
   static constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
@@ -224,7 +222,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
 }
 
 // ---------------------------------------------------------------- attend
-// Where each warp reads the plan: shared-memory copies when they fit.
+// Where each warp reads the plan.  The tables stay in global memory (L1 /
+// L2 hits): copying them into shared memory at kernel start delayed every
+// warp's first load by several microseconds per step.
 struct Tables {
   const int* gpref;       // [n_grp + 1] item prefix over groups
   const int* n_union;     // [n_grp]
@@ -276,13 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing);
   int4* metas = reinterpret_cast<int4*>(bars + kWarps * C::kStages);
   int* s_gpref = reinterpret_cast<int*>(metas + kWarps * C::kStages);
-  uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_gpref + kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
-  const int n_slots = geo.n_grp * geo.umax;
-
-  // ---- shared set-up: barriers, group prefix, plan tables
+  // ---- shared set-up: barriers, group prefix
   if (tid == 0) {
     for (int s = 0; s < kWarps * C::kStages; ++s) ptx::mbar_init(&bars[s], 1);
     ptx::fence_mbar_init();
@@ -293,38 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::pdl_launch_dependents();
   Tables tb;
   tb.gpref = s_gpref;
-  if (geo.tables_in_smem) {
-    int* nu_s = reinterpret_cast<int*>(s_tab);
-    int* sp_s = nu_s + geo.n_grp;
-    uint32_t* mk_s = reinterpret_cast<uint32_t*>(sp_s + n_slots);
-    uint16_t* q_s = reinterpret_cast<uint16_t*>(mk_s + n_slots);
-    const int nq_rows = geo.n_grp * geo.g;  // B * Hq
-    uint8_t* rk_s = reinterpret_cast<uint8_t*>(q_s + nq_rows * C::kQStride);
-    for (int x = tid; x < geo.n_grp; x += kThreads) nu_s[x] = plan.n_union[x];
-    for (int x = tid; x < n_slots; x += kThreads) {
-      sp_s[x] = plan.span[x];
-      mk_s[x] = plan.mask[x];
-    }
-    for (int x = tid; x < n_slots * 4; x += kThreads)
-      reinterpret_cast<uint32_t*>(rk_s)[x] = reinterpret_cast<const uint32_t*>(plan.rank)[x];
-    for (int x = tid; x < nq_rows * (D / 2); x += kThreads) {
-      const int r = x / (D / 2), c = x - r * (D / 2);
-      reinterpret_cast<uint32_t*>(q_s + r * C::kQStride)[c] = reinterpret_cast<const uint32_t*>(Q)[x];
-    }
-    tb.n_union = nu_s;
-    tb.span = sp_s;
-    tb.mask = mk_s;
-    tb.rank = rk_s;
-    tb.q = q_s;
-    tb.q_stride = C::kQStride;
-  } else {
-    tb.n_union = plan.n_union;
-    tb.span = plan.span;
-    tb.mask = plan.mask;
-    tb.rank = plan.rank;
-    tb.q = static_cast<const uint16_t*>(Q);
-    tb.q_stride = D;
-  }
+  tb.n_union = plan.n_union;
+  tb.span = plan.span;
+  tb.mask = plan.mask;
+  tb.rank = plan.rank;
+  tb.q = static_cast<const uint16_t*>(Q);
+  tb.q_stride = D;
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < geo.n_grp; base += 32) {
@@ -611,7 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 2 J and bytes 4-7 k-step 2 J + 1; Q's fragments are built with the same
 // d-to-k map, so every product still pairs K[t][d] with Q[h][d].
 namespace q8 {
-constexpr int kStages = 3;
+// Twelve warps of two stages: an 8-bit tile is half the bytes of a 16-bit
+// one, so the same ring holds twice the warps, which hide the conversion
+// and MMA latency of each tile.
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 2;
 constexpr int kKBytes = kTile * 128;   // 32 rows of 128 int8
 constexpr int kVBytes = kTile * 128;   // 128 d-rows of 32 tokens
 constexpr int kSBytes = 2 * kTile * 4; // ks then vs
@@ -621,7 +597,6 @@ constexpr size_t kRingS = (size_t)kWarps * kStages * kSBytes;
 constexpr size_t kBars = (size_t)kWarps * kStages * 8;
 constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
 constexpr size_t kFixed = 1024 + kRingK + kRingV + kRingS + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
-constexpr int kQStride = 128 + 8;
 
 // First 32-aligned tile start and tile count of tokens [t0, t1).
 __device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kTile - 1); }
@@ -631,7 +606,7 @@ __device__ __forceinline__ int tiles(int64_t t0, int64_t t1) {
 }  // namespace q8
 
 template <int DT, int NG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(q8::kThreads, 1)
     decode_attend_q8_kernel(const __grid_constant__ CUtensorMap tmK, const int8_t* __restrict__ Vq,
                             const float* __restrict__ Ks, const float* __restrict__ Vs, int64_t L_cap,
                             const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
@@ -643,16 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ringV = ringK + q8::kRingK;
   uint8_t* ringS = ringV + q8::kRingV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ringS + q8::kRingS);
-  int4* metas = reinterpret_cast<int4*>(bars + kWarps * q8::kStages);
-  int* s_gpref = reinterpret_cast<int*>(metas + kWarps * q8::kStages);
-  uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_gpref + kMaxGroups + 1);
+  int4* metas = reinterpret_cast<int4*>(bars + q8::kWarps * q8::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metas + q8::kWarps * q8::kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
-  const int n_slots = geo.n_grp * geo.umax;
-
   if (tid == 0) {
-    for (int s = 0; s < kWarps * q8::kStages; ++s) ptx::mbar_init(&bars[s], 1);
+    for (int s = 0; s < q8::kWarps * q8::kStages; ++s) ptx::mbar_init(&bars[s], 1);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmK);
   }
@@ -660,38 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::pdl_launch_dependents();
   Tables tb;
   tb.gpref = s_gpref;
-  if (geo.tables_in_smem) {
-    int* nu_s = reinterpret_cast<int*>(s_tab);
-    int* sp_s = nu_s + geo.n_grp;
-    uint32_t* mk_s = reinterpret_cast<uint32_t*>(sp_s + n_slots);
-    uint16_t* q_s = reinterpret_cast<uint16_t*>(mk_s + n_slots);
-    const int nq_rows = geo.n_grp * geo.g;
-    uint8_t* rk_s = reinterpret_cast<uint8_t*>(q_s + nq_rows * q8::kQStride);
-    for (int x = tid; x < geo.n_grp; x += kThreads) nu_s[x] = plan.n_union[x];
-    for (int x = tid; x < n_slots; x += kThreads) {
-      sp_s[x] = plan.span[x];
-      mk_s[x] = plan.mask[x];
-    }
-    for (int x = tid; x < n_slots * 4; x += kThreads)
-      reinterpret_cast<uint32_t*>(rk_s)[x] = reinterpret_cast<const uint32_t*>(plan.rank)[x];
-    for (int x = tid; x < nq_rows * (D / 2); x += kThreads) {
-      const int r = x / (D / 2), c = x - r * (D / 2);
-      reinterpret_cast<uint32_t*>(q_s + r * q8::kQStride)[c] = reinterpret_cast<const uint32_t*>(Q)[x];
-    }
-    tb.n_union = nu_s;
-    tb.span = sp_s;
-    tb.mask = mk_s;
-    tb.rank = rk_s;
-    tb.q = q_s;
-    tb.q_stride = q8::kQStride;
-  } else {
-    tb.n_union = plan.n_union;
-    tb.span = plan.span;
-    tb.mask = plan.mask;
-    tb.rank = plan.rank;
-    tb.q = static_cast<const uint16_t*>(Q);
-    tb.q_stride = D;
-  }
+  tb.n_union = plan.n_union;
+  tb.span = plan.span;
+  tb.mask = plan.mask;
+  tb.rank = plan.rank;
+  tb.q = static_cast<const uint16_t*>(Q);
+  tb.q_stride = D;
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < geo.n_grp; base += 32) {
@@ -835,11 +781,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* svs = sks + kTile;
 
     // S^T = Kq Q^T per 16-token fragment t
-    float s[NG][kSub][4];
+    float s[NG][kSub][4], s2[NG][kSub][4];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
-      for (int t = 0; t < kSub; ++t) s[ng][t][0] = s[ng][t][1] = s[ng][t][2] = s[ng][t][3] = 0.f;
+      for (int t = 0; t < kSub; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[ng][t][i] = s2[ng][t][i] = 0.f;
 #pragma unroll
     for (int J = 0; J < D / 32; ++J) {
 #pragma unroll
@@ -856,10 +804,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
           ptx::mma16816<DT_F16>(s[ng][t], a0, qf[ng][J][0], qf[ng][J][1]);
-          ptx::mma16816<DT_F16>(s[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
+          ptx::mma16816<DT_F16>(s2[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
         }
       }
     }
+    // the odd k-steps accumulated apart (two independent MMA chains per fragment)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[ng][t][i] += s2[ng][t][i];
     // rows (tokens) r8 and r8 + 8 of each fragment: K / V scales, validity
     const int64_t tbase = q8::tile_base(cur.t0) + (int64_t)mt.w * kTile;
     float ksc[kSub][2], vsc[kSub][2];
@@ -1075,11 +1030,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
 }
 
-size_t tables_bytes(const Problem& pr) {
-  const size_t n_grp = (size_t)pr.B * pr.Hkv;
-  const size_t slots = n_grp * ((size_t)pr.g * pr.topk + 1);
-  return n_grp * 4 + slots * (4 + 4 + 16) + (size_t)pr.B * pr.Hq * (pr.d + 8) * 2;
-}
 
 // The plan's workspace pointers and the geometry of a decode step.
 void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
@@ -1105,7 +1055,6 @@ void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
   geo.pos = pos;
   geo.ell = pos / pr.S;
   geo.scale_log2e = pr.scale * kLog2e;
-  geo.tables_in_smem = 0;
 }
 
 template <int DT>
@@ -1116,9 +1065,7 @@ cudaError_t launch_typed_q8(const Problem& pr, const void* Q, int64_t pos, const
   Plan plan;
   Geo geo;
   plan_geo(pr, pos, ws, plan, geo);
-  const size_t tb = tables_bytes(pr);
-  geo.tables_in_smem = q8::kFixed + tb <= (size_t)kSmemLimit;
-  const size_t smem = q8::kFixed + (geo.tables_in_smem ? tb : 0);
+  const size_t smem = q8::kFixed;
   uint32_t* err = ws_error(ws);
   CUtensorMap tmK;
   cudaError_t e = make_q8_tmap(&tmK, Kq, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
@@ -1129,7 +1076,7 @@ cudaError_t launch_typed_q8(const Problem& pr, const void* Q, int64_t pos, const
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), smem, st, tmK, Vq, Ks, Vs, pr.L_cap, Q, plan,
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(q8::kThreads), smem, st, tmK, Vq, Ks, Vs, pr.L_cap, Q, plan,
                  geo, err);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st,
@@ -1164,9 +1111,7 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const vo
   geo.pos = pos;
   geo.ell = pos / pr.S;
   geo.scale_log2e = pr.scale * kLog2e;
-  const size_t tb = tables_bytes(pr);
-  geo.tables_in_smem = Cf::kFixed + tb <= (size_t)kSmemLimit;
-  const size_t smem = Cf::kFixed + (geo.tables_in_smem ? tb : 0);
+  const size_t smem = Cf::kFixed;
   uint32_t* err = ws_error(ws);
 
   CUtensorMap tmK, tmV;
