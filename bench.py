@@ -156,7 +156,8 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 # from.  They are reported as the roofline's "traffic" only for the workload
 # they were measured on.
 NCU_TRAFFIC = {
-    "decode_1m": (None, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
+    "decode_1m": (2.189e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
+    "decode_1m_q8": (1.133e8, "profiles/decode_1m_launches.md: plan + 8-bit attend + merge per step"),
     "prefill_chunk_vs_1m": (3.856e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
 }
 
@@ -402,7 +403,8 @@ def bench_decode_q8(w, dev, steps, ws_n):
             "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
             "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic_of(w.name + "_q8")[0],
+                         "traffic_source": traffic_of(w.name + "_q8")[1],
                          "kernel": "ssa_attend_decode_q8 (plan + gathered 8-bit K/V attend + merge)",
                          "peak_source": pk["source"]},
             "device_error_bits": err}
