@@ -112,7 +112,14 @@ Layout layout(const Problem& pr) {
 // One CTA per (b, kv-head), one warp per query head of the group.  Also
 // empties the (m, l) slots of the group's partials: a slot that no item
 // writes keeps m = -inf and the merge skips it.
+//
+// The position of span j in the union U is the number of distinct selected
+// spans below j.  Up to kPlanBits candidates it is read off a bitmap of the
+// selected spans (a prefix popcount over its words); beyond that, each
+// span's position comes from binary searches in the heads' sorted lists.
 constexpr int kPlanThreads = kMaxG * 32;
+constexpr int kPlanWords = 512;
+constexpr int64_t kPlanBits = kPlanWords * 32;
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t* __restrict__ sel,
                                                                    Plan plan, Geo geo,
@@ -122,6 +129,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
   __shared__ int cpref[kMaxG][kMaxK + 1];  // prefix counts of canonical entries
   __shared__ uint8_t canon[kMaxG][kMaxK];
   __shared__ uint32_t smask[kMaxG * kMaxK + 1];
+  __shared__ uint32_t bits[kPlanWords];     // selected spans (bitmap path)
+  __shared__ int wpref[kPlanWords + 1];     // popcount of the words below
+  __shared__ int s_nu;
 
   const int grp = blockIdx.x;
   const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
@@ -139,6 +149,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
     for (int x = tid; x < nparts; x += kPlanThreads) ml[x] = make_float2(-INFINITY, 0.f);
   }
   for (int x = tid; x < kMaxG * kMaxK + 1; x += kPlanThreads) smask[x] = 0u;
+  const bool bitmap = geo.ell <= kPlanBits;
+  const int nw = bitmap ? (int)((geo.ell + 31) >> 5) : 0;
+  for (int x = tid; x < nw; x += kPlanThreads) bits[x] = 0u;
   if (warp < g) {
     const int32_t* row = sel + (int64_t)(b * geo.Hq + kvh * g + warp) * k;
     const int j0 = lane < k ? __ldg(row + lane) : -1;
@@ -151,65 +164,105 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
     if (lane == 0) nv[warp] = used;
   }
   __syncthreads();
-  // canonical entry: no lower head of the group holds the same span
-  if (warp < g) {
-    uint32_t bal[2];
+  const int gbase = grp * umax;
+  if (bitmap) {
+    if (warp < g) {
+      if (lane < nv[warp]) atomicOr(&bits[sj[warp][lane] >> 5], 1u << (sj[warp][lane] & 31));
+      if (lane + 32 < nv[warp]) atomicOr(&bits[sj[warp][lane + 32] >> 5], 1u << (sj[warp][lane + 32] & 31));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int run = 0;
+      for (int base = 0; base < nw; base += 32) {
+        const int c = base + lane < nw ? __popc(bits[base + lane]) : 0;
+        int v = c;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int r = lane + 32 * hh;
-      bool c = false;
-      if (r < nv[warp]) {
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, v, off);
+          if (lane >= off) v += o;
+        }
+        if (base + lane < nw) wpref[base + lane] = run + v - c;
+        run += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) s_nu = run;
+    }
+    __syncthreads();
+    if (warp < g) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = lane + 32 * hh;
+        if (r >= nv[warp]) continue;
         const int j = sj[warp][r];
-        bool dup = false;
+        const int p = wpref[j >> 5] + __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u));
+        // the first head to claim the position writes the span
+        if (atomicOr(&smask[p], 1u << warp) == 0u) plan.span[gbase + p] = j;
+        plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
+      }
+    }
+  } else {
+    // canonical entry: no lower head of the group holds the same span
+    if (warp < g) {
+      uint32_t bal[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = lane + 32 * hh;
+        bool c = false;
+        if (r < nv[warp]) {
+          const int j = sj[warp][r];
+          bool dup = false;
+#pragma unroll
+          for (int h2 = 0; h2 < kMaxG; ++h2) {
+            if (h2 < warp) {
+              int lo = 0, hi = nv[h2];
+              while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
+              }
+              dup |= lo < nv[h2] && sj[h2][lo] == j;
+            }
+          }
+          c = !dup;
+          canon[warp][r] = c ? 1 : 0;
+        }
+        bal[hh] = __ballot_sync(0xffffffffu, c);
+      }
+      cpref[warp][lane] = __popc(bal[0] & lt);
+      cpref[warp][lane + 32] = __popc(bal[0]) + __popc(bal[1] & lt);
+      if (lane == 0) cpref[warp][64] = __popc(bal[0]) + __popc(bal[1]);
+    }
+    __syncthreads();
+    // position of span j in U = number of distinct spans below j
+    if (warp < g) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = lane + 32 * hh;
+        if (r >= nv[warp]) continue;
+        const int j = sj[warp][r];
+        int p = 0;
 #pragma unroll
         for (int h2 = 0; h2 < kMaxG; ++h2) {
-          if (h2 < warp) {
+          if (h2 < g) {
             int lo = 0, hi = nv[h2];
             while (lo < hi) {
               const int mid = (lo + hi) >> 1;
               if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
             }
-            dup |= lo < nv[h2] && sj[h2][lo] == j;
+            p += cpref[h2][lo];
           }
         }
-        c = !dup;
-        canon[warp][r] = c ? 1 : 0;
+        if (canon[warp][r]) plan.span[gbase + p] = j;
+        atomicOr(&smask[p], 1u << warp);
+        plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
       }
-      bal[hh] = __ballot_sync(0xffffffffu, c);
     }
-    cpref[warp][lane] = __popc(bal[0] & lt);
-    cpref[warp][lane + 32] = __popc(bal[0]) + __popc(bal[1] & lt);
-    if (lane == 0) cpref[warp][64] = __popc(bal[0]) + __popc(bal[1]);
-  }
-  __syncthreads();
-  // position of span j in U = number of distinct spans below j
-  const int gbase = grp * umax;
-  if (warp < g) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int r = lane + 32 * hh;
-      if (r >= nv[warp]) continue;
-      const int j = sj[warp][r];
-      int p = 0;
-#pragma unroll
-      for (int h2 = 0; h2 < kMaxG; ++h2) {
-        if (h2 < g) {
-          int lo = 0, hi = nv[h2];
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
-          }
-          p += cpref[h2][lo];
-        }
-      }
-      if (canon[warp][r]) plan.span[gbase + p] = j;
-      atomicOr(&smask[p], 1u << warp);
-      plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
+    if (tid == 0) {
+      int n = 0;
+      for (int h = 0; h < g; ++h) n += cpref[h][nv[h]];
+      s_nu = n;
     }
   }
   __syncthreads();
-  int nu = 0;
-  for (int h = 0; h < g; ++h) nu += cpref[h][nv[h]];
+  const int nu = s_nu;
   for (int p = tid; p < nu; p += kPlanThreads) plan.mask[gbase + p] = smask[p];
   if (tid < g) plan.rank[(size_t)(gbase + nu) * 16 + tid] = (uint8_t)k;
   if (tid == 0) {
