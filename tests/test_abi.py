@@ -111,3 +111,28 @@ def test_route_group_validation_and_workspace():
     assert call(p, ws=ctypes.c_void_p(4096), wsn=16) == ssa.SSA_ERR_WORKSPACE
     assert call(p, Q=None) == ssa.SSA_ERR_INVALID_ARG
     assert call(ssa.params(1, 8, 3, 128, 4096, 64, 8, 1)) == ssa.SSA_ERR_INVALID_ARG
+
+
+@needs_no_gpu
+def test_q8_validation():
+    L = ssa.lib()
+    P, I8 = ctypes.c_void_p, ctypes.c_int64
+    L.ssa_quantize_kv.argtypes = [ctypes.POINTER(ssa.ssa_params), P, P, I8, I8, P, P, P, P, P]
+    L.ssa_build_summaries_q8.argtypes = [ctypes.POINTER(ssa.ssa_params), P, P, I8, I8, P, P]
+    L.ssa_attend_decode_q8.argtypes = [ctypes.POINTER(ssa.ssa_params), P, I8, P, P, P, P, P, P, P, P,
+                                       ctypes.c_size_t, P]
+    p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
+    q = lambda p, t0, t1, **kw: L.ssa_quantize_kv(ctypes.byref(p), FAKE, kw.get("V", FAKE), t0, t1, FAKE, FAKE,
+                                                  FAKE, FAKE, None)
+    assert q(p, 0, 4097) == ssa.SSA_ERR_INVALID_ARG             # past L
+    assert q(p, 10, 5) == ssa.SSA_ERR_INVALID_ARG
+    assert q(p, 0, 10, V=None) == ssa.SSA_ERR_INVALID_ARG
+    assert q(ssa.params(1, 8, 2, 128, 4001, 64, 8, torch.bfloat16), 0, 10) == ssa.SSA_ERR_UNSUPPORTED  # L_cap % 32
+    assert L.ssa_build_summaries_q8(ctypes.byref(p), FAKE, FAKE, 0, 65, FAKE, None) == ssa.SSA_ERR_INVALID_ARG
+    need = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE)
+    d = lambda p, pos, ws, n: L.ssa_attend_decode_q8(ctypes.byref(p), FAKE, pos, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                     FAKE, None, ws, n, None)
+    assert d(p, 4096, FAKE, need) == ssa.SSA_ERR_INVALID_ARG          # pos == L
+    assert d(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
+    assert d(ssa.params(1, 8, 2, 64, 4096, 64, 8, torch.bfloat16), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    assert d(ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.float32), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
