@@ -377,6 +377,41 @@ def bench_decode_group(w, dev, steps, ws_n):
             "device_error_bits": err}
 
 
+def bench_decode_10m(dev, steps, ws_n):
+    """Decode with a 10M-token cache (S 3072, 3255 candidate spans), per-head
+    selection, to set against the 1M line: the pages report decode slowing by
+    about 30% from 1M to 10M."""
+    w = W.DECODE_10M
+    db = DecodeBench(w, dev)
+    st = torch.cuda.current_stream(dev)
+    db.build_summaries()
+    per_q = db.algorithmic_bytes()
+    n = w.n_q
+    reps = max(1, steps // n)
+    g_step = db.graph(db.step, n)
+    g_att = db.graph(db.attend, n)
+    g_step.replay()
+    g_att.replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
+    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
+    err = ssa.ssa_workspace_error(db.ws)
+    attend_bytes = sum(a for a, _ in per_q) / n
+    pk = peaks()
+    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
+    out = {"workload": w.name, "L": w.L, "S": w.S,
+           "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
+           "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                        "peak_source": pk["source"]},
+           "device_error_bits": err}
+    del db
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_decode_q8(w, dev, steps, ws_n):
     """The same decode workload over the 8-bit cache (per-head selection on
     the summaries of the dequantised keys): a step streams the same spans
@@ -691,6 +726,8 @@ def main():
                     help="skip the decode line with group-shared selection")
     ap.add_argument("--no-q8", action="store_true",
                     help="skip the decode line over the 8-bit cache")
+    ap.add_argument("--no-10m", action="store_true",
+                    help="skip the decode line with a 10M-token cache")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
@@ -727,6 +764,9 @@ def main():
     if not args.no_decode and not args.no_q8:
         q8 = bench_decode_q8(w, dev, min(steps, 4096), ws_n)
         torch.cuda.empty_cache()
+    d10 = None
+    if not args.no_decode and not args.no_10m and not args.decode_L:
+        d10 = bench_decode_10m(dev, min(steps, 2048), ws_n)
     if not args.no_prefill:
         wp = W.PREFILL_1M
         if args.prefill_128k:
@@ -760,6 +800,9 @@ def main():
         line["decode_group_shared"] = grp
     if q8 is not None:
         line["decode_q8"] = q8
+    if d10 is not None:
+        d10["vs_1m"] = d10["value"] / dec["tok_s"] if dec["tok_s"] else None
+        line["decode_10m"] = d10
     if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1
             and not (args.decode_L or args.prefill_L or args.prefill_chunk or args.prefill_128k)):
         torch.cuda.empty_cache()
