@@ -1,5 +1,6 @@
-"""Decode with incremental summary maintenance (the survey's next row #4):
-the cache grows one token per step, and when a step's position starts a new
+"""Decode with incremental summary maintenance (superlinear release post,
+geeks.co.kr/post/2077, "why this matters": the cache is kept and grows with
+the conversation instead of being re-processed): the cache grows one token per step, and when a step's position starts a new
 span, the span just completed gets its summary (one ssa_build_summaries call
 over that span) before the query routes.  Selections and outputs must equal
 the oracle's on the full cache, where every candidate span's summary is the
