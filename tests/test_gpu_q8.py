@@ -195,3 +195,59 @@ def test_q8_entry_points_reject_what_they_do_not_take():
     with pytest.raises(ssa.SSAError) as e:
         ssa.ssa_quantize_kv(p, t, t, 0, 129, i8, f, i8, f)                 # t_end > L
     assert e.value.status == ssa.SSA_ERR_INVALID_ARG
+
+
+def test_decode_q8_1m_sampled_steps():
+    """The 8-bit decode at the full 1M size, in the launch configuration the
+    benchmark times (whole-cache quantisation and summaries, then route +
+    attend per step): eight of the 256 steps, every head.  The oracle works on
+    the dequantised cache, held on the host as fp32 (q * s rounded once to
+    fp32, a 2^-24 relative change, far inside the tolerance)."""
+    w = W.DECODE_1M
+    steps = list(range(0, w.n_q, 32))
+    n_rows = int(np.prod(w.q_shape[:-1]))
+    attempt = torch.zeros(n_rows, dtype=torch.int32)
+    inp = W.Inputs(w, attempt=attempt)
+    dev = torch.device("cuda")
+    Kd, Vd = inp.k(dev), inp.v(dev)
+    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+    Kq, Ks, Vq, Vs = ssa.q8_cache(p)
+    ssa.ssa_quantize_kv(p, Kd, Vd, 0, w.L, Kq, Ks, Vq, Vs)
+    summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+    ssa.ssa_build_summaries_q8(p, Kq, Ks, 0, w.n_spans, summ)
+    del Kd, Vd
+    # host side: the dequantised cache (row-major V from the tile layout)
+    Kdq = torch.from_numpy(Kq.cpu().numpy().astype(np.float32) * Ks.cpu().numpy()[..., None])
+    Vdq = torch.from_numpy(unpack_vq(Vq).astype(np.float32) * Vs.cpu().numpy()[..., None])
+    summ_o = oracle.summaries(Kdq, w.L, w.S)
+    Q = inp.q()
+    for _ in range(32):
+        margins = [oracle.route(Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous(), w.q_pos0 + s, summ_o,
+                                w.Hkv, w.S, w.topk)[1] for s in steps]
+        bad_rows = []
+        for s, m in zip(steps, margins):
+            for r in np.nonzero(m < MARGIN)[0]:
+                bad_rows.append(s * w.B * w.Hq + int(r))
+        if not bad_rows:
+            break
+        attempt[np.array(bad_rows)] += 1
+        Q = inp.q()
+    else:
+        raise RuntimeError("margins not reached")
+    ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE)
+    Qd = Q.cuda()
+    for s in steps:
+        pos = w.q_pos0 + s
+        q = Qd[s].contiguous()
+        sel = torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
+        O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=dev)
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        ssa.ssa_route(p, q, 1, pos, summ, sel)
+        ssa.ssa_attend_decode_q8(p, q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+        qh = Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous()
+        sel_o, _ = oracle.route(qh, pos, summ_o, w.Hkv, w.S, w.topk)
+        assert np.array_equal(sel.reshape(-1, w.topk).cpu().numpy(), sel_o), pos
+        O_o, lse_o, _ = oracle.attend(qh.float(), Kdq, Vdq, pos, w.S, sel_o)
+        assert max_abs(O.reshape(-1, w.d).cpu(), O_o) <= TOL[w.dtype]
+        assert max_abs(lse.reshape(-1).cpu(), lse_o) <= LSE_TOL[w.dtype]
+    assert ssa.ssa_workspace_error(ws) == 0
