@@ -729,12 +729,13 @@ def main():
     ap.add_argument("--no-10m", action="store_true",
                     help="skip the decode line with a 10M-token cache")
     args = ap.parse_args()
-    ws_n, rank, local = dist_setup()
     if args.impl == "reference":
+        # the oracle runs on the host cores only: no process group, no GPU
         args.steps = args.steps if args.steps is not None else 3
         args.warmup = args.warmup if args.warmup is not None else 1
-        run_reference(args, ws_n, rank)
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
+    ws_n, rank, local = dist_setup()
     steps = args.steps if args.steps is not None else 8192
     warmup = max(3, args.warmup if args.warmup is not None else 512)
     dev = torch.device("cuda", local)
