@@ -156,8 +156,7 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 # from.  They are reported as the roofline's "traffic" only for the workload
 # they were measured on.
 NCU_TRAFFIC = {
-    "decode_1m": (2.189e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
-    "decode_1m_q8": (1.133e8, "profiles/decode_1m_launches.md: plan + 8-bit attend + merge per step"),
+    "decode_1m": (2.188e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
     "prefill_chunk_vs_1m": (3.856e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
 }
 

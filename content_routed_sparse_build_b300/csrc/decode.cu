@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   it_next = __shfl_sync(0xffffffffu, it_next, 0);
   bool exhausted = false;
 
+  const uint64_t pol_stream = ptx::policy_evict_first();  // K / V are read once per step
   // Loads the next tile into `stage`; returns false when no work is left.
   auto issue = [&](int stage) -> bool {
     if (iss_tile == iss.ntiles) {
@@ -410,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int y = (int)(iss.t0 + (int64_t)iss_tile * kTile);
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        ptx::tma_load_3d(dK + bx * C::kBox, &tmK, &fb[stage], bx * 64, y, iss.grp);
-        ptx::tma_load_3d(dV + bx * C::kBox, &tmV, &fb[stage], bx * 64, y, iss.grp);
+        ptx::tma_load_3d_hint(dK + bx * C::kBox, &tmK, &fb[stage], bx * 64, y, iss.grp, pol_stream);
+        ptx::tma_load_3d_hint(dV + bx * C::kBox, &tmV, &fb[stage], bx * 64, y, iss.grp, pol_stream);
       }
     }
     ++iss_tile;
@@ -726,6 +727,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   if (lane == 0) it_next = atomicAdd(plan.counter, 1);
   it_next = __shfl_sync(0xffffffffu, it_next, 0);
   bool exhausted = false;
+  const uint64_t pol_stream = ptx::policy_evict_first();  // K rows are read once per step
 
   auto issue = [&](int stage) -> bool {
     if (iss_tile == iss.ntiles) {
@@ -746,7 +748,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       ptx::mbar_arrive_expect_tx(&fb[stage], q8::kKBytes + q8::kVBytes + q8::kSBytes);
       const int64_t y = q8::tile_base(iss.t0) + (int64_t)iss_tile * kTile;
       uint8_t* dS = wS + stage * q8::kSBytes;
-      ptx::tma_load_3d(wK + stage * q8::kKBytes, &tmK, &fb[stage], 0, (int)y, iss.grp);
+      ptx::tma_load_3d_hint(wK + stage * q8::kKBytes, &tmK, &fb[stage], 0, (int)y, iss.grp, pol_stream);
       ptx::bulk_load(wV + stage * q8::kVBytes, Vq + ((int64_t)iss.grp * tiles_per_head + y / kTile) * (D * kTile),
                      q8::kVBytes, &fb[stage]);
       ptx::bulk_load(dS, Ks + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);

@@ -166,6 +166,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
 
   const float* sbase = summ + (int64_t)(b * Hkv + kvh) * ns_cap * D;
   const int half = tid & 1;
+  const uint64_t pol_keep = ptx::policy_evict_last();  // the summaries are read every step
   for (int64_t jb = lo; jb < hi; jb += kBlk) {
     {
       const int jj = tid >> 1;
@@ -177,7 +178,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
         const float4* src = reinterpret_cast<const float4*>(sbase + j * D + half * HD);
         float4 sv[NL];
 #pragma unroll
-        for (int i = 0; i < NL; ++i) sv[i] = __ldg(src + i);
+        for (int i = 0; i < NL; ++i) sv[i] = ptx::ldg_hint(src + i, pol_keep);
 #pragma unroll
         for (int i = 0; i < NL; ++i) {
 #pragma unroll
