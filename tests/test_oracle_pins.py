@@ -409,3 +409,22 @@ def test_dequantized_summaries_and_attention_accept_f64():
     assert np.array_equal(Kd.numpy(), q.astype(np.float64) * s.astype(np.float64)[..., None])
     summ = oracle.summaries(Kd, 32, 8)
     assert np.allclose(summ[0, 0], Kd.numpy()[0, 0].reshape(4, 8, 4).mean(axis=1), rtol=0, atol=1e-15)
+
+
+def test_f64_inputs_match_their_f32_values_exactly():
+    # the fp64 input path (used for dequantised caches) widens nothing: the
+    # same values given as fp32 and as fp64 produce identical oracle results
+    g = torch.Generator().manual_seed(6)
+    B, Hq, Hkv, L, d, S, k = 1, 4, 2, 96, 8, 16, 2
+    Q = torch.randn((B, Hq, L, d), generator=g)
+    K = torch.randn((B, Hkv, L, d), generator=g)
+    V = torch.randn((B, Hkv, L, d), generator=g)
+    s32 = oracle.summaries(K, L, S)
+    s64 = oracle.summaries(K.double(), L, S)
+    assert np.array_equal(s32, s64)
+    sel32, m32 = oracle.route(Q, 0, s32, Hkv, S, k)
+    sel64, m64 = oracle.route(Q.double(), 0, s64, Hkv, S, k)
+    assert np.array_equal(sel32, sel64) and np.array_equal(m32, m64)
+    o32, l32, _ = oracle.attend(Q, K, V, 0, S, sel32)
+    o64, l64, _ = oracle.attend(Q.double(), K.double(), V.double(), 0, S, sel32)
+    assert np.array_equal(o32, o64) and np.array_equal(l32, l64)
