@@ -41,6 +41,10 @@ DECODE_CASES = [
                n_q=4, q_pos0=4092, chunk=1, needles=2, seed=23),
     W.Workload("case_decode_bf16_g16_small_ell", "decode", 1, 16, 1, 128, 5000, 512, 16, BF16,
                n_q=3, q_pos0=4997, chunk=1, seed=24),
+    # 16,499 candidate spans: more than the plan's bitmap covers (16,384), so
+    # the union positions come from its binary-search path
+    W.Workload("case_decode_bf16_many_spans", "decode", 1, 8, 1, 64, 16500 * 64, 64, 8, BF16,
+               n_q=2, q_pos0=16500 * 64 - 2, chunk=1, seed=25),
 ]
 
 
