@@ -21,7 +21,6 @@ namespace cg = cooperative_groups;
 namespace ssa {
 namespace {
 
-constexpr int kMaxG = 16;   // query heads per kv-head
 constexpr int kMaxK = 64;   // topk limit
 constexpr int kCluster = 16; // CTAs splitting one kv-head's candidates in decode
 
