@@ -292,6 +292,8 @@ typedef struct {
  * half while the other half is written to the file.  The copies follow
  * whatever was enqueued on `stream` before.  Unlike every other entry
  * point, this call returns only when the file is complete (or on error).
+ * It allocates no device memory; it creates two CUDA events for the
+ * hand-off between the halves and destroys them before returning.
  * Requires 0 <= n_tokens <= L (params.L).
  * Returns SSA_ERR_INVALID_ARG for bad arguments (checked before anything
  * touches the GPU or the file), SSA_ERR_IO when the file cannot be
