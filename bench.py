@@ -3,12 +3,21 @@
 Headline (``value``): decode tok/s per attention layer at a 1M-token cache
 (B=1, Hq=32, Hkv=4, d=128, S=1024, k=16, bf16): one step = route one new
 query token per head (scores over 1023 span summaries + top-16) and attend
-its selected spans plus its local span.  The ``prefill`` object reports the
-chunked prefill of 8192 queries against the same-shaped 1M cache (summaries
-of the chunk's spans, route, attend).  Both run through the C ABI on inputs
-already resident in HBM; ``e2e`` repeats the decode through the same calls
-with the query copied in from pinned host memory and the output copied back
+its selected spans plus its local span.  ``roofline`` divides the step's
+gathered K/V bytes plus the summary bytes its route reads by the whole
+step's time.  ``e2e`` repeats the decode through the same C-ABI calls with
+the query copied in from pinned host memory and the output copied back
 every step.
+
+Further lines, each with its own roofline and, on rank 0 of a one-GPU run,
+the oracle timed on the host cores (``cpu_baseline``):
+  prefill          8192 queries against a 1M cache (summaries + route + attend)
+  prefill_128k     the whole 128K prefill, 16 chunks of 8192
+  tiny_prefill     the 4096-query fp32 case
+  decode_10m       decode at a 10M-token cache
+  decode_group_shared, decode_q8   decode with one top-k per kv-head group,
+                   and over the 8-bit cache
+  dense_comparison the same shapes through dense attention (PyTorch SDPA)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Multi-GPU (torchrun, one process per GPU): every rank runs an independent
@@ -272,6 +281,31 @@ def replay_ms(g, reps, stream):
     return a.elapsed_time(b)
 
 
+def decode_graphs(db, steps):
+    """CUDA graphs whose replays run exactly `steps` decode steps: a graph of
+    the workload's n_q distinct queries replayed steps // n_q times, then a
+    graph of the remainder.  Returns [(graph, replays)]."""
+    n = db.w.n_q
+    reps, rem = divmod(steps, n)
+    plan = []
+    if reps:
+        plan.append((db.graph(db.step, n), reps, n))
+    if rem:
+        plan.append((db.graph(db.step, rem), 1, rem))
+    return plan
+
+
+def replay_plan(plan):
+    for g, r, _ in plan:
+        for _ in range(r):
+            g.replay()
+
+
+def plan_text(plan, steps):
+    return "%d decode steps as CUDA-graph replays (%s); every graph was replayed during warm-up" % (
+        steps, " + ".join("%d-step graph x %d" % (k, r) for _, r, k in plan))
+
+
 def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     db = DecodeBench(w, dev)
     st = torch.cuda.current_stream(dev)
@@ -288,12 +322,14 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     per_q = db.algorithmic_bytes()
 
     n = w.n_q
-    reps, rem = divmod(steps, n)
-    g_step = db.graph(db.step, n)
-    g_rem = db.graph(db.step, rem) if rem else None
+    plan = decode_graphs(db, steps)
     g_att = db.graph(db.attend, n)          # attend only, on the selections routed above
-    for _ in range(max(1, -(-warmup // n))):
-        g_step.replay()
+    # warm-up: every graph the timed region replays is replayed first (the
+    # first replay of a graph carries its upload), at least `warmup` steps
+    done = 0
+    while done < max(warmup, 1):
+        replay_plan(plan)
+        done += steps
     g_att.replay()
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
@@ -301,15 +337,12 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
         torch.cuda.synchronize()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(st)
-        for _ in range(reps):
-            g_step.replay()
-        if g_rem is not None:
-            g_rem.replay()
+        replay_plan(plan)
         stop.record(st)
         torch.cuda.synchronize()
         barrier(ws_n)
     total_ms = start.elapsed_time(stop)
-    att_reps = max(1, reps)
+    att_reps = max(1, -(-steps // n))
     attend_ms = replay_ms(g_att, att_reps, st) / (att_reps * n) * steps
     err = ssa.ssa_workspace_error(db.ws)
     total_ms_max = max_over_ranks(total_ms, ws_n)
@@ -317,7 +350,9 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     attend_bytes = sum(per_q[s % n][0] for s in range(steps))
     route_bytes = sum(per_q[s % n][1] for s in range(steps))
     pk = peaks()
-    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
+    step_gbs = (attend_bytes + route_bytes) / (total_ms_max * 1e-3) / 1e9
+    att_gbs = attend_bytes / (attend_ms * 1e-3) / 1e9
+    tr, tr_src = traffic_of(w.name)
     res = {
         "tok_s": job_throughput(steps, total_ms_max * 1e-3, ws_n),
         "ms_per_step": total_ms_max / steps,
@@ -325,19 +360,24 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
         "route_plus_gaps_ms_per_step": (total_ms - attend_ms) / steps,
         "attend_bytes_per_step": attend_bytes / steps,
         "route_bytes_per_step": route_bytes / steps,
-        "step_bytes_gbs": (attend_bytes + route_bytes) / (total_ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                     "traffic": traffic_of(w.name)[0], "traffic_source": traffic_of(w.name)[1],
-                     "kernel": "ssa_attend_decode (plan + gathered K/V attend + merge), timed as "
-                               "one CUDA-graph node group",
-                     "peak_source": pk["source"]},
+        # the headline fraction: gathered K/V plus summary bytes of a step
+        # over the whole step's time (route, attend and every gap between)
+        "roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(step_gbs / pk["hbm_gbs"], 4),
+                     "traffic": tr, "traffic_source": tr_src,
+                     "kernel": "whole decode step (route + attend), %d launches per step, timed as "
+                               "CUDA-graph replays" % launches_per_decode_step(w),
+                     "bytes": "gathered K/V of the union of each kv-head group's selected spans plus "
+                              "the causal local span, plus the candidate summaries the route reads, "
+                              "per step, from the run's own selections",
+                     "peak_source": pk["source"],
+                     "attend_only": {"achieved": round(att_gbs, 1), "frac": round(att_gbs / pk["hbm_gbs"], 4),
+                                     "what": "the attend launches alone, replayed apart from the route"}},
         "summaries": {"ms": summ_ms, "gbs": summ_bytes / (summ_ms * 1e-3) / 1e9,
                       "frac": summ_bytes / (summ_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
         "clocks": clk.summary(),
         "device_error_bits": err,
-        "timing": "CUDA graph of %d decode steps replayed %d times%s" % (
-            n, reps, " + %d-step remainder" % rem if rem else ""),
+        "timing": plan_text(plan, steps),
     }
     res["e2e"] = bench_decode_e2e(db, min(steps, 2048))
     if cpu_leg:
@@ -345,67 +385,72 @@ def bench_decode(w, dev, steps, warmup, ws_n, cpu_leg):
     return res, db
 
 
+def time_decode_variant(db, steps, ws_n):
+    """Times `steps` decode steps of a variant (graphs warmed first) and the
+    attend launches alone; returns (step ms, attend ms, per-query bytes, plan)."""
+    st = torch.cuda.current_stream(db.dev)
+    db.build_summaries()
+    per_q = db.algorithmic_bytes()
+    n = db.w.n_q
+    plan = decode_graphs(db, steps)
+    g_att = db.graph(db.attend, n)
+    replay_plan(plan)
+    g_att.replay()
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    replay_plan(plan)
+    b.record(st)
+    torch.cuda.synchronize()
+    step_ms = max_over_ranks(a.elapsed_time(b), ws_n) / steps
+    att_reps = max(1, -(-steps // n))
+    attend_ms = replay_ms(g_att, att_reps, st) / (att_reps * n)
+    return step_ms, attend_ms, per_q, plan
+
+
+def variant_line(db, steps, ws_n, extra):
+    w = db.w
+    step_ms, attend_ms, per_q, plan = time_decode_variant(db, steps, ws_n)
+    n = w.n_q
+    attend_bytes = sum(per_q[s % n][0] for s in range(steps)) / steps
+    route_bytes = sum(per_q[s % n][1] for s in range(steps)) / steps
+    err = ssa.ssa_workspace_error(db.ws)
+    if db.wsg is not None:
+        err |= ssa.ssa_workspace_error(db.wsg)
+    pk = peaks()
+    step_gbs = (attend_bytes + route_bytes) / (step_ms * 1e-3) / 1e9
+    att_gbs = attend_bytes / (attend_ms * 1e-3) / 1e9
+    out = {"workload": w.name, "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s",
+           "ms_per_step": step_ms, "steps": steps, "timing": plan_text(plan, steps),
+           "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
+           "route_bytes_per_step": route_bytes,
+           "roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(step_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                        "kernel": "whole decode step (route + attend)", "peak_source": pk["source"],
+                        "attend_only": {"achieved": round(att_gbs, 1), "frac": round(att_gbs / pk["hbm_gbs"], 4)}},
+           "device_error_bits": err}
+    out.update(extra)
+    return out
+
+
 def bench_decode_group(w, dev, steps, ws_n):
     """The same decode workload with group-shared selection (one top-k per
     kv-head group): each group's heads attend the same k spans, so a step
     streams k spans plus the local span per kv-head."""
     db = DecodeBench(w, dev, group=True)
-    st = torch.cuda.current_stream(dev)
-    db.build_summaries()
-    per_q = db.algorithmic_bytes()
-    n = w.n_q
-    reps = max(1, steps // n)
-    g_step = db.graph(db.step, n)
-    g_att = db.graph(db.attend, n)
-    g_step.replay()
-    g_att.replay()
-    torch.cuda.synchronize()
-    barrier(ws_n)
-    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
-    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
-    err = ssa.ssa_workspace_error(db.ws) | ssa.ssa_workspace_error(db.wsg)
-    attend_bytes = sum(a for a, _ in per_q) / n
-    pk = peaks()
-    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
-    return {"workload": w.name, "routing": "group-shared (one top-k per kv-head group)",
-            "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
-            "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
-                         "peak_source": pk["source"]},
-            "device_error_bits": err}
+    return variant_line(db, steps, ws_n, {"routing": "group-shared (one top-k per kv-head group)"})
 
 
-def bench_decode_10m(dev, steps, ws_n):
+def bench_decode_10m(dev, steps, ws_n, cpu_leg):
     """Decode with a 10M-token cache (S 3072, 3255 candidate spans), per-head
     selection, to set against the 1M line: the pages report decode slowing by
     about 30% from 1M to 10M."""
     w = W.DECODE_10M
     db = DecodeBench(w, dev)
-    st = torch.cuda.current_stream(dev)
-    db.build_summaries()
-    per_q = db.algorithmic_bytes()
-    n = w.n_q
-    reps = max(1, steps // n)
-    g_step = db.graph(db.step, n)
-    g_att = db.graph(db.attend, n)
-    g_step.replay()
-    g_att.replay()
-    torch.cuda.synchronize()
-    barrier(ws_n)
-    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
-    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
-    err = ssa.ssa_workspace_error(db.ws)
-    attend_bytes = sum(a for a, _ in per_q) / n
-    pk = peaks()
-    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
-    out = {"workload": w.name, "L": w.L, "S": w.S,
-           "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
-           "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
-           "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
-                        "peak_source": pk["source"]},
-           "device_error_bits": err}
+    out = variant_line(db, steps, ws_n, {"L": w.L, "S": w.S})
+    if cpu_leg:
+        out["cpu_baseline"] = cpu_baseline_decode_10m(db)
     del db
     torch.cuda.empty_cache()
     return out
@@ -416,32 +461,10 @@ def bench_decode_q8(w, dev, steps, ws_n):
     the summaries of the dequantised keys): a step streams the same spans
     at 2 d + 8 bytes per token instead of 4 d."""
     db = DecodeBench(w, dev, q8=True)
-    st = torch.cuda.current_stream(dev)
-    db.build_summaries()
-    per_q = db.algorithmic_bytes()
-    n = w.n_q
-    reps = max(1, steps // n)
-    g_step = db.graph(db.step, n)
-    g_att = db.graph(db.attend, n)
-    g_step.replay()
-    g_att.replay()
-    torch.cuda.synchronize()
-    barrier(ws_n)
-    step_ms = max_over_ranks(replay_ms(g_step, reps, st), ws_n) / (reps * n)
-    attend_ms = replay_ms(g_att, reps, st) / (reps * n)
-    err = ssa.ssa_workspace_error(db.ws)
-    attend_bytes = sum(a for a, _ in per_q) / n
-    pk = peaks()
-    achieved = attend_bytes / (attend_ms * 1e-3) / 1e9
-    return {"workload": w.name, "cache": "8-bit K / V, one fp32 scale per token row; fp32 summaries",
-            "value": job_throughput(1, step_ms * 1e-3, ws_n), "unit": "tok/s", "ms_per_step": step_ms,
-            "attend_ms_per_step": attend_ms, "attend_bytes_per_step": attend_bytes,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic_of(w.name + "_q8")[0],
-                         "traffic_source": traffic_of(w.name + "_q8")[1],
-                         "kernel": "ssa_attend_decode_q8 (plan + gathered 8-bit K/V attend + merge)",
-                         "peak_source": pk["source"]},
-            "device_error_bits": err}
+    out = variant_line(db, steps, ws_n, {"cache": "8-bit K / V, one fp32 scale per token row; fp32 summaries"})
+    tr, tr_src = traffic_of(w.name + "_q8")
+    out["roofline"]["traffic"], out["roofline"]["traffic_source"] = tr, tr_src
+    return out
 
 
 def bench_decode_e2e(db: DecodeBench, steps: int):
@@ -518,6 +541,56 @@ def cpu_baseline_decode(db: DecodeBench, budget_s: float = 15.0):
     return {"value": n / dt, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": "%d of the %d decode steps (route + attend per step; summaries of the 1M "
                       "cache built beforehand, untimed)" % (n, w.n_q)}
+
+
+def cpu_baseline_decode_10m(db: DecodeBench, n_steps: int = 12):
+    """The oracle on the host cores on sampled steps of the 10M decode.  The
+    20 GB cache is never held on the host: the oracle's summaries come from
+    host regenerations of span ranges and each step's attention runs on the
+    compacted cache of its selected spans (both prepared untimed); the timed
+    part is the oracle's route and attend of every sampled step."""
+    import oracle
+    from oracle import streamed
+    w = db.w
+    inp = db.inp
+    Q = inp.q("cpu")
+    summ = streamed.summaries_streamed(inp)
+    steps = np.linspace(0, w.n_q - 1, n_steps).astype(int)
+    tot = 0.0
+    for s in steps:
+        t = w.q_pos0 + int(s)
+        q = Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous()
+        t0 = time.perf_counter()
+        sel, _ = oracle.route(q, t, summ, w.Hkv, w.S, w.topk)
+        tot += time.perf_counter() - t0
+        for _, qc, Kc, Vc, pos, sel_c in streamed.compact_decode_step(inp, Q[s], sel, t):
+            t0 = time.perf_counter()
+            oracle.attend(qc, Kc, Vc, pos, w.S, sel_c)
+            tot += time.perf_counter() - t0
+    return {"value": len(steps) / tot, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": "%d of the %d decode steps, evenly spaced (route over the 3255 candidate summaries + "
+                      "attend on each step's compacted cache of selected spans; summaries and compaction "
+                      "untimed)" % (len(steps), w.n_q)}
+
+
+def cpu_baseline_prefill_rows(w: W.Workload, inp: W.Inputs, Q, K, V, q_pos0: int, n_q: int,
+                              budget_s: float = 10.0, batch: int = 512, seed: int = 5):
+    """The oracle's route + attend on random (query, head) rows of one chunk
+    of queries, for about budget_s seconds.  Returns (rows per second, rows)."""
+    import oracle
+    summ = oracle.summaries(K, q_pos0 + n_q, w.S, 0, (q_pos0 + n_q) // w.S)
+    n_rows = w.B * w.Hq * n_q
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(n_rows)
+    done, tot = 0, 0.0
+    while done < n_rows and tot < budget_s:
+        rows = np.sort(order[done: done + batch])
+        t0 = time.perf_counter()
+        sel, _ = oracle.route(Q, q_pos0, summ, w.Hkv, w.S, w.topk, rows=rows)
+        oracle.attend(Q, K, V, q_pos0, w.S, sel, rows=rows)
+        tot += time.perf_counter() - t0
+        done += len(rows)
+    return done / tot, done
 
 
 # --------------------------------------------------------------------- prefill
@@ -624,7 +697,19 @@ def bench_dense_comparison(dev, flush, decode_step_ms, prefill_1m_ms):
     return out
 
 
-def bench_prefill(w, dev, steps, warmup, ws_n, flush):
+def tensor_roofline(flop: float, ms: float, what: str, traffic=None, traffic_source=None):
+    """Selected-span FLOP over time against the measured burst bf16 peak (a
+    chunk of a few milliseconds is a kernel timed on its own, not a seconds-
+    long loop under the power cap); the sustained-peak fraction rides along."""
+    pk = peaks()
+    achieved = flop / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic, "traffic_source": traffic_source,
+            "kernel": what, "peak_source": pk["source"] + " burst bf16",
+            "frac_of_sustained": round(achieved / pk["bf16_tflops_sustained"], 4)}
+
+
+def bench_prefill(w, dev, steps, warmup, ws_n, flush, cpu_leg):
     pb = PrefillBench(w, dev)
     st = pb.stream
     fl = pb.flops()
@@ -647,20 +732,169 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush):
     attend_ms = sum(x.elapsed_time(y) for x, y in evs) / steps
     ms = max_over_ranks(tot / steps, ws_n)
     err = ssa.ssa_workspace_error(pb.ws)
-    pk = peaks()
-    achieved = fl / (attend_ms * 1e-3) / 1e12
-    return {
+    tr, tr_src = traffic_of(w.name)
+    out = {
         "workload": w.name, "value": job_throughput(w.n_q, ms * 1e-3, ws_n), "unit": "tok/s",
         "ms_per_step": ms, "attend_ms": attend_ms, "steps": steps,
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": round(achieved / pk["bf16_tflops_sustained"], 4),
-                     "traffic": traffic_of(w.name)[0], "traffic_source": traffic_of(w.name)[1],
-                     "kernel": "attend_prefill (4*d FLOP per attended token per query head)",
-                     "peak_source": pk["source"] + " sustained bf16"},
+        "l2": "flushed before every timed chunk (256 MiB write)",
+        "roofline": tensor_roofline(fl, ms, "whole chunk: summaries + route + attend (4*d FLOP per attended "
+                                            "token per query head over the selected spans and the local span)"),
+        "attend_roofline": tensor_roofline(fl, attend_ms, "attend path alone (dispatch + attend + merge)", tr, tr_src),
         "selected_span_tflop_per_step": fl / 1e12,
         "device_error_bits": err,
     }
+    if cpu_leg:
+        inp = pb.inp
+        Q, K, V = inp.q("cpu"), inp.k("cpu"), inp.v("cpu")
+        rps, n = cpu_baseline_prefill_rows(w, inp, Q, K, V, w.q_pos0, w.n_q)
+        import oracle
+        out["cpu_baseline"] = {"value": rps / w.Hq, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+                               "sample": "%d random (query, head) rows of the chunk's %d, route + attend; "
+                                         "tok/s = rows/s / Hq" % (n, w.B * w.Hq * w.n_q)}
+        del Q, K, V
+    del pb
+    torch.cuda.empty_cache()
+    return out
+
+
+class Prefill128kBench:
+    """The whole 128K prefill: 16 chunks of 8192 queries, each one's K / V
+    already in the cache; a chunk builds the summaries of the spans it
+    completes, routes its queries and attends them."""
+
+    def __init__(self, w: W.Workload, dev):
+        self.w = w
+        self.dev = dev
+        self.inp = W.Inputs(w)
+        self.K = self.inp.k(dev)
+        self.V = self.inp.v(dev)
+        Q = self.inp.q(dev)                                   # [B, Hq, L, d]
+        self.chunks = []
+        for c0 in range(0, w.n_q, w.chunk):
+            n = min(w.chunk, w.n_q - c0)
+            self.chunks.append((c0, n, Q[:, :, c0:c0 + n].contiguous()))
+        del Q
+        self.p_full = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+        self.summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+        self.sel = [torch.empty((w.B, w.Hq, n, w.topk), dtype=torch.int32, device=dev) for _, n, _ in self.chunks]
+        self.O = [torch.empty_like(q) for _, _, q in self.chunks]
+        self.lse = [torch.empty((w.B, w.Hq, n), dtype=torch.float32, device=dev) for _, n, _ in self.chunks]
+        self.ws = ssa.workspace(self.p_full, w.chunk, ssa.SSA_OP_PREFILL, dev)
+        self.ws_route = ssa.workspace(self.p_full, w.chunk, ssa.SSA_OP_ROUTE, dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def run(self, evs=None):
+        w = self.w
+        for c, (c0, n, q) in enumerate(self.chunks):
+            L_now = c0 + n
+            p = ssa.params(w.B, w.Hq, w.Hkv, w.d, L_now, w.S, w.topk, w.dtype, L_cap=w.L)
+            ssa.ssa_build_summaries(p, self.K, c0 // w.S, (L_now + w.S - 1) // w.S, self.summ, self.stream)
+            ssa.ssa_route(p, q, n, c0, self.summ, self.sel[c], None, self.ws_route, self.stream)
+            ssa.ssa_attend_prefill(p, q, n, c0, self.K, self.V, self.sel[c], self.O[c], self.lse[c], self.ws,
+                                   self.stream)
+            if evs is not None:
+                evs[c].record(self.stream)
+
+    def flops(self):
+        w = self.w
+        self.run()
+        tot = 0.0
+        for c, (c0, n, _) in enumerate(self.chunks):
+            sel = self.sel[c].cpu().numpy()
+            nsel = (sel >= 0).sum(axis=-1)
+            pos = c0 + np.arange(n)
+            local = pos - (pos // w.S) * w.S + 1
+            tot += float(4 * w.d * (nsel * w.S + local[None, None, :]).sum())
+        return tot
+
+
+def bench_prefill_128k(dev, steps, ws_n, flush, cpu_leg):
+    """The 128K chunked prefill as a whole: 131072 / (time of all 16 chunks)."""
+    w = W.PREFILL_128K
+    pb = Prefill128kBench(w, dev)
+    st = pb.stream
+    fl = pb.flops()
+    pb.run()
+    torch.cuda.synchronize()
+    nch = len(pb.chunks)
+    tot, per_chunk = 0.0, np.zeros(nch)
+    barrier(ws_n)
+    for _ in range(steps):
+        flush_l2(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nch)]
+        a.record(st)
+        pb.run(evs)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(evs[-1])
+        prev = a
+        for c in range(nch):
+            per_chunk[c] += prev.elapsed_time(evs[c])
+            prev = evs[c]
+    barrier(ws_n)
+    ms = max_over_ranks(tot / steps, ws_n)
+    err = ssa.ssa_workspace_error(pb.ws)
+    out = {"workload": w.name, "value": job_throughput(w.n_q, ms * 1e-3, ws_n), "unit": "tok/s",
+           "ms_per_prefill": ms, "steps": steps, "chunks": nch,
+           "ms_per_chunk": [round(x / steps, 4) for x in per_chunk],
+           "l2": "flushed before every timed prefill (256 MiB write); K / V are 512 MiB",
+           "roofline": tensor_roofline(fl, ms, "all 16 chunks: summaries + route + attend (4*d FLOP per attended "
+                                               "token per query head)"),
+           "selected_span_tflop": fl / 1e12, "device_error_bits": err}
+    if cpu_leg:
+        import oracle
+        inp = pb.inp
+        Q, K, V = inp.q("cpu"), inp.k("cpu"), inp.v("cpu")
+        c0 = w.n_q - w.chunk
+        # rows drawn from the whole prefill at once: each row's oracle cost is
+        # its route over its own candidates plus its attention, so the sample
+        # stands for every chunk, early and late
+        rps, n = cpu_baseline_prefill_rows(w, inp, Q, K, V, 0, w.n_q, budget_s=10.0)
+        out["cpu_baseline"] = {"value": rps / w.Hq, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+                               "sample": "%d random (query, head) rows drawn from all 131072 queries, route + "
+                                         "attend; tok/s = rows/s / Hq" % n}
+        del Q, K, V
+    del pb
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_tiny(dev, steps, ws_n, cpu_leg):
+    """The tiny fp32 prefill (4096 queries, 4 heads, d 64, S 64, k 8) in one
+    chunk: summaries + route + attend, tok/s = 4096 / time."""
+    w = W.TINY_PREFILL
+    inp = W.Inputs(w)
+    Q, K, V = inp.q(dev), inp.k(dev), inp.v(dev)
+    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+    summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+    sel = torch.empty((w.B, w.Hq, w.n_q, w.topk), dtype=torch.int32, device=dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
+    ws = ssa.workspace(p, w.n_q, ssa.SSA_OP_PREFILL, dev)
+    wsr = ssa.workspace(p, w.n_q, ssa.SSA_OP_ROUTE, dev)
+    st = torch.cuda.current_stream(dev)
+
+    def run():
+        ssa.ssa_build_summaries(p, K, 0, w.n_spans, summ)
+        ssa.ssa_route(p, Q, w.n_q, 0, summ, sel, None, wsr)
+        ssa.ssa_attend_prefill(p, Q, w.n_q, 0, K, V, sel, O, lse, ws)
+
+    ms = max_over_ranks(time_ms(run, max(steps, 3), 3, st), ws_n)
+    out = {"workload": w.name, "value": job_throughput(w.n_q, ms * 1e-3, ws_n), "unit": "tok/s",
+           "ms_per_step": ms, "steps": max(steps, 3),
+           "roofline": {"bound": "n/a", "note": "fp32 parity workload of 4096 queries; no roofline claimed"},
+           "device_error_bits": ssa.ssa_workspace_error(ws)}
+    if cpu_leg:
+        import oracle
+        Qh, Kh, Vh = inp.q("cpu"), inp.k("cpu"), inp.v("cpu")
+        t0 = time.perf_counter()
+        summ_o = oracle.summaries(Kh, w.L, w.S)
+        sel_o, _ = oracle.route(Qh, 0, summ_o, w.Hkv, w.S, w.topk)
+        oracle.attend(Qh, Kh, Vh, 0, w.S, sel_o)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": w.n_q / dt, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+                               "sample": "the whole workload: summaries + route + attend of all 4096 queries"}
+    return out
 
 
 # --------------------------------------------------------------------- reference arm
@@ -712,8 +946,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-L", type=int, default=None,
                     help="shrink the decode cache (profiling runs on a smaller case)")
-    ap.add_argument("--prefill-128k", action="store_true",
-                    help="time the last 8192-query chunk of the 128K prefill workload instead")
     ap.add_argument("--prefill-L", type=int, default=None,
                     help="shrink the prefill cache (profiling runs on a smaller case)")
     ap.add_argument("--prefill-chunk", type=int, default=None,
@@ -727,6 +959,10 @@ def main():
                     help="skip the decode line over the 8-bit cache")
     ap.add_argument("--no-10m", action="store_true",
                     help="skip the decode line with a 10M-token cache")
+    ap.add_argument("--no-128k", action="store_true",
+                    help="skip the whole 128K chunked prefill")
+    ap.add_argument("--no-tiny", action="store_true",
+                    help="skip the tiny fp32 prefill")
     args = ap.parse_args()
     if args.impl == "reference":
         # the oracle runs on the host cores only: no process group, no GPU
@@ -735,11 +971,13 @@ def main():
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
     ws_n, rank, local = dist_setup()
-    steps = args.steps if args.steps is not None else 8192
-    warmup = max(3, args.warmup if args.warmup is not None else 512)
+    steps = args.steps if args.steps is not None else 2048
+    warmup = max(3, args.warmup if args.warmup is not None else 256)
     dev = torch.device("cuda", local)
     ssa.lib()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (126 MB)
+    cpu_leg = rank == 0 and ws_n == 1 and not args.no_cpu_baseline
+    small = bool(args.decode_L or args.prefill_L or args.prefill_chunk)
 
     w = W.DECODE_1M
     if args.decode_L:
@@ -747,36 +985,12 @@ def main():
     if args.no_decode:
         dec = {"tok_s": None, "ms_per_step": None, "roofline": None, "e2e": None, "clocks": None,
                "attend_ms_per_step": None, "route_plus_gaps_ms_per_step": None,
-               "attend_bytes_per_step": None, "route_bytes_per_step": None, "step_bytes_gbs": None,
+               "attend_bytes_per_step": None, "route_bytes_per_step": None,
                "summaries": None, "device_error_bits": None, "timing": None}
     else:
-        dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg=(rank == 0 and ws_n == 1
-                                                                     and not args.no_cpu_baseline))
+        dec, db = bench_decode(w, dev, steps, warmup, ws_n, cpu_leg)
         del db
     torch.cuda.empty_cache()
-    pre = None
-    grp = None
-    if not args.no_decode and not args.no_group:
-        torch.cuda.empty_cache()
-        grp = bench_decode_group(w, dev, min(steps, 4096), ws_n)
-        torch.cuda.empty_cache()
-    q8 = None
-    if not args.no_decode and not args.no_q8:
-        q8 = bench_decode_q8(w, dev, min(steps, 4096), ws_n)
-        torch.cuda.empty_cache()
-    d10 = None
-    if not args.no_decode and not args.no_10m and not args.decode_L:
-        d10 = bench_decode_10m(dev, min(steps, 2048), ws_n)
-    if not args.no_prefill:
-        wp = W.PREFILL_1M
-        if args.prefill_128k:
-            wp = W.PREFILL_128K.with_(name="prefill_128k_last_chunk", n_q=8192, chunk=8192,
-                                      q_pos0=W.PREFILL_128K.L - 8192)
-        elif args.prefill_L or args.prefill_chunk:
-            L = args.prefill_L or wp.L
-            n = args.prefill_chunk or wp.n_q
-            wp = wp.with_(name="prefill_%d_vs_%d" % (n, L), L=L, n_q=n, chunk=n, q_pos0=L - n)
-        pre = bench_prefill(wp, dev, args.prefill_steps, 2, ws_n, flush)
     line = {
         "metric": METRIC, "value": dec["tok_s"], "unit": "tok/s", "n_gpus": ws_n, "steps": steps,
         "warmup": warmup, "ms_per_step": dec["ms_per_step"], "higher_is_better": True,
@@ -784,34 +998,48 @@ def main():
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "L": w.L,
                    "S": w.S, "topk": w.topk, "queries": "%d distinct decode queries at positions "
                    "%d..%d, cycled" % (w.n_q, w.q_pos0, w.last_pos),
-                   "l2": "inputs larger than L2: 2 GiB K/V cache, ~250 MB gathered per step",
+                   "l2": "inputs larger than L2: 2 GiB K/V cache, ~220 MB gathered per step",
                    "parallelism": "replicas" if ws_n > 1 else "single GPU"},
         "roofline": dec["roofline"],
         "e2e": dec["e2e"],
         "clocks": dec["clocks"],
-        "gpu_launches": None,
+        "gpu_launches": steps * launches_per_decode_step(w) if not args.no_decode else 0,
         "decode_detail": {k: dec[k] for k in ("attend_ms_per_step", "route_plus_gaps_ms_per_step",
                                                "attend_bytes_per_step", "route_bytes_per_step",
-                                               "step_bytes_gbs", "summaries", "device_error_bits",
-                                               "timing")},
+                                               "summaries", "device_error_bits", "timing")},
     }
-    line["gpu_launches"] = steps * launches_per_decode_step(w)
-    if grp is not None:
-        line["decode_group_shared"] = grp
-    if q8 is not None:
-        line["decode_q8"] = q8
-    if d10 is not None:
-        d10["vs_1m"] = d10["value"] / dec["tok_s"] if dec["tok_s"] else None
-        line["decode_10m"] = d10
-    if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1
-            and not (args.decode_L or args.prefill_L or args.prefill_chunk or args.prefill_128k)):
-        torch.cuda.empty_cache()
-        line["dense_comparison"] = bench_dense_comparison(dev, flush, dec["ms_per_step"],
-                                                          pre["ms_per_step"])
-    if pre is not None:
-        line["prefill"] = pre
     if "cpu_baseline" in dec:
         line["cpu_baseline"] = dec["cpu_baseline"]
+    if not args.no_decode and not args.no_group:
+        line["decode_group_shared"] = bench_decode_group(w, dev, steps, ws_n)
+        torch.cuda.empty_cache()
+    if not args.no_decode and not args.no_q8:
+        line["decode_q8"] = bench_decode_q8(w, dev, steps, ws_n)
+        torch.cuda.empty_cache()
+    if not args.no_decode and not args.no_10m and not small:
+        d10 = bench_decode_10m(dev, steps, ws_n, cpu_leg)
+        d10["vs_1m"] = d10["value"] / dec["tok_s"] if dec["tok_s"] else None
+        line["decode_10m"] = d10
+        torch.cuda.empty_cache()
+    pre = None
+    if not args.no_prefill:
+        wp = W.PREFILL_1M
+        if args.prefill_L or args.prefill_chunk:
+            L = args.prefill_L or wp.L
+            n = args.prefill_chunk or wp.n_q
+            wp = wp.with_(name="prefill_%d_vs_%d" % (n, L), L=L, n_q=n, chunk=n, q_pos0=L - n)
+        pre = bench_prefill(wp, dev, args.prefill_steps, 2, ws_n, flush, cpu_leg)
+        line["prefill"] = pre
+        torch.cuda.empty_cache()
+    if not args.no_prefill and not args.no_128k and not small:
+        line["prefill_128k"] = bench_prefill_128k(dev, max(1, args.prefill_steps // 2), ws_n, flush, cpu_leg)
+        torch.cuda.empty_cache()
+    if not args.no_tiny and not small:
+        line["tiny_prefill"] = bench_tiny(dev, args.prefill_steps, ws_n, cpu_leg)
+        torch.cuda.empty_cache()
+    if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1 and not small):
+        torch.cuda.empty_cache()
+        line["dense_comparison"] = bench_dense_comparison(dev, flush, dec["ms_per_step"], pre["ms_per_step"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:

@@ -21,3 +21,23 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The margin check's report: per case, the rows whose selection was
+    checked, the query rows the generator redrew to reach the 1e-3 margin,
+    and the smallest k-th / (k+1)-th oracle score margin left."""
+    harness = sys.modules.get("harness")
+    if harness is None or not getattr(harness, "MARGIN_REPORT", None):
+        return
+    tr = terminalreporter
+    tr.section("selection margins (oracle k-th minus (k+1)-th score)")
+    tr.write_line("%-40s %10s %10s %8s %12s" % ("case", "rows", "ranked", "redrawn", "min margin"))
+    for e in harness.MARGIN_REPORT:
+        mm = "-" if e["min_margin"] is None else "%.3e" % e["min_margin"]
+        tr.write_line("%-40s %10d %10d %8d %12s" % (e["case"], e["rows"], e["ranked_rows"], e["redrawn"], mm))
+    path = os.environ.get("SSA_MARGIN_REPORT")
+    if path:
+        import json
+        with open(path, "w") as f:
+            json.dump(harness.MARGIN_REPORT, f, indent=1)

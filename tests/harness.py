@@ -21,6 +21,22 @@ MARGIN = 1e-3
 TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float16: 2e-2}
 LSE_TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-3, torch.float16: 1e-3}
 
+# What the margin check found, one entry per checked case: printed at the end
+# of the run by conftest.py (and written as JSON where SSA_MARGIN_REPORT
+# names a file).
+MARGIN_REPORT: list[dict] = []
+
+
+def report_margins(case: str, margin, redrawn: int) -> None:
+    """Records a case's oracle margins (k-th minus (k+1)-th score of each
+    checked row; +inf for rows with no more candidates than k) and how many
+    query rows the generator redrew to reach MARGIN."""
+    m = np.asarray(margin, dtype=np.float64).reshape(-1)
+    ranked = m[np.isfinite(m)]
+    MARGIN_REPORT.append({"case": case, "rows": int(m.size), "ranked_rows": int(ranked.size),
+                          "redrawn": int(redrawn),
+                          "min_margin": float(ranked.min()) if ranked.size else None})
+
 
 def params_of(w: W.Workload, L: int | None = None, topk: int | None = None) -> ssa.ssa_params:
     return ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L if L is None else L, w.S,
@@ -72,6 +88,7 @@ def margin_checked_inputs(w: W.Workload, max_rounds: int = 64):
         sel, margin = orc.route_all(Q)
         bad = _bad_rows(w, margin)
         if len(bad) == 0:
+            report_margins(w.name, margin, redrawn)
             return inp, Q, K, orc, sel, margin, redrawn
         redrawn += len(bad)
         attempt[bad] += 1
