@@ -165,7 +165,7 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 # from.  They are reported as the roofline's "traffic" only for the workload
 # they were measured on.
 NCU_TRAFFIC = {
-    "decode_1m": (2.188e8, "profiles/decode_1m_launches.md: plan + attend + merge per step"),
+    "decode_1m": (None, "profiles/decode_1m_launches.md: not yet captured for the two-launch step"),
     "prefill_chunk_vs_1m": (3.856e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
 }
 
@@ -230,6 +230,11 @@ class DecodeBench:
                                   self.O, self.lse, self.ws)
 
     def step(self, i):
+        if not (self.group or self.q8):
+            # the whole step in one call: route (which also plans) + attend
+            ssa.ssa_decode_step(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.K, self.V, self.sels[i],
+                                self.O, self.lse, self.ws)
+            return
         self.route(i)
         self.attend(i)
 
@@ -469,8 +474,8 @@ def bench_decode_q8(w, dev, steps, ws_n):
 
 def bench_decode_e2e(db: DecodeBench, steps: int):
     """Same decode through the C ABI with host buffers: every step copies its
-    query in from pinned host memory, routes and attends it, copies the
-    output back and waits for it.  The calls go straight to the C ABI and to
+    query in from pinned host memory, runs ssa_decode_step (route + attend),
+    copies the output back and waits for it.  The calls go straight to the C ABI and to
     the CUDA runtime's cudaMemcpyAsync (ctypes, arguments prepared once), so
     the loop measures the library and the copies, not Python tensor calls."""
     w = db.w
@@ -498,8 +503,7 @@ def bench_decode_e2e(db: DecodeBench, steps: int):
         i = s % w.n_q
         pos = w.q_pos0 + i
         rc = rt.cudaMemcpyAsync(qd, qh[i], nbytes, 1, sp)
-        rc |= L.ssa_route(pp, qd, 1, pos, summ, sel, None, None, 0, sp)
-        rc |= L.ssa_attend_decode(pp, qd, pos, K, V, sel, od, None, ws, wsn, sp)
+        rc |= L.ssa_decode_step(pp, qd, pos, summ, K, V, sel, od, None, ws, wsn, sp)
         rc |= rt.cudaMemcpyAsync(oh, od, nbytes, 2, sp)
         rc |= rt.cudaStreamSynchronize(sp)
         return rc
@@ -961,6 +965,8 @@ def main():
                     help="skip the decode line with a 10M-token cache")
     ap.add_argument("--no-128k", action="store_true",
                     help="skip the whole 128K chunked prefill")
+    ap.add_argument("--no-chunk", action="store_true",
+                    help="skip the 8192-query chunk against the 1M cache")
     ap.add_argument("--no-tiny", action="store_true",
                     help="skip the tiny fp32 prefill")
     args = ap.parse_args()
@@ -1022,7 +1028,7 @@ def main():
         line["decode_10m"] = d10
         torch.cuda.empty_cache()
     pre = None
-    if not args.no_prefill:
+    if not args.no_prefill and not args.no_chunk:
         wp = W.PREFILL_1M
         if args.prefill_L or args.prefill_chunk:
             L = args.prefill_L or wp.L
@@ -1048,11 +1054,10 @@ def main():
 
 
 def launches_per_decode_step(w) -> int:
-    """Kernels one decode step launches: route (1) + attend (plan, split
-    attention and merge on the 16-bit path; one row kernel otherwise)."""
-    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
-    fast = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE) > 256
-    return 1 + (3 if fast else 1)
+    """Kernels one ssa_decode_step launches: on the 16-bit path the route
+    (which also builds the plan) and the attend (which also merges); the
+    fp32 path runs the route and one row kernel."""
+    return 2
 
 
 if __name__ == "__main__":

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   ssa_route            span scores + top-k selection
   ssa_route_group      one top-k per kv-head group (summed scores of its heads)
   ssa_attend_decode    one query per head, split over spans, LSE merge
+  ssa_decode_step      route + attend of one decode step (two launches)
   ssa_attend_prefill   a chunk of queries, span-major tiles, LSE merge
   ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
   ssa_quantize_kv / ssa_build_summaries_q8 / ssa_attend_decode_q8
@@ -82,6 +83,7 @@ def lib() -> ctypes.CDLL:
         L.ssa_route_group.argtypes = [PP, _P, _I64, _I64, _P, _P, _P, _P, _SZ, _P]
         L.ssa_attend_decode.argtypes = [PP, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.ssa_attend_prefill.argtypes = [PP, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]
+        L.ssa_decode_step.argtypes = [PP, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         L.ssa_workspace_size.argtypes = [PP, _I64, ctypes.c_int]
         L.ssa_workspace_size.restype = _SZ
         L.ssa_workspace_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
@@ -89,7 +91,7 @@ def lib() -> ctypes.CDLL:
         L.ssa_status_string.restype = ctypes.c_char_p
         L.ssa_version.restype = ctypes.c_int
         for name in ("ssa_build_summaries", "ssa_route", "ssa_route_group", "ssa_attend_decode",
-                     "ssa_attend_prefill", "ssa_workspace_error"):
+                     "ssa_attend_prefill", "ssa_decode_step", "ssa_workspace_error"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -174,6 +176,15 @@ def ssa_attend_decode(p: ssa_params, Q: torch.Tensor, pos: int, K: torch.Tensor,
     rc = lib().ssa_attend_decode(ctypes.byref(p), _ptr(Q), int(pos), _ptr(K), _ptr(V), _ptr(sel),
                                  _ptr(O), _ptr(lse), wp, wn, _stream(stream))
     _check(rc, "ssa_attend_decode")
+
+
+def ssa_decode_step(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor, K: torch.Tensor,
+                    V: torch.Tensor, sel: torch.Tensor, O: torch.Tensor, lse: torch.Tensor | None,
+                    ws: torch.Tensor | None, stream=None) -> None:
+    wp, wn = _ws_args(ws)
+    rc = lib().ssa_decode_step(ctypes.byref(p), _ptr(Q), int(pos), _ptr(summ), _ptr(K), _ptr(V), _ptr(sel),
+                               _ptr(O), _ptr(lse), wp, wn, _stream(stream))
+    _check(rc, "ssa_decode_step")
 
 
 def ssa_attend_prefill(p: ssa_params, Q: torch.Tensor, n_q: int, q_pos0: int, K: torch.Tensor,

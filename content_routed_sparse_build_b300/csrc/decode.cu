@@ -6,57 +6,43 @@
 // (stork.ai): exact attention over the content-selected subset.  The local
 // span [l*S, pos] is always attended.
 //
-// Three kernels:
+// Two kernels (plan building and the merges are in decode_plan.cuh):
 //  plan    one CTA per (b, kv-head): validates the g heads' selections and
 //          builds their union U (ascending, local span last) with, per span,
 //          the mask of heads that chose it and each head's rank for it.
 //  attend  persistent, one CTA per SM, six independent warps.  Work items
 //          are (group, span of U, chunk of CH tokens), handed out by an
-//          atomic counter.  Each warp runs its own two-stage ring of 32-token
-//          K / V tiles loaded by TMA (128-byte swizzle, mbarrier completion),
-//          each tile computed as two 16-token fragments.  The MMAs are
-//          transposed so that the query group fits the n8 side of
-//          mma.sync: S^T = K Q^T (tokens x heads) and O^T += V^T P^T
-//          (d x heads), P^T turned into the B operand by movmatrix.  An
-//          online softmax runs per head (column); at the end of an item the
-//          warp writes one partial (m, l, o) per head that chose the span.
-//          Every K / V byte of the union is read once.
-//  merge   one CTA per (b, q-head): combines the head's partials (span
-//          order, then chunk order) into O and lse.
+//          atomic counter (each group's local span first).  Each warp runs
+//          its own two-stage ring of 32-token K / V tiles loaded by TMA
+//          (128-byte swizzle, mbarrier completion), each tile computed as two
+//          16-token fragments.  The MMAs are transposed so that the query
+//          group fits the n8 side of mma.sync: S^T = K Q^T (tokens x heads)
+//          and O^T += V^T P^T (d x heads), P^T turned into the B operand by
+//          movmatrix.  An online softmax runs per head (column); at the end
+//          of an item the warp writes one partial (m, l, o) per head that
+//          chose the span.  Every K / V byte of the union is read once.  The
+//          warp that finishes a span's last chunk merges its chunks, and the
+//          one that finishes a head's last span writes the head's O and lse.
 // Softmax runs in base 2: scores are scaled by scale * log2(e).
+#include "decode_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace ssa {
 namespace {
 
+using dplan::Geo;
+using dplan::Plan;
+using dplan::kMaxG;
+using dplan::kMaxK;
+
 constexpr int kTile = 32;     // tokens per ring stage
 constexpr int kSub = kTile / 16;  // m16 fragments per tile
 constexpr int kWarps = 6;     // independent warps per CTA (6 x 2 stages x 16 KB of K / V ring)
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxG = 16;
-constexpr int kMaxK = 64;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 227 * 1024;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-
-struct Plan {
-  int* n_union;     // [n_grp]   |U| including the local span
-  int* n_items;     // [n_grp]   work items of the group
-  int* span;        // [n_grp][umax]
-  uint32_t* mask;   // [n_grp][umax] heads (bit r = head kvh*g + r) that attend the span
-  uint8_t* rank;    // [n_grp][umax][16] position of the span in each head's sel row (topk = local)
-  int* counter;     // work-item counter of the attend kernel
-  float* ml;        // [B*Hq][topk+1][C][2]  (m, l) per partial, base-2 m
-  float* po;        // [B*Hq][topk+1][C][D]  unnormalised partial outputs
-};
-
-struct Geo {
-  int Hq, Hkv, g, topk, S, C, CH, umax, n_grp;
-  int64_t pos, ell;
-  float scale_log2e;
-};
 
 template <int D>
 struct Cfg {
@@ -84,7 +70,7 @@ int chunk_tokens(const Problem& pr, int n_warps_total) {
 }
 
 struct Layout {
-  size_t n_union, n_items, span, mask, rank, counter, ml, po, total;
+  size_t n_union, n_items, span, mask, rank, counter, n_used, span_done, head_done, ml, po, total;
   int C, CH;
 };
 
@@ -102,6 +88,9 @@ Layout layout(const Problem& pr) {
   l.mask = off; off = align256(off + n_grp * umax * 4);
   l.rank = off; off = align256(off + n_grp * umax * 16);
   l.counter = off; off = align256(off + 4);
+  l.n_used = off; off = align256(off + (size_t)pr.B * pr.Hq * 4);
+  l.span_done = off; off = align256(off + n_grp * umax * 4);
+  l.head_done = off; off = align256(off + (size_t)pr.B * pr.Hq * 4);
   l.ml = off; off = align256(off + parts * 2 * 4);
   l.po = off; off = align256(off + parts * (size_t)pr.d * 4);
   l.total = off;
@@ -109,49 +98,20 @@ Layout layout(const Problem& pr) {
 }
 
 // ---------------------------------------------------------------- plan
-// One CTA per (b, kv-head), one warp per query head of the group.  Also
-// empties the (m, l) slots of the group's partials: a slot that no item
-// writes keeps m = -inf and the merge skips it.
-//
-// The position of span j in the union U is the number of distinct selected
-// spans below j.  Up to kPlanBits candidates it is read off a bitmap of the
-// selected spans (a prefix popcount over its words); beyond that, each
-// span's position comes from binary searches in the heads' sorted lists.
+// One CTA per (b, kv-head), one warp per query head of the group: reads and
+// validates the heads' sel rows, then builds the group's plan.
 constexpr int kPlanThreads = kMaxG * 32;
-constexpr int kPlanWords = 512;
-constexpr int64_t kPlanBits = kPlanWords * 32;
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t* __restrict__ sel,
                                                                    Plan plan, Geo geo,
                                                                    uint32_t* __restrict__ err) {
-  __shared__ int sj[kMaxG][kMaxK];         // used spans of each head, ascending
-  __shared__ int nv[kMaxG];
-  __shared__ int cpref[kMaxG][kMaxK + 1];  // prefix counts of canonical entries
-  __shared__ uint8_t canon[kMaxG][kMaxK];
-  __shared__ uint32_t smask[kMaxG * kMaxK + 1];
-  __shared__ uint32_t bits[kPlanWords];     // selected spans (bitmap path)
-  __shared__ int wpref[kPlanWords + 1];     // popcount of the words below
-  __shared__ int s_nu;
-
+  __shared__ dplan::PlanSmem ps;
   const int grp = blockIdx.x;
   const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
   const int g = geo.g, k = geo.topk, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int umax = geo.umax;
-  const uint32_t lt = (1u << lane) - 1u;
-
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
-  if (grp == 0 && tid == 0) *plan.counter = 0;
-  {
-    const int nparts = g * (k + 1) * geo.C;
-    float2* ml = reinterpret_cast<float2*>(plan.ml) + (int64_t)(b * geo.Hq + kvh * g) * (k + 1) * geo.C;
-    for (int x = tid; x < nparts; x += kPlanThreads) ml[x] = make_float2(-INFINITY, 0.f);
-  }
-  for (int x = tid; x < kMaxG * kMaxK + 1; x += kPlanThreads) smask[x] = 0u;
-  const bool bitmap = geo.ell <= kPlanBits;
-  const int nw = bitmap ? (int)((geo.ell + 31) >> 5) : 0;
-  for (int x = tid; x < nw; x += kPlanThreads) bits[x] = 0u;
   if (warp < g) {
     const int32_t* row = sel + (int64_t)(b * geo.Hq + kvh * g + warp) * k;
     const int j0 = lane < k ? __ldg(row + lane) : -1;
@@ -159,119 +119,11 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
     bool bad;
     const int used = warp_sel_prefix(j0, j1, lane, k, geo.ell, &bad);
     if (bad && lane == 0) flag_error(err, SSA_DEVERR_BAD_SELECTION);
-    if (lane < used) sj[warp][lane] = j0;
-    if (lane + 32 < used) sj[warp][lane + 32] = j1;
-    if (lane == 0) nv[warp] = used;
+    if (lane < used) ps.sj[warp][lane] = j0;
+    if (lane + 32 < used) ps.sj[warp][lane + 32] = j1;
+    if (lane == 0) ps.nv[warp] = used;
   }
-  __syncthreads();
-  const int gbase = grp * umax;
-  if (bitmap) {
-    if (warp < g) {
-      if (lane < nv[warp]) atomicOr(&bits[sj[warp][lane] >> 5], 1u << (sj[warp][lane] & 31));
-      if (lane + 32 < nv[warp]) atomicOr(&bits[sj[warp][lane + 32] >> 5], 1u << (sj[warp][lane + 32] & 31));
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int run = 0;
-      for (int base = 0; base < nw; base += 32) {
-        const int c = base + lane < nw ? __popc(bits[base + lane]) : 0;
-        int v = c;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int o = __shfl_up_sync(0xffffffffu, v, off);
-          if (lane >= off) v += o;
-        }
-        if (base + lane < nw) wpref[base + lane] = run + v - c;
-        run += __shfl_sync(0xffffffffu, v, 31);
-      }
-      if (lane == 0) s_nu = run;
-    }
-    __syncthreads();
-    if (warp < g) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = lane + 32 * hh;
-        if (r >= nv[warp]) continue;
-        const int j = sj[warp][r];
-        const int p = wpref[j >> 5] + __popc(bits[j >> 5] & ((1u << (j & 31)) - 1u));
-        // the first head to claim the position writes the span
-        if (atomicOr(&smask[p], 1u << warp) == 0u) plan.span[gbase + p] = j;
-        plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
-      }
-    }
-  } else {
-    // canonical entry: no lower head of the group holds the same span
-    if (warp < g) {
-      uint32_t bal[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = lane + 32 * hh;
-        bool c = false;
-        if (r < nv[warp]) {
-          const int j = sj[warp][r];
-          bool dup = false;
-#pragma unroll
-          for (int h2 = 0; h2 < kMaxG; ++h2) {
-            if (h2 < warp) {
-              int lo = 0, hi = nv[h2];
-              while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
-              }
-              dup |= lo < nv[h2] && sj[h2][lo] == j;
-            }
-          }
-          c = !dup;
-          canon[warp][r] = c ? 1 : 0;
-        }
-        bal[hh] = __ballot_sync(0xffffffffu, c);
-      }
-      cpref[warp][lane] = __popc(bal[0] & lt);
-      cpref[warp][lane + 32] = __popc(bal[0]) + __popc(bal[1] & lt);
-      if (lane == 0) cpref[warp][64] = __popc(bal[0]) + __popc(bal[1]);
-    }
-    __syncthreads();
-    // position of span j in U = number of distinct spans below j
-    if (warp < g) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = lane + 32 * hh;
-        if (r >= nv[warp]) continue;
-        const int j = sj[warp][r];
-        int p = 0;
-#pragma unroll
-        for (int h2 = 0; h2 < kMaxG; ++h2) {
-          if (h2 < g) {
-            int lo = 0, hi = nv[h2];
-            while (lo < hi) {
-              const int mid = (lo + hi) >> 1;
-              if (sj[h2][mid] < j) lo = mid + 1; else hi = mid;
-            }
-            p += cpref[h2][lo];
-          }
-        }
-        if (canon[warp][r]) plan.span[gbase + p] = j;
-        atomicOr(&smask[p], 1u << warp);
-        plan.rank[(size_t)(gbase + p) * 16 + warp] = (uint8_t)r;
-      }
-    }
-    if (tid == 0) {
-      int n = 0;
-      for (int h = 0; h < g; ++h) n += cpref[h][nv[h]];
-      s_nu = n;
-    }
-  }
-  __syncthreads();
-  const int nu = s_nu;
-  for (int p = tid; p < nu; p += kPlanThreads) plan.mask[gbase + p] = smask[p];
-  if (tid < g) plan.rank[(size_t)(gbase + nu) * 16 + tid] = (uint8_t)k;
-  if (tid == 0) {
-    plan.span[gbase + nu] = (int)geo.ell;
-    plan.mask[gbase + nu] = (1u << g) - 1u;
-    plan.n_union[grp] = nu + 1;
-    const int64_t n_local = geo.pos - geo.ell * geo.S + 1;
-    plan.n_items[grp] = nu * geo.C + (int)((n_local + geo.CH - 1) / geo.CH);
-  }
+  dplan::plan_build<kPlanThreads / 32>(grp, ps, plan, geo);
 }
 
 // ---------------------------------------------------------------- attend
@@ -302,15 +154,18 @@ __device__ __forceinline__ void decode_item(int it, const Tables& tb, const Geo&
   x.grp = lo;
   const int li = it - tb.gpref[lo];
   const int nu = tb.n_union[lo];
-  if (li < (nu - 1) * geo.C) {
-    x.u = li / geo.C;
-    x.c = li - x.u * geo.C;
+  // the local span's chunks come first: its merge (all g heads) is the
+  // largest, and this way it never ends a step
+  const int nlc = dplan::local_chunks(geo);
+  if (li >= nlc) {
+    x.u = (li - nlc) / geo.C;
+    x.c = li - nlc - x.u * geo.C;
     const int64_t j = tb.span[lo * geo.umax + x.u];
     x.t0 = j * geo.S + (int64_t)x.c * geo.CH;
     x.t1 = min(x.t0 + geo.CH, (j + 1) * geo.S);
   } else {
     x.u = nu - 1;
-    x.c = li - (nu - 1) * geo.C;
+    x.c = li;
     x.t0 = geo.ell * geo.S + (int64_t)x.c * geo.CH;
     x.t1 = min(x.t0 + geo.CH, geo.pos + 1);
   }
@@ -320,7 +175,8 @@ __device__ __forceinline__ void decode_item(int it, const Tables& tb, const Geo&
 template <int DT, int D, int NG>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
+                         const void* __restrict__ Q, Plan plan, Geo geo, void* __restrict__ O,
+                         float* __restrict__ lse, uint32_t* __restrict__ err) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -435,22 +291,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rows r8 and r8 + 8 of each 16-row fragment.
   const int q4 = lane & 3, r8 = lane >> 2;
   const int mi = lane >> 3, rr = lane & 7;
-  uint32_t qb[NG][D / 16][2];
-  float o[NG][D / 16][4];
-  float m[NG][2], l[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
   int stage = 0;
   uint32_t phase = 0;
+  bool alive = true;
 #pragma unroll 1
-  while (inflight > 0) {
+  while (alive && inflight > 0) {
+    // one work item; its accumulators live only inside this body, so the
+    // merge after it has their registers
+    uint32_t qb[NG][D / 16][2];
+    float o[NG][D / 16][4];
+    float m[NG][2], l[NG][2];
+#pragma unroll 1
+    for (int tile = 0;; ++tile) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
       if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      alive = false;
       break;
     }
     const int4 mt = meta[stage];
-    if (mt.w == 0) {
+    if (tile == 0) {
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
@@ -592,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage = 0;
       phase ^= 1u;
     }
-    if (!last) continue;
+    if (last) break;
+    }  // tiles of the item
+    if (!alive) break;
 
     // ---- item epilogue: one partial per head that attends this span
     const int slot_idx = cur.grp * geo.umax + cur.u;
@@ -618,6 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }
+    }
+    // publish the partials; the span's last chunk merges it (and, through
+    // it, every head it completes)
+    __threadfence();
+    __syncwarp();
+    int done = 0;
+    if (lane == 0) done = atomicAdd(plan.span_done + slot_idx, 1);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    const int nch = cur.u == tb.n_union[cur.grp] - 1 ? dplan::local_chunks(geo) : geo.C;
+    if (done == nch - 1) {
+      __threadfence();
+      dplan::tail_merge<DT, D, 8>(plan, geo, cur.grp, cur.u, nch, hmask, O, lse, lane);
     }
   }
 }
@@ -663,7 +539,8 @@ template <int DT, int NG>
 __global__ void __launch_bounds__(q8::kThreads, 1)
     decode_attend_q8_kernel(const __grid_constant__ CUtensorMap tmK, const int8_t* __restrict__ Vq,
                             const float* __restrict__ Ks, const float* __restrict__ Vs, int64_t L_cap,
-                            const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
+                            const void* __restrict__ Q, Plan plan, Geo geo, void* __restrict__ O,
+                            float* __restrict__ lse, uint32_t* __restrict__ err) {
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -770,22 +647,27 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   }
 
   const int q4 = lane & 3, r8 = lane >> 2;
-  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
-  float o[NG][D / 16][4];
-  float m[NG][2], l[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
   int stage = 0;
   uint32_t phase = 0;
+  bool alive = true;
 #pragma unroll 1
-  while (inflight > 0) {
+  while (alive && inflight > 0) {
+    // one work item; its accumulators live only inside this body
+    uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+    float o[NG][D / 16][4];
+    float m[NG][2], l[NG][2];
+#pragma unroll 1
+    for (int tile = 0;; ++tile) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
       if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      alive = false;
       break;
     }
     const int4 mt = meta[stage];
-    if (mt.w == 0) {
+    if (tile == 0) {
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
@@ -969,7 +851,9 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       stage = 0;
       phase ^= 1u;
     }
-    if (!last) continue;
+    if (last) break;
+    }  // tiles of the item
+    if (!alive) break;
 
     const int slot_idx = cur.grp * geo.umax + cur.u;
     const uint32_t hmask = tb.mask[slot_idx];
@@ -995,96 +879,20 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }
     }
-  }
-}
-
-// ---------------------------------------------------------------- merge
-// One CTA per (b, q-head): its (topk + 1) * C partial slots, in (span rank,
-// chunk) order, split into 8 contiguous runs, one per warp; empty slots
-// (m = -inf) are skipped.  The warps' results are then combined in order.
-constexpr int kMergeWarps = 8;
-constexpr int kBatch = 8;
-
-template <int DT, int D>
-__global__ void __launch_bounds__(kMergeWarps * 32)
-    decode_merge_kernel(Plan plan, Geo geo, void* __restrict__ O, float* __restrict__ lse) {
-  constexpr int E = D / 32;  // columns per lane
-  __shared__ float wm[kMergeWarps], wl[kMergeWarps];
-  __shared__ float wo[kMergeWarps][D];
-  const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  ptx::pdl_wait();
-  ptx::pdl_launch_dependents();
-  const int nslots = (geo.topk + 1) * geo.C;
-  const int per = (nslots + kMergeWarps - 1) / kMergeWarps;
-  const int s0 = warp * per, s1 = min(s0 + per, nslots);
-  const int64_t base = (int64_t)row * nslots;
-  const float2* ml = reinterpret_cast<const float2*>(plan.ml);
-  float M = -INFINITY, Ls = 0.f, acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int sb = s0; sb < s1; sb += 32) {
-    const int sl = sb + lane;
-    const float2 mlv = sl < s1 ? ml[base + sl] : make_float2(-INFINITY, 0.f);
-    uint32_t nz = __ballot_sync(0xffffffffu, mlv.x != -INFINITY);
-    while (nz) {
-      int ids[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        ids[i] = nz ? __ffs(nz) - 1 : -1;
-        nz &= nz ? nz - 1u : 0u;
-      }
-      float po[kBatch][E];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (ids[i] >= 0) {
-          const float* src = plan.po + (base + sb + ids[i]) * D + lane * E;
-          if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            po[i][0] = v.x; po[i][1] = v.y; po[i][2] = v.z; po[i][3] = v.w;
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            po[i][0] = v.x; po[i][1] = v.y;
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (ids[i] < 0) continue;
-        const float pm = __shfl_sync(0xffffffffu, mlv.x, ids[i]);
-        const float pl = __shfl_sync(0xffffffffu, mlv.y, ids[i]);
-        const float Mn = fmaxf(M, pm);
-        const float a = exp2f(M - Mn), bb = exp2f(pm - Mn);
-        Ls = Ls * a + pl * bb;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + po[i][e] * bb;
-        M = Mn;
-      }
+    // publish the partials; the span's last chunk merges it (and, through
+    // it, every head it completes)
+    __threadfence();
+    __syncwarp();
+    int done = 0;
+    if (lane == 0) done = atomicAdd(plan.span_done + slot_idx, 1);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    const int nch = cur.u == tb.n_union[cur.grp] - 1 ? dplan::local_chunks(geo) : geo.C;
+    if (done == nch - 1) {
+      __threadfence();
+      dplan::tail_merge<DT, D, 2>(plan, geo, cur.grp, cur.u, nch, hmask, O, lse, lane);
     }
   }
-  if (lane == 0) {
-    wm[warp] = M;
-    wl[warp] = Ls;
-  }
-#pragma unroll
-  for (int e = 0; e < E; ++e) wo[warp][lane * E + e] = acc[e];
-  __syncthreads();
-  if (threadIdx.x < D) {
-    const int col = threadIdx.x;
-    float Mt = -INFINITY;
-    for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, wm[w]);
-    float Lt = 0.f, ot = 0.f;
-    for (int w = 0; w < kMergeWarps; ++w) {
-      if (wm[w] == -INFINITY) continue;
-      const float f = exp2f(wm[w] - Mt);
-      Lt += wl[w] * f;
-      ot += wo[w][col] * f;
-    }
-    store_elem<DT>(O, (int64_t)row * D + col, ot / Lt);
-    if (lse && col == 0) lse[row] = Mt * kLn2 + logf(Lt);
-  }
 }
-
 
 // The plan's workspace pointers and the geometry of a decode step.
 void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
@@ -1096,6 +904,9 @@ void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
   plan.mask = reinterpret_cast<uint32_t*>(w8 + lay.mask);
   plan.rank = w8 + lay.rank;
   plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
+  plan.n_used = reinterpret_cast<int*>(w8 + lay.n_used);
+  plan.span_done = reinterpret_cast<int*>(w8 + lay.span_done);
+  plan.head_done = reinterpret_cast<int*>(w8 + lay.head_done);
   plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
   plan.po = reinterpret_cast<float*>(w8 + lay.po);
   geo.Hq = pr.Hq;
@@ -1113,15 +924,10 @@ void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
 }
 
 template <int DT>
-cudaError_t launch_typed_q8(const Problem& pr, const void* Q, int64_t pos, const int8_t* Kq, const float* Ks,
-                            const int8_t* Vq, const float* Vs, const int32_t* sel, void* O, float* lse, void* ws,
-                            cudaStream_t st) {
+cudaError_t attend_q8(const Problem& pr, const void* Q, const int8_t* Kq, const float* Ks, const int8_t* Vq,
+                      const float* Vs, void* O, float* lse, const Plan& plan, const Geo& geo, uint32_t* err,
+                      cudaStream_t st) {
   constexpr int D = 128;
-  Plan plan;
-  Geo geo;
-  plan_geo(pr, pos, ws, plan, geo);
-  const size_t smem = q8::kFixed;
-  uint32_t* err = ws_error(ws);
   CUtensorMap tmK;
   cudaError_t e = make_q8_tmap(&tmK, Kq, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
   if (e != cudaSuccess) return e;
@@ -1129,62 +935,25 @@ cudaError_t launch_typed_q8(const Problem& pr, const void* Q, int64_t pos, const
   static bool attr_done[2][kMaxDevices] = {};
   e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(attend, dim3(device_sm_count()), dim3(q8::kThreads), smem, st, tmK, Vq, Ks, Vs, pr.L_cap, Q, plan,
-                 geo, err);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st,
-                    plan, geo, O, lse);
+  return launch_pdl(attend, dim3(device_sm_count()), dim3(q8::kThreads), q8::kFixed, st, tmK, Vq, Ks, Vs,
+                    pr.L_cap, Q, plan, geo, O, lse, err);
 }
 
 template <int DT, int D>
-cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const void* K, const void* V,
-                         const int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
+cudaError_t attend_16(const Problem& pr, const void* Q, const void* K, const void* V, void* O, float* lse,
+                      const Plan& plan, const Geo& geo, uint32_t* err, cudaStream_t st) {
   using Cf = Cfg<D>;
-  const Layout lay = layout(pr);
-  uint8_t* w8 = static_cast<uint8_t*>(ws);
-  Plan plan;
-  plan.n_union = reinterpret_cast<int*>(w8 + lay.n_union);
-  plan.n_items = reinterpret_cast<int*>(w8 + lay.n_items);
-  plan.span = reinterpret_cast<int*>(w8 + lay.span);
-  plan.mask = reinterpret_cast<uint32_t*>(w8 + lay.mask);
-  plan.rank = w8 + lay.rank;
-  plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
-  plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
-  plan.po = reinterpret_cast<float*>(w8 + lay.po);
-  Geo geo;
-  geo.Hq = pr.Hq;
-  geo.Hkv = pr.Hkv;
-  geo.g = pr.g;
-  geo.topk = pr.topk;
-  geo.S = pr.S;
-  geo.C = lay.C;
-  geo.CH = lay.CH;
-  geo.umax = pr.g * pr.topk + 1;
-  geo.n_grp = pr.B * pr.Hkv;
-  geo.pos = pos;
-  geo.ell = pos / pr.S;
-  geo.scale_log2e = pr.scale * kLog2e;
-  const size_t smem = Cf::kFixed;
-  uint32_t* err = ws_error(ws);
-
   CUtensorMap tmK, tmV;
   cudaError_t e = make_kv_tmap(&tmK, K, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
   if (e != cudaSuccess) return e;
   e = make_kv_tmap(&tmV, V, pr.dtype, D, pr.L, pr.L_cap, (int64_t)pr.B * pr.Hkv, kTile);
   if (e != cudaSuccess) return e;
-
   auto attend = pr.g <= 8 ? decode_attend_kernel<DT, D, 1> : decode_attend_kernel<DT, D, 2>;
   static bool attr_done[2][kMaxDevices] = {};
   e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), smem, st, tmK, tmV, Q, plan, geo, err);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st,
-                    plan, geo, O, lse);
+  return launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), Cf::kFixed, st, tmK, tmV, Q, plan, geo, O,
+                    lse, err);
 }
 
 }  // namespace
@@ -1192,8 +961,14 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t pos, const vo
 cudaError_t launch_attend_decode_q8(const Problem& pr, const void* Q, int64_t pos, const int8_t* Kq,
                                     const float* Ks, const int8_t* Vq, const float* Vs, const int32_t* sel,
                                     void* O, float* lse, void* ws, cudaStream_t st) {
-  if (pr.dtype == DT_BF16) return launch_typed_q8<DT_BF16>(pr, Q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws, st);
-  return launch_typed_q8<DT_F16>(pr, Q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws, st);
+  Plan plan;
+  Geo geo;
+  plan_geo(pr, pos, ws, plan, geo);
+  uint32_t* err = ws_error(ws);
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  if (pr.dtype == DT_BF16) return attend_q8<DT_BF16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
+  return attend_q8<DT_F16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
 }
 
 bool decode_fast_supported(const Problem& pr) {
@@ -1203,15 +978,31 @@ bool decode_fast_supported(const Problem& pr) {
 
 size_t decode_ws_bytes(const Problem& pr) { return layout(pr).total - kWsHeader; }
 
+void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo) {
+  plan_geo(pr, pos, ws, *plan, *geo);
+}
+
+cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,
+                                         float* lse, const dplan::Plan& plan, const dplan::Geo& geo,
+                                         uint32_t* err, cudaStream_t st) {
+  if (pr.d == 128) {
+    if (pr.dtype == DT_BF16) return attend_16<DT_BF16, 128>(pr, Q, K, V, O, lse, plan, geo, err, st);
+    return attend_16<DT_F16, 128>(pr, Q, K, V, O, lse, plan, geo, err, st);
+  }
+  if (pr.dtype == DT_BF16) return attend_16<DT_BF16, 64>(pr, Q, K, V, O, lse, plan, geo, err, st);
+  return attend_16<DT_F16, 64>(pr, Q, K, V, O, lse, plan, geo, err, st);
+}
+
 cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, const void* K,
                                  const void* V, const int32_t* sel, void* O, float* lse, void* ws,
                                  cudaStream_t st) {
-  if (pr.d == 128) {
-    if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 128>(pr, Q, pos, K, V, sel, O, lse, ws, st);
-    return launch_typed<DT_F16, 128>(pr, Q, pos, K, V, sel, O, lse, ws, st);
-  }
-  if (pr.dtype == DT_BF16) return launch_typed<DT_BF16, 64>(pr, Q, pos, K, V, sel, O, lse, ws, st);
-  return launch_typed<DT_F16, 64>(pr, Q, pos, K, V, sel, O, lse, ws, st);
+  Plan plan;
+  Geo geo;
+  plan_geo(pr, pos, ws, plan, geo);
+  uint32_t* err = ws_error(ws);
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_attend_decode_planned(pr, Q, K, V, O, lse, plan, geo, err, st);
 }
 
 }  // namespace ssa

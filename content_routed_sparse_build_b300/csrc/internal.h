@@ -113,6 +113,12 @@ cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, 
                                  const void* V, const int32_t* sel, void* O, float* lse, void* ws,
                                  cudaStream_t st);
 
+// A whole decode step (16-bit types, the fast decode path): route with the
+// plan built in the route kernel's cluster, then attend with the merges in
+// the attend kernel's tail -- two launches.
+cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, const float* summ, const void* K,
+                               const void* V, int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
+
 // Prefill attention fast path (16-bit types): dispatch, span tiles, merge.
 size_t prefill_ws_bytes(const Problem& pr, int64_t n_q);
 bool prefill_fast_supported(const Problem& pr);

@@ -13,6 +13,7 @@
 // best k (score, span) pairs in shared memory.
 #include <cooperative_groups.h>
 
+#include "decode_plan.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -126,13 +127,18 @@ __device__ __forceinline__ void fold_block(float* lsv, int* lsj, const float* sc
 // all of its summary loads in flight at once, the two halves then added.
 // Each block is folded into per-head lists; finally CTA `rank` merges head
 // rank (+16) over the cluster's lists through distributed shared memory.
+//
+// With PLAN (a whole decode step), each final list is also pushed into CTA
+// 0's shared memory, and CTA 0 then builds the group's decode plan
+// (decode_plan.cuh) for the attend kernel that follows: the step needs no
+// separate plan kernel.
 constexpr int kBlk = 128;
 
-template <int DT, int D, int G, int NE>
+template <int DT, int D, int G, int NE, bool PLAN>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
     route_decode_kernel(const void* __restrict__ Q, const float* __restrict__ summ,
                         int32_t* __restrict__ sel, float* __restrict__ sel_score, int Hq, int Hkv,
-                        int64_t pos, int S, int topk, int64_t ns_cap) {
+                        int64_t pos, int S, int topk, int64_t ns_cap, dplan::Plan plan, dplan::Geo geo) {
   constexpr int HD = D / 2;          // dims per lane
   constexpr int HPAD = HD + 4;       // padded half stride, keeps the two halves in other banks
   constexpr int NL = HD / 4;         // float4 loads per lane
@@ -140,6 +146,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
   __shared__ float sc_s[G][kBlk];
   __shared__ float lsv_s[G][kMaxK];
   __shared__ int lsj_s[G][kMaxK];
+  __shared__ dplan::PlanSmem ps;     // CTA 0 of a PLAN cluster: the group's final lists and plan scratch
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -245,6 +252,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
           const int p = base + __popc(bal & ((1u << lane) - 1u));
           out[p] = vj[i];
           if (osc) osc[p] = v[i];
+          if constexpr (PLAN) cluster.map_shared_rank(&ps.sj[h][0], 0)[p] = vj[i];
         }
         base += __popc(bal);
       }
@@ -252,9 +260,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
         out[e] = -1;
         if (osc) osc[e] = __int_as_float(0x7fc00000);
       }
+      if constexpr (PLAN) {
+        if (lane == 0) *cluster.map_shared_rank(&ps.nv[h], 0) = base;
+      }
     }
   }
   cluster.sync();
+  if constexpr (PLAN) {
+    if (rank == 0) dplan::plan_build<8>(b * Hkv + kvh, ps, plan, geo);
+  }
 }
 
 // ---------------------------------------------------------------- prefill
@@ -395,9 +409,10 @@ __global__ void __launch_bounds__(256) route_prefill_kernel(
   }
 }
 
-template <int DT, int D, int G, int NE>
+template <int DT, int D, int G, int NE, bool PLAN>
 cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
-                                int32_t* sel, float* sel_score, cudaStream_t st) {
+                                int32_t* sel, float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo,
+                                cudaStream_t st) {
   dim3 grid(kCluster, pr.Hkv, pr.B);
   // a cluster of 16 is above the portable size of 8: the kernel opts in once per device
   static bool attr_done[kMaxDevices] = {};
@@ -405,30 +420,37 @@ cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, NE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, NE, PLAN>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_pdl(route_decode_kernel<DT, D, G, NE>, grid, dim3(256), 0, st, Q, summ, sel,
-                    sel_score, pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap);
+  return launch_pdl(route_decode_kernel<DT, D, G, NE, PLAN>, grid, dim3(256), 0, st, Q, summ, sel,
+                    sel_score, pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap, plan, geo);
 }
 
-template <int DT, int D, int G>
+template <int DT, int D, int G, bool PLAN>
 cudaError_t decode_route_ne(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
-                            int32_t* sel, float* sel_score, cudaStream_t st) {
+                            int32_t* sel, float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo,
+                            cudaStream_t st) {
   // entries per lane of the final cluster merge: kCluster * topk / 32
-  if (pr.topk <= 16) return launch_decode_route<DT, D, G, 8>(pr, Q, q_pos0, summ, sel, sel_score, st);
-  return launch_decode_route<DT, D, G, 32>(pr, Q, q_pos0, summ, sel, sel_score, st);
+  if (pr.topk <= 16)
+    return launch_decode_route<DT, D, G, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return launch_decode_route<DT, D, G, 32, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+}
+
+template <int DT, int D, bool PLAN>
+cudaError_t decode_route_g(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ, int32_t* sel,
+                           float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo, cudaStream_t st) {
+  if (pr.g <= 4) return decode_route_ne<DT, D, 4, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.g <= 8) return decode_route_ne<DT, D, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return decode_route_ne<DT, D, 16, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
 }
 
 template <int DT, int D>
 cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st) {
-  if (n_q == 1) {
-    if (pr.g <= 4) return decode_route_ne<DT, D, 4>(pr, Q, q_pos0, summ, sel, sel_score, st);
-    if (pr.g <= 8) return decode_route_ne<DT, D, 8>(pr, Q, q_pos0, summ, sel, sel_score, st);
-    return decode_route_ne<DT, D, 16>(pr, Q, q_pos0, summ, sel, sel_score, st);
-  }
+  if (n_q == 1) return decode_route_g<DT, D, false>(pr, Q, q_pos0, summ, sel, sel_score, {}, {}, st);
   const size_t smem = prefill_smem_bytes<D>(pr.topk);
   static bool attr_done[kMaxDevices] = {};
   cudaError_t e = ensure_smem_attr(route_prefill_kernel<DT, D>, prefill_smem_bytes<D>(kMaxK), attr_done);
@@ -442,6 +464,22 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t 
 }
 
 }  // namespace
+
+cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, const float* summ, const void* K,
+                               const void* V, int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
+  dplan::Plan plan;
+  dplan::Geo geo;
+  decode_plan_args(pr, pos, ws, &plan, &geo);
+  cudaError_t e;
+  if (pr.d == 128)
+    e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
+                            : decode_route_g<DT_F16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
+  else
+    e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
+                            : decode_route_g<DT_F16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
+  if (e != cudaSuccess) return e;
+  return launch_attend_decode_planned(pr, Q, K, V, O, lse, plan, geo, ws_error(ws), st);
+}
 
 cudaError_t launch_route(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st) {

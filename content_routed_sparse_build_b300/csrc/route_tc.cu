@@ -40,7 +40,11 @@ struct RCfg {
   static constexpr int kQBytes = (D / 64) * kRegion;
   static constexpr int kPlane = (D / 64) * kRegionB;   // one plane of a block
   static constexpr int kStage = 3 * kPlane;
-  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + 2 * kStage + 256;
+  // per selection warp: its 32 rows' scores of one 32-span chunk, row-major
+  // with a padded stride (conflict-free stores, any-column loads)
+  static constexpr int kStageStride = 33;
+  static constexpr int kPick = 4 * 32 * kStageStride * 4;
+  static constexpr size_t kSmem = 1024 + (size_t)kQBytes + 2 * kStage + 256 + kPick;
 };
 
 template <int DT>
@@ -117,21 +121,6 @@ struct Top16 {
   }
 };
 
-// r[p] for a runtime p in [0, 32): a 5-level select tree over the static
-// register array.
-__device__ __forceinline__ float pick32(const uint32_t (&r)[32], int p) {
-  float t16[16], t8[8], t4[4], t2[2];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) t16[i] = __uint_as_float((p & 1) ? r[2 * i + 1] : r[2 * i]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) t8[i] = (p & 2) ? t16[2 * i + 1] : t16[2 * i];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) t4[i] = (p & 4) ? t8[2 * i + 1] : t8[2 * i];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) t2[i] = (p & 8) ? t4[2 * i + 1] : t4[2 * i];
-  return (p & 16) ? t2[1] : t2[0];
-}
-
 template <int DT, int D>
 __global__ void __launch_bounds__(kRouteThreads, 2)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmP, const void* __restrict__ Q, int32_t* __restrict__ sel,
@@ -151,6 +140,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2)
   uint64_t* s_free = bar + 7;   // [2]
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 9);
   volatile int* abort = reinterpret_cast<volatile int*>(bar + 10);
+  float* pick = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bar) + 256);  // [4 warps][32][33]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int g = Hq / Hkv;
@@ -258,6 +248,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2)
     Top16 best;
     best.init();
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float* my_pick = pick + (warp * 32 + lane) * C::kStageStride;
     for (int blk = 0; blk < nblk; ++blk) {
       const int st = blk & 1;
       if (!ptx::mbar_wait(&s_full[st], (uint32_t)((blk >> 1) & 1))) {
@@ -276,19 +267,40 @@ __global__ void __launch_bounds__(kRouteThreads, 2)
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&s_free[st]);
         }
-        // candidates of this chunk that beat the current 16th best
         const int j0 = jb + q * 32;
+        // spans j0 + c with c >= nvalid are no candidates of this row (only
+        // its last chunk has any)
+        const int64_t nvalid = ell - j0;
+        if (nvalid < 32) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c >= nvalid) rr[c] = 0xff800000u;  // -inf
+        }
+        // the chunk's best score first: most chunks of most rows have none
+        // above the current 16th best and stop here
+        float mx = __uint_as_float(rr[0]);
+#pragma unroll
+        for (int c = 1; c < 31; c += 2) mx = ptx::max3(mx, __uint_as_float(rr[c]), __uint_as_float(rr[c + 1]));
+        mx = fmaxf(mx, __uint_as_float(rr[31]));
         const float t0 = best.thr();
+        if (!__any_sync(0xffffffffu, mx > t0)) continue;
+        // candidates that beat the current 16th best
         uint32_t pass = 0;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (j0 + c < ell && __uint_as_float(rr[c]) > t0) pass |= 1u << c;
+          if (__uint_as_float(rr[c]) > t0) pass |= 1u << c;
+        // the lane's row of scores, so that any column can be read back by
+        // index (a load instead of a select tree over the registers)
+        if (pass) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) my_pick[c] = __uint_as_float(rr[c]);
+        }
         // insert them in lockstep across the warp, lowest span first
         while (__any_sync(0xffffffffu, pass != 0u)) {
           if (pass) {
             const int p = __ffs(pass) - 1;
             pass &= pass - 1u;
-            best.push(pick32(rr, p), j0 + p);
+            best.push(my_pick[p], j0 + p);
           }
         }
       }

@@ -162,6 +162,24 @@ SSA_API int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, c
                       size_t ws_bytes, void* stream);
 
 /*
+ * One whole decode step: ssa_route with n_q = 1 at q_pos0 = pos, then
+ * ssa_attend_decode on its selections (superlinear post, key-idea section:
+ * each new token scores the candidate spans, keeps the top k and attends
+ * their tokens plus its own span).  Same arguments, layouts and results as
+ * those two calls in sequence: sel [B, Hq, topk] receives the selections,
+ * O [B, Hq, d] and lse [B, Hq] (nullable) the outputs; ws as for
+ * ssa_attend_decode (ssa_workspace_size(p, 1, SSA_OP_DECODE) bytes).
+ * On the 16-bit fast path the step is two kernel launches instead of the
+ * separate calls' four: the route kernel also builds the attend plan, and
+ * the attend kernel merges the partial outputs in its tail.  Other shapes
+ * (fp32) run the two calls' kernels in sequence.
+ * Requires 0 <= pos < L; summaries of spans 0 .. floor(pos / S) - 1 built.
+ */
+SSA_API int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
+                            const void* K, const void* V, int32_t* sel, void* O, float* lse,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Chunked-prefill attention for n_q queries at positions q_pos0 .. q_pos0 +
  * n_q - 1 (superlinear post: chunked prefill against the kept cache; the
  * attention itself as for ssa_attend_decode).  Work is dispatched span-major:

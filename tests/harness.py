@@ -128,8 +128,11 @@ class GpuRun:
             j1 = (L + w.S - 1) // w.S
         ssa.ssa_build_summaries(p, self.K, j0, j1, self.summ)
 
-    def decode(self, steps: range | None = None, want_scores: bool = False):
-        """Route + attend for decode steps; returns host (sel, O, lse[, scores])."""
+    def decode(self, steps: range | None = None, want_scores: bool = False, fused: bool = False):
+        """Route + attend for decode steps; returns host (sel, O, lse[, scores], err).
+
+        fused: each step is one ssa_decode_step call (the benchmark's path)
+        instead of ssa_route then ssa_attend_decode."""
         w = self.w
         p = self.p_full
         ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE, self.dev)
@@ -141,8 +144,11 @@ class GpuRun:
             sc = torch.empty(sel.shape, dtype=torch.float32, device=self.dev) if want_scores else None
             O = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=self.dev)
             lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=self.dev)
-            ssa.ssa_route(p, q, 1, w.q_pos0 + s, self.summ, sel, sc)
-            ssa.ssa_attend_decode(p, q, w.q_pos0 + s, self.K, self.V, sel, O, lse, ws)
+            if fused:
+                ssa.ssa_decode_step(p, q, w.q_pos0 + s, self.summ, self.K, self.V, sel, O, lse, ws)
+            else:
+                ssa.ssa_route(p, q, 1, w.q_pos0 + s, self.summ, sel, sc)
+                ssa.ssa_attend_decode(p, q, w.q_pos0 + s, self.K, self.V, sel, O, lse, ws)
             sels.append(sel)
             outs.append(O)
             lses.append(lse)

@@ -97,6 +97,12 @@ def test_decode_1m_all_steps():
     O_o, lse_o = oracle_outputs_decode(orc, Q, V, sel_o, steps)
     assert max_abs(O_g, O_o) <= TOL[w.dtype]
     assert max_abs(lse_g, lse_o) <= LSE_TOL[w.dtype]
+    # the benchmark's path: one ssa_decode_step per step
+    sel_f, O_f, lse_f, err = run.decode(fused=True)
+    assert err == 0
+    assert np.array_equal(sel_f, sel_o)
+    assert max_abs(O_f, O_o) <= TOL[w.dtype]
+    assert max_abs(lse_f, lse_o) <= LSE_TOL[w.dtype]
     q4, sel_p, same, O_p, lse_p, t = _probe_decode(w, inp, run, orc.summ)
     O_po, lse_po, _ = oracle.attend(q4, K, V, t, w.S, sel_p)
     assert max_abs(O_p[same], O_po[same]) <= TOL[w.dtype]
@@ -221,6 +227,11 @@ def test_decode_10m_all_steps():
     sel_g, O_g, lse_g, err = run.decode()
     assert err == 0
     assert np.array_equal(sel_g, sel_o)
+    # the benchmark's path gives the same selections and bit-identical outputs
+    sel_f, O_f, lse_f, err = run.decode(fused=True)
+    assert err == 0
+    assert np.array_equal(sel_f, sel_o)
+    assert torch.equal(O_f, O_g) and torch.equal(lse_f, lse_g)
     # the probe routes on the device cache; its outputs are checked compacted too
     q4, sel_p, same, O_p, lse_p, t_p = _probe_decode(w, inp, run, summ)
     del Kd, Vd, run

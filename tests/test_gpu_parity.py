@@ -76,6 +76,27 @@ def test_decode_parity(w):
     assert max_abs(lse_g, lse_o) <= LSE_TOL[w.dtype]
 
 
+@pytest.mark.parametrize("w", DECODE_CASES, ids=lambda w: w.name)
+def test_decode_step_parity(w):
+    """ssa_decode_step (route with the plan built in its cluster, attend with
+    the merges in its tail) against the oracle and against the two calls."""
+    inp, Q, K, orc, sel_o, margin, redrawn = margin_checked_inputs(w)
+    V = inp.v()
+    run = GpuRun(w, Q, K, V)
+    run.summaries()
+    sel_g, O_g, lse_g, err = run.decode(fused=True)
+    assert err == 0
+    assert np.array_equal(sel_g, sel_o)
+    O_o, lse_o = oracle_outputs_decode(orc, Q, V, sel_o, range(w.n_q))
+    assert max_abs(O_g, O_o) <= TOL[w.dtype]
+    assert max_abs(lse_g, lse_o) <= LSE_TOL[w.dtype]
+    sel_2, O_2, lse_2, err2 = run.decode()
+    assert err2 == 0 and np.array_equal(sel_2, sel_g)
+    if w.dtype != F32:
+        # same kernels for the attention, the same merge order: identical bits
+        assert torch.equal(O_2, O_g) and torch.equal(lse_2, lse_g)
+
+
 def test_summaries_parity_fp32_exactish():
     w = W.Workload("case_summ", "decode", 2, 4, 2, 128, 5000, 96, 4, BF16, n_q=1, q_pos0=4999,
                    chunk=1, seed=31)
