@@ -1055,9 +1055,11 @@ def main():
 
 def launches_per_decode_step(w) -> int:
     """Kernels one ssa_decode_step launches: on the 16-bit path the route
-    (which also builds the plan) and the attend (which also merges); the
-    fp32 path runs the route and one row kernel."""
-    return 2
+    (which also builds the attend plan), the split attention and the merge;
+    the fp32 path runs the route and one row kernel."""
+    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+    fast = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE) > 256
+    return 3 if fast else 2
 
 
 if __name__ == "__main__":

@@ -6,23 +6,24 @@
 // (stork.ai): exact attention over the content-selected subset.  The local
 // span [l*S, pos] is always attended.
 //
-// Two kernels (plan building and the merges are in decode_plan.cuh):
+// Three kernels (the plan itself is built by decode_plan.cuh, here or, for a
+// whole decode step, inside the route kernel):
 //  plan    one CTA per (b, kv-head): validates the g heads' selections and
 //          builds their union U (ascending, local span last) with, per span,
 //          the mask of heads that chose it and each head's rank for it.
 //  attend  persistent, one CTA per SM, six independent warps.  Work items
 //          are (group, span of U, chunk of CH tokens), handed out by an
-//          atomic counter (each group's local span first).  Each warp runs
-//          its own two-stage ring of 32-token K / V tiles loaded by TMA
-//          (128-byte swizzle, mbarrier completion), each tile computed as two
-//          16-token fragments.  The MMAs are transposed so that the query
-//          group fits the n8 side of mma.sync: S^T = K Q^T (tokens x heads)
-//          and O^T += V^T P^T (d x heads), P^T turned into the B operand by
-//          movmatrix.  An online softmax runs per head (column); at the end
-//          of an item the warp writes one partial (m, l, o) per head that
-//          chose the span.  Every K / V byte of the union is read once.  The
-//          warp that finishes a span's last chunk merges its chunks, and the
-//          one that finishes a head's last span writes the head's O and lse.
+//          atomic counter.  Each warp runs its own two-stage ring of 32-token
+//          K / V tiles loaded by TMA (128-byte swizzle, mbarrier completion),
+//          each tile computed as two 16-token fragments.  The MMAs are
+//          transposed so that the query group fits the n8 side of
+//          mma.sync: S^T = K Q^T (tokens x heads) and O^T += V^T P^T
+//          (d x heads), P^T turned into the B operand by movmatrix.  An
+//          online softmax runs per head (column); at the end of an item the
+//          warp writes one partial (m, l, o) per head that chose the span.
+//          Every K / V byte of the union is read once.
+//  merge   one CTA per (b, q-head): combines the head's partials (span
+//          order, then chunk order) into O and lse.
 // Softmax runs in base 2: scores are scaled by scale * log2(e).
 #include "decode_plan.cuh"
 #include "internal.h"
@@ -42,6 +43,7 @@ constexpr int kWarps = 6;     // independent warps per CTA (6 x 2 stages x 16 KB
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 227 * 1024;
+constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -70,7 +72,7 @@ int chunk_tokens(const Problem& pr, int n_warps_total) {
 }
 
 struct Layout {
-  size_t n_union, n_items, span, mask, rank, counter, n_used, span_done, head_done, ml, po, total;
+  size_t n_union, n_items, span, mask, rank, counter, ml, po, total;
   int C, CH;
 };
 
@@ -88,9 +90,6 @@ Layout layout(const Problem& pr) {
   l.mask = off; off = align256(off + n_grp * umax * 4);
   l.rank = off; off = align256(off + n_grp * umax * 16);
   l.counter = off; off = align256(off + 4);
-  l.n_used = off; off = align256(off + (size_t)pr.B * pr.Hq * 4);
-  l.span_done = off; off = align256(off + n_grp * umax * 4);
-  l.head_done = off; off = align256(off + (size_t)pr.B * pr.Hq * 4);
   l.ml = off; off = align256(off + parts * 2 * 4);
   l.po = off; off = align256(off + parts * (size_t)pr.d * 4);
   l.total = off;
@@ -154,18 +153,15 @@ __device__ __forceinline__ void decode_item(int it, const Tables& tb, const Geo&
   x.grp = lo;
   const int li = it - tb.gpref[lo];
   const int nu = tb.n_union[lo];
-  // the local span's chunks come first: its merge (all g heads) is the
-  // largest, and this way it never ends a step
-  const int nlc = dplan::local_chunks(geo);
-  if (li >= nlc) {
-    x.u = (li - nlc) / geo.C;
-    x.c = li - nlc - x.u * geo.C;
+  if (li < (nu - 1) * geo.C) {
+    x.u = li / geo.C;
+    x.c = li - x.u * geo.C;
     const int64_t j = tb.span[lo * geo.umax + x.u];
     x.t0 = j * geo.S + (int64_t)x.c * geo.CH;
     x.t1 = min(x.t0 + geo.CH, (j + 1) * geo.S);
   } else {
     x.u = nu - 1;
-    x.c = li;
+    x.c = li - (nu - 1) * geo.C;
     x.t0 = geo.ell * geo.S + (int64_t)x.c * geo.CH;
     x.t1 = min(x.t0 + geo.CH, geo.pos + 1);
   }
@@ -175,8 +171,7 @@ __device__ __forceinline__ void decode_item(int it, const Tables& tb, const Geo&
 template <int DT, int D, int NG>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const void* __restrict__ Q, Plan plan, Geo geo, void* __restrict__ O,
-                         float* __restrict__ lse, uint32_t* __restrict__ err) {
+                         const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -291,28 +286,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // rows r8 and r8 + 8 of each 16-row fragment.
   const int q4 = lane & 3, r8 = lane >> 2;
   const int mi = lane >> 3, rr = lane & 7;
+  uint32_t qb[NG][D / 16][2];
+  float o[NG][D / 16][4];
+  float m[NG][2], l[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
   int stage = 0;
   uint32_t phase = 0;
-  bool alive = true;
 #pragma unroll 1
-  while (alive && inflight > 0) {
-    // one work item; its accumulators live only inside this body, so the
-    // merge after it has their registers
-    uint32_t qb[NG][D / 16][2];
-    float o[NG][D / 16][4];
-    float m[NG][2], l[NG][2];
-#pragma unroll 1
-    for (int tile = 0;; ++tile) {
+  while (inflight > 0) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
       if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
-      alive = false;
       break;
     }
     const int4 mt = meta[stage];
-    if (tile == 0) {
+    if (mt.w == 0) {
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
@@ -454,9 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage = 0;
       phase ^= 1u;
     }
-    if (last) break;
-    }  // tiles of the item
-    if (!alive) break;
+    if (!last) continue;
 
     // ---- item epilogue: one partial per head that attends this span
     const int slot_idx = cur.grp * geo.umax + cur.u;
@@ -482,18 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }
-    }
-    // publish the partials; the span's last chunk merges it (and, through
-    // it, every head it completes)
-    __threadfence();
-    __syncwarp();
-    int done = 0;
-    if (lane == 0) done = atomicAdd(plan.span_done + slot_idx, 1);
-    done = __shfl_sync(0xffffffffu, done, 0);
-    const int nch = cur.u == tb.n_union[cur.grp] - 1 ? dplan::local_chunks(geo) : geo.C;
-    if (done == nch - 1) {
-      __threadfence();
-      dplan::tail_merge<DT, D, 8>(plan, geo, cur.grp, cur.u, nch, hmask, O, lse, lane);
     }
   }
 }
@@ -539,8 +514,7 @@ template <int DT, int NG>
 __global__ void __launch_bounds__(q8::kThreads, 1)
     decode_attend_q8_kernel(const __grid_constant__ CUtensorMap tmK, const int8_t* __restrict__ Vq,
                             const float* __restrict__ Ks, const float* __restrict__ Vs, int64_t L_cap,
-                            const void* __restrict__ Q, Plan plan, Geo geo, void* __restrict__ O,
-                            float* __restrict__ lse, uint32_t* __restrict__ err) {
+                            const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -647,27 +621,22 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   }
 
   const int q4 = lane & 3, r8 = lane >> 2;
+  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+  float o[NG][D / 16][4];
+  float m[NG][2], l[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
   int stage = 0;
   uint32_t phase = 0;
-  bool alive = true;
 #pragma unroll 1
-  while (alive && inflight > 0) {
-    // one work item; its accumulators live only inside this body
-    uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
-    float o[NG][D / 16][4];
-    float m[NG][2], l[NG][2];
-#pragma unroll 1
-    for (int tile = 0;; ++tile) {
+  while (inflight > 0) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
       if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
-      alive = false;
       break;
     }
     const int4 mt = meta[stage];
-    if (tile == 0) {
+    if (mt.w == 0) {
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
@@ -851,9 +820,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       stage = 0;
       phase ^= 1u;
     }
-    if (last) break;
-    }  // tiles of the item
-    if (!alive) break;
+    if (!last) continue;
 
     const int slot_idx = cur.grp * geo.umax + cur.u;
     const uint32_t hmask = tb.mask[slot_idx];
@@ -879,20 +846,96 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }
     }
-    // publish the partials; the span's last chunk merges it (and, through
-    // it, every head it completes)
-    __threadfence();
-    __syncwarp();
-    int done = 0;
-    if (lane == 0) done = atomicAdd(plan.span_done + slot_idx, 1);
-    done = __shfl_sync(0xffffffffu, done, 0);
-    const int nch = cur.u == tb.n_union[cur.grp] - 1 ? dplan::local_chunks(geo) : geo.C;
-    if (done == nch - 1) {
-      __threadfence();
-      dplan::tail_merge<DT, D, 2>(plan, geo, cur.grp, cur.u, nch, hmask, O, lse, lane);
-    }
   }
 }
+
+// ---------------------------------------------------------------- merge
+// One CTA per (b, q-head): its (topk + 1) * C partial slots, in (span rank,
+// chunk) order, split into 8 contiguous runs, one per warp; empty slots
+// (m = -inf) are skipped.  The warps' results are then combined in order.
+constexpr int kMergeWarps = 8;
+constexpr int kBatch = 8;
+
+template <int DT, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    decode_merge_kernel(Plan plan, Geo geo, void* __restrict__ O, float* __restrict__ lse) {
+  constexpr int E = D / 32;  // columns per lane
+  __shared__ float wm[kMergeWarps], wl[kMergeWarps];
+  __shared__ float wo[kMergeWarps][D];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int nslots = (geo.topk + 1) * geo.C;
+  const int per = (nslots + kMergeWarps - 1) / kMergeWarps;
+  const int s0 = warp * per, s1 = min(s0 + per, nslots);
+  const int64_t base = (int64_t)row * nslots;
+  const float2* ml = reinterpret_cast<const float2*>(plan.ml);
+  float M = -INFINITY, Ls = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int sb = s0; sb < s1; sb += 32) {
+    const int sl = sb + lane;
+    const float2 mlv = sl < s1 ? ml[base + sl] : make_float2(-INFINITY, 0.f);
+    uint32_t nz = __ballot_sync(0xffffffffu, mlv.x != -INFINITY);
+    while (nz) {
+      int ids[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        ids[i] = nz ? __ffs(nz) - 1 : -1;
+        nz &= nz ? nz - 1u : 0u;
+      }
+      float po[kBatch][E];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (ids[i] >= 0) {
+          const float* src = plan.po + (base + sb + ids[i]) * D + lane * E;
+          if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            po[i][0] = v.x; po[i][1] = v.y; po[i][2] = v.z; po[i][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            po[i][0] = v.x; po[i][1] = v.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (ids[i] < 0) continue;
+        const float pm = __shfl_sync(0xffffffffu, mlv.x, ids[i]);
+        const float pl = __shfl_sync(0xffffffffu, mlv.y, ids[i]);
+        const float Mn = fmaxf(M, pm);
+        const float a = exp2f(M - Mn), bb = exp2f(pm - Mn);
+        Ls = Ls * a + pl * bb;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + po[i][e] * bb;
+        M = Mn;
+      }
+    }
+  }
+  if (lane == 0) {
+    wm[warp] = M;
+    wl[warp] = Ls;
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) wo[warp][lane * E + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int col = threadIdx.x;
+    float Mt = -INFINITY;
+    for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, wm[w]);
+    float Lt = 0.f, ot = 0.f;
+    for (int w = 0; w < kMergeWarps; ++w) {
+      if (wm[w] == -INFINITY) continue;
+      const float f = exp2f(wm[w] - Mt);
+      Lt += wl[w] * f;
+      ot += wo[w][col] * f;
+    }
+    store_elem<DT>(O, (int64_t)row * D + col, ot / Lt);
+    if (lse && col == 0) lse[row] = Mt * kLn2 + logf(Lt);
+  }
+}
+
 
 // The plan's workspace pointers and the geometry of a decode step.
 void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
@@ -904,9 +947,6 @@ void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
   plan.mask = reinterpret_cast<uint32_t*>(w8 + lay.mask);
   plan.rank = w8 + lay.rank;
   plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
-  plan.n_used = reinterpret_cast<int*>(w8 + lay.n_used);
-  plan.span_done = reinterpret_cast<int*>(w8 + lay.span_done);
-  plan.head_done = reinterpret_cast<int*>(w8 + lay.head_done);
   plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
   plan.po = reinterpret_cast<float*>(w8 + lay.po);
   geo.Hq = pr.Hq;
@@ -935,8 +975,11 @@ cudaError_t attend_q8(const Problem& pr, const void* Q, const int8_t* Kq, const 
   static bool attr_done[2][kMaxDevices] = {};
   e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attend, dim3(device_sm_count()), dim3(q8::kThreads), q8::kFixed, st, tmK, Vq, Ks, Vs,
-                    pr.L_cap, Q, plan, geo, O, lse, err);
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(q8::kThreads), q8::kFixed, st, tmK, Vq, Ks, Vs, pr.L_cap, Q,
+                 plan, geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st, plan, geo, O,
+                    lse);
 }
 
 template <int DT, int D>
@@ -952,8 +995,10 @@ cudaError_t attend_16(const Problem& pr, const void* Q, const void* K, const voi
   static bool attr_done[2][kMaxDevices] = {};
   e = ensure_smem_attr(attend, kSmemLimit, attr_done[pr.g <= 8 ? 0 : 1]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), Cf::kFixed, st, tmK, tmV, Q, plan, geo, O,
-                    lse, err);
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(kThreads), Cf::kFixed, st, tmK, tmV, Q, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st, plan, geo, O,
+                    lse);
 }
 
 }  // namespace

@@ -14,12 +14,9 @@
 // writes one partial (m, l, o) per head of mask[u] into slot
 // [row][rank][c], row = b * Hq + head.
 //
-// Merge.  The last item to finish a span of U (a per-span arrival count)
-// combines that span's chunk partials in chunk order, per head, into the
-// chunk-0 slot; the last span to finish a head (a per-head count) combines
-// the head's span partials in rank order (ascending span, the local span
-// last) into O and lse.  No warp ever waits for another: whoever finishes
-// last does the work, so the merges need no barrier and cannot hang.
+// The attend kernel leaves one partial per (head, rank, chunk); a merge
+// kernel combines each head's partials in that order into O and lse, and
+// skips the slots no item wrote (m = -inf: the plan empties them).
 #pragma once
 
 #include "internal.h"
@@ -32,7 +29,6 @@ constexpr int kMaxG = 16;
 constexpr int kMaxK = 64;
 constexpr int kPlanWords = 512;
 constexpr int64_t kPlanBits = kPlanWords * 32;  // candidates the bitmap path covers
-constexpr float kLn2 = 0.6931471805599453f;
 
 struct Plan {
   int* n_union;       // [n_grp]   |U| including the local span
@@ -41,9 +37,6 @@ struct Plan {
   uint32_t* mask;     // [n_grp][umax] heads (bit r = head kvh*g + r) that attend the span
   uint8_t* rank;      // [n_grp][umax][16] position of the span in each head's sel row (topk = local)
   int* counter;       // work-item counter of the attend kernel
-  int* n_used;        // [B*Hq] used entries of each head's sel row
-  int* span_done;     // [n_grp][umax] chunks of each entry of U finished
-  int* head_done;     // [B*Hq] entries of U of each head merged
   float* ml;          // [B*Hq][topk+1][C][2]  (m, l) per partial, base-2 m
   float* po;          // [B*Hq][topk+1][C][D]  unnormalised partial outputs
 };
@@ -73,8 +66,10 @@ struct PlanSmem {
   int nu;
 };
 
-// Builds group grp's plan from s.sj / s.nv with all NW warps of the CTA and
-// resets the group's arrival counts (and, for group 0, the item counter).
+// Builds group grp's plan from s.sj / s.nv with all NW warps of the CTA,
+// empties the (m, l) slots of the group's partials (a slot that no item
+// writes keeps m = -inf and the merge skips it) and, for group 0, resets the
+// item counter.
 // The position of span j in U is the number of distinct selected spans below
 // j: up to kPlanBits candidates it is read off a bitmap of the selected spans
 // (a prefix popcount over its words); beyond that, from binary searches in
@@ -89,6 +84,11 @@ __device__ __forceinline__ void plan_build(int grp, PlanSmem& s, const Plan& pla
   const int row0 = b * geo.Hq + kvh * g;
   const uint32_t lt = (1u << lane) - 1u;
   if (grp == 0 && tid == 0) *plan.counter = 0;
+  {
+    const int nparts = g * (k + 1) * geo.C;
+    float2* ml = reinterpret_cast<float2*>(plan.ml) + (int64_t)row0 * (k + 1) * geo.C;
+    for (int x = tid; x < nparts; x += NT) ml[x] = make_float2(-INFINITY, 0.f);
+  }
   for (int x = tid; x < kMaxG * kMaxK + 1; x += NT) s.smask[x] = 0u;
   const bool bitmap = geo.ell <= kPlanBits;
   const int nw = bitmap ? (int)((geo.ell + 31) >> 5) : 0;
@@ -188,128 +188,12 @@ __device__ __forceinline__ void plan_build(int grp, PlanSmem& s, const Plan& pla
   __syncthreads();
   const int nu = s.nu;
   for (int p = tid; p < nu; p += NT) plan.mask[gbase + p] = s.smask[p];
-  for (int p = tid; p <= nu; p += NT) plan.span_done[gbase + p] = 0;
-  if (tid < g) {
-    plan.rank[(size_t)(gbase + nu) * 16 + tid] = (uint8_t)k;
-    plan.n_used[row0 + tid] = s.nv[tid];
-    plan.head_done[row0 + tid] = 0;
-  }
+  if (tid < g) plan.rank[(size_t)(gbase + nu) * 16 + tid] = (uint8_t)k;
   if (tid == 0) {
     plan.span[gbase + nu] = (int)geo.ell;
     plan.mask[gbase + nu] = (1u << g) - 1u;
     plan.n_union[grp] = nu + 1;
     plan.n_items[grp] = nu * geo.C + local_chunks(geo);
-  }
-}
-
-// ---------------------------------------------------------------- merges
-// Partials are written during the attend kernel by other SMs, so they are
-// read through L2 (ld.global.cg), never through a possibly stale L1 line.
-template <int D>
-__device__ __forceinline__ void load_part(const float* po, int64_t slot, int lane, float (&v)[D / 32]) {
-  const float* src = po + slot * D + lane * (D / 32);
-  if constexpr (D == 128) {
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-  } else {
-    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-    v[0] = x.x; v[1] = x.y;
-  }
-}
-
-// Folds partial slots slot_of(0 .. n) into (M, Ls, acc), in that order,
-// with up to NB slots' loads in flight at once.
-template <int D, int NB, typename F>
-__device__ __forceinline__ void fold_slots(const Plan& plan, F slot_of, int n, int lane, float& M, float& Ls,
-                                           float (&acc)[D / 32]) {
-  constexpr int E = D / 32;
-  constexpr int kMergeBatch = NB;
-  const float2* ml = reinterpret_cast<const float2*>(plan.ml);
-  for (int s0 = 0; s0 < n; s0 += kMergeBatch) {
-    float2 mv[kMergeBatch];
-    float ov[kMergeBatch][E];
-#pragma unroll
-    for (int i = 0; i < kMergeBatch; ++i) {
-      if (s0 + i < n) {
-        const int64_t sl = slot_of(s0 + i);
-        mv[i] = __ldcg(ml + sl);
-        load_part<D>(plan.po, sl, lane, ov[i]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kMergeBatch; ++i) {
-      if (s0 + i >= n || mv[i].x == -INFINITY) continue;
-      const float Mn = fmaxf(M, mv[i].x);
-      const float a = exp2f(M - Mn), bb = exp2f(mv[i].x - Mn);
-      Ls = Ls * a + mv[i].y * bb;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + ov[i][e] * bb;
-      M = Mn;
-    }
-  }
-}
-
-// Called by the warp whose item was the last of entry u of group grp's U
-// (after a fence that made the other items' partials visible): merges the
-// entry's chunks per head, then counts the entry for each of its heads and
-// merges every head whose last entry this was into O and lse.  NB partials'
-// loads are in flight at once.  It is a call, not inlined: it runs once per
-// span, and inlined into the attend loop its registers would crowd the
-// loop's.
-template <int DT, int D, int NB>
-__device__ __noinline__ void tail_merge(const Plan& plan, const Geo& geo, int grp, int u, int nch, uint32_t hmask,
-                                        void* __restrict__ O, float* __restrict__ lse, int lane) {
-  constexpr int E = D / 32;
-  const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
-  const int row0 = b * geo.Hq + kvh * geo.g;
-  const int slot_idx = grp * geo.umax + u;
-  const int kp1 = geo.topk + 1;
-  float2* ml = reinterpret_cast<float2*>(plan.ml);
-  if (nch > 1) {
-    for (uint32_t hm = hmask; hm; hm &= hm - 1u) {
-      const int r = __ffs(hm) - 1;
-      const int rk = plan.rank[(size_t)slot_idx * 16 + r];
-      const int64_t base = ((int64_t)(row0 + r) * kp1 + rk) * geo.C;
-      float M = -INFINITY, Ls = 0.f, acc[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = 0.f;
-      fold_slots<D, NB>(plan, [&](int c) { return base + c; }, nch, lane, M, Ls, acc);
-      float* dst = plan.po + base * D + lane * E;
-      if constexpr (E == 4) {
-        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
-      }
-      if (lane == 0) ml[base] = make_float2(M, Ls);
-    }
-    __threadfence();
-    __syncwarp();
-  }
-  // count the entry for its heads; the heads it completes are merged here
-  bool fin = false;
-  if (lane < geo.g && ((hmask >> lane) & 1u)) {
-    const int row = row0 + lane;
-    const int old = atomicAdd(plan.head_done + row, 1);
-    fin = old == __ldg(plan.n_used + row);  // entries per head: used spans + the local span
-  }
-  const uint32_t fm = __ballot_sync(0xffffffffu, fin);
-  if (!fm) return;
-  __threadfence();
-  for (uint32_t m2 = fm; m2; m2 &= m2 - 1u) {
-    const int r = __ffs(m2) - 1;
-    const int64_t row = row0 + r;
-    const int used = __ldg(plan.n_used + row);
-    const int topk = geo.topk, C = geo.C;
-    float M = -INFINITY, Ls = 0.f, acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    // the head's used spans in rank order (ascending span), then the local span
-    fold_slots<D, NB>(plan, [&](int i) { return (row * kp1 + (i < used ? i : topk)) * C; }, used + 1, lane, M, Ls,
-                  acc);
-    const float inv = 1.f / Ls;
-#pragma unroll
-    for (int e = 0; e < E; ++e) store_elem<DT>(O, row * D + lane * E + e, acc[e] * inv);
-    if (lse && lane == 0) lse[row] = M * kLn2 + logf(Ls);
   }
 }
 
@@ -319,8 +203,8 @@ __device__ __noinline__ void tail_merge(const Plan& plan, const Geo& geo, int gr
 namespace ssa {
 
 // decode.cu: the plan pointers and geometry of a decode step at `pos` in the
-// decode workspace ws, and the attend launch of a step whose plan an earlier
-// kernel on the stream has built (O and lse written by its tail merges).
+// decode workspace ws, and the attend + merge launches of a step whose plan
+// an earlier kernel on the stream has built.
 void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo);
 cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,
                                          float* lse, const dplan::Plan& plan, const dplan::Geo& geo,

@@ -15,6 +15,8 @@
 //
 // The work itself is ssa_attend_decode unchanged: this file only finds the
 // block, prepares it once per device and passes it as the workspace.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -28,29 +30,51 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[SSA_NOALLOC_SCRATCH_BYTES];
 
 struct DeviceScratch {
-  void* addr = nullptr;  // device address of g_decode_scratch on this device
-  bool ready = false;    // address looked up and header cleared
+  CUcontext ctx = nullptr;  // context the address below belongs to
+  void* addr = nullptr;     // device address of g_decode_scratch in that context
 };
 
 std::mutex g_setup_mutex;
 DeviceScratch g_scratch[ssa::kMaxDevices];
 
-// Looks up the block of the current device and clears its header (the error
-// record must start at zero; the plan kernel resets everything else it
-// reads).  Done once per device; the clear is ordered on `st` before this
-// call's kernels.
+// The driver's cuCtxGetCurrent, through the runtime's entry-point query (the
+// library links no driver library of its own).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }
+  return fn;
+}
+
+// Looks up the block in the current device's current context (every call)
+// and clears its header once per context (the error record must start at
+// zero; the plan kernel resets everything else it reads): after
+// cudaDeviceReset the device has a new context, whose block may sit
+// elsewhere, and the clear runs again.  The clear is ordered on `st` before
+// this call's kernels.
 int setup_current_device(cudaStream_t st, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return SSA_ERR_CUDA;
   if (dev < 0 || dev >= ssa::kMaxDevices) return SSA_ERR_UNSUPPORTED;
+  // the lookup also makes the device's (primary) context current if no call
+  // has yet; it is a host-side table lookup and allocates nothing
+  void* p = nullptr;
+  if (cudaGetSymbolAddress((void**)&p, g_decode_scratch) != cudaSuccess || p == nullptr) return SSA_ERR_CUDA;
+  auto get_ctx = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SSA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceScratch& s = g_scratch[dev];
-  if (!s.ready) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress((void**)&p, g_decode_scratch) != cudaSuccess || p == nullptr) return SSA_ERR_CUDA;
+  if (s.ctx != ctx || s.addr != p) {
     if (cudaMemsetAsync(p, 0, ssa::kWsHeader, st) != cudaSuccess) return SSA_ERR_CUDA;
     s.addr = p;
-    s.ready = true;
+    s.ctx = ctx;
   }
   *out = s.addr;
   return SSA_OK;

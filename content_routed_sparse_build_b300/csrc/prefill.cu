@@ -148,8 +148,12 @@ __global__ void __launch_bounds__(256) prefill_count_kernel(const int32_t* __res
 }
 
 // ---------------------------------------------------------------- scan
-// One CTA of 1024 threads: exclusive scan of the bucket counts, the span
-// tiles, then the local tiles (queries of one local span, 128 / g at a time).
+// One CTA of 1024 threads: exclusive scan of the bucket counts, then the
+// table of tile pairs.  A pair is two tiles of 128 rows that share one key
+// range: rows [256 p, 256 p + 128) and [256 p + 128, 256 p + 256) of a
+// bucket (entry {bucket, 256 p, rows of tile A, rows of tile B}), then, per
+// local span, 2 * 128 / g consecutive queries (entry {-1 - bh, first query,
+// queries of tile A, queries of tile B}).  Tile B may be empty.
 constexpr int kScanThreads = 1024;
 
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tmp, int64_t* total) {
@@ -188,15 +192,17 @@ __global__ void __launch_bounds__(kScanThreads) prefill_scan_kernel(PrefArgs a) 
   for (int64_t base = 0; base < a.n_buckets; base += kScanThreads) {
     const int64_t bk = base + threadIdx.x;
     const int c = bk < a.n_buckets ? a.counts[bk] : 0;
-    const int nt = (c + kTileRows - 1) / kTileRows;
+    const int nt = (c + 2 * kTileRows - 1) / (2 * kTileRows);
     int64_t tot_e, tot_t;
     const int64_t pe = block_exclusive_scan(c, tmp, &tot_e) + carry_e;
     const int64_t pt = block_exclusive_scan(nt, tmp, &tot_t) + carry_t;
     if (bk < a.n_buckets) {
       a.offsets[bk] = (int)pe;
       a.cursors[bk] = (int)pe;
-      for (int t = 0; t < nt; ++t)
-        a.tiles[pt + t] = make_int4((int)bk, t * kTileRows, min(kTileRows, c - t * kTileRows), 0);
+      for (int t = 0; t < nt; ++t) {
+        const int r0 = 2 * t * kTileRows;
+        a.tiles[pt + t] = make_int4((int)bk, r0, min(kTileRows, c - r0), max(0, min(kTileRows, c - r0 - kTileRows)));
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -219,13 +225,16 @@ __global__ void __launch_bounds__(kScanThreads) prefill_scan_kernel(PrefArgs a) 
       qa = pa - a.q_pos0;
       qn = pb - pa;
     }
-    const int64_t nt = qn > 0 ? (qn + mq - 1) / mq : 0;
+    const int64_t nt = qn > 0 ? (qn + 2 * mq - 1) / (2 * mq) : 0;
     int64_t tot;
     const int64_t pt = block_exclusive_scan(nt, tmp, &tot) + carry_t;
     if (e < bh_n * nspan) {
       const int bh = (int)(e / nspan);
-      for (int64_t t = 0; t < nt; ++t)
-        a.tiles[pt + t] = make_int4(-1 - bh, (int)(qa + t * mq), (int)min(mq, qn - t * mq), 0);
+      for (int64_t t = 0; t < nt; ++t) {
+        const int64_t q0 = t * 2 * mq;
+        a.tiles[pt + t] = make_int4(-1 - bh, (int)(qa + q0), (int)min(mq, qn - q0),
+                                    (int)max((int64_t)0, min(mq, qn - q0 - mq)));
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) carry_t += tot;
@@ -279,52 +288,46 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 // ---------------------------------------------------------------- attend
 template <int D>
 struct ACfg {
-  static constexpr int kRegion = kTileRows * 128;      // 128 rows x 128 bytes
-  static constexpr int kQBytes = (D / 64) * kRegion;    // Q tile, D/64 regions
-  static constexpr int kKVBytes = (D / 64) * kRegion;   // one K (or V) block of 128 tokens
-  // two stages each: a K slot is free once S of its block is done (s_full),
-  // a V slot once O += P V of its block is done (p_free); with two stages
-  // those barriers can never run two phases ahead of the producer's wait
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
-  // small state first (barriers, pair exchange, tile metadata), then the
-  // 1024-byte aligned operand buffers: Q[2], K[kKStages], V[kVStages]
-  static constexpr int kBarBytes = 256;
-  static constexpr int kXchgBytes = 2 * 2 * kTileRows * 4;
-  static constexpr int kMetaBytes = 2 * 16 + 2 * kTileRows * 4;
-  static constexpr int kSlotBytes = 2 * kTileRows * 8;  // pending tile: partial slot per softmax thread
-  static constexpr int kSmallBytes = ((kBarBytes + kXchgBytes + kMetaBytes + kSlotBytes + 1023) / 1024) * 1024;
-  static constexpr size_t kSmem =
-      1024 + kSmallBytes + 2 * (size_t)kQBytes + (size_t)(kKStages + kVStages) * kKVBytes;
-  // tensor memory: S0 [0, 128), S1 [128, 256) (P of a block is written over
-  // the S columns it came from), then the two key-half accumulators
-  // O0 [256, 256 + D) and O1 [256 + D, 256 + 2 D)
+  static constexpr int kRegion = kTileRows * 128;       // 128 rows x 128 bytes
+  static constexpr int kQTile = (D / 64) * kRegion;      // one 128-row Q tile
+  static constexpr int kQBuf = 2 * kQTile;               // the Q of a pair (tiles A and B)
+  static constexpr int kKV = (D / 64) * kRegion;         // one K or V block of 128 tokens
+  // one ring for both: K(0), V(0), K(1), V(1), ...  A K slot is free once
+  // both tiles' S of its block are done, a V slot once both P V are.
+  static constexpr int kSlots = 3;
+  static constexpr size_t kOperands = 2 * (size_t)kQBuf + (size_t)kSlots * kKV;
+  static constexpr int kSmallBytes = 512;                // barriers and the two pair entries
+  static constexpr size_t kSmem = 1024 + kOperands + kSmallBytes;
+  // tensor memory: S_A [0, 128), S_B [128, 256) (the P of a block is written
+  // over the S columns it came from), O_A [256, 256 + D), O_B [256 + D, 256 + 2 D)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;
 };
 
-constexpr int kSoftWarps = 8;      // two warps per tensor-memory lane quarter
-constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1, kQWarp = kSoftWarps + 2;
-constexpr int kAttThreads = (kSoftWarps + 3) * 32;
+constexpr int kSoftWarps = 8;      // warps 0-3: tile A, 4-7: tile B (one lane quarter each)
+constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1, kQWarp = kSoftWarps + 2;  // Q loaders: 10, 11
+constexpr int kAttThreads = (kSoftWarps + 4) * 32;
 
-struct Tile {
-  int kind_bh;  // bucket (>= 0) or -1 - bh
-  int row0, nrows;
+struct Pair {
+  int kind_bh;          // bucket (>= 0) or -1 - bh
   int bh;
+  int row0;             // span pairs: bucket row of tile A's first row (tile B: 128 rows on)
+  int n[2];             // rows of tiles A and B (0: no tile B)
+  int64_t i0;           // local pairs: tile A's first query (tile B: 128 / g queries on)
   int64_t key0, key_end;  // keys [key0, key_end)
   int nkb;
-  int64_t i0;              // local tiles: first query index
 };
 
-__device__ __forceinline__ Tile decode_tile(const PrefArgs& a, int4 v) {
-  Tile x;
+__device__ __forceinline__ Pair decode_pair(const PrefArgs& a, int4 v) {
+  Pair x;
   x.kind_bh = v.x;
   if (v.x >= 0) {
     const int64_t bk = v.x;
     x.bh = (int)(bk / a.ns_cap);
     const int64_t j = bk - (int64_t)x.bh * a.ns_cap;
     x.row0 = v.y;
-    x.nrows = v.z;
+    x.n[0] = v.z;
+    x.n[1] = v.w;
     x.key0 = j * a.S;
     x.key_end = x.key0 + a.S;
     x.i0 = 0;
@@ -332,36 +335,57 @@ __device__ __forceinline__ Tile decode_tile(const PrefArgs& a, int4 v) {
     x.bh = -1 - v.x;
     x.i0 = v.y;
     x.row0 = 0;
-    x.nrows = v.z * a.g;
+    x.n[0] = v.z * a.g;
+    x.n[1] = v.w * a.g;
     const int64_t t0 = a.q_pos0 + v.y;
     x.key0 = (t0 / a.S) * a.S;
-    x.key_end = t0 + v.z;  // up to the last query's own position
+    const int64_t mq = kTileRows / a.g;
+    const int64_t last = v.w > 0 ? v.y + mq + v.w - 1 : v.y + v.z - 1;  // last query of the pair
+    x.key_end = a.q_pos0 + last + 1;
   }
   x.nkb = (int)((x.key_end - x.key0 + kKeyBlk - 1) / kKeyBlk);
   return x;
 }
 
-// Row r of a local tile: query i0 + r / g of head kvh * g + r % g.
-__device__ __forceinline__ int64_t local_row(const PrefArgs& a, const Tile& x, int r, int64_t* i_out) {
+// Row r of tile t (0 = A, 1 = B) of a pair: its row of Q / sel / partials
+// (-1 when the tile has no such row), its rank in the row's sel (topk for the
+// local span) and, for local pairs, its query position.
+__device__ __forceinline__ int64_t pair_row(const PrefArgs& a, const Pair& x, int t, int r, int* rank,
+                                            int64_t* tpos, uint32_t* err) {
+  *rank = a.topk;
+  *tpos = x.key_end - 1;
+  if (r >= x.n[t]) return -1;
+  if (x.kind_bh >= 0) {
+    const int e = a.rows[(int64_t)a.offsets[x.kind_bh] + x.row0 + t * kTileRows + r];
+    const int64_t row = (int64_t)(e >> 6);
+    if (e < 0 || row >= (int64_t)a.B * a.Hq * a.n_q || (e & 63) >= a.topk) {
+      flag_error(err, SSA_DEVERR_OVERFLOW);
+      return -1;
+    }
+    *rank = e & 63;
+    return row;
+  }
   const int b = x.bh / a.Hkv, kvh = x.bh - b * a.Hkv;
-  const int64_t i = x.i0 + r / a.g;
+  const int64_t i = x.i0 + (int64_t)t * (kTileRows / a.g) + r / a.g;
   const int h = kvh * a.g + r % a.g;
-  *i_out = i;
+  *tpos = a.q_pos0 + i;
   return (int64_t)(b * a.Hq + h) * a.n_q + i;
 }
 
-// Warp roles: 0-7 softmax (warps w and w + 4 share the tensor-memory lanes
-// of quarter w % 4 and split the key / output columns), 8 TMA producer of
-// the K / V blocks, 9 MMA issuer, 10 Q loader.
+// Warp roles: 0-3 softmax of tile A and 4-7 of tile B (warp w owns tensor-
+// memory lanes 32 (w % 4) .. + 31: one row per thread), 8 TMA producer of the
+// K / V blocks, 9 MMA issuer, 10 and 11 Q loaders of tiles A and B.
 //
-// Block g (a global count of key blocks over this CTA's tiles):
-//   S(g) = Q K(g)^T       -> tensor memory S[g % 2]
-//   P(g) = 2^(S c - m)    -> tensor memory P[g % 2] (16-bit, written by the softmax warps)
-//   O   += P(g) V(g)      A operand read from tensor memory
-// The softmax of block g waits only for O += P(g - 2) V (its P buffer), or
-// for O += P(g - 1) V when it must rescale O.  The Q loader fills the other
-// Q buffer while a tile runs, so the next tile's first S can start while
-// the softmax warps write the previous tile's partials.
+// Both tiles of a pair stream the same key blocks.  Per block b the MMA
+// thread issues, in this order,
+//   O_A += P_A(b-1) V(b-1),  S_A(b) = Q_A K(b)^T,  O_B += P_B(b-1) V(b-1),  S_B(b) = Q_B K(b)^T
+// (one S buffer per tile: S_X(b) overwrites P_X(b-1), which the tensor pipe
+// has read by then because it runs one thread's MMAs in order).  While one
+// tile's warps turn S into P = 2^(S c - m) (16-bit, written over S), the
+// tensor pipe works on the other tile.  O_X is rescaled only when the
+// running maximum grows by more than 2^8.  A tile's epilogue (one partial
+// (m, l, normalised o) per row) runs after the next pair's first P is out,
+// so that waiting for its last P V overlaps that softmax.
 template <int DT, int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
     prefill_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -370,38 +394,36 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(base);
-  uint64_t* q_full = bar + 0;    // [2] Q tile and its metadata loaded
-  uint64_t* q_empty = bar + 2;   // [2] last S of the tile done + partials written
-  uint64_t* k_full = bar + 4;    // [2]
-  uint64_t* v_full = bar + 6;    // [2]
-  uint64_t* s_full = bar + 8;    // [2] S of the buffer's last block done (its K slot is free)
-  uint64_t* p_full = bar + 10;   // [2 buffers][2 halves]
-  uint64_t* p_free = bar + 14;   // [2] O += P V of the buffer's last block done (its V slot is free)
-  uint64_t* o_free = bar + 24;   // O read out by the epilogue
-  uint64_t* drain = bar + 25;    // every MMA issued has completed
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 26);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 27);
-  float* xchg = reinterpret_cast<float*>(base + C::kBarBytes);   // [2 halves][m, l][128 rows]
-  int4* tinfo = reinterpret_cast<int4*>(base + C::kBarBytes + C::kXchgBytes);  // [2] tile entries
-  int* meta = reinterpret_cast<int*>(tinfo + 2);                  // [2][128] bucket entries or -1
-  int64_t* pslot = reinterpret_cast<int64_t*>(meta + 2 * kTileRows);  // [256] pending partial slot or -1
-  uint8_t* sQ = base + C::kSmallBytes;
-  uint8_t* sK = sQ + 2 * C::kQBytes;
-  uint8_t* sV = sK + C::kKStages * C::kKVBytes;
+  uint8_t* sQ = base;                                // [2 buffers][2 tiles]
+  uint8_t* sKV = sQ + 2 * C::kQBuf;                  // [kSlots]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + C::kSlots * C::kKV);
+  uint64_t* q_full = bar + 0;     // [2] Q of a pair and its entry loaded
+  uint64_t* q_empty = bar + 2;    // [2] last S of the pair done + every softmax warp read the entry
+  uint64_t* kv_full = bar + 4;    // [3]
+  uint64_t* kv_empty = bar + 7;   // [3]
+  uint64_t* s_full = bar + 10;    // [2 tiles] S of the tile's block done
+  uint64_t* p_full = bar + 12;    // [2 tiles] P of the tile's block written (4 warps)
+  uint64_t* pv_done = bar + 14;   // [2 tiles] O += P V of the tile's block done
+  uint64_t* o_free = bar + 16;    // [2 tiles] O read out by the tile's epilogue (4 warps)
+  uint64_t* drain = bar + 18;     // every MMA issued has completed
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 19);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 20);
+  int4* tinfo = reinterpret_cast<int4*>(bar + 22);  // [2] pair entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&q_full[s], 1);
+      ptx::mbar_init(&q_full[s], 2);
       ptx::mbar_init(&q_empty[s], 1 + kSoftWarps);
-      ptx::mbar_init(&k_full[s], 1);
-      ptx::mbar_init(&v_full[s], 1);
       ptx::mbar_init(&s_full[s], 1);
-      ptx::mbar_init(&p_free[s], 1);
-      for (int h = 0; h < 2; ++h) ptx::mbar_init(&p_full[2 * s + h], kSoftWarps / 2);
+      ptx::mbar_init(&p_full[s], kSoftWarps / 2);
+      ptx::mbar_init(&pv_done[s], 1);
+      ptx::mbar_init(&o_free[s], kSoftWarps / 2);
     }
-    ptx::mbar_init(o_free, kSoftWarps);
+    for (int s = 0; s < C::kSlots; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
     ptx::mbar_init(drain, 1);
     *abort = 0;
     ptx::fence_mbar_init();
@@ -417,7 +439,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   const uint32_t tmem = *tmem_base;
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
-  const int ntiles = a.ntiles[0];
+  const int npairs = a.ntiles[0];
 
   auto fail = [&](uint32_t bit) {
     flag_error(err, bit);
@@ -426,103 +448,95 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------ K / V producer
-    // Loads in the order the MMAs consume them: K(g), then V(g - 1).
+    // Ring use u: K(b) for u = 2 b, V(b) for u = 2 b + 1, in slot u % 3.
     if (lane == 0) {
-      int64_t g = 0;
-      int prev_bh = 0, prev_y = 0;
-      bool have_prev = false, ok = true;
-      auto load_v = [&](int64_t gv, int bh, int y) -> bool {
-        const int st = (int)(gv % C::kVStages);
-        if (gv >= 2 && !ptx::mbar_wait(&p_free[(gv - 2) & 1], (uint32_t)(((gv - 2) >> 1) & 1))) return false;
-        ptx::mbar_arrive_expect_tx(&v_full[st], C::kKVBytes);
-#pragma unroll
-        for (int r = 0; r < D / 64; ++r)
-          ptx::tma_load_3d(sV + st * C::kKVBytes + r * C::kRegion, &tmV, &v_full[st], r * 64, y, bh);
-        return true;
-      };
-      for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x) {
-        const Tile x = decode_tile(a, a.tiles[t]);
-        for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
-          const int st = (int)(g % C::kKStages);
-          if (g >= 2 && !ptx::mbar_wait(&s_full[(g - 2) & 1], (uint32_t)(((g - 2) >> 1) & 1))) {
-            ok = false;
-            break;
-          }
+      int64_t u = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < npairs && ok && !*abort; t += gridDim.x) {
+        const Pair x = decode_pair(a, a.tiles[t]);
+        for (int kb = 0; kb < x.nkb && ok; ++kb) {
           const int y = (int)(x.key0 + (int64_t)kb * kKeyBlk);
-          ptx::mbar_arrive_expect_tx(&k_full[st], C::kKVBytes);
+#pragma unroll 1
+          for (int part = 0; part < 2; ++part, ++u) {
+            const int sl = (int)(u % C::kSlots);
+            if (u >= C::kSlots && !ptx::mbar_wait(&kv_empty[sl], (uint32_t)(((u - C::kSlots) / C::kSlots) & 1))) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&kv_full[sl], C::kKV);
 #pragma unroll
-          for (int r = 0; r < D / 64; ++r)
-            ptx::tma_load_3d(sK + st * C::kKVBytes + r * C::kRegion, &tmK, &k_full[st], r * 64, y, x.bh);
-          if (have_prev && !load_v(g - 1, prev_bh, prev_y)) {
-            ok = false;
-            break;
+            for (int r = 0; r < D / 64; ++r)
+              ptx::tma_load_3d(sKV + sl * C::kKV + r * C::kRegion, part == 0 ? &tmK : &tmV, &kv_full[sl], r * 64, y,
+                               x.bh);
           }
-          prev_bh = x.bh;
-          prev_y = y;
-          have_prev = true;
         }
       }
-      if (ok && have_prev) ok = load_v(g - 1, prev_bh, prev_y);
       if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
       // let every load this thread issued land before the CTA can exit
-      const int64_t nk = g, nv = have_prev ? g : 0;
-      for (int s = 0; s < C::kKStages; ++s) {
-        if (nk <= s) break;
-        const int64_t last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
-        if (!ptx::mbar_wait(&k_full[s], (uint32_t)((last / C::kKStages) & 1))) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
-      }
-      for (int s = 0; s < C::kVStages; ++s) {
-        if (nv <= s) break;
-        const int64_t last = s + ((nv - 1 - s) / C::kVStages) * C::kVStages;
-        if (!ptx::mbar_wait(&v_full[s], (uint32_t)((last / C::kVStages) & 1))) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
-      }
+      for (int64_t v = u - C::kSlots < 0 ? 0 : u - C::kSlots; v < u; ++v)
+        if (!ptx::mbar_wait(&kv_full[v % C::kSlots], (uint32_t)((v / C::kSlots) & 1)))
+          flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
     }
-  } else if (warp == kQWarp) {
-    // ------------------------------------------------ Q loader
-    // Gathers the tile's 128 query rows into the swizzled K-major Q buffer
-    // and publishes the tile entry and the rows' bucket entries.
-    int tcount = 0;
-    for (int t = blockIdx.x; t < ntiles && !*abort; t += gridDim.x, ++tcount) {
-      const int qb = tcount & 1;
-      if (tcount >= 2 && !ptx::mbar_wait(&q_empty[qb], (uint32_t)(((tcount - 2) >> 1) & 1))) {
+  } else if (warp >= kQWarp) {
+    // ------------------------------------------------ Q loaders
+    // Warp kQWarp + t gathers the 128 query rows of tile t of the pair into
+    // the swizzled K-major Q buffer; the tile-A warp publishes the pair
+    // entry.  Each lane's four row entries are loaded together first, so a
+    // tile costs two memory round trips before its copies start.
+    const int tt = warp - kQWarp;
+    int pc = 0;
+    for (int t = blockIdx.x; t < npairs && !*abort; t += gridDim.x, ++pc) {
+      const int qb = pc & 1;
+      if (pc >= 2 && !ptx::mbar_wait(&q_empty[qb], (uint32_t)(((pc - 2) >> 1) & 1))) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
       const int4 v = a.tiles[t];
-      const Tile x = decode_tile(a, v);
-      if (lane == 0) tinfo[qb] = v;
-      const int64_t off0 = x.kind_bh >= 0 ? (int64_t)a.offsets[x.kind_bh] + x.row0 : 0;
-      uint8_t* q = sQ + qb * C::kQBytes;
-#pragma unroll 1
-      for (int rr = 0; rr < kTileRows / 32; ++rr) {
-        const int r = rr * 32 + lane;
-        int64_t qrow = -1;
-        int entry = -1;
-        if (r < x.nrows) {
-          if (x.kind_bh >= 0) {
-            const int e = a.rows[off0 + r];
-            const int64_t row = (int64_t)(e >> 6);
-            if (e < 0 || row >= (int64_t)a.B * a.Hq * a.n_q || (e & 63) >= a.topk) {
+      const Pair x = decode_pair(a, v);
+      if (tt == 0 && lane == 0) tinfo[qb] = v;
+      int64_t qrow[kTileRows / 32];
+      if (x.kind_bh >= 0) {
+        const int64_t off = (int64_t)__ldg(a.offsets + x.kind_bh) + x.row0 + tt * kTileRows;
+        int e[kTileRows / 32];
+#pragma unroll
+        for (int i = 0; i < kTileRows / 32; ++i) {
+          const int r = i * 32 + lane;
+          e[i] = r < x.n[tt] ? __ldg(a.rows + off + r) : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < kTileRows / 32; ++i) {
+          const int64_t row = (int64_t)(e[i] >> 6);
+          qrow[i] = -1;
+          if (i * 32 + lane < x.n[tt]) {
+            if (e[i] < 0 || row >= (int64_t)a.B * a.Hq * a.n_q || (e[i] & 63) >= a.topk)
               flag_error(err, SSA_DEVERR_OVERFLOW);
-            } else {
-              qrow = row;
-              entry = e;
-            }
-          } else {
-            int64_t i;
-            qrow = local_row(a, x, r, &i);
+            else
+              qrow[i] = row;
           }
         }
-        meta[qb * kTileRows + r] = entry;
-        const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow < 0 ? 0 : qrow) * (int64_t)D * 2;
-        const uint32_t n = qrow < 0 ? 0u : 16u;
-        const uint32_t rsw = (uint32_t)(r & 7);
+      } else {
 #pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) {
-          uint8_t* dst = q + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ rsw) << 4);
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
-                       "l"(src + ch * 16), "r"(n)
-                       : "memory");
+        for (int i = 0; i < kTileRows / 32; ++i) {
+          int rank;
+          int64_t tpos;
+          qrow[i] = pair_row(a, x, tt, i * 32 + lane, &rank, &tpos, err);
+        }
+      }
+      if (x.n[tt] > 0) {
+        uint8_t* qt = sQ + qb * C::kQBuf + tt * C::kQTile;
+#pragma unroll
+        for (int i = 0; i < kTileRows / 32; ++i) {
+          const int r = i * 32 + lane;
+          const uint8_t* src = static_cast<const uint8_t*>(Q) + (qrow[i] < 0 ? 0 : qrow[i]) * (int64_t)D * 2;
+          const uint32_t n = qrow[i] < 0 ? 0u : 16u;
+          const uint32_t rsw = (uint32_t)(r & 7);
+#pragma unroll
+          for (int ch = 0; ch < D / 8; ++ch) {
+            uint8_t* dst = qt + (ch >> 3) * C::kRegion + r * 128 + ((((uint32_t)ch & 7) ^ rsw) << 4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst)),
+                         "l"(src + ch * 16), "r"(n)
+                         : "memory");
+          }
         }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -537,70 +551,94 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const int ab16 = DT == DT_BF16 ? 1 : 0;
       const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
       const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
-      const uint32_t aQ0 = ptx::smem_u32(sQ), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
-      int64_t g = 0;
-      int64_t pend = -1;        // block whose O += P V is still to be issued
-      bool pend_first = false;  // ... first block of its tile (overwrites O)
-      int pend_tile = 0;
-      // O_h += P_h V_h for the two key halves h of block gg: P_h sits in
-      // tensor memory over the S columns of its half, V_h is rows
-      // [64 h, 64 h + 64) of the block's V tile.
-      auto issue_pv = [&](int64_t gg, bool first, int tc_) -> bool {
-        if (first && tc_ > 0 && !ptx::mbar_wait(o_free, (uint32_t)((tc_ - 1) & 1))) return false;
-        const int pb = (int)(gg & 1), sv = (int)(gg % C::kVStages);
-        const uint32_t par = (uint32_t)((gg >> 1) & 1);
-        if (!ptx::mbar_wait(&v_full[sv], (uint32_t)((gg / C::kVStages) & 1))) return false;
-        const uint32_t vbase = aV + sv * C::kKVBytes;
+      const uint32_t aQ0 = ptx::smem_u32(sQ), aKV = ptx::smem_u32(sKV);
+      int64_t u = 0;                   // ring uses consumed
+      int64_t npx[2] = {0, 0};         // pairs with tile X so far (o_free phases)
+      // the previous block, whose P V follow this block's S
+      bool pend = false, pend_b = false, pend_first = false;
+      int pend_slot = 0;
+      uint32_t pend_par = 0;
+      int64_t pend_g[2] = {0, 0};      // block counts of the tiles at the previous block
+      int64_t pend_np[2] = {0, 0};     // ... and their pair counts
+      int64_t g[2] = {0, 0};           // blocks of tile X issued
+      auto issue_pv = [&](int tx) -> bool {
+        // O_X += P_X V: P_X sits in tensor memory over S_X, V is the block in
+        // pend_slot.  The first block of a pair overwrites O_X, which the
+        // tile's previous epilogue must have read out.
+        if (pend_first && pend_np[tx] > 1 && !ptx::mbar_wait(&o_free[tx], (uint32_t)((pend_np[tx] - 2) & 1)))
+          return false;
+        if (!ptx::mbar_wait(&kv_full[pend_slot], pend_par)) return false;
+        if (!ptx::mbar_wait(&p_full[tx], (uint32_t)(pend_g[tx] & 1))) return false;
+        tc::fence_after();
+        const uint32_t tP = tmem + tx * 128;
+        const uint32_t tO = tmem + C::kColO + tx * D;
+        const uint32_t vbase = aKV + pend_slot * C::kKV;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!ptx::mbar_wait(&p_full[2 * pb + h], par)) return false;
-          tc::fence_after();
-          const uint32_t tP = tmem + pb * 128 + h * 64;
-          const uint32_t tOh = tmem + C::kColO + h * D;
-#pragma unroll
-          for (int k = 0; k < kKeyBlk / 32; ++k) {
-            const uint64_t vd = tc::sdesc_sw128(vbase + (h * (kKeyBlk / 32) + k) * 2048, C::kRegion, 1024);
-            tc::mma_ts(tOh, tP + k * 8, vd, id_pv, (first && k == 0) ? 0u : 1u);
-          }
+        for (int k = 0; k < kKeyBlk / 16; ++k) {
+          const uint64_t vd = tc::sdesc_sw128(vbase + k * 2048, C::kRegion, 1024);
+          tc::mma_ts(tO, tP + k * 8, vd, id_pv, (pend_first && k == 0) ? 0u : 1u);
         }
-        tc::commit(&p_free[pb]);
+        tc::commit(&pv_done[tx]);
         return true;
       };
+      auto issue_s = [&](int tx, uint32_t aQ, int ks) {
+        const uint32_t kbase = aKV + ks * C::kKV;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
+          const uint64_t kd = tc::sdesc_sw128(kbase + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
+          tc::mma(tmem + tx * 128, qd, kd, id_qk, k > 0 ? 1u : 0u);
+        }
+        tc::commit(&s_full[tx]);
+      };
       bool ok = true;
-      int tcount = 0;
-      for (int t = blockIdx.x; t < ntiles && ok && !*abort; t += gridDim.x, ++tcount) {
-        const int qb = tcount & 1;
-        if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((tcount >> 1) & 1))) {
+      int pc = 0;
+      for (int t = blockIdx.x; t < npairs && ok && !*abort; t += gridDim.x, ++pc) {
+        const int qb = pc & 1;
+        if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((pc >> 1) & 1))) {
           ok = false;
           break;
         }
         tc::fence_after();
-        const Tile x = decode_tile(a, tinfo[qb]);
-        const uint32_t aQ = aQ0 + qb * C::kQBytes;
-        for (int kb = 0; kb < x.nkb && ok; ++kb, ++g) {
-          const int sb = (int)(g & 1);
-          const int sk = (int)(g % C::kKStages);
-          // S(g) overwrites S[g % 2], which holds P(g - 2): its O += P V was
-          // issued before, and the tensor pipe runs this thread's MMAs in order
-          ok = ptx::mbar_wait(&k_full[sk], (uint32_t)((g / C::kKStages) & 1));
-          if (!ok) break;
+        const Pair x = decode_pair(a, tinfo[qb]);
+        const bool hb = x.n[1] > 0;
+        npx[0] += 1;
+        npx[1] += hb ? 1 : 0;
+        const uint32_t aQA = aQ0 + qb * C::kQBuf, aQB = aQA + C::kQTile;
+        for (int kb = 0; kb < x.nkb && ok; ++kb) {
+          const int ks = (int)(u % C::kSlots);
+          // P_A(b-1) V(b-1) before S_A(b) overwrites P_A(b-1)
+          if (pend && !(ok = issue_pv(0))) break;
+          if (!(ok = ptx::mbar_wait(&kv_full[ks], (uint32_t)((u / C::kSlots) & 1)))) break;
           tc::fence_after();
-          const uint32_t kbase = aK + sk * C::kKVBytes;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t qd = tc::sdesc_sw128(aQ + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
-            const uint64_t kd = tc::sdesc_sw128(kbase + (k >> 2) * C::kRegion + (k & 3) * 32, 16, 1024);
-            tc::mma(tmem + sb * 128, qd, kd, id_qk, k > 0 ? 1u : 0u);
+          issue_s(0, aQA, ks);
+          if (pend) {
+            if (pend_b && !(ok = issue_pv(1))) break;
+            tc::commit(&kv_empty[pend_slot]);  // V(b-1) read by both tiles
           }
-          tc::commit(&s_full[sb]);
+          if (hb) issue_s(1, aQB, ks);
+          tc::commit(&kv_empty[ks]);           // K(b) read by both tiles
           if (kb == x.nkb - 1) tc::commit(&q_empty[qb]);
-          if (pend >= 0) ok = issue_pv(pend, pend_first, pend_tile);
-          pend = g;
+          ++u;
+          pend = true;
+          pend_b = hb;
           pend_first = kb == 0;
-          pend_tile = tcount;
+          pend_slot = (int)(u % C::kSlots);
+          pend_par = (uint32_t)((u / C::kSlots) & 1);
+          ++u;
+          pend_g[0] = g[0]++;
+          pend_np[0] = npx[0];
+          if (hb) {
+            pend_g[1] = g[1]++;
+            pend_np[1] = npx[1];
+          }
         }
       }
-      if (ok && pend >= 0 && !*abort) ok = issue_pv(pend, pend_first, pend_tile);
+      if (ok && pend && !*abort) {
+        ok = issue_pv(0);
+        if (ok && pend_b) ok = issue_pv(1);
+        if (ok) tc::commit(&kv_empty[pend_slot]);
+      }
       if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
       // every MMA issued completes before the tensor memory is released
       tc::commit(drain);
@@ -608,215 +646,153 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
   } else {
     // ------------------------------------------------ softmax warps
-    // Warp (quarter, half) owns tensor-memory lanes 32 quarter .. + 31 (its
-    // rows) and the keys of one half of every block.  It keeps its own
-    // running max and sum for its half and writes P of its half over the S
-    // columns it read; O_half accumulates only that half's keys.  The two
-    // halves of a row meet once per tile, in the epilogue: with M = max(m0,
-    // m1), O = (2^(m0 - M) O0 + 2^(m1 - M) O1) / (2^(m0 - M) l0 + 2^(m1 - M) l1).
-    const int quarter = warp & 3, half = warp >> 2;
+    // Warp w handles tile tx = w / 4 and rows r = 32 (w % 4) + lane: one row
+    // per thread, all 128 keys of each block.
+    const int tx = warp >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int pair_bar = 1 + quarter;  // named barrier of the warp pair
+    const uint32_t tS = tmem + tx * 128 + lane_off;
+    const uint32_t tO = tmem + C::kColO + tx * D + lane_off;
     const float c = a.scale_log2e;
-    constexpr int KH = kKeyBlk / 2;    // key columns per half
-    constexpr int OH = D / 2;          // output columns this warp writes
-    const uint32_t tOown = tmem + C::kColO + half * D + lane_off;   // this half's accumulator
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-    int64_t gb = 0;
-    int tcount = 0;
-    // the previous tile's epilogue, still to run
-    // (its rows' m and l wait in xchg, its partial slots in pslot: only the
-    // flag stays in registers while the next tile runs)
+    int64_t gx = 0;                    // blocks of this tile processed
+    // the previous pair's epilogue, still to run: its row's partial slot,
+    // (m, l) and the block whose P V it waits for
     bool pend = false;
-    // Epilogue of the pending tile: combine the halves' accumulators into
-    // this warp's output columns [half * D / 2, + D / 2), normalised, to the
-    // row's partial slot.  Returns false when a bounded wait gave up.
+    int64_t pslot = -1, pgx = 0;
+    float pm = 0.f, pl = 1.f;
     auto epilogue = [&]() -> bool {
       pend = false;
-      const int64_t glast = gb - 1;  // the pending tile's last block: every call site has gb one past it
-      if (!ptx::mbar_wait(&p_free[glast & 1], (uint32_t)((glast >> 1) & 1))) return false;
+      if (!ptx::mbar_wait(&pv_done[tx], (uint32_t)(pgx & 1))) return false;
       tc::fence_after();
-      pair_sync();
-      const float m0 = xchg[r], l0 = xchg[128 + r];
-      const float m1 = xchg[256 + r], l1 = xchg[256 + 128 + r];
-      const int64_t slot = pslot[threadIdx.x];
-      pair_sync();
-      const float M = fmaxf(m0, m1);
-      const float w0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - M);
-      const float w1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
-      const float lt = l0 * w0 + l1 * w1;
-      const float inv = 1.f / lt;
-      const float s0 = w0 * inv, s1 = w1 * inv;
-      const uint32_t tO0 = tmem + C::kColO + lane_off + half * OH;
-      const uint32_t tO1 = tO0 + D;
-      uint16_t* dst = a.po + slot * D + half * OH;  // 32-byte aligned: the slot is D * 2 bytes
-      // 32 columns at a time: read both accumulators, combine, store
-#pragma unroll
-      for (int q = 0; q < OH / 32; ++q) {
-        uint32_t o0[32], o1[32], pk[16];
-        tc::ld32x2(tO0 + q * 32, o0, tO1 + q * 32, o1);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = ptx::pack2<DT>(
-              __uint_as_float(o0[2 * j]) * s0 + __uint_as_float(o1[2 * j]) * s1,
-              __uint_as_float(o0[2 * j + 1]) * s0 + __uint_as_float(o1[2 * j + 1]) * s1);
-        if (slot >= 0) {
-          ptx::st_global_v8(dst + 32 * q, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
-          ptx::st_global_v8(dst + 32 * q + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
-        }
+      // read all of O_X under one wait and release it at once (the next
+      // pair's first P V may then overwrite it), then normalise and store
+      uint32_t o[D];
+      if constexpr (D == 128) {
+        tc::ld64x2(tO, *reinterpret_cast<uint32_t(*)[64]>(&o[0]), tO + 64, *reinterpret_cast<uint32_t(*)[64]>(&o[64]));
+      } else {
+        tc::ld64(tO, *reinterpret_cast<uint32_t(*)[64]>(&o[0]));
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_relaxed(o_free);
-      if (slot >= 0 && half == 0) a.pml[slot] = make_float2(M, lt);
+      if (lane == 0) ptx::mbar_arrive_relaxed(&o_free[tx]);
+      if (pslot >= 0) {
+        const float inv = 1.f / pl;
+        uint16_t* dst = a.po + pslot * D;  // 32-byte aligned: a slot is D * 2 bytes
+#pragma unroll
+        for (int q = 0; q < D / 16; ++q) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = ptx::pack2<DT>(__uint_as_float(o[16 * q + 2 * j]) * inv, __uint_as_float(o[16 * q + 2 * j + 1]) * inv);
+          ptx::st_global_v8(dst + 16 * q, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+        }
+        a.pml[pslot] = make_float2(pm, pl);
+      }
       return true;
     };
-    // No abort check here: both warps of a pair must walk the same tiles
-    // (they meet at a named barrier per tile); they leave only through
-    // bounded waits, which time out together.
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-      const int qb = tcount & 1;
-      if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((tcount >> 1) & 1))) {
-        fail(SSA_DEVERR_WAIT_TIMEOUT);
+    bool ok = true;
+    int pc = 0;
+    for (int t = blockIdx.x; t < npairs; t += gridDim.x, ++pc) {
+      const int qb = pc & 1;
+      if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((pc >> 1) & 1))) {
+        ok = false;
         break;
       }
-      const Tile x = decode_tile(a, tinfo[qb]);
-      // row identity
-      int64_t qrow = -1;  // row of Q / sel / partials
-      int rank = a.topk;
-      int64_t tpos = 0;   // query position (local tiles)
-      if (x.kind_bh >= 0) {
-        const int e = meta[qb * kTileRows + r];
-        if (e >= 0) {
-          qrow = (int64_t)(e >> 6);
-          rank = e & 63;
-        }
-      } else if (r < x.nrows) {
-        int64_t i;
-        qrow = local_row(a, x, r, &i);
-        tpos = a.q_pos0 + i;
-      }
-      // the tile entry and row entries are in registers now: the loader may
-      // reuse them (with the Q buffer, once the tile's last S is done)
+      const int4 v = tinfo[qb];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
+      const Pair x = decode_pair(a, v);
+      if (x.n[tx] == 0) {
+        // no tile B in this pair: the pending epilogue cannot wait for it
+        if (pend && !(ok = epilogue())) break;
+        continue;
+      }
+      int rank;
+      int64_t tpos;
+      const int64_t qrow = pair_row(a, x, tx, r, &rank, &tpos, err);
       float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int kb = 0; kb < x.nkb && ok; ++kb) {
-        const int64_t g = gb + kb;
-        const int st = (int)(g & 1);
-        // the previous tile's epilogue, once this tile's first P is out
-        if (kb == 1 && pend && !epilogue()) {
-          ok = false;
-          break;
-        }
-        if (!ptx::mbar_wait(&s_full[st], (uint32_t)((g >> 1) & 1))) {
-          ok = false;
-          break;
-        }
+      for (int kb = 0; kb < x.nkb && ok; ++kb, ++gx) {
+        if (!(ok = ptx::mbar_wait(&s_full[tx], (uint32_t)(gx & 1)))) break;
         tc::fence_after();
-        // valid keys of this block: [0, klim)
+        // valid keys of this block for this row: [0, klim)
         const int64_t kstart = x.key0 + (int64_t)kb * kKeyBlk;
         int64_t klim = x.key_end - kstart;
         if (x.kind_bh < 0) klim = min(klim, tpos - kstart + 1);
-        const int64_t hlim = klim - half * KH;  // valid keys of this half
-        const bool partial = hlim < KH;
-        static_assert(KH == 64, "one 64-column load per half row");
-        const uint32_t tS = tmem + st * 128 + lane_off + half * KH;
-        uint32_t sr[64];
-        tc::ld64(tS, sr);
-        float mx = -INFINITY;
+        const bool partial = klim < kKeyBlk;
+        uint32_t sr[128];
+        tc::ld64x2(tS, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]), tS + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
         if (partial) {
 #pragma unroll
-          for (int j = 0; j < KH; ++j)
-            if (j < hlim) mx = fmaxf(mx, __uint_as_float(sr[j]));
-        } else {
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int j = 0; j < KH; j += 8)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              m4[u] = ptx::max3(m4[u], __uint_as_float(sr[j + 2 * u]), __uint_as_float(sr[j + 2 * u + 1]));
-          mx = ptx::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+          for (int j = 0; j < 128; ++j)
+            if (j >= klim) sr[j] = 0xff800000u;  // -inf
         }
-        mx *= c;
-        // rescale O_half only when this half's max grows by more than 2^8
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 128; j += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            m4[u] = ptx::max3(m4[u], __uint_as_float(sr[j + 2 * u]), __uint_as_float(sr[j + 2 * u + 1]));
+        const float mx = ptx::max3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * c;
+        // rescale O only when this row's max grows by more than 2^8
         float m_new = m;
-        if (kb == 0) {
-          m_new = mx;
-        } else if (mx > m + kRescaleLog2) {
-          m_new = mx;
-        }
+        if (kb == 0 || mx > m + kRescaleLog2) m_new = mx;
         const bool need = kb > 0 && m_new != m;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_half += P_half(g - 1) V must be complete before it is rescaled
-          if (!ptx::mbar_wait(&p_free[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1))) {
-            ok = false;
-            break;
+        const float nb = m_new == -INFINITY ? 0.f : -m_new;
+        // P = 2^(s c - m) as 16-bit pairs over the S columns just read, in two
+        // halves of 64 keys (two partial sums keep the adds off one chain)
+        float lsum = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+          float la = 0.f, lb = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[64 * hf + j]), c, nb));
+            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[64 * hf + j + 1]), c, nb));
+            la += p0;
+            lb += p1;
+            pk[j / 2] = ptx::pack2<DT>(p0, p1);
           }
+          lsum += la + lb;
+          if (hf == 0)
+            tc::st32_nowait(tS, pk);
+          else
+            tc::st32(tS + 32, pk);  // its wait covers both stores
+        }
+        // the rescale runs after P is out (the S values are dead by then) and
+        // before P is released to the tensor pipe
+        if (__any_sync(0xffffffffu, need)) {
+          // O += P V of the previous block must be complete before O is rescaled
+          if (!(ok = ptx::mbar_wait(&pv_done[tx], (uint32_t)((gx - 1) & 1)))) break;
           tc::fence_after();
           const float f = need ? ptx::ex2(m - m_new) : 1.f;
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t rr[32];
-            tc::ld32(tOown + q * 32, rr);
+            tc::ld32(tO + q * 32, rr);
 #pragma unroll
             for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-            tc::st32(tOown + q * 32, rr);
+            tc::st32(tO + q * 32, rr);
           }
           l *= f;
         }
         m = m_new;
-        const float nb = m == -INFINITY ? 0.f : -m;
-        // P_half = 2^(s c - m) as 16-bit pairs, over the S columns just read
-        uint32_t pk[32];
-        if (!partial) {
-          // two partial sums keep the adds off one dependency chain
-          float la = 0.f, lb = 0.f;
-#pragma unroll
-          for (int j = 0; j < KH; j += 2) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb));
-            la += p0;
-            lb += p1;
-            pk[j / 2] = ptx::pack2<DT>(p0, p1);
-          }
-          l += la + lb;
-        } else {
-#pragma unroll
-          for (int j = 0; j < KH; j += 2) {
-            const float p0 = j < hlim ? ptx::ex2(fmaf(__uint_as_float(sr[j]), c, nb)) : 0.f;
-            const float p1 = j + 1 < hlim ? ptx::ex2(fmaf(__uint_as_float(sr[j + 1]), c, nb)) : 0.f;
-            l += p0 + p1;
-            pk[j / 2] = ptx::pack2<DT>(p0, p1);
-          }
-        }
-        tc::st32(tS, pk);
+        l += lsum;
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_relaxed(&p_full[2 * st + half]);
+        if (lane == 0) ptx::mbar_arrive_relaxed(&p_full[tx]);
+        // the previous pair's epilogue, once this pair's first P is out
+        if (kb == 0 && pend && !(ok = epilogue())) break;
       }
-      if (!ok) {
-        fail(SSA_DEVERR_WAIT_TIMEOUT);
-        break;
-      }
-      // a one-block tile has not run the previous epilogue yet
-      if (ok && pend && !epilogue()) ok = false;
-      if (!ok) {
-        fail(SSA_DEVERR_WAIT_TIMEOUT);
-        break;
-      }
-      // this tile's epilogue runs after the next tile's first block (or
-      // after the last tile), so that waiting for its last O += P V overlaps
-      // the next tile's softmax
+      if (!ok) break;
       pend = true;
-      xchg[half * 256 + r] = m;
-      xchg[half * 256 + 128 + r] = l;
-      pslot[threadIdx.x] = qrow >= 0 ? qrow * (a.topk + 1) + rank : -1;
-      gb += x.nkb;
+      pslot = qrow >= 0 ? qrow * (a.topk + 1) + rank : -1;
+      pm = m;
+      pl = l;
+      pgx = gx - 1;
     }
-    if (pend && !epilogue()) fail(SSA_DEVERR_WAIT_TIMEOUT);
+    if (ok && pend) ok = epilogue();
+    if (!ok) fail(SSA_DEVERR_WAIT_TIMEOUT);
   }
   __syncthreads();
   tc::fence_after();

@@ -39,9 +39,9 @@
  *   No kernel traps or asserts.
  *   Workspace: `ws` is caller-owned device memory of at least
  *   ssa_workspace_size(...) bytes, 256-byte aligned, zeroed once before its
- *   first use.  Its first 16 bytes are the sticky error record; the rest is
- *   scratch that one call may overwrite, so calls that share a workspace
- *   must be ordered on one stream.
+ *   first use.  Its first 256 bytes are a header whose first uint32 is the
+ *   sticky error record; the rest is scratch that one call may overwrite, so
+ *   calls that share a workspace must be ordered on one stream.
  *   Supported: d in {64, 128}; S >= 1; 1 <= topk <= 64; Hq a multiple of
  *   Hkv with Hq / Hkv <= 16; dtype fp32, bf16 or fp16.  Other values return
  *   SSA_ERR_UNSUPPORTED.
@@ -210,14 +210,17 @@ SSA_API int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, 
  * Arguments, layouts and the returned status are those of
  * ssa_attend_decode, plus:
  *   scratch  nullable; receives the device address of the block, whose
- *            first 16 bytes are the sticky device error record.  Read it with
- *            ssa_workspace_error(*scratch, ...).  The library keeps ownership.
+ *            first uint32 is the sticky device error record, as in any
+ *            workspace.  Read it with ssa_workspace_error(*scratch, ...).
+ *            The library keeps ownership.
  * Limit: if ssa_workspace_size(p, 1, SSA_OP_DECODE) exceeds
  *   SSA_NOALLOC_SCRATCH_BYTES, returns SSA_ERR_WORKSPACE and enqueues
  *   nothing; use ssa_attend_decode with a workspace of that size instead.
- * Set-up: the first call on a device (the current one) looks up the block's
- *   address and enqueues a clear of its error record on `stream`.  Make
- *   that first call before any stream capture begins.
+ * Set-up: every call looks up the block's address in the current device's
+ *   current context (a host-side lookup); the first call in a context also
+ *   enqueues a clear of its error record on `stream`.  Make that first call
+ *   before any stream capture begins, and again after cudaDeviceReset (the
+ *   device's next context gets its own block and its own first call).
  * Races: every call on one device shares the block.  Calls that can overlap
  *   in time (two streams, two host threads) corrupt each other's results and
  *   error record; keep them on one stream.

@@ -30,8 +30,8 @@ def test_traffic_figures_cite_committed_profiles():
 
 
 def test_launch_count_per_decode_step():
-    # ssa_decode_step: route (+ plan) and attend (+ merges) on the 16-bit path
-    assert bench.launches_per_decode_step(W.DECODE_1M) == 2
+    # ssa_decode_step: route (+ plan), attend and merge on the 16-bit path
+    assert bench.launches_per_decode_step(W.DECODE_1M) == 3
     # fp32 decode: route + attend rows
     w32 = W.DECODE_1M.with_(dtype=torch.float32)
     assert bench.launches_per_decode_step(w32) == 2
