@@ -19,6 +19,7 @@ Entry points (same names as the C ABI):
   ssa_snapshot_save / ssa_snapshot_load / ssa_snapshot_read_header
                        the cache rows and summaries of a session, to and from a file
   ssa_workspace_size / ssa_workspace_error / ssa_status_string
+  ssa_attend_path      which implementation an attention call takes
 """
 from __future__ import annotations
 
@@ -126,6 +127,17 @@ def ssa_status_string(status: int) -> str:
 
 def ssa_workspace_size(p: ssa_params, n_q: int, op: int) -> int:
     return int(lib().ssa_workspace_size(ctypes.byref(p), int(n_q), int(op)))
+
+
+SSA_PATH_INVALID, SSA_PATH_FAST, SSA_PATH_ROWS = 0, 1, 2
+
+
+def ssa_attend_path(p: ssa_params, n_q: int, op: int) -> int:
+    """Which implementation an attention call takes (SSA_PATH_*); host only."""
+    f = lib().ssa_attend_path
+    f.argtypes = [ctypes.POINTER(ssa_params), _I64, ctypes.c_int]
+    f.restype = ctypes.c_int
+    return int(f(ctypes.byref(p), int(n_q), int(op)))
 
 
 def workspace(p: ssa_params, n_q: int, op: int, device=None) -> torch.Tensor | None:

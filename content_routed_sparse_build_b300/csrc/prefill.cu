@@ -290,12 +290,13 @@ template <int D>
 struct ACfg {
   static constexpr int kRegion = kTileRows * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = (D / 64) * kRegion;      // one 128-row Q tile
-  static constexpr int kQBuf = 2 * kQTile;               // the Q of a pair (tiles A and B)
   static constexpr int kKV = (D / 64) * kRegion;         // one K or V block of 128 tokens
   // one ring for both: K(0), V(0), K(1), V(1), ...  A K slot is free once
-  // both tiles' S of its block are done, a V slot once both P V are.
-  static constexpr int kSlots = 3;
-  static constexpr size_t kOperands = 2 * (size_t)kQBuf + (size_t)kSlots * kKV;
+  // both tiles' S of its block are done, a V slot once both P V are.  Four
+  // slots hold the block in use and the next one: tile A's Q is double
+  // buffered, tile B's single (its next rows load once its last S is done).
+  static constexpr int kSlots = 4;
+  static constexpr size_t kOperands = 3 * (size_t)kQTile + (size_t)kSlots * kKV;
   static constexpr int kSmallBytes = 512;                // barriers and the two pair entries
   static constexpr size_t kSmem = 1024 + kOperands + kSmallBytes;
   // tensor memory: S_A [0, 128), S_B [128, 256) (the P of a block is written
@@ -394,26 +395,29 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = base;                                // [2 buffers][2 tiles]
-  uint8_t* sKV = sQ + 2 * C::kQBuf;                  // [kSlots]
+  uint8_t* sQA = base;                               // [2 buffers] tile A's Q
+  uint8_t* sQB = sQA + 2 * C::kQTile;                // tile B's Q
+  uint8_t* sKV = sQB + C::kQTile;                    // [kSlots]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + C::kSlots * C::kKV);
-  uint64_t* q_full = bar + 0;     // [2] Q of a pair and its entry loaded
+  uint64_t* q_full = bar + 0;     // [2] tile A's Q of a pair and the pair entry loaded
   uint64_t* q_empty = bar + 2;    // [2] last S of the pair done + every softmax warp read the entry
-  uint64_t* kv_full = bar + 4;    // [3]
-  uint64_t* kv_empty = bar + 7;   // [3]
-  uint64_t* s_full = bar + 10;    // [2 tiles] S of the tile's block done
-  uint64_t* p_full = bar + 12;    // [2 tiles] P of the tile's block written (4 warps)
-  uint64_t* pv_done = bar + 14;   // [2 tiles] O += P V of the tile's block done
-  uint64_t* o_free = bar + 16;    // [2 tiles] O read out by the tile's epilogue (4 warps)
-  uint64_t* drain = bar + 18;     // every MMA issued has completed
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 19);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 20);
-  int4* tinfo = reinterpret_cast<int4*>(bar + 22);  // [2] pair entries
+  uint64_t* kv_full = bar + 4;    // [4]
+  uint64_t* kv_empty = bar + 8;   // [4]
+  uint64_t* s_full = bar + 12;    // [2 tiles] S of the tile's block done
+  uint64_t* p_full = bar + 14;    // [2 tiles] P of the tile's block written (4 warps)
+  uint64_t* pv_done = bar + 16;   // [2 tiles] O += P V of the tile's block done
+  uint64_t* o_free = bar + 18;    // [2 tiles] O read out by the tile's epilogue (4 warps)
+  uint64_t* drain = bar + 20;     // every MMA issued has completed
+  uint64_t* qb_full = bar + 21;   // tile B's Q of the pair loaded (every pair)
+  uint64_t* qb_empty = bar + 22;  // last S of the pair done: tile B's buffer is free (every pair)
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 23);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 24);
+  int4* tinfo = reinterpret_cast<int4*>(bar + 26);  // [2] pair entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&q_full[s], 2);
+      ptx::mbar_init(&q_full[s], 1);
       ptx::mbar_init(&q_empty[s], 1 + kSoftWarps);
       ptx::mbar_init(&s_full[s], 1);
       ptx::mbar_init(&p_full[s], kSoftWarps / 2);
@@ -425,6 +429,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       ptx::mbar_init(&kv_empty[s], 1);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(qb_full, 1);
+    ptx::mbar_init(qb_empty, 1);
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -481,19 +487,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // ------------------------------------------------ Q loaders
     // Warp kQWarp + t gathers the 128 query rows of tile t of the pair into
     // the swizzled K-major Q buffer; the tile-A warp publishes the pair
-    // entry.  Each lane's four row entries are loaded together first, so a
-    // tile costs two memory round trips before its copies start.
+    // entry.  Tile A's buffer is double buffered; tile B's is single, so
+    // its warp loads the pair's row entries first and starts the copies as
+    // soon as the previous pair's last S has read the buffer.
     const int tt = warp - kQWarp;
     int pc = 0;
     for (int t = blockIdx.x; t < npairs && !*abort; t += gridDim.x, ++pc) {
       const int qb = pc & 1;
-      if (pc >= 2 && !ptx::mbar_wait(&q_empty[qb], (uint32_t)(((pc - 2) >> 1) & 1))) {
-        fail(SSA_DEVERR_WAIT_TIMEOUT);
-        break;
-      }
       const int4 v = a.tiles[t];
       const Pair x = decode_pair(a, v);
-      if (tt == 0 && lane == 0) tinfo[qb] = v;
       int64_t qrow[kTileRows / 32];
       if (x.kind_bh >= 0) {
         const int64_t off = (int64_t)__ldg(a.offsets + x.kind_bh) + x.row0 + tt * kTileRows;
@@ -522,8 +524,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           qrow[i] = pair_row(a, x, tt, i * 32 + lane, &rank, &tpos, err);
         }
       }
+      const bool free_buf = tt == 0 ? (pc < 2 || ptx::mbar_wait(&q_empty[qb], (uint32_t)(((pc - 2) >> 1) & 1)))
+                                    : (pc < 1 || ptx::mbar_wait(qb_empty, (uint32_t)((pc - 1) & 1)));
+      if (!free_buf) {
+        fail(SSA_DEVERR_WAIT_TIMEOUT);
+        break;
+      }
+      if (tt == 0 && lane == 0) tinfo[qb] = v;
       if (x.n[tt] > 0) {
-        uint8_t* qt = sQ + qb * C::kQBuf + tt * C::kQTile;
+        uint8_t* qt = tt == 0 ? sQA + qb * C::kQTile : sQB;
 #pragma unroll
         for (int i = 0; i < kTileRows / 32; ++i) {
           const int r = i * 32 + lane;
@@ -542,7 +551,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&q_full[qb]);
+      if (lane == 0) ptx::mbar_arrive(tt == 0 ? &q_full[qb] : qb_full);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const int ab16 = DT == DT_BF16 ? 1 : 0;
       const uint32_t id_qk = tc::idesc_f16(128, kKeyBlk, ab16, 0, 0);
       const uint32_t id_pv = tc::idesc_f16(128, D, ab16, 0, 1);
-      const uint32_t aQ0 = ptx::smem_u32(sQ), aKV = ptx::smem_u32(sKV);
+      const uint32_t aQA0 = ptx::smem_u32(sQA), aQB = ptx::smem_u32(sQB), aKV = ptx::smem_u32(sKV);
       int64_t u = 0;                   // ring uses consumed
       int64_t npx[2] = {0, 0};         // pairs with tile X so far (o_free phases)
       // the previous block, whose P V follow this block's S
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const bool hb = x.n[1] > 0;
         npx[0] += 1;
         npx[1] += hb ? 1 : 0;
-        const uint32_t aQA = aQ0 + qb * C::kQBuf, aQB = aQA + C::kQTile;
+        const uint32_t aQA = aQA0 + qb * C::kQTile;
         for (int kb = 0; kb < x.nkb && ok; ++kb) {
           const int ks = (int)(u % C::kSlots);
           // P_A(b-1) V(b-1) before S_A(b) overwrites P_A(b-1)
@@ -616,9 +625,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             if (pend_b && !(ok = issue_pv(1))) break;
             tc::commit(&kv_empty[pend_slot]);  // V(b-1) read by both tiles
           }
-          if (hb) issue_s(1, aQB, ks);
+          if (hb) {
+            // tile B's Q of this pair (its single buffer) must be in
+            if (kb == 0 && !(ok = ptx::mbar_wait(qb_full, (uint32_t)(pc & 1)))) break;
+            tc::fence_after();
+            issue_s(1, aQB, ks);
+          }
           tc::commit(&kv_empty[ks]);           // K(b) read by both tiles
-          if (kb == x.nkb - 1) tc::commit(&q_empty[qb]);
+          if (kb == x.nkb - 1) {
+            tc::commit(&q_empty[qb]);
+            tc::commit(qb_empty);
+          }
           ++u;
           pend = true;
           pend_b = hb;

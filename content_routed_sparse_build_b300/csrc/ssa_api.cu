@@ -89,6 +89,14 @@ const char* ssa_status_string(int status) {
   }
 }
 
+int ssa_attend_path(const ssa_params* p, int64_t n_q, int op) {
+  Problem pr;
+  if (check_params(p, &pr) != SSA_OK || n_q < 0) return SSA_PATH_INVALID;
+  if (op == SSA_OP_DECODE) return decode_fast_supported(pr) ? SSA_PATH_FAST : SSA_PATH_ROWS;
+  if (op == SSA_OP_PREFILL) return prefill_fast(pr, n_q) ? SSA_PATH_FAST : SSA_PATH_ROWS;
+  return SSA_PATH_INVALID;
+}
+
 size_t ssa_workspace_size(const ssa_params* p, int64_t n_q, int op) {
   Problem pr;
   if (check_params(p, &pr) != SSA_OK || n_q < 0) return 0;

@@ -345,6 +345,25 @@ SSA_API int ssa_snapshot_load(const ssa_params* p, const char* path, void* K, vo
  */
 SSA_API int ssa_snapshot_read_header(const char* path, ssa_snapshot_header* out);
 
+/* Implementation an attention call takes (ssa_attend_path). */
+typedef enum {
+  SSA_PATH_INVALID = 0, /* the parameters are invalid or unsupported */
+  SSA_PATH_FAST = 1,    /* 16-bit fast path: split / span-major tiles on the tensor cores */
+  SSA_PATH_ROWS = 2     /* one warp per query row on the CUDA cores (fp32, or shapes the fast path does not take) */
+} ssa_path;
+
+/*
+ * Which implementation ssa_attend_decode (op = SSA_OP_DECODE; also
+ * ssa_decode_step) or ssa_attend_prefill (op = SSA_OP_PREFILL, n_q queries)
+ * takes for these parameters; SSA_PATH_INVALID for other ops or when the
+ * parameters would be rejected.  Both paths compute the same attention (the
+ * row kernel is slower); this lets a caller see the choice without timing
+ * it.  Host only, no GPU.  The prefill fast path needs bf16 / fp16, d in
+ * {64, 128}, 128 divisible by Hq / Hkv and B * Hq * n_q < 2^25; the decode
+ * fast path needs bf16 / fp16 and B * Hkv <= 1024.
+ */
+SSA_API int ssa_attend_path(const ssa_params* p, int64_t n_q, int op);
+
 /*
  * Bytes of workspace the operation needs for n_q queries (n_q is ignored
  * for SSA_OP_DECODE), or 0 when the parameters are invalid or unsupported

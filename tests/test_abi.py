@@ -154,3 +154,23 @@ def test_decode_step_validation():
     assert step(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
     assert step(p, 10, FAKE, need - 1) == ssa.SSA_ERR_WORKSPACE
     assert step(ssa.params(1, 8, 2, 96, 4096, 64, 8, 1), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+
+
+def test_attend_path_reports_the_implementation():
+    """The fast paths and the row kernel are chosen by the parameters alone;
+    the query says which one a call takes."""
+    P = lambda **kw: ssa.params(kw.get("B", 1), kw.get("Hq", 32), kw.get("Hkv", 4), kw.get("d", 128), 1 << 20, 1024,
+                                16, kw.get("dt", torch.bfloat16))
+    assert ssa.ssa_attend_path(P(), 1, ssa.SSA_OP_DECODE) == ssa.SSA_PATH_FAST
+    assert ssa.ssa_attend_path(P(), 8192, ssa.SSA_OP_PREFILL) == ssa.SSA_PATH_FAST
+    assert ssa.ssa_attend_path(P(dt=torch.float16, d=64), 8192, ssa.SSA_OP_PREFILL) == ssa.SSA_PATH_FAST
+    # fp32 takes the row kernel in both
+    assert ssa.ssa_attend_path(P(dt=torch.float32), 1, ssa.SSA_OP_DECODE) == ssa.SSA_PATH_ROWS
+    assert ssa.ssa_attend_path(P(dt=torch.float32), 4096, ssa.SSA_OP_PREFILL) == ssa.SSA_PATH_ROWS
+    # 128 / g not whole: prefill tiles of 128 rows cannot hold whole queries
+    assert ssa.ssa_attend_path(P(Hq=12, Hkv=1), 100, ssa.SSA_OP_PREFILL) == ssa.SSA_PATH_ROWS
+    # row ids past the 32-bit bucket entries
+    assert ssa.ssa_attend_path(P(B=4, Hq=32), 1 << 18, ssa.SSA_OP_PREFILL) == ssa.SSA_PATH_ROWS
+    # invalid parameters, other ops
+    assert ssa.ssa_attend_path(P(d=96), 1, ssa.SSA_OP_DECODE) == ssa.SSA_PATH_INVALID
+    assert ssa.ssa_attend_path(P(), 1, ssa.SSA_OP_ROUTE) == ssa.SSA_PATH_INVALID
