@@ -8,7 +8,8 @@ seeded input generator regenerates on the host for any range:
 
 * ``summaries_streamed``: the oracle's span means of a whole cache, computed
   from host regenerations of span ranges, so the 20 GB cache is never held.
-* ``compact_decode_step``: one decode step's attention as a smaller problem.
+* ``compact_decode_step``: one decode step's attention as a smaller problem
+  (rows regenerated on the host, or read by a caller-given function).
   For one kv-head it holds only the union of its query heads' selected spans
   (ascending) followed by the causal part of the local span.  Attention over
   a token set does not depend on where the tokens sit, so the compacted
@@ -41,7 +42,11 @@ def summaries_streamed(inp, spans_per_part: int = 128) -> np.ndarray:
     return out
 
 
-def compact_decode_step(inp, q_step: torch.Tensor, sel_step: np.ndarray, t: int):
+def _regenerate(inp, which: str, bh: int, parts) -> torch.Tensor:
+    return torch.cat([inp.kv_rows(which, bh, a, e) for a, e in parts])
+
+
+def compact_decode_step(inp, q_step: torch.Tensor, sel_step: np.ndarray, t: int, fetch=None):
     """The decode step at position t as one compacted problem per (b, kv-head).
 
     q_step [B, Hq, d] (host), sel_step [B*Hq, k] (the step's selections).
@@ -49,7 +54,15 @@ def compact_decode_step(inp, q_step: torch.Tensor, sel_step: np.ndarray, t: int)
     where rows are the step's row indices (b * Hq + head) of the kv-head's
     query heads and (q, K, V, pos, sel) are the arguments of oracle.attend
     for the compacted cache.
+
+    ``fetch(which, bh, parts)`` returns the host rows of the half-open row
+    ranges ``parts`` of K or V ("k" / "v") of flattened kv-head bh, one range
+    after the other.  By default the rows are regenerated on the host; a
+    caller that holds the same generated cache elsewhere may read it there.
     """
+    if fetch is None:
+        def fetch(which, bh, parts):
+            return _regenerate(inp, which, bh, parts)
     w = inp.w
     ell = t // w.S
     for bh in range(w.B * w.Hkv):
@@ -58,8 +71,8 @@ def compact_decode_step(inp, q_step: torch.Tensor, sel_step: np.ndarray, t: int)
         sel_h = sel_step[rows]
         union = np.unique(sel_h[sel_h >= 0])
         parts = [(int(j) * w.S, (int(j) + 1) * w.S) for j in union] + [(ell * w.S, t + 1)]
-        Kc = torch.cat([inp.kv_rows("k", bh, a, e) for a, e in parts]).reshape(1, 1, -1, w.d)
-        Vc = torch.cat([inp.kv_rows("v", bh, a, e) for a, e in parts]).reshape(1, 1, -1, w.d)
+        Kc = fetch("k", bh, parts).reshape(1, 1, -1, w.d)
+        Vc = fetch("v", bh, parts).reshape(1, 1, -1, w.d)
         remap = {int(j): i for i, j in enumerate(union)}
         sel_c = np.full(sel_h.shape, -1, np.int32)
         for r in range(sel_h.shape[0]):

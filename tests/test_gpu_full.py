@@ -21,7 +21,7 @@ The 10M decode case never holds the 20 GB cache on the host: the oracle's
 summaries come from host regenerations of span ranges, and each step's
 outputs are checked on a compacted cache that holds only the kv-head's
 selected spans (in ascending order) followed by its local span (see
-oracle/streamed.py).
+oracle/streamed.py), its rows read from the generator's device fill.
 """
 import numpy as np
 import pytest
@@ -234,12 +234,22 @@ def test_decode_10m_all_steps():
     assert torch.equal(O_f, O_g) and torch.equal(lse_f, lse_g)
     # the probe routes on the device cache; its outputs are checked compacted too
     q4, sel_p, same, O_p, lse_p, t_p = _probe_decode(w, inp, run, summ)
-    del Kd, Vd, run
+    del run
     torch.cuda.empty_cache()
     cases = [(w.q_pos0 + s, Q[s], sel_o[s], O_g[s], lse_g[s], None) for s in range(w.n_q)]
     cases.append((t_p, q4.reshape(w.B, w.Hq, w.d), sel_p, O_p, lse_p, same))
+    # The compacted caches are read from the device copy of the generated
+    # cache (the generator's device fill equals its host regeneration bit for
+    # bit: test_gpu_synth.py), gathered on the device and copied back.
+    kv = {"k": Kd, "v": Vd}
+
+    def fetch(which, bh, parts):
+        b, h = divmod(bh, w.Hkv)
+        idx = torch.cat([torch.arange(a, e, dtype=torch.int64) for a, e in parts]).to(dev)
+        return kv[which][b, h].index_select(0, idx).cpu()
+
     for t, q, sel_s, O_s, lse_s, keep in cases:
-        for rows, qc, Kc, Vc, pos, sel_c in streamed.compact_decode_step(inp, q, sel_s, t):
+        for rows, qc, Kc, Vc, pos, sel_c in streamed.compact_decode_step(inp, q, sel_s, t, fetch):
             O_o, lse_o, _ = oracle.attend(qc, Kc, Vc, pos, w.S, sel_c)
             m = np.ones(len(rows), bool) if keep is None else keep[rows]
             assert max_abs(O_s[rows][m], O_o[m]) <= TOL[w.dtype], t
