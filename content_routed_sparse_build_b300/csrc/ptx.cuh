@@ -30,6 +30,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Split cluster barrier: arrive (release) now, wait (acquire) later.  Every
+// thread of every CTA of the cluster takes part in each phase.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -152,6 +161,10 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
 }
 
 // 16-byte read-only load with an L2 cache policy.
+// Warms L2 with the 128-byte line holding p, kept with evict-last priority.
+__device__ __forceinline__ void prefetch_l2_evict_last(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ float4 ldg_hint(const float4* p, uint64_t pol) {
   float4 v;
   asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"

@@ -32,121 +32,107 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Marks the k best of the warp's entries.  Entry (i, lane) is the i-th
-// register of the lane; the entries' order (i major, lane minor) must be
-// ascending span index, so that among equal keys the earlier entry is the
-// lower span.  Finds the k-th largest key T by a bitwise search on the
-// key's bits (one warp-wide count per bit), takes every key above T and the
-// first entries equal to T.  Returns the lane's bitmask of chosen entries.
-template <int NV>
-__device__ __forceinline__ uint32_t warp_select(const uint32_t (&key)[NV], int k, int lane) {
-  int nv = 0;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) nv += key[i] != 0u;
-  nv = __reduce_add_sync(0xffffffffu, nv);
-  uint32_t chosen = 0u;
-  if (nv <= k) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (key[i] != 0u) chosen |= 1u << i;
-    return chosen;
-  }
-  uint32_t T = 0u;
-#pragma unroll 1
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    int c = 0;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) c += key[i] >= cand;
-    if (__reduce_add_sync(0xffffffffu, c) >= k) T = cand;
-  }
-  int gt = 0;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) gt += key[i] > T;
-  int need = k - __reduce_add_sync(0xffffffffu, gt);
-  const uint32_t lt_mask = (1u << lane) - 1u;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const uint32_t eq = __ballot_sync(0xffffffffu, key[i] == T);
-    const bool take = key[i] > T || (key[i] == T && __popc(eq & lt_mask) < need);
-    need -= min(need, __popc(eq));
-    if (take) chosen |= 1u << i;
-  }
-  return chosen;
-}
-
-// Replaces a head's list (topk entries, ascending spans, invalid = kNoSpan)
-// by the topk best of the list and one block of 128 scores (spans jb ..);
-// NL = 0 when the list is still empty.
-template <int NL>
-__device__ __forceinline__ void fold_block(float* lsv, int* lsj, const float* sc, int64_t jb,
-                                           int64_t hi, int lane, int topk) {
-  constexpr int NV = NL + 4;
-  float v[NV];
-  int vj[NV];
-  uint32_t key[NV];
-#pragma unroll
-  for (int i = 0; i < NL; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < topk ? lsv[e] : -INFINITY;
-    vj[i] = e < topk ? lsj[e] : kNoSpan;
-    key[i] = vj[i] == kNoSpan ? 0u : score_key(v[i]);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t jj = jb + lane + 32 * i;
-    const bool ok = jj < hi;
-    v[NL + i] = ok ? sc[lane + 32 * i] : -INFINITY;
-    vj[NL + i] = ok ? (int)jj : kNoSpan;
-    key[NL + i] = ok ? score_key(v[NL + i]) : 0u;
-  }
-  const uint32_t chosen = warp_select<NV>(key, topk, lane);
-  __syncwarp();
-  int base = 0;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const bool c = (chosen >> i) & 1u;
-    const uint32_t bal = __ballot_sync(0xffffffffu, c);
-    if (c) {
-      const int p = base + __popc(bal & ((1u << lane) - 1u));
-      lsv[p] = v[i];
-      lsj[p] = vj[i];
-    }
-    base += __popc(bal);
-  }
-  for (int e = base + lane; e < topk; e += 32) {
-    lsv[e] = -INFINITY;
-    lsj[e] = kNoSpan;
-  }
-}
-
 // ---------------------------------------------------------------- decode
-// grid (kCluster, Hkv, B), one cluster per (b, kv-head).  CTA `rank` scores
-// candidates [rank*chunk, (rank+1)*chunk) for all g heads of the group in
-// blocks of 256: two lanes per candidate, each summing one half of d with
-// all of its summary loads in flight at once, the two halves then added.
-// Each block is folded into per-head lists; finally CTA `rank` merges head
-// rank (+16) over the cluster's lists through distributed shared memory.
-//
-// With PLAN (a whole decode step), each final list is also pushed into CTA
-// 0's shared memory, and CTA 0 then builds the group's decode plan
-// (decode_plan.cuh) for the attend kernel that follows: the step needs no
-// separate plan kernel.
-constexpr int kBlk = 128;
+// A candidate of the decode router is one 64-bit entry: the score's key in
+// the high word, the complement of the span in the low word.  One unsigned
+// comparison then orders by score and, among equal scores, puts the lower
+// span first; entries are distinct (spans are), and 0 means "none".
+__device__ __forceinline__ uint64_t make_entry(float s, int64_t j) {
+  return ((uint64_t)score_key(s) << 32) | (uint32_t)~(uint32_t)j;
+}
+__device__ __forceinline__ int entry_span(uint64_t e) { return (int)~(uint32_t)e; }
+__device__ __forceinline__ float entry_score(uint64_t e) {
+  const uint32_t k = (uint32_t)(e >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
-template <int DT, int D, int G, int NE, bool PLAN>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
+// Warp lists of 32 * E entries: element e = i * 32 + lane sits in register
+// i of the lane.  Bitonic networks (Batcher): a compare-exchange stage of
+// distance j inside runs of length k leaves the larger entry at the lower
+// index when the run is to end descending ((e & k) == 0), else the smaller.
+template <int E>
+__device__ __forceinline__ void bitonic_stage(uint64_t (&a)[E], int j, int k, int lane) {
+  if (j >= 32) {
+    const int jj = j >> 5;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if (i & jj) continue;
+      const int i2 = i | jj;
+      const bool desc = ((i * 32 + lane) & k) == 0;
+      const uint64_t hi = umax64(a[i], a[i2]), lo = umin64(a[i], a[i2]);
+      a[i] = desc ? hi : lo;
+      a[i2] = desc ? lo : hi;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const uint64_t p = __shfl_xor_sync(0xffffffffu, a[i], j);
+      const int e = i * 32 + lane;
+      const bool take_max = ((e & j) == 0) == ((e & k) == 0);
+      a[i] = take_max ? umax64(a[i], p) : umin64(a[i], p);
+    }
+  }
+}
+
+// Sorts the warp's 32 * E entries descending.
+template <int E>
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&a)[E], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32 * E; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) bitonic_stage<E>(a, j, k, lane);
+}
+
+// L <- the best 32 * E of L and B, both descending, descending.  The
+// element-wise maximum of L and reversed B is a bitonic sequence that holds
+// the best 32 * E of the two; one merge network sorts it.
+template <int E>
+__device__ __forceinline__ void merge_best_desc(uint64_t (&L)[E], const uint64_t (&B)[E], int lane) {
+#pragma unroll
+  for (int i = 0; i < E; ++i) L[i] = umax64(L[i], __shfl_sync(0xffffffffu, B[E - 1 - i], 31 - lane));
+#pragma unroll
+  for (int j = 16 * E; j > 0; j >>= 1) bitonic_stage<E>(L, j, 32 * E, lane);
+}
+
+// grid (kCluster, Hkv, B), one cluster of 16 CTAs per (b, kv-head), 256
+// threads.  CTA `rank` owns candidates [rank*chunk, (rank+1)*chunk).
+//  scores   blocks of 64 candidates, four lanes per candidate, every head
+//           of the group per thread.  Lane quarter qq sums the dimensions d
+//           with (d / 4) % 4 == qq in increasing order; the quarters are
+//           added as (q0 + q1) + (q2 + q3).  The CTA's summaries are
+//           prefetched into L2 before the kernel waits for its predecessor.
+//  level 1  one warp per head sorts each block and merges it into its list
+//           of the best LC = 32 * E >= k entries so far, kept in registers.
+//  level 2  every CTA sends its list of head h to CTA h; after a cluster
+//           barrier CTA h merges its 16 lists in a four-level tree.  The
+//           best k of the result are its winners, written in ascending span
+//           order.
+// With PLAN (a whole decode step) the winners also go to CTA 0, which after
+// a second cluster barrier builds the group's decode plan (decode_plan.cuh)
+// for the attend kernel that follows.
+constexpr int kBlk = 64;
+
+template <int G, int D, int E>
+struct DecodeRouteSmem {
+  static constexpr int kQS = D / 4 + 4;  // floats per lane quarter of a q row (padded)
+  float q[G][4 * kQS];
+  uint64_t sc[G][kBlk];                  // the block's entries per head (0 = none)
+  uint64_t recv[kCluster][32 * E];       // the lists of this CTA's head, one per CTA
+  dplan::PlanSmem ps;                    // winners in span order and plan scratch (CTA 0)
+};
+
+template <int DT, int D, int G, int E, bool PLAN>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
     route_decode_kernel(const void* __restrict__ Q, const float* __restrict__ summ,
                         int32_t* __restrict__ sel, float* __restrict__ sel_score, int Hq, int Hkv,
                         int64_t pos, int S, int topk, int64_t ns_cap, dplan::Plan plan, dplan::Geo geo) {
-  constexpr int HD = D / 2;          // dims per lane
-  constexpr int HPAD = HD + 4;       // padded half stride, keeps the two halves in other banks
-  constexpr int NL = HD / 4;         // float4 loads per lane
-  __shared__ __align__(16) float q_s[G][2 * HPAD];
-  __shared__ float sc_s[G][kBlk];
-  __shared__ float lsv_s[G][kMaxK];
-  __shared__ int lsj_s[G][kMaxK];
-  __shared__ dplan::PlanSmem ps;     // CTA 0 of a PLAN cluster: the group's final lists and plan scratch
+  using Sm = DecodeRouteSmem<G, D, E>;
+  constexpr int kQS = Sm::kQS;
+  constexpr int NL = D / 16;          // float4 loads per lane per candidate
+  constexpr int HPW = (G + 7) / 8;    // heads per warp
+  __shared__ __align__(16) Sm sm;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -157,40 +143,54 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
   const int64_t chunk = (ell + kCluster - 1) / kCluster;
   const int64_t lo = min(ell, (int64_t)rank * chunk);
   const int64_t hi = min(ell, lo + chunk);
+  const int qq = tid & 3, cj = tid >> 2;  // lane quarter, candidate of the block
 
-  for (int x = tid; x < G * kMaxK; x += 256) {
-    lsv_s[x / kMaxK][x % kMaxK] = -INFINITY;
-    lsj_s[x / kMaxK][x % kMaxK] = kNoSpan;
-  }
+  const float* sbase = summ + (int64_t)(b * Hkv + kvh) * ns_cap * D;
+  // the summaries do not depend on the predecessor's results in a decode
+  // step, but they may be its output in general: only warm L2 before the wait
+  for (int64_t line = lo * (D / 32) + tid; line < hi * (D / 32); line += 256)
+    ptx::prefetch_l2_evict_last(sbase + line * 32);
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
+
+  const uint64_t pol_keep = ptx::policy_evict_last();  // the summaries are read every step
+  float4 sv[NL];
+  auto load_block = [&](int64_t jb) {
+    const int64_t j = jb + cj;
+    if (j < hi) {
+      const float4* src = reinterpret_cast<const float4*>(sbase + j * D);
+#pragma unroll
+      for (int i = 0; i < NL; ++i) sv[i] = ptx::ldg_hint(src + 4 * i + qq, pol_keep);
+    }
+  };
+  if (lo < hi) load_block(lo);
   for (int x = tid; x < g * D; x += 256) {
-    const int hl = x / D, c = x - hl * D;
-    q_s[hl][(c / HD) * HPAD + (c % HD)] = load_elem<DT>(Q, (int64_t)(b * Hq + kvh * g + hl) * D + c);
+    const int hl = x / D, d = x - hl * D;
+    const int f = d >> 2;
+    sm.q[hl][(f & 3) * kQS + 4 * (f >> 2) + (d & 3)] =
+        load_elem<DT>(Q, (int64_t)(b * Hq + kvh * g + hl) * D + d);
   }
   __syncthreads();
 
-  const float* sbase = summ + (int64_t)(b * Hkv + kvh) * ns_cap * D;
-  const int half = tid & 1;
-  const uint64_t pol_keep = ptx::policy_evict_last();  // the summaries are read every step
+  uint64_t L[HPW][E];  // this warp's level-1 lists (heads warp, warp + 8)
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh)
+#pragma unroll
+    for (int i = 0; i < E; ++i) L[hh][i] = 0ull;
+
   for (int64_t jb = lo; jb < hi; jb += kBlk) {
     {
-      const int jj = tid >> 1;
-      const int64_t j = jb + jj;
+      const int64_t j = jb + cj;
       float acc[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[h] = 0.f;
       if (j < hi) {
-        const float4* src = reinterpret_cast<const float4*>(sbase + j * D + half * HD);
-        float4 sv[NL];
-#pragma unroll
-        for (int i = 0; i < NL; ++i) sv[i] = ptx::ldg_hint(src + i, pol_keep);
 #pragma unroll
         for (int i = 0; i < NL; ++i) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             if (h < g) {
-              const float4 qv = *reinterpret_cast<const float4*>(&q_s[h][half * HPAD + 4 * i]);
+              const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][qq * kQS + 4 * i]);
               acc[h] = fmaf(qv.x, sv[i].x, acc[h]);
               acc[h] = fmaf(qv.y, sv[i].y, acc[h]);
               acc[h] = fmaf(qv.z, sv[i].z, acc[h]);
@@ -202,72 +202,95 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         if (h < g) {
-          const float other = __shfl_xor_sync(0xffffffffu, acc[h], 1);
-          if (half == 0) sc_s[h][jj] = j < hi ? acc[h] + other : -INFINITY;
+          float a = acc[h];
+          a += __shfl_xor_sync(0xffffffffu, a, 1);
+          a += __shfl_xor_sync(0xffffffffu, a, 2);
+          if (qq == 0) sm.sc[h][cj] = j < hi ? make_entry(a, j) : 0ull;
         }
       }
     }
+    if (jb + kBlk < hi) load_block(jb + kBlk);
     __syncthreads();
-    // fold this block into the head's list (list entries come first: their
-    // spans are below every span of the block; the first block has no list)
-    for (int h = warp; h < g; h += 8) {
-      if (jb == lo)
-        fold_block<0>(lsv_s[h], lsj_s[h], sc_s[h], jb, hi, lane, topk);
-      else
-        fold_block<2>(lsv_s[h], lsj_s[h], sc_s[h], jb, hi, lane, topk);
+#pragma unroll
+    for (int hh = 0; hh < HPW; ++hh) {
+      const int h = warp + 8 * hh;
+      if (h < g) {
+        uint64_t blk[2] = {sm.sc[h][lane], sm.sc[h][lane + 32]};
+        bitonic_sort_desc<2>(blk, lane);
+        if constexpr (E == 1) {
+          const uint64_t top[1] = {blk[0]};
+          merge_best_desc<1>(L[hh], top, lane);
+        } else {
+          merge_best_desc<2>(L[hh], blk, lane);
+        }
+      }
     }
     __syncthreads();
   }
-
-  cluster.sync();
-  // final: CTA `rank` selects head rank (+16) from the cluster's lists, which
-  // concatenated in rank order are ascending in span index
-  if (warp == 0) {
-    for (int h = rank; h < g; h += kCluster) {
-      float v[NE];
-      int vj[NE];
-      uint32_t key[NE];
+  // level 2: list of head h -> CTA h
 #pragma unroll
-      for (int i = 0; i < NE; ++i) {
-        const int e = i * 32 + lane;  // entry e = src * topk + s
-        const int src = e / topk, s = e - src * topk;
-        v[i] = -INFINITY;
-        vj[i] = kNoSpan;
-        if (src < kCluster) {
-          v[i] = cluster.map_shared_rank(&lsv_s[h][0], src)[s];
-          vj[i] = cluster.map_shared_rank(&lsj_s[h][0], src)[s];
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int h = warp + 8 * hh;
+    if (h < g) {
+      uint64_t* dst = cluster.map_shared_rank(&sm.recv[rank][0], h);
+#pragma unroll
+      for (int i = 0; i < E; ++i) dst[i * 32 + lane] = L[hh][i];
+    }
+  }
+  cluster.sync();
+  if (rank < g) {
+    const int h = rank;
+    for (int lev = 0; lev < 4; ++lev) {
+      const int a = warp << (lev + 1), c = a + (1 << lev);
+      if (c < kCluster) {
+        uint64_t A[E], Bv[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          A[i] = sm.recv[a][i * 32 + lane];
+          Bv[i] = sm.recv[c][i * 32 + lane];
         }
-        key[i] = vj[i] == kNoSpan ? 0u : score_key(v[i]);
+        merge_best_desc<E>(A, Bv, lane);
+#pragma unroll
+        for (int i = 0; i < E; ++i) sm.recv[a][i * 32 + lane] = A[i];
       }
-      const uint32_t chosen = warp_select<NE>(key, topk, lane);
+      __syncthreads();
+    }
+    if (warp == 0) {
+      // the best k, in ascending span order (spans are distinct)
+      const uint64_t* w = sm.recv[0];
+      int n = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int x = lane + 32 * i;
+        n += __popc(__ballot_sync(0xffffffffu, x < topk && w[x] != 0ull));
+      }
       const int64_t row = (int64_t)b * Hq + kvh * g + h;
       int32_t* out = sel + row * topk;
       float* osc = sel_score ? sel_score + row * topk : nullptr;
-      int base = 0;
+      int* pj = PLAN ? cluster.map_shared_rank(&sm.ps.sj[h][0], 0) : nullptr;
 #pragma unroll
-      for (int i = 0; i < NE; ++i) {
-        const bool c = (chosen >> i) & 1u;
-        const uint32_t bal = __ballot_sync(0xffffffffu, c);
-        if (c) {
-          const int p = base + __popc(bal & ((1u << lane) - 1u));
-          out[p] = vj[i];
-          if (osc) osc[p] = v[i];
-          if constexpr (PLAN) cluster.map_shared_rank(&ps.sj[h][0], 0)[p] = vj[i];
+      for (int i = 0; i < 2; ++i) {
+        const int x = lane + 32 * i;
+        if (x < n) {
+          const int jx = entry_span(w[x]);
+          int p = 0;
+          for (int y = 0; y < n; ++y) p += entry_span(w[y]) < jx;
+          out[p] = jx;
+          if (osc) osc[p] = entry_score(w[x]);
+          if constexpr (PLAN) pj[p] = jx;
+        } else if (x < topk) {
+          out[x] = -1;
+          if (osc) osc[x] = __int_as_float(0x7fc00000);
         }
-        base += __popc(bal);
-      }
-      for (int e = base + lane; e < topk; e += 32) {
-        out[e] = -1;
-        if (osc) osc[e] = __int_as_float(0x7fc00000);
       }
       if constexpr (PLAN) {
-        if (lane == 0) *cluster.map_shared_rank(&ps.nv[h], 0) = base;
+        if (lane == 0) *cluster.map_shared_rank(&sm.ps.nv[h], 0) = n;
       }
     }
   }
-  cluster.sync();
   if constexpr (PLAN) {
-    if (rank == 0) dplan::plan_build<8>(b * Hkv + kvh, ps, plan, geo);
+    cluster.sync();
+    if (rank == 0) dplan::plan_build<8>(b * Hkv + kvh, sm.ps, plan, geo);
   }
 }
 
@@ -409,7 +432,7 @@ __global__ void __launch_bounds__(256) route_prefill_kernel(
   }
 }
 
-template <int DT, int D, int G, int NE, bool PLAN>
+template <int DT, int D, int G, int E, bool PLAN>
 cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
                                 int32_t* sel, float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo,
                                 cudaStream_t st) {
@@ -420,31 +443,29 @@ cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, NE, PLAN>,
+    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, E, PLAN>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_pdl(route_decode_kernel<DT, D, G, NE, PLAN>, grid, dim3(256), 0, st, Q, summ, sel,
-                    sel_score, pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap, plan, geo);
+  return launch_pdl(route_decode_kernel<DT, D, G, E, PLAN>, grid, dim3(256), 0, st, Q, summ, sel, sel_score,
+                    pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap, plan, geo);
 }
 
 template <int DT, int D, int G, bool PLAN>
-cudaError_t decode_route_ne(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
-                            int32_t* sel, float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo,
-                            cudaStream_t st) {
-  // entries per lane of the final cluster merge: kCluster * topk / 32
-  if (pr.topk <= 16)
-    return launch_decode_route<DT, D, G, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  return launch_decode_route<DT, D, G, 32, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+cudaError_t decode_route_e(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ, int32_t* sel,
+                           float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo, cudaStream_t st) {
+  // level-1 lists of 32 entries hold the best k for k <= 32, else 64
+  if (pr.topk <= 32) return launch_decode_route<DT, D, G, 1, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return launch_decode_route<DT, D, G, 2, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
 }
 
 template <int DT, int D, bool PLAN>
 cudaError_t decode_route_g(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ, int32_t* sel,
                            float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo, cudaStream_t st) {
-  if (pr.g <= 4) return decode_route_ne<DT, D, 4, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  if (pr.g <= 8) return decode_route_ne<DT, D, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  return decode_route_ne<DT, D, 16, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.g <= 4) return decode_route_e<DT, D, 4, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.g <= 8) return decode_route_e<DT, D, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return decode_route_e<DT, D, 16, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
 }
 
 template <int DT, int D>
