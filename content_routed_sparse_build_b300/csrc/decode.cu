@@ -12,8 +12,8 @@
 //          builds their union U (ascending, local span last) with, per span,
 //          the mask of heads that chose it and each head's rank for it.
 //  attend  persistent, one CTA per SM, six independent warps.  Work items
-//          are (group, span of U, chunk of CH tokens), handed out by an
-//          atomic counter.  Each warp runs its own two-stage ring of 32-token
+//          are (group, span of U, chunk of CH tokens): a warp's first item
+//          is fixed by its index, later ones come from an atomic counter.  Each warp runs its own two-stage ring of 32-token
 //          K / V tiles loaded by TMA (128-byte swizzle, mbarrier completion),
 //          each tile computed as two 16-token fragments.  The MMAs are
 //          transposed so that the query group fits the n8 side of
@@ -233,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // made when two tiles of the current one remain to be issued, so that the
   // atomic's round trip is hidden without reserving work for long (which
   // would unbalance the tail).
-  int it_next = 0, it_claim = 0;
+  // the first item of every warp is fixed; later ones come from the counter
+  const int n_static = (int)gridDim.x * (int)(blockDim.x >> 5);
+  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = 0;
   bool have_next = true, claim_issued = false;
-  if (lane == 0) it_next = atomicAdd(plan.counter, 1);
-  it_next = __shfl_sync(0xffffffffu, it_next, 0);
   bool exhausted = false;
 
   const uint64_t pol_stream = ptx::policy_evict_first();  // K / V are read once per step
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ++iss_tile;
     if (!claim_issued && iss.ntiles - iss_tile <= 2) {
-      if (lane == 0) it_claim = atomicAdd(plan.counter, 1);
+      if (lane == 0) it_claim = atomicAdd(plan.counter, 1) + n_static;
       claim_issued = true;
     }
     return true;
@@ -573,10 +573,10 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   iss.grp = iss.u = iss.c = 0;
   iss.t0 = iss.t1 = 0;
   int iss_tile = 0;
-  int it_next = 0, it_claim = 0;
+  // the first item of every warp is fixed; later ones come from the counter
+  const int n_static = (int)gridDim.x * (int)(blockDim.x >> 5);
+  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = 0;
   bool have_next = true, claim_issued = false;
-  if (lane == 0) it_next = atomicAdd(plan.counter, 1);
-  it_next = __shfl_sync(0xffffffffu, it_next, 0);
   bool exhausted = false;
   const uint64_t pol_stream = ptx::policy_evict_first();  // K rows are read once per step
 
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
     }
     ++iss_tile;
     if (!claim_issued && iss.ntiles - iss_tile <= 2) {
-      if (lane == 0) it_claim = atomicAdd(plan.counter, 1);
+      if (lane == 0) it_claim = atomicAdd(plan.counter, 1) + n_static;
       claim_issued = true;
     }
     return true;

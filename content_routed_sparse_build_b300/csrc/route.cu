@@ -45,6 +45,25 @@ __device__ __forceinline__ float entry_score(uint64_t e) {
   const uint32_t k = (uint32_t)(e >> 32);
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
+// The 16 bytes w as fp32 values: eight 16-bit or four fp32 elements.
+template <int DT>
+__device__ __forceinline__ void unpack16(const uint4& w, float (&f)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == DT_F32) {
+      f[i] = __uint_as_float(u[i]);
+    } else if constexpr (DT == DT_BF16) {
+      f[2 * i] = __uint_as_float(u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+      const float2 v = __half22float2(h);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+}
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
@@ -164,11 +183,30 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
     }
   };
   if (lo < hi) load_block(lo);
-  for (int x = tid; x < g * D; x += 256) {
-    const int hl = x / D, d = x - hl * D;
-    const int f = d >> 2;
-    sm.q[hl][(f & 3) * kQS + 4 * (f >> 2) + (d & 3)] =
-        load_elem<DT>(Q, (int64_t)(b * Hq + kvh * g + hl) * D + d);
+  {
+    // the group's g rows of Q are contiguous: 16-byte loads, all in flight
+    constexpr int V = DT == DT_F32 ? 4 : 8;  // elements per 16 bytes
+    const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(Q) +
+                                                       (int64_t)(b * Hq + kvh * g) * D * (16 / V));
+    const int nvec = g * D / V;
+    uint4 raw[(G * D / V + 255) / 256];
+#pragma unroll
+    for (int u = 0; u < (G * D / V + 255) / 256; ++u)
+      if (tid + 256 * u < nvec) raw[u] = qsrc[tid + 256 * u];
+#pragma unroll
+    for (int u = 0; u < (G * D / V + 255) / 256; ++u) {
+      const int x = tid + 256 * u;
+      if (x < nvec) {
+        float f[8];
+        unpack16<DT>(raw[u], f);
+#pragma unroll
+        for (int c = 0; c < V; c += 4) {
+          const int e = x * V + c, hl = e / D, d = e - hl * D, ff = d >> 2;
+          *reinterpret_cast<float4*>(&sm.q[hl][(ff & 3) * kQS + 4 * (ff >> 2)]) =
+              make_float4(f[c], f[c + 1], f[c + 2], f[c + 3]);
+        }
+      }
+    }
   }
   __syncthreads();
 
