@@ -159,14 +159,17 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
     return units_per_rank * ws / seconds
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) that
-# ncu measured for the dominant kernels of the two default workloads, as the
-# kernels stand in this tree; each figure names the profile summary it comes
-# from.  They are reported as the roofline's "traffic" only for the workload
-# they were measured on.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) that ncu measured
+# for the roofline's unit, as the kernels stand in this tree; each figure
+# names the profile summary it comes from.  The decode step's figure was
+# captured on a 256K cache (a full-size capture may take one counter pass
+# only) and scaled to the 1M step by each kernel's unit: the attend reads by
+# the gathered bytes, the route's by the candidate count; the partial and
+# merge bytes do not change.  The prefill attend kernel changed after its last
+# full-size capture, so its line reports no traffic.
 NCU_TRAFFIC = {
-    "decode_1m": (None, "profiles/decode_1m_launches.md: not yet captured for the two-launch step"),
-    "prefill_chunk_vs_1m": (3.856e9, "profiles/prefill_chunk_1m_launches.md: prefill_attend_kernel"),
+    "decode_1m": (2.219e8, "profiles/decode_1m_launches.md: route + attend + merge of one step, "
+                           "256K capture scaled to 1M"),
 }
 
 
@@ -230,8 +233,13 @@ class DecodeBench:
                                   self.O, self.lse, self.ws)
 
     def step(self, i):
-        if not (self.group or self.q8):
-            # the whole step in one call: route (which also plans) + attend
+        # the whole step in one call where the library has one: route (which
+        # also plans) + attend + merge
+        if self.q8:
+            ssa.ssa_decode_step_q8(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.Kq, self.Ks, self.Vq,
+                                   self.Vs, self.sels[i], self.O, self.lse, self.ws)
+            return
+        if not self.group:
             ssa.ssa_decode_step(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.K, self.V, self.sels[i],
                                 self.O, self.lse, self.ws)
             return

@@ -11,10 +11,10 @@ Entry points (same names as the C ABI):
   ssa_route            span scores + top-k selection
   ssa_route_group      one top-k per kv-head group (summed scores of its heads)
   ssa_attend_decode    one query per head, split over spans, LSE merge
-  ssa_decode_step      route + attend of one decode step (two launches)
+  ssa_decode_step      route + attend of one decode step (three launches)
   ssa_attend_prefill   a chunk of queries, span-major tiles, LSE merge
   ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
-  ssa_quantize_kv / ssa_build_summaries_q8 / ssa_attend_decode_q8
+  ssa_quantize_kv / ssa_build_summaries_q8 / ssa_attend_decode_q8 / ssa_decode_step_q8
                        the 8-bit cache: quantised rows, their summaries, decode over them
   ssa_snapshot_save / ssa_snapshot_load / ssa_snapshot_read_header
                        the cache rows and summaries of a session, to and from a file
@@ -277,6 +277,17 @@ def ssa_attend_decode_q8(p: ssa_params, Q: torch.Tensor, pos: int, Kq: torch.Ten
     wp, wn = _ws_args(ws)
     _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(Kq), _ptr(Ks), _ptr(Vq), _ptr(Vs), _ptr(sel), _ptr(O),
              _ptr(lse), wp, wn, _stream(stream)), "ssa_attend_decode_q8")
+
+
+def ssa_decode_step_q8(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor, Kq: torch.Tensor,
+                       Ks: torch.Tensor, Vq: torch.Tensor, Vs: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
+                       lse: torch.Tensor | None, ws: torch.Tensor | None, stream=None) -> None:
+    f = lib().ssa_decode_step_q8
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(summ), _ptr(Kq), _ptr(Ks), _ptr(Vq), _ptr(Vs), _ptr(sel),
+             _ptr(O), _ptr(lse), wp, wn, _stream(stream)), "ssa_decode_step_q8")
 
 
 SSA_SNAPSHOT_MAGIC = b"SSAKVSN1"

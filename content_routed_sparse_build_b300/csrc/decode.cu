@@ -1038,6 +1038,14 @@ cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const
   return attend_16<DT_F16, 64>(pr, Q, K, V, O, lse, plan, geo, err, st);
 }
 
+cudaError_t launch_attend_decode_q8_planned(const Problem& pr, const void* Q, const int8_t* Kq, const float* Ks,
+                                            const int8_t* Vq, const float* Vs, void* O, float* lse,
+                                            const dplan::Plan& plan, const dplan::Geo& geo, uint32_t* err,
+                                            cudaStream_t st) {
+  if (pr.dtype == DT_BF16) return attend_q8<DT_BF16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
+  return attend_q8<DT_F16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
+}
+
 cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, const void* K,
                                  const void* V, const int32_t* sel, void* O, float* lse, void* ws,
                                  cudaStream_t st) {

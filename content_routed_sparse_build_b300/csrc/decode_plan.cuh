@@ -203,11 +203,15 @@ __device__ __forceinline__ void plan_build(int grp, PlanSmem& s, const Plan& pla
 namespace ssa {
 
 // decode.cu: the plan pointers and geometry of a decode step at `pos` in the
-// decode workspace ws, and the attend + merge launches of a step whose plan
-// an earlier kernel on the stream has built.
+// decode workspace ws, and the attend + merge launches (16-bit or 8-bit
+// cache) of a step whose plan an earlier kernel on the stream has built.
 void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo);
 cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,
                                          float* lse, const dplan::Plan& plan, const dplan::Geo& geo,
                                          uint32_t* err, cudaStream_t st);
+cudaError_t launch_attend_decode_q8_planned(const Problem& pr, const void* Q, const int8_t* Kq, const float* Ks,
+                                            const int8_t* Vq, const float* Vs, void* O, float* lse,
+                                            const dplan::Plan& plan, const dplan::Geo& geo, uint32_t* err,
+                                            cudaStream_t st);
 
 }  // namespace ssa

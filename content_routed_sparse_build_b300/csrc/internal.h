@@ -118,6 +118,9 @@ cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, 
 // the attend kernel's tail -- two launches.
 cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, const float* summ, const void* K,
                                const void* V, int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos, const float* summ,
+                                  const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
+                                  int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
 
 // Prefill attention fast path (16-bit types): dispatch, span tiles, merge.
 size_t prefill_ws_bytes(const Problem& pr, int64_t n_q);

@@ -244,6 +244,26 @@ int ssa_attend_decode_q8(const ssa_params* p, const void* Q, int64_t pos, const 
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const float* summ, const int8_t* Kq,
+                       const float* Ks, const int8_t* Vq, const float* Vs, int32_t* sel, void* O, float* lse,
+                       void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.d != 128 || pr.L_cap % 32 != 0 || (pr.dtype != SSA_BF16 && pr.dtype != SSA_F16) ||
+      !decode_fast_supported(pr))
+    return SSA_ERR_UNSUPPORTED;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !summ || !Kq || !Ks || !Vq || !Vs || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(summ) || !aligned16(Kq) || !aligned16(Ks) || !aligned16(Vq) ||
+      !aligned16(Vs) || !aligned16(O))
+    return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  return cuda_status(launch_decode_step_q8(pr, Q, pos, summ, Kq, Ks, Vq, Vs, sel, O, lse, ws,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int ssa_workspace_error(void* ws, uint32_t* bits, void* stream) {
   if (!ws) return SSA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

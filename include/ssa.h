@@ -169,10 +169,10 @@ SSA_API int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, c
  * those two calls in sequence: sel [B, Hq, topk] receives the selections,
  * O [B, Hq, d] and lse [B, Hq] (nullable) the outputs; ws as for
  * ssa_attend_decode (ssa_workspace_size(p, 1, SSA_OP_DECODE) bytes).
- * On the 16-bit fast path the step is two kernel launches instead of the
- * separate calls' four: the route kernel also builds the attend plan, and
- * the attend kernel merges the partial outputs in its tail.  Other shapes
- * (fp32) run the two calls' kernels in sequence.
+ * On the 16-bit fast path the step is three kernel launches instead of the
+ * separate calls' four: the route kernel's cluster also builds the attend
+ * plan, then the split attention and the log-sum-exp merge run.  Other
+ * shapes (fp32) run the two calls' kernels in sequence.
  * Requires 0 <= pos < L; summaries of spans 0 .. floor(pos / S) - 1 built.
  */
 SSA_API int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
@@ -274,6 +274,20 @@ SSA_API int ssa_build_summaries_q8(const ssa_params* p, const int8_t* Kq, const 
 SSA_API int ssa_attend_decode_q8(const ssa_params* p, const void* Q, int64_t pos, const int8_t* Kq,
                                  const float* Ks, const int8_t* Vq, const float* Vs, const int32_t* sel,
                                  void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One whole decode step over the 8-bit cache: ssa_route with n_q = 1 at
+ * q_pos0 = pos, then ssa_attend_decode_q8 on its selections, in three kernel
+ * launches (the route kernel's cluster also builds the attend plan).  Same
+ * arguments, layouts, requirements and results as those two calls in
+ * sequence: summ are the fp32 summaries (ssa_build_summaries_q8), sel
+ * [B, Hq, topk] receives the selections, O [B, Hq, d] and lse [B, Hq]
+ * (nullable) the outputs.  Returns SSA_ERR_UNSUPPORTED where
+ * ssa_attend_decode_q8 does.
+ */
+SSA_API int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
+                               const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
+                               int32_t* sel, void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Cache snapshots (superlinear release post, geeks.co.kr/post/2077, "why

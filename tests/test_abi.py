@@ -136,6 +136,19 @@ def test_q8_validation():
     assert d(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
     assert d(ssa.params(1, 8, 2, 64, 4096, 64, 8, torch.bfloat16), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
     assert d(ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.float32), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    # the fused 8-bit step takes what the 8-bit attention takes, plus the summaries
+    L.ssa_decode_step_q8.argtypes = [ctypes.POINTER(ssa.ssa_params), P, I8, P, P, P, P, P, P, P, P, P,
+                                     ctypes.c_size_t, P]
+    st = lambda p, pos, ws, n, **kw: L.ssa_decode_step_q8(
+        ctypes.byref(p), FAKE, pos, kw.get("summ", FAKE), FAKE, FAKE, FAKE, FAKE, kw.get("sel", FAKE), FAKE, None,
+        ws, n, None)
+    assert st(p, 4096, FAKE, need) == ssa.SSA_ERR_INVALID_ARG         # pos == L
+    assert st(p, 10, FAKE, need, summ=None) == ssa.SSA_ERR_INVALID_ARG
+    assert st(p, 10, FAKE, need, sel=None) == ssa.SSA_ERR_INVALID_ARG
+    assert st(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
+    assert st(p, 10, FAKE, need - 1) == ssa.SSA_ERR_WORKSPACE
+    assert st(ssa.params(1, 8, 2, 64, 4096, 64, 8, torch.bfloat16), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    assert st(ssa.params(1, 8, 2, 128, 4001, 64, 8, torch.bfloat16), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
 
 
 @needs_no_gpu

@@ -167,6 +167,10 @@ def test_decode_q8_matches_oracle_on_the_dequantised_cache(w):
         lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
         ssa.ssa_route(p, q, 1, pos, summ, sel)
         ssa.ssa_attend_decode_q8(p, q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+        # the fused step takes the same decisions and gives the same bits
+        sel2, O2, lse2 = torch.empty_like(sel), torch.empty_like(O), torch.empty_like(lse)
+        ssa.ssa_decode_step_q8(p, q, pos, summ, Kq, Ks, Vq, Vs, sel2, O2, lse2, ws)
+        assert torch.equal(sel2, sel) and torch.equal(O2, O) and torch.equal(lse2, lse), pos
         qh = Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous()
         sel_o, _ = oracle.route(qh, pos, summ_o, w.Hkv, w.S, w.topk)
         assert np.array_equal(sel.reshape(-1, w.topk).cpu().numpy(), sel_o), pos
@@ -183,7 +187,8 @@ def test_q8_entry_points_reject_what_they_do_not_take():
     sel = torch.zeros(64, dtype=torch.int32, device="cuda")
     p = ssa.params(1, 8, 2, 128, 100, 64, 4, torch.bfloat16, L_cap=100)     # L_cap not a multiple of 32
     for call in (lambda: ssa.ssa_quantize_kv(p, t, t, 0, 10, i8, f, i8, f),
-                 lambda: ssa.ssa_attend_decode_q8(p, t, 5, i8, f, i8, f, sel, t, None, None)):
+                 lambda: ssa.ssa_attend_decode_q8(p, t, 5, i8, f, i8, f, sel, t, None, None),
+                 lambda: ssa.ssa_decode_step_q8(p, t, 5, f, i8, f, i8, f, sel, t, None, None)):
         with pytest.raises(ssa.SSAError) as e:
             call()
         assert e.value.status == ssa.SSA_ERR_UNSUPPORTED
@@ -244,6 +249,10 @@ def test_decode_q8_1m_sampled_steps():
         lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         ssa.ssa_route(p, q, 1, pos, summ, sel)
         ssa.ssa_attend_decode_q8(p, q, pos, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+        # the fused step takes the same decisions and gives the same bits
+        sel2, O2, lse2 = torch.empty_like(sel), torch.empty_like(O), torch.empty_like(lse)
+        ssa.ssa_decode_step_q8(p, q, pos, summ, Kq, Ks, Vq, Vs, sel2, O2, lse2, ws)
+        assert torch.equal(sel2, sel) and torch.equal(O2, O) and torch.equal(lse2, lse), pos
         qh = Q[s].reshape(w.B, w.Hq, 1, w.d).contiguous()
         sel_o, _ = oracle.route(qh, pos, summ_o, w.Hkv, w.S, w.topk)
         assert np.array_equal(sel.reshape(-1, w.topk).cpu().numpy(), sel_o), pos
