@@ -14,19 +14,19 @@
 //  count    per (b, query head, 128 queries): validates sel rows and counts
 //           each bucket's rows (shared-memory histogram, one global atomic
 //           per non-empty bucket)
-//  scan     one CTA: bucket offsets, the tile table (span tiles, then local
-//           tiles)
+//  scan     one CTA: bucket offsets, the table of tile pairs (span pairs,
+//           then local pairs): two tiles of 128 rows that share one key range
 //  scatter  writes each row's id and its rank in the sel row into its
 //           bucket
-//  attend   persistent, one CTA per SM, eleven warps.  A loader warp
-//           gathers each tile's 128 query rows into one of two Q buffers
-//           (128-byte swizzled K-major operand) ahead of use; a TMA warp
-//           streams key / value blocks of 128 tokens through their own
-//           rings; one thread issues tcgen05.mma: S = Q K^T into tensor
-//           memory (double buffered), then O += P V with P read from tensor
-//           memory.  Eight softmax warps (two per row quarter, one row per
-//           thread, each warp half of the keys) turn S into P = 2^(S c - m)
-//           (16-bit, double buffered in tensor memory), rescale O only when
+//  attend   persistent, one CTA per SM, twelve warps, one pair at a time.
+//           Two loader warps gather the pair's query rows into 128-byte
+//           swizzled K-major Q buffers ahead of use (tile A's double
+//           buffered); a TMA warp streams the shared key / value blocks of
+//           128 tokens through a four-slot ring; one thread issues
+//           tcgen05.mma, alternating the tiles: S = Q K^T into tensor
+//           memory, then O += P V with P read from tensor memory.  Eight
+//           softmax warps (four per tile, one row per thread) turn S into
+//           P = 2^(S c - m) (16-bit, written over S), rescale O only when
 //           the running maximum grows by more than 2^8, and end each tile
 //           by writing one partial (m, l, normalised o) per row.
 //  merge    per (b, head, query): combines the row's partials (its spans in

@@ -10,7 +10,7 @@
 // of the dimension, never on the span's position in a tile, so spans with
 // identical summaries get identical scores and tie exactly.  Scores never
 // leave the chip: each kernel keeps, per query row, a running list of its
-// best k (score, span) pairs in shared memory.
+// best (score, span) pairs in registers or shared memory.
 #include <cooperative_groups.h>
 
 #include "decode_plan.cuh"
