@@ -648,16 +648,26 @@ class PrefillBench:
             ssa.ssa_build_summaries(pre, self.K, 0, self.j0, self.summ)
 
     def step(self, ev=None):
+        """One chunk; ev (optional): three events, recorded before the route,
+        before the attend path and at the end."""
         w = self.w
         ssa.ssa_build_summaries(self.p, self.K, self.j0, self.j1, self.summ, self.stream)
+        if ev is not None:
+            ev[0].record(self.stream)
         ssa.ssa_route(self.p, self.Q, w.n_q, w.q_pos0, self.summ, self.sel, None, self.ws_route,
                       self.stream)
         if ev is not None:
-            ev[0].record(self.stream)
+            ev[1].record(self.stream)
         ssa.ssa_attend_prefill(self.p, self.Q, w.n_q, w.q_pos0, self.K, self.V, self.sel, self.O,
                                self.lse, self.ws, self.stream)
         if ev is not None:
-            ev[1].record(self.stream)
+            ev[2].record(self.stream)
+
+    def route_flops(self):
+        """2 * d FLOP per candidate span per (query, head): the scores the router must compute."""
+        w = self.w
+        cand = (w.q_pos0 + np.arange(w.n_q)) // w.S
+        return float(2 * w.d * w.B * w.Hq * cand.sum())
 
     def flops(self):
         w = self.w
@@ -743,8 +753,7 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush, cpu_leg):
     fl = pb.flops()
     for _ in range(warmup):
         pb.step()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     tot = 0.0
     barrier(ws_n)
     torch.cuda.synchronize()
@@ -757,7 +766,9 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush, cpu_leg):
         torch.cuda.synchronize()
         tot += a.elapsed_time(b)
     barrier(ws_n)
-    attend_ms = sum(x.elapsed_time(y) for x, y in evs) / steps
+    route_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    attend_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    rfl = pb.route_flops()
     ms = max_over_ranks(tot / steps, ws_n)
     err = ssa.ssa_workspace_error(pb.ws)
     tr, tr_src = traffic_of(w.name)
@@ -768,6 +779,10 @@ def bench_prefill(w, dev, steps, warmup, ws_n, flush, cpu_leg):
         "roofline": tensor_roofline(fl, ms, "whole chunk: summaries + route + attend (4*d FLOP per attended "
                                             "token per query head over the selected spans and the local span)"),
         "attend_roofline": tensor_roofline(fl, attend_ms, "attend path alone (dispatch + attend + merge)", tr, tr_src),
+        "route_ms": route_ms,
+        "route_roofline": tensor_roofline(rfl, route_ms, "route alone (split + tensor-core scores + top-k): "
+                                                         "2*d FLOP per candidate span per query head; the split "
+                                                         "summaries make the tensor cores issue 3x that"),
         "selected_span_tflop_per_step": fl / 1e12,
         "device_error_bits": err,
     }
