@@ -1,0 +1,155 @@
+"""Edge cases of the CUDA path against the oracle: exact score ties on a
+large scale, the first positions of a cache, and an empty chunk.
+
+Ties.  With integer keys and queries every summary is a multiple of 1/S and
+every score is exact in fp32 as in double, so the GPU and the oracle see
+the same scores and equal scores must resolve the same way (the lower span
+first).  A cache whose spans repeat with a period P makes ties the rule:
+every span of one residue class mod P has the same summary, so a query's
+best k are the lowest spans of its best residues.  A query of zeros scores
+every span 0, so its k best are spans 0 .. k-1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import content_routed_sparse_build_b300 as ssa
+import oracle
+from synth import workloads as W
+
+from harness import LSE_TOL, TOL, GpuRun, max_abs
+
+pytestmark = pytest.mark.gpu
+
+BF16 = torch.bfloat16
+
+
+def _periodic_cache(B, Hkv, L, d, S, P, seed):
+    """Integer K (values -2..2) whose span j equals span j mod P; normal V."""
+    rng = np.random.default_rng(seed)
+    base = rng.integers(-2, 3, (B, Hkv, P * S, d)).astype(np.float32)
+    reps = -(-L // (P * S))
+    K = np.tile(base, (1, 1, reps, 1))[:, :, :L]
+    V = rng.standard_normal((B, Hkv, L, d)).astype(np.float32)
+    return torch.from_numpy(K).to(BF16), torch.from_numpy(V).to(BF16)
+
+
+def _int_queries(shape, seed):
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(rng.integers(-1, 2, shape).astype(np.float32)).to(BF16)
+
+
+@pytest.mark.parametrize("topk", [16, 64])
+def test_decode_periodic_cache_ties(topk):
+    B, Hq, Hkv, d, S, P = 1, 16, 2, 128, 64, 5
+    L = 64 * 300 + 17
+    n = 4
+    K, V = _periodic_cache(B, Hkv, L, d, S, P, seed=31)
+    Q = _int_queries((n, B, Hq, d), seed=32)
+    w = W.Workload("ties_decode", "decode", B, Hq, Hkv, d, L, S, topk, BF16, n_q=n, q_pos0=L - n, chunk=1)
+    summ = oracle.summaries(K, L, S)
+    sel_o = np.stack([oracle.route(Q[s].reshape(B, Hq, 1, d).contiguous(), w.q_pos0 + s, summ, Hkv, S, topk)[0]
+                      for s in range(n)])
+    run = GpuRun(w, Q, K, V)
+    run.summaries()
+    for fused in (False, True):
+        sel_g, O_g, lse_g, err = run.decode(fused=fused)
+        assert err == 0
+        assert np.array_equal(sel_g, sel_o)
+    for s in range(n):
+        O_o, lse_o, _ = oracle.attend(Q[s].reshape(B, Hq, 1, d).contiguous(), K, V, w.q_pos0 + s, S, sel_o[s])
+        assert max_abs(O_g[s], O_o) <= TOL[BF16]
+        assert max_abs(lse_g[s], lse_o) <= LSE_TOL[BF16]
+
+
+def test_prefill_periodic_cache_ties():
+    """The tensor-core router (k <= 16) and the span-major attention."""
+    B, Hq, Hkv, d, S, P, topk = 1, 8, 2, 128, 64, 7, 16
+    L = 64 * 200
+    n = 512
+    K, V = _periodic_cache(B, Hkv, L, d, S, P, seed=33)
+    Q = _int_queries((B, Hq, n, d), seed=34)
+    w = W.Workload("ties_prefill", "prefill", B, Hq, Hkv, d, L, S, topk, BF16, n_q=n, q_pos0=L - n, chunk=n)
+    summ = oracle.summaries(K, L, S)
+    sel_o, _ = oracle.route(Q, L - n, summ, Hkv, S, topk)
+    run = GpuRun(w, Q, K, V)
+    sel_g, O_g, lse_g, err = run.prefill()
+    assert err == 0
+    assert np.array_equal(sel_g, sel_o)
+    O_o, lse_o, _ = oracle.attend(Q, K, V, L - n, S, sel_o)
+    assert max_abs(O_g, O_o) <= TOL[BF16]
+    assert max_abs(lse_g, lse_o) <= LSE_TOL[BF16]
+
+
+def test_zero_queries_take_the_lowest_spans():
+    B, Hq, Hkv, d, S, topk = 1, 8, 2, 128, 64, 16
+    L = 64 * 100 + 5
+    rng = np.random.default_rng(35)
+    K = torch.from_numpy(rng.standard_normal((B, Hkv, L, d)).astype(np.float32)).to(BF16)
+    V = torch.from_numpy(rng.standard_normal((B, Hkv, L, d)).astype(np.float32)).to(BF16)
+    # decode
+    n = 3
+    Qd = torch.zeros((n, B, Hq, d), dtype=BF16)
+    wd = W.Workload("zero_q_decode", "decode", B, Hq, Hkv, d, L, S, topk, BF16, n_q=n, q_pos0=L - n, chunk=1)
+    run = GpuRun(wd, Qd, K, V)
+    run.summaries()
+    want = np.broadcast_to(np.arange(topk, dtype=np.int32), (n, B * Hq, topk))
+    for fused in (False, True):
+        sel_g, O_g, lse_g, err = run.decode(fused=fused)
+        assert err == 0
+        assert np.array_equal(sel_g, want)
+    O_o, lse_o, _ = oracle.attend(Qd[0].reshape(B, Hq, 1, d).contiguous(), K, V, L - n, S, want[0])
+    assert max_abs(O_g[0], O_o) <= TOL[BF16]
+    # prefill chunk (tensor-core router)
+    m = 256
+    Qp = torch.zeros((B, Hq, m, d), dtype=BF16)
+    wp = W.Workload("zero_q_prefill", "prefill", B, Hq, Hkv, d, L, S, topk, BF16, n_q=m, q_pos0=L - m, chunk=m)
+    sel_p, O_p, lse_p, err = GpuRun(wp, Qp, K, V).prefill()
+    assert err == 0
+    assert np.array_equal(sel_p, np.broadcast_to(np.arange(topk, dtype=np.int32), sel_p.shape))
+
+
+@pytest.mark.parametrize("pos", [0, 1, 63, 64, 65, 127])
+def test_first_positions(pos):
+    """Decode at the start of a cache: no candidate at all (pos < S), then
+    one complete span with a one-token local span (pos = S)."""
+    B, Hq, Hkv, d, S, topk = 1, 8, 2, 128, 64, 4
+    L = pos + 1
+    rng = np.random.default_rng(36 + pos)
+    K = torch.from_numpy(rng.standard_normal((B, Hkv, L, d)).astype(np.float32)).to(BF16)
+    V = torch.from_numpy(rng.standard_normal((B, Hkv, L, d)).astype(np.float32)).to(BF16)
+    Q = torch.from_numpy(rng.standard_normal((1, B, Hq, d)).astype(np.float32)).to(BF16)
+    w = W.Workload("first_positions", "decode", B, Hq, Hkv, d, L, S, topk, BF16, n_q=1, q_pos0=pos, chunk=1)
+    summ = oracle.summaries(K, L, S)
+    q4 = Q[0].reshape(B, Hq, 1, d).contiguous()
+    sel_o, _ = oracle.route(q4, pos, summ, Hkv, S, topk)
+    O_o, lse_o, _ = oracle.attend(q4, K, V, pos, S, sel_o)
+    run = GpuRun(w, Q, K, V)
+    run.summaries()
+    for fused in (False, True):
+        sel_g, O_g, lse_g, err = run.decode(fused=fused)
+        assert err == 0
+        assert np.array_equal(sel_g[0], sel_o)
+        assert max_abs(O_g[0], O_o) <= TOL[BF16]
+        assert max_abs(lse_g[0], lse_o) <= LSE_TOL[BF16]
+    if pos == 0:
+        # one token: the output is its value row
+        assert max_abs(O_g[0], V[0, np.arange(Hq) // (Hq // Hkv), 0]) <= TOL[BF16]
+
+
+def test_empty_chunk_is_a_no_op():
+    B, Hq, Hkv, d, S, topk = 1, 8, 2, 128, 64, 4
+    L = 256
+    p = ssa.params(B, Hq, Hkv, d, L, S, topk, BF16)
+    dev = torch.device("cuda")
+    Q = torch.zeros((B, Hq, 1, d), dtype=BF16, device=dev)
+    K = torch.zeros((B, Hkv, L, d), dtype=BF16, device=dev)
+    summ = torch.zeros((B, Hkv, L // S, d), dtype=torch.float32, device=dev)
+    sel = torch.full((B, Hq, 1, topk), 7, dtype=torch.int32, device=dev)
+    O = torch.full((B, Hq, 1, d), 3.0, dtype=BF16, device=dev)
+    ws = ssa.workspace(p, 1, ssa.SSA_OP_PREFILL, dev)
+    ssa.ssa_route(p, Q, 0, 10, summ, sel, None, ssa.workspace(p, 1, ssa.SSA_OP_ROUTE, dev))
+    ssa.ssa_attend_prefill(p, Q, 0, 10, K, K, sel, O, None, ws)
+    torch.cuda.synchronize()
+    assert ssa.ssa_workspace_error(ws) == 0
+    assert bool((sel == 7).all()) and bool((O == 3.0).all())

@@ -45,6 +45,11 @@ DECODE_CASES = [
     # the union positions come from its binary-search path
     W.Workload("case_decode_bf16_many_spans", "decode", 1, 8, 1, 64, 16500 * 64, 64, 8, BF16,
                n_q=2, q_pos0=16500 * 64 - 2, chunk=1, seed=25),
+    # k above 32: the decode router's 64-entry lists
+    W.Workload("case_decode_bf16_k64", "decode", 1, 16, 2, 128, 300 * 256 + 50, 256, 64, BF16,
+               n_q=3, q_pos0=300 * 256 + 47, chunk=1, needles=4, seed=26),
+    W.Workload("case_decode_f16_d64_g16_k40", "decode", 1, 16, 1, 64, 200 * 64 + 10, 64, 40, F16,
+               n_q=3, q_pos0=200 * 64 + 7, chunk=1, seed=27),
 ]
 
 
@@ -78,8 +83,9 @@ def test_decode_parity(w):
 
 @pytest.mark.parametrize("w", DECODE_CASES, ids=lambda w: w.name)
 def test_decode_step_parity(w):
-    """ssa_decode_step (route with the plan built in its cluster, attend with
-    the merges in its tail) against the oracle and against the two calls."""
+    """ssa_decode_step (route with the plan built in its cluster, then the
+    split attention and the merge) against the oracle and against the two
+    calls."""
     inp, Q, K, orc, sel_o, margin, redrawn = margin_checked_inputs(w)
     V = inp.v()
     run = GpuRun(w, Q, K, V)
