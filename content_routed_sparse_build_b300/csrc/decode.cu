@@ -72,7 +72,7 @@ int chunk_tokens(const Problem& pr, int n_warps_total) {
 }
 
 struct Layout {
-  size_t n_union, n_items, span, mask, rank, counter, ml, po, total;
+  size_t n_union, n_items, span, mask, rank, counter, ml, po, q, total;
   int C, CH;
 };
 
@@ -92,6 +92,7 @@ Layout layout(const Problem& pr) {
   l.counter = off; off = align256(off + 4);
   l.ml = off; off = align256(off + parts * 2 * 4);
   l.po = off; off = align256(off + parts * (size_t)pr.d * 4);
+  l.q = off; off = align256(off + (size_t)pr.B * pr.Hq * pr.d * 2);
   l.total = off;
   return l;
 }
@@ -949,6 +950,7 @@ void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
   plan.counter = reinterpret_cast<int*>(w8 + lay.counter);
   plan.ml = reinterpret_cast<float*>(w8 + lay.ml);
   plan.po = reinterpret_cast<float*>(w8 + lay.po);
+  plan.q = reinterpret_cast<uint16_t*>(w8 + lay.q);
   geo.Hq = pr.Hq;
   geo.Hkv = pr.Hkv;
   geo.g = pr.g;

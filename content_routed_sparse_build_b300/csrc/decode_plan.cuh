@@ -39,6 +39,7 @@ struct Plan {
   int* counter;       // work-item counter of the attend kernel
   float* ml;          // [B*Hq][topk+1][C][2]  (m, l) per partial, base-2 m
   float* po;          // [B*Hq][topk+1][C][D]  unnormalised partial outputs
+  uint16_t* q;        // [B*Hq][D]  the step's 16-bit queries, copied by the route of a whole step
 };
 
 struct Geo {

@@ -193,6 +193,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
 #pragma unroll
     for (int u = 0; u < (G * D / V + 255) / 256; ++u)
       if (tid + 256 * u < nvec) raw[u] = qsrc[tid + 256 * u];
+    if constexpr (PLAN && DT != DT_F32) {
+      // the attend kernel reads the step's queries from this device copy, so
+      // that Q may also be page-locked host memory read once over the link
+      if (rank == 0) {
+        uint4* qdst = reinterpret_cast<uint4*>(plan.q + (int64_t)(b * Hq + kvh * g) * D);
+#pragma unroll
+        for (int u = 0; u < (G * D / V + 255) / 256; ++u)
+          if (tid + 256 * u < nvec) qdst[tid + 256 * u] = raw[u];
+      }
+    }
 #pragma unroll
     for (int u = 0; u < (G * D / V + 255) / 256; ++u) {
       const int x = tid + 256 * u;
@@ -537,7 +547,7 @@ cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, co
     e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
                             : decode_route_g<DT_F16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
   if (e != cudaSuccess) return e;
-  return launch_attend_decode_planned(pr, Q, K, V, O, lse, plan, geo, ws_error(ws), st);
+  return launch_attend_decode_planned(pr, plan.q, K, V, O, lse, plan, geo, ws_error(ws), st);
 }
 
 cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos, const float* summ,
@@ -550,7 +560,7 @@ cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos,
                             ? decode_route_g<DT_BF16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
                             : decode_route_g<DT_F16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
   if (e != cudaSuccess) return e;
-  return launch_attend_decode_q8_planned(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, ws_error(ws), st);
+  return launch_attend_decode_q8_planned(pr, plan.q, Kq, Ks, Vq, Vs, O, lse, plan, geo, ws_error(ws), st);
 }
 
 cudaError_t launch_route(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,

@@ -45,6 +45,20 @@ constexpr int kVersion = 100;  // 0.1.0
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A pointer the kernels may dereference: device or managed memory, or
+// page-locked host memory mapped into the device's address space at the same
+// address (unified addressing).  Null passes (optional arguments).
+bool device_accessible(const void* p) {
+  if (!p) return true;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SSA_OK : SSA_ERR_CUDA; }
 
 // The tensor-core prefill path takes 16-bit inputs whose row ids fit its
@@ -172,8 +186,12 @@ int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, const float
   rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
   if (rc != SSA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (decode_fast_supported(pr))
+  if (decode_fast_supported(pr)) {
+    // Q, sel, O and lse may live in mapped page-locked host memory
+    if (!device_accessible(Q) || !device_accessible(sel) || !device_accessible(O) || !device_accessible(lse))
+      return SSA_ERR_INVALID_ARG;
     return cuda_status(launch_decode_step(pr, Q, pos, summ, K, V, sel, O, lse, ws, st));
+  }
   // fp32 (or shapes the fast path does not take): the two calls in sequence
   rc = cuda_status(launch_route(pr, Q, 1, pos, summ, sel, nullptr, st));
   if (rc != SSA_OK) return rc;
@@ -260,6 +278,8 @@ int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const fl
     return SSA_ERR_INVALID_ARG;
   rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
   if (rc != SSA_OK) return rc;
+  if (!device_accessible(Q) || !device_accessible(sel) || !device_accessible(O) || !device_accessible(lse))
+    return SSA_ERR_INVALID_ARG;
   return cuda_status(launch_decode_step_q8(pr, Q, pos, summ, Kq, Ks, Vq, Vs, sel, O, lse, ws,
                                            static_cast<cudaStream_t>(stream)));
 }

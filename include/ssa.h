@@ -173,6 +173,12 @@ SSA_API int ssa_attend_decode(const ssa_params* p, const void* Q, int64_t pos, c
  * separate calls' four: the route kernel's cluster also builds the attend
  * plan, then the split attention and the log-sum-exp merge run.  Other
  * shapes (fp32) run the two calls' kernels in sequence.
+ * On the 16-bit fast path Q, sel, O and lse may also be page-locked host
+ * memory mapped into the device's address space (cudaHostAlloc or
+ * cudaHostRegister under unified addressing): the route kernel reads Q once
+ * and keeps a copy in ws for the attention, and sel, O and lse are written
+ * in place, so a step needs no separate copies.  Any other host pointer
+ * there is SSA_ERR_INVALID_ARG.
  * Requires 0 <= pos < L; summaries of spans 0 .. floor(pos / S) - 1 built.
  */
 SSA_API int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
@@ -283,7 +289,8 @@ SSA_API int ssa_attend_decode_q8(const ssa_params* p, const void* Q, int64_t pos
  * sequence: summ are the fp32 summaries (ssa_build_summaries_q8), sel
  * [B, Hq, topk] receives the selections, O [B, Hq, d] and lse [B, Hq]
  * (nullable) the outputs.  Returns SSA_ERR_UNSUPPORTED where
- * ssa_attend_decode_q8 does.
+ * ssa_attend_decode_q8 does.  Q, sel, O and lse may be mapped page-locked
+ * host memory as for ssa_decode_step.
  */
 SSA_API int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
                                const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,

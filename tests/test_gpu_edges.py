@@ -153,3 +153,50 @@ def test_empty_chunk_is_a_no_op():
     torch.cuda.synchronize()
     assert ssa.ssa_workspace_error(ws) == 0
     assert bool((sel == 7).all()) and bool((O == 3.0).all())
+
+
+@pytest.mark.parametrize("q8", [False, True])
+def test_decode_step_with_mapped_host_buffers(q8):
+    """The one-call steps take page-locked host Q, sel, O and lse directly
+    (the route reads Q once over the link, the merge writes O in place) and
+    give the same bits as with device buffers; pageable host memory is
+    refused before anything is launched."""
+    w = W.DECODE_1M.with_(name="host_buffers", L=1 << 18, q_pos0=(1 << 18) - 4, n_q=4)
+    inp = W.Inputs(w)
+    dev = torch.device("cuda")
+    K, V = inp.k(dev), inp.v(dev)
+    Q = inp.q()
+    p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
+    summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
+    ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE, dev)
+    if q8:
+        Kq, Ks, Vq, Vs = ssa.q8_cache(p, dev)
+        ssa.ssa_quantize_kv(p, K, V, 0, w.L, Kq, Ks, Vq, Vs)
+        ssa.ssa_build_summaries_q8(p, Kq, Ks, 0, w.n_spans, summ)
+
+        def step(q, pos, sel, O, lse):
+            ssa.ssa_decode_step_q8(p, q, pos, summ, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+    else:
+        ssa.ssa_build_summaries(p, K, 0, w.n_spans, summ)
+
+        def step(q, pos, sel, O, lse):
+            ssa.ssa_decode_step(p, q, pos, summ, K, V, sel, O, lse, ws)
+    for s in range(w.n_q):
+        pos = w.q_pos0 + s
+        qd = Q[s].to(dev)
+        sel_d = torch.empty((w.B, w.Hq, 1, w.topk), dtype=torch.int32, device=dev)
+        O_d = torch.empty((w.B, w.Hq, w.d), dtype=w.dtype, device=dev)
+        lse_d = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        step(qd, pos, sel_d, O_d, lse_d)
+        qh = Q[s].contiguous().pin_memory()
+        sel_h = torch.empty(sel_d.shape, dtype=torch.int32).pin_memory()
+        O_h = torch.empty(O_d.shape, dtype=w.dtype).pin_memory()
+        lse_h = torch.empty(lse_d.shape, dtype=torch.float32).pin_memory()
+        step(qh, pos, sel_h, O_h, lse_h)
+        torch.cuda.synchronize()
+        assert torch.equal(sel_h, sel_d.cpu()) and torch.equal(O_h, O_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    assert ssa.ssa_workspace_error(ws) == 0
+    # pageable host memory: an argument error, nothing launched
+    with pytest.raises(ssa.SSAError) as e:
+        step(Q[0].contiguous(), w.q_pos0, sel_d, O_d, lse_d)
+    assert e.value.status == ssa.SSA_ERR_INVALID_ARG
