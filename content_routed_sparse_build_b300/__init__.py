@@ -20,6 +20,8 @@ Entry points (same names as the C ABI):
                        the cache rows and summaries of a session, to and from a file
   ssa_workspace_size / ssa_workspace_error / ssa_status_string
   ssa_attend_path      which implementation an attention call takes
+  ssa_selftest_wait_timeout
+                       a bounded wait run out on purpose: the status path of every kernel
 """
 from __future__ import annotations
 
@@ -277,6 +279,16 @@ def ssa_attend_decode_q8(p: ssa_params, Q: torch.Tensor, pos: int, Kq: torch.Ten
     wp, wn = _ws_args(ws)
     _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(Kq), _ptr(Ks), _ptr(Vq), _ptr(Vs), _ptr(sel), _ptr(O),
              _ptr(lse), wp, wn, _stream(stream)), "ssa_attend_decode_q8")
+
+
+def ssa_selftest_wait_timeout(limit_ns: int, ws: torch.Tensor, stream=None) -> None:
+    """Runs the bounded-wait self test: a wait on a barrier nothing completes
+    gives up after limit_ns and records SSA_DEVERR_WAIT_TIMEOUT in ws."""
+    f = lib().ssa_selftest_wait_timeout
+    f.argtypes = [ctypes.c_uint64, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(int(limit_ns), wp, wn, _stream(stream)), "ssa_selftest_wait_timeout")
 
 
 def ssa_decode_step_q8(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor, Kq: torch.Tensor,

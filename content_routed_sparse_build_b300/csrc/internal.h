@@ -121,6 +121,7 @@ cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, co
 cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos, const float* summ,
                                   const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
                                   int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 // Prefill attention fast path (16-bit types): dispatch, span tiles, merge.
 size_t prefill_ws_bytes(const Problem& pr, int64_t n_q);

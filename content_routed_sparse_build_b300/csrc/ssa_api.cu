@@ -284,6 +284,12 @@ int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const fl
                                            static_cast<cudaStream_t>(stream)));
 }
 
+int ssa_selftest_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  if (limit_ns > 1000000000ull) return SSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kWsHeader) return SSA_ERR_WORKSPACE;
+  return cuda_status(launch_wait_selftest(ws_error(ws), limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
 int ssa_workspace_error(void* ws, uint32_t* bits, void* stream) {
   if (!ws) return SSA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -401,6 +401,18 @@ SSA_API size_t ssa_workspace_size(const ssa_params* p, int64_t n_q, int op);
  */
 SSA_API int ssa_workspace_error(void* ws, uint32_t* bits, void* stream);
 
+/*
+ * Diagnostic with no counterpart in the pages: one thread waits limit_ns
+ * nanoseconds (at most 1 s) on a barrier that nothing completes, as the
+ * library's kernels wait for their bulk copies and tensor-core work, gives
+ * up, ORs SSA_DEVERR_WAIT_TIMEOUT into the error record of ws (ws_bytes >=
+ * 256) and returns; no copy or tensor-core work is in flight.  It shows that
+ * a wait that runs out comes back as a status the host reads
+ * (ssa_workspace_error) and leaves the context usable.  SSA_ERR_INVALID_ARG
+ * above 1 s; SSA_ERR_WORKSPACE for a missing or short ws.
+ */
+SSA_API int ssa_selftest_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+
 /* Static text for a status code (never NULL). */
 SSA_API const char* ssa_status_string(int status);
 

@@ -187,3 +187,12 @@ def test_attend_path_reports_the_implementation():
     # invalid parameters, other ops
     assert ssa.ssa_attend_path(P(d=96), 1, ssa.SSA_OP_DECODE) == ssa.SSA_PATH_INVALID
     assert ssa.ssa_attend_path(P(), 1, ssa.SSA_OP_ROUTE) == ssa.SSA_PATH_INVALID
+
+
+@needs_no_gpu
+def test_selftest_wait_validation():
+    L = ssa.lib()
+    L.ssa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert L.ssa_selftest_wait_timeout(2_000_000_000, FAKE, 256, None) == ssa.SSA_ERR_INVALID_ARG  # above 1 s
+    assert L.ssa_selftest_wait_timeout(1000, None, 0, None) == ssa.SSA_ERR_WORKSPACE
+    assert L.ssa_selftest_wait_timeout(1000, FAKE, 255, None) == ssa.SSA_ERR_WORKSPACE
