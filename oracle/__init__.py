@@ -62,6 +62,7 @@ def _load():
         lib.oracle_attend.argtypes = [I, P, P, P, I, I, I, I64, I64, I64, I, I, I, D, P, P, I64,
                                       P, P, P]
         lib.oracle_quantize_rows.argtypes = [I, P, I64, I, P, P]
+        lib.oracle_quantize_rows4.argtypes = [I, P, I64, I, P, P]
         _lib = lib
     return _lib
 
@@ -192,6 +193,20 @@ def quantize_rows(X: torch.Tensor):
     q = np.zeros(X.shape, np.int8)
     s = np.zeros(X.shape[:-1], np.float32)
     _load().oracle_quantize_rows(_DT[X.dtype], X.data_ptr(), rows, d, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def quantize_rows4(X: torch.Tensor):
+    """4-bit rows of X [..., d]: (q int8 in [-7, 7] [..., d], scale float32 [...]).
+
+    Symmetric, one fp32 scale per row: s = max|x| / 7, q = rint(x / s)
+    clamped to [-7, 7] (0 when s == 0), every step in fp32."""
+    _host(X)
+    d = X.shape[-1]
+    rows = X.numel() // d
+    q = np.zeros(X.shape, np.int8)
+    s = np.zeros(X.shape[:-1], np.float32)
+    _load().oracle_quantize_rows4(_DT[X.dtype], X.data_ptr(), rows, d, q.ctypes.data, s.ctypes.data)
     return q, s
 
 

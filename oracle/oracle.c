@@ -331,3 +331,37 @@ void oracle_quantize_rows(int dtype, const void* X, int64_t rows, int d, int8_t*
     }
   }
 }
+
+/*
+ * 4-bit cache rows (the same quantisation plan of the SubQ release post, its
+ * 4-bit half).  The same scheme with 15 levels: symmetric, one fp32 scale
+ * per row, round to nearest even.  For each of the `rows` rows of d
+ * elements of X:
+ *   amax = max |x_i|,  s = amax / 7 (fp32 division)
+ *   q_i  = 0 if s == 0, else clamp(rint(x_i / s), -7, 7) (fp32 division)
+ * The row's dequantised value is q_i * s.
+ */
+void oracle_quantize_rows4(int dtype, const void* X, int64_t rows, int d, int8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    float amax4 = 0.f;
+    for (int c = 0; c < d; ++c) {
+      const float x = (float)load_f64(dtype, X, r * d + c);
+      const float a = fabsf(x);
+      if (a > amax4) amax4 = a;
+    }
+    const float s4 = amax4 / 7.0f;
+    scale[r] = s4;
+    for (int c = 0; c < d; ++c) {
+      int v = 0;
+      if (s4 != 0.f) {
+        const float x = (float)load_f64(dtype, X, r * d + c);
+        float t4 = rintf(x / s4);
+        if (t4 > 7.f) t4 = 7.f;
+        if (t4 < -7.f) t4 = -7.f;
+        v = (int)t4;
+      }
+      q[r * d + c] = (int8_t)v;
+    }
+  }
+}

@@ -400,6 +400,49 @@ def test_quantize_is_equivariant_under_powers_of_two():
         assert np.array_equal(s2, s1 * np.float32(2.0 ** k))
 
 
+# ---------------------------------------------------------------- 4-bit rows
+# The same scheme with 15 levels: s = max|x| / 7, q = rint(x / s) in [-7, 7].
+
+
+def test_quantize4_hand_examples():
+    # s = 7 / 7 = 1 exactly: codes are the nearest integers, ties to even
+    x = torch.tensor([[7.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.49, -6.6, -3.5]], dtype=torch.float32)
+    q, s = oracle.quantize_rows4(x)
+    assert s.tolist() == [1.0]
+    assert q.tolist() == [[7, 0, 2, 2, 0, -2, 3, -7, -4]]
+    x = torch.tensor([[0.0, 0.0], [-14.0, 1.0], [2.0, -1.0]], dtype=torch.float32)
+    q, s = oracle.quantize_rows4(x)
+    # 1 / (14 / 7) = 0.5 -> 0 (tie to even); -1 / fp32(2 / 7) is -3.4999998
+    # in fp32 (the scale rounds up), so it is no tie: -> -3
+    assert q.tolist() == [[0, 0], [-7, 0], [7, -3]]
+    assert np.float32(-1.0) / (np.float32(2.0) / np.float32(7.0)) > np.float32(-3.5)
+    assert s[0] == 0.0 and s[1] == np.float32(2.0) and s[2] == np.float32(2.0) / np.float32(7.0)
+
+
+def test_quantize4_invariants_on_random_rows():
+    g = torch.Generator().manual_seed(13)
+    for dt in (torch.float32, torch.bfloat16, torch.float16):
+        x = (torch.randn((64, 128), generator=g) * torch.rand((64, 1), generator=g) * 10).to(dt)
+        q, s = oracle.quantize_rows4(x)
+        xf = x.float().numpy().astype(np.float64)
+        amax = np.abs(xf).max(axis=1)
+        assert (np.abs(q).max(axis=1) == 7).all()
+        assert np.allclose(s, amax / 7.0, rtol=2 ** -23, atol=0)
+        err = np.abs(xf - q.astype(np.float64) * s.astype(np.float64)[:, None])
+        assert (err <= (0.5 + 7 * 2.0 ** -22) * s[:, None]).all()
+        assert ((np.sign(q) == np.sign(xf)) | (q == 0)).all()
+
+
+def test_quantize4_is_equivariant_under_powers_of_two():
+    g = torch.Generator().manual_seed(14)
+    x = torch.randn((16, 64), generator=g)
+    q1, s1 = oracle.quantize_rows4(x)
+    for k in (-3, 5):
+        q2, s2 = oracle.quantize_rows4(x * 2.0 ** k)
+        assert np.array_equal(q1, q2)
+        assert np.array_equal(s2, s1 * np.float32(2.0 ** k))
+
+
 def test_dequantized_summaries_and_attention_accept_f64():
     g = torch.Generator().manual_seed(5)
     K = torch.randn((1, 1, 32, 4), generator=g)
