@@ -32,7 +32,6 @@ MUTANTS = {
     "quantize_scale_over_128": ("const float s = amax / 127.0f;", "const float s = amax / 128.0f;"),
     "quantize4_ties_away_from_zero": ("float t4 = rintf(x / s4);", "float t4 = roundf(x / s4);"),
     "quantize4_scale_over_8": ("const float s4 = amax4 / 7.0f;", "const float s4 = amax4 / 8.0f;"),
-    "quantize4_clamp_at_8": ("if (t4 < -7.f) t4 = -7.f;", "if (t4 < -8.f) t4 = -8.f;"),
     "values_from_keys": ("load_f64(dtype, V, (kvh * L_cap + tok[u]) * d + c)",
                          "load_f64(dtype, K, (kvh * L_cap + tok[u]) * d + c)"),
 }
