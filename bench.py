@@ -15,8 +15,8 @@ the oracle timed on the host cores (``cpu_baseline``):
   prefill_128k     the whole 128K prefill, 16 chunks of 8192
   tiny_prefill     the 4096-query fp32 case
   decode_10m       decode at a 10M-token cache
-  decode_group_shared, decode_q8   decode with one top-k per kv-head group,
-                   and over the 8-bit cache
+  decode_group_shared, decode_q8, decode_q4   decode with one top-k per
+                   kv-head group, and over the 8-bit and 4-bit caches
   dense_comparison the same shapes through dense attention (PyTorch SDPA)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -188,11 +188,12 @@ class DecodeBench:
     the cache.  A step routes one query token per head and attends it; the
     256 steps are captured once in a CUDA graph and replayed."""
 
-    def __init__(self, w: W.Workload, dev, group: bool = False, q8: bool = False):
+    def __init__(self, w: W.Workload, dev, group: bool = False, q8: bool = False, q4: bool = False):
         self.w = w
         self.dev = dev
         self.group = group                                     # group-shared selection
         self.q8 = q8                                           # attend over the 8-bit cache
+        self.q4 = q4                                           # attend over the 4-bit cache
         self.inp = W.Inputs(w)
         self.K = self.inp.k(dev)
         self.V = self.inp.v(dev)
@@ -210,10 +211,18 @@ class DecodeBench:
         if q8:
             self.Kq, self.Ks, self.Vq, self.Vs = ssa.q8_cache(self.p, dev)
             ssa.ssa_quantize_kv(self.p, self.K, self.V, 0, w.L, self.Kq, self.Ks, self.Vq, self.Vs)
+        if q4:
+            self.Kq, self.Ks, self.Vq, self.Vs = ssa.q4_cache(self.p, dev)
+            ssa.ssa_quantize_kv4(self.p, self.K, self.V, 0, w.L, self.Kq, self.Ks, self.Vq, self.Vs)
+        if q8 or q4:
+            del self.K, self.V                                 # the quantised cache is what a step reads
+            torch.cuda.empty_cache()
 
     def build_summaries(self):
         if self.q8:
             ssa.ssa_build_summaries_q8(self.p, self.Kq, self.Ks, 0, self.w.n_spans, self.summ)
+        elif self.q4:
+            ssa.ssa_build_summaries_q4(self.p, self.Kq, self.Ks, 0, self.w.n_spans, self.summ)
         else:
             ssa.ssa_build_summaries(self.p, self.K, 0, self.w.n_spans, self.summ)
 
@@ -228,6 +237,9 @@ class DecodeBench:
         if self.q8:
             ssa.ssa_attend_decode_q8(self.p, self.qs[i], self.w.q_pos0 + i, self.Kq, self.Ks, self.Vq, self.Vs,
                                      self.sels[i], self.O, self.lse, self.ws)
+        elif self.q4:
+            ssa.ssa_attend_decode_q4(self.p, self.qs[i], self.w.q_pos0 + i, self.Kq, self.Ks, self.Vq, self.Vs,
+                                     self.sels[i], self.O, self.lse, self.ws)
         else:
             ssa.ssa_attend_decode(self.p, self.qs[i], self.w.q_pos0 + i, self.K, self.V, self.sels[i],
                                   self.O, self.lse, self.ws)
@@ -237,6 +249,10 @@ class DecodeBench:
         # also plans) + attend + merge
         if self.q8:
             ssa.ssa_decode_step_q8(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.Kq, self.Ks, self.Vq,
+                                   self.Vs, self.sels[i], self.O, self.lse, self.ws)
+            return
+        if self.q4:
+            ssa.ssa_decode_step_q4(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.Kq, self.Ks, self.Vq,
                                    self.Vs, self.sels[i], self.O, self.lse, self.ws)
             return
         if not self.group:
@@ -277,7 +293,8 @@ class DecodeBench:
                 for g in range(w.Hkv):
                     u = np.unique(sel[b, g][sel[b, g] >= 0])
                     kv_rows += len(u) * w.S + (pos - ell * w.S + 1)
-            row_bytes = (2 * w.d + 8) if self.q8 else w.d * el * 2       # K + V (+ two fp32 scales)
+            # K + V (+ two fp32 scales)
+            row_bytes = (2 * w.d + 8) if self.q8 else (w.d + 8) if self.q4 else w.d * el * 2
             attend = kv_rows * row_bytes + 2 * w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
             route = w.B * w.Hkv * ell * w.d * 4 + w.B * w.Hq * w.d * el + w.B * w.Hq * w.topk * 4
             out.append((attend, route))
@@ -493,6 +510,18 @@ def bench_decode_q8(w, dev, steps, ws_n):
     out = variant_line(db, steps, ws_n, {"cache": "8-bit K / V, one fp32 scale per token row; fp32 summaries"})
     tr, tr_src = traffic_of(w.name + "_q8")
     out["roofline"]["traffic"], out["roofline"]["traffic_source"] = tr, tr_src
+    return out
+
+
+def bench_decode_q4(w, dev, steps, ws_n):
+    """The same decode workload over the 4-bit cache: a step streams the
+    same spans at d + 8 bytes per token."""
+    db = DecodeBench(w, dev, q4=True)
+    out = variant_line(db, steps, ws_n, {"cache": "4-bit K / V, one fp32 scale per token row; fp32 summaries"})
+    tr, tr_src = traffic_of(w.name + "_q4")
+    out["roofline"]["traffic"], out["roofline"]["traffic_source"] = tr, tr_src
+    del db
+    torch.cuda.empty_cache()
     return out
 
 
@@ -1027,6 +1056,8 @@ def main():
                     help="skip the decode line with group-shared selection")
     ap.add_argument("--no-q8", action="store_true",
                     help="skip the decode line over the 8-bit cache")
+    ap.add_argument("--no-q4", action="store_true",
+                    help="skip the decode line over the 4-bit cache")
     ap.add_argument("--no-10m", action="store_true",
                     help="skip the decode line with a 10M-token cache")
     ap.add_argument("--no-128k", action="store_true",
@@ -1087,6 +1118,9 @@ def main():
         torch.cuda.empty_cache()
     if not args.no_decode and not args.no_q8:
         line["decode_q8"] = bench_decode_q8(w, dev, steps, ws_n)
+        torch.cuda.empty_cache()
+    if not args.no_decode and not args.no_q4:
+        line["decode_q4"] = bench_decode_q4(w, dev, steps, ws_n)
         torch.cuda.empty_cache()
     if not args.no_decode and not args.no_10m and not small:
         d10 = bench_decode_10m(dev, steps, ws_n, cpu_leg)

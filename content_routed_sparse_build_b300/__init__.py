@@ -16,6 +16,8 @@ Entry points (same names as the C ABI):
   ssa_attend_decode_noalloc  ssa_attend_decode on a library-owned scratch block
   ssa_quantize_kv / ssa_build_summaries_q8 / ssa_attend_decode_q8 / ssa_decode_step_q8
                        the 8-bit cache: quantised rows, their summaries, decode over them
+  ssa_quantize_kv4 / ssa_build_summaries_q4 / ssa_attend_decode_q4 / ssa_decode_step_q4
+                       the same for the 4-bit cache
   ssa_snapshot_save / ssa_snapshot_load / ssa_snapshot_read_header
                        the cache rows and summaries of a session, to and from a file
   ssa_workspace_size / ssa_workspace_error / ssa_status_string
@@ -279,6 +281,61 @@ def ssa_attend_decode_q8(p: ssa_params, Q: torch.Tensor, pos: int, Kq: torch.Ten
     wp, wn = _ws_args(ws)
     _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(Kq), _ptr(Ks), _ptr(Vq), _ptr(Vs), _ptr(sel), _ptr(O),
              _ptr(lse), wp, wn, _stream(stream)), "ssa_attend_decode_q8")
+
+
+def q4_cache(p: ssa_params, device=None):
+    """Zeroed 4-bit cache tensors (Kq4, Ks, Vq4, Vs) laid out for p (d = 128,
+    L_cap a multiple of 32): Kq4 and Vq4 as int32 words [B, Hkv, L_cap / 32,
+    512], the scales fp32 [B, Hkv, L_cap]."""
+    L_cap = p.L_cap or p.L
+    if L_cap % 32 or p.d != 128:
+        raise ValueError("the 4-bit cache needs d == 128 and L_cap % 32 == 0")
+    dev = device if device is not None else torch.device("cuda")
+    Kq4 = torch.zeros((p.B, p.Hkv, L_cap // 32, 512), dtype=torch.int32, device=dev)
+    Vq4 = torch.zeros((p.B, p.Hkv, L_cap // 32, 512), dtype=torch.int32, device=dev)
+    Ks = torch.empty((p.B, p.Hkv, L_cap), dtype=torch.float32, device=dev)
+    Vs = torch.empty((p.B, p.Hkv, L_cap), dtype=torch.float32, device=dev)
+    return Kq4, Ks, Vq4, Vs
+
+
+def ssa_quantize_kv4(p: ssa_params, K: torch.Tensor, V: torch.Tensor, t_begin: int, t_end: int, Kq4: torch.Tensor,
+                     Ks: torch.Tensor, Vq4: torch.Tensor, Vs: torch.Tensor, stream=None) -> None:
+    f = lib().ssa_quantize_kv4
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _P, _I64, _I64, _P, _P, _P, _P, _P]
+    f.restype = ctypes.c_int
+    _check(f(ctypes.byref(p), _ptr(K), _ptr(V), int(t_begin), int(t_end), _ptr(Kq4), _ptr(Ks), _ptr(Vq4), _ptr(Vs),
+             _stream(stream)), "ssa_quantize_kv4")
+
+
+def ssa_build_summaries_q4(p: ssa_params, Kq4: torch.Tensor, Ks: torch.Tensor, span_begin: int, span_end: int,
+                           summ: torch.Tensor, stream=None) -> None:
+    f = lib().ssa_build_summaries_q4
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _P, _I64, _I64, _P, _P]
+    f.restype = ctypes.c_int
+    _check(f(ctypes.byref(p), _ptr(Kq4), _ptr(Ks), int(span_begin), int(span_end), _ptr(summ), _stream(stream)),
+           "ssa_build_summaries_q4")
+
+
+def ssa_attend_decode_q4(p: ssa_params, Q: torch.Tensor, pos: int, Kq4: torch.Tensor, Ks: torch.Tensor,
+                         Vq4: torch.Tensor, Vs: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
+                         lse: torch.Tensor | None, ws: torch.Tensor | None, stream=None) -> None:
+    f = lib().ssa_attend_decode_q4
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(Kq4), _ptr(Ks), _ptr(Vq4), _ptr(Vs), _ptr(sel), _ptr(O),
+             _ptr(lse), wp, wn, _stream(stream)), "ssa_attend_decode_q4")
+
+
+def ssa_decode_step_q4(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor, Kq4: torch.Tensor,
+                       Ks: torch.Tensor, Vq4: torch.Tensor, Vs: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
+                       lse: torch.Tensor | None, ws: torch.Tensor | None, stream=None) -> None:
+    f = lib().ssa_decode_step_q4
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(summ), _ptr(Kq4), _ptr(Ks), _ptr(Vq4), _ptr(Vs), _ptr(sel),
+             _ptr(O), _ptr(lse), wp, wn, _stream(stream)), "ssa_decode_step_q4")
 
 
 def ssa_selftest_wait_timeout(limit_ns: int, ws: torch.Tensor, stream=None) -> None:

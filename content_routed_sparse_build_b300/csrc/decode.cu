@@ -850,6 +850,368 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- attend, 4-bit cache
+// The same work items, plan and merge over the 4-bit cache of quant.cu
+// (d = 128).  A ring stage holds one 32-token tile: the 2 KB K block and the
+// 2 KB V block, both laid out for the fragments (quant.cu), and the tile's K
+// and V scales, all by bulk copies.  A thread reads one 32-bit word per
+// fragment row and turns its eight nibbles into four fp16 pairs exactly
+// (each nibble, the code + 8, becomes the low mantissa bits of the fp16
+// 1024 + n; subtracting 1032 leaves the code).  The dimension and token
+// orders of the words are those of the 8-bit kernel's fragments, so Q's
+// fragments, the scaling and the softmax are the 8-bit kernel's.
+namespace q4 {
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 2;
+constexpr int kKBytes = 2048;          // 32 tokens x 128 nibbles
+constexpr int kVBytes = 2048;          // 128 d-rows x 32 nibbles
+constexpr int kSBytes = 2 * kTile * 4; // ks then vs
+constexpr size_t kRingK = (size_t)kWarps * kStages * kKBytes;
+constexpr size_t kRingV = (size_t)kWarps * kStages * kVBytes;
+constexpr size_t kRingS = (size_t)kWarps * kStages * kSBytes;
+constexpr size_t kBars = (size_t)kWarps * kStages * 8;
+constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
+constexpr size_t kFixed = 1024 + kRingK + kRingV + kRingS + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+
+__device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kTile - 1); }
+__device__ __forceinline__ int tiles(int64_t t0, int64_t t1) {
+  return (int)((t1 - tile_base(t0) + kTile - 1) / kTile);
+}
+}  // namespace q4
+
+template <int DT, int NG>
+__global__ void __launch_bounds__(q4::kThreads, 1)
+    decode_attend_q4_kernel(const uint32_t* __restrict__ Kq4, const uint32_t* __restrict__ Vq4,
+                            const float* __restrict__ Ks, const float* __restrict__ Vs, int64_t L_cap,
+                            const void* __restrict__ Q, Plan plan, Geo geo, uint32_t* __restrict__ err) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ringK = smem;
+  uint8_t* ringV = ringK + q4::kRingK;
+  uint8_t* ringS = ringV + q4::kRingV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ringS + q4::kRingS);
+  int4* metas = reinterpret_cast<int4*>(bars + q4::kWarps * q4::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metas + q4::kWarps * q4::kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < q4::kWarps * q4::kStages; ++s) ptx::mbar_init(&bars[s], 1);
+    ptx::fence_mbar_init();
+  }
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  Tables tb;
+  tb.gpref = s_gpref;
+  tb.n_union = plan.n_union;
+  tb.span = plan.span;
+  tb.mask = plan.mask;
+  tb.rank = plan.rank;
+  tb.q = static_cast<const uint16_t*>(Q);
+  tb.q_stride = D;
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < geo.n_grp; base += 32) {
+      const int gi = base + lane;
+      int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+      }
+      if (gi < geo.n_grp) s_gpref[gi + 1] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) s_gpref[0] = 0;
+  }
+  __syncthreads();
+  const int total = s_gpref[geo.n_grp];
+
+  uint8_t* wK = ringK + (size_t)warp * q4::kStages * q4::kKBytes;
+  uint8_t* wV = ringV + (size_t)warp * q4::kStages * q4::kVBytes;
+  uint8_t* wS = ringS + (size_t)warp * q4::kStages * q4::kSBytes;
+  uint64_t* fb = bars + warp * q4::kStages;
+  int4* meta = metas + warp * q4::kStages;
+  const int64_t tiles_per_head = L_cap / kTile;
+
+  Item iss;
+  iss.ntiles = 0;
+  iss.grp = iss.u = iss.c = 0;
+  iss.t0 = iss.t1 = 0;
+  int iss_tile = 0;
+  // the first item of every warp is fixed; later ones come from the counter
+  const int n_static = (int)gridDim.x * (int)(blockDim.x >> 5);
+  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = 0;
+  bool have_next = true, claim_issued = false;
+  bool exhausted = false;
+
+  auto issue = [&](int stage) -> bool {
+    if (iss_tile == iss.ntiles) {
+      if (!have_next) it_next = __shfl_sync(0xffffffffu, it_claim, 0);
+      if (it_next >= total) {
+        exhausted = true;
+        return false;
+      }
+      decode_item(it_next, tb, geo, iss);
+      iss.ntiles = q4::tiles(iss.t0, iss.t1);
+      iss_tile = 0;
+      have_next = false;
+      claim_issued = false;
+    }
+    if (lane == 0) {
+      meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ptx::mbar_arrive_expect_tx(&fb[stage], q4::kKBytes + q4::kVBytes + q4::kSBytes);
+      const int64_t y = q4::tile_base(iss.t0) + (int64_t)iss_tile * kTile;
+      uint8_t* dS = wS + stage * q4::kSBytes;
+      const int64_t blk = ((int64_t)iss.grp * tiles_per_head + y / kTile) * 512;
+      ptx::bulk_load(wK + stage * q4::kKBytes, Kq4 + blk, q4::kKBytes, &fb[stage]);
+      ptx::bulk_load(wV + stage * q4::kVBytes, Vq4 + blk, q4::kVBytes, &fb[stage]);
+      ptx::bulk_load(dS, Ks + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
+      ptx::bulk_load(dS + kTile * 4, Vs + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
+    }
+    ++iss_tile;
+    if (!claim_issued && iss.ntiles - iss_tile <= 2) {
+      if (lane == 0) it_claim = atomicAdd(plan.counter, 1) + n_static;
+      claim_issued = true;
+    }
+    return true;
+  };
+
+  int inflight = 0;
+#pragma unroll 1
+  for (int s = 0; s < q4::kStages; ++s) {
+    if (exhausted || !issue(s)) break;
+    ++inflight;
+  }
+
+  const int q4 = lane & 3, r8 = lane >> 2;
+  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+  float o[NG][D / 16][4];
+  float m[NG][2], l[NG][2];
+  Item cur;
+  cur.grp = cur.u = cur.c = cur.ntiles = 0;
+  cur.t0 = cur.t1 = 0;
+  int stage = 0;
+  uint32_t phase = 0;
+#pragma unroll 1
+  while (inflight > 0) {
+    if (!ptx::mbar_wait(&fb[stage], phase)) {
+      if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    const int4 mt = meta[stage];
+    if (mt.w == 0) {
+      cur.grp = mt.x;
+      cur.u = mt.y;
+      cur.c = mt.z;
+      {
+        const int nu = tb.n_union[cur.grp];
+        if (cur.u < nu - 1) {
+          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
+          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
+        } else {
+          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
+          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
+        }
+        cur.ntiles = q4::tiles(cur.t0, cur.t1);
+      }
+      const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        const int h = ng * 8 + r8;
+        const bool ok = h < geo.g;
+        const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
+#pragma unroll
+        for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            uint32_t v = 0u;
+            if (ok) {
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(qr + 32 * J + 8 * q4 + 2 * pr);
+              if constexpr (DT == DT_BF16) {
+                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+                v = ptx::pack2<DT_F16>(lo, hi);
+              } else {
+                v = w;
+              }
+            }
+            qf[ng][J][pr] = v;
+          }
+        }
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) o[ng][mt2][0] = o[ng][mt2][1] = o[ng][mt2][2] = o[ng][mt2][3] = 0.f;
+        m[ng][0] = m[ng][1] = -INFINITY;
+        l[ng][0] = l[ng][1] = 0.f;
+      }
+    }
+    const uint32_t aK = ptx::smem_u32(wK + stage * q4::kKBytes);
+    const uint32_t aV = ptx::smem_u32(wV + stage * q4::kVBytes);
+    const float* sks = reinterpret_cast<const float*>(wS + stage * q4::kSBytes);
+    const float* svs = sks + kTile;
+
+    // S^T = Kq Q^T per 16-token fragment t
+    float s[NG][kSub][4], s2[NG][kSub][4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[ng][t][i] = s2[ng][t][i] = 0.f;
+#pragma unroll
+    for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        const int ra = t * 16 + r8, rb = ra + 8;
+        const uint32_t wa = ptx::lds32(aK + ((J * kTile + ra) * 4 + q4) * 4);
+        const uint32_t wb = ptx::lds32(aK + ((J * kTile + rb) * 4 + q4) * 4);
+        uint32_t a0[4], a1[4];
+        ptx::u4x8_to_f16x2(wa, a0[0], a0[2], a1[0], a1[2]);
+        ptx::u4x8_to_f16x2(wb, a0[1], a0[3], a1[1], a1[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          ptx::mma16816<DT_F16>(s[ng][t], a0, qf[ng][J][0], qf[ng][J][1]);
+          ptx::mma16816<DT_F16>(s2[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
+        }
+      }
+    }
+    // the odd k-steps accumulated apart (two independent MMA chains per fragment)
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[ng][t][i] += s2[ng][t][i];
+    // rows (tokens) r8 and r8 + 8 of each fragment: K / V scales, validity
+    const int64_t tbase = q4::tile_base(cur.t0) + (int64_t)mt.w * kTile;
+    float ksc[kSub][2], vsc[kSub][2];
+    bool valid[kSub][2];
+#pragma unroll
+    for (int t = 0; t < kSub; ++t)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int row = t * 16 + r8 + 8 * i;
+        const int64_t tok = tbase + row;
+        valid[t][i] = tok >= cur.t0 && tok < cur.t1;
+        ksc[t][i] = sks[row];
+        vsc[t][i] = svs[row];
+      }
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        s[ng][t][0] = valid[t][0] ? s[ng][t][0] * ksc[t][0] : -INFINITY;
+        s[ng][t][1] = valid[t][0] ? s[ng][t][1] * ksc[t][0] : -INFINITY;
+        s[ng][t][2] = valid[t][1] ? s[ng][t][2] * ksc[t][1] : -INFINITY;
+        s[ng][t][3] = valid[t][1] ? s[ng][t][3] * ksc[t][1] : -INFINITY;
+      }
+    const float c = geo.scale_log2e;
+    uint32_t pb[NG][kSub][2];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      float mx[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float v = fmaxf(s[ng][0][i], s[ng][0][i + 2]);
+#pragma unroll
+        for (int t = 1; t < kSub; ++t) v = fmaxf(v, fmaxf(s[ng][t][i], s[ng][t][i + 2]));
+        v *= c;
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        mx[i] = fmaxf(m[ng][i], v);
+      }
+      float nb[2], alpha[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float bse = mx[i] == -INFINITY ? 0.f : mx[i];
+        nb[i] = -bse;
+        alpha[i] = exp2f(m[ng][i] - bse);
+        m[ng][i] = mx[i];
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
+        const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
+        const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
+        const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
+        ls0 += p0 + p2;
+        ls1 += p1 + p3;
+        // the V scale of each token weights its P (0 for masked tokens,
+        // whose scale slot may hold anything)
+        const float v0 = valid[t][0] ? vsc[t][0] : 0.f, v1 = valid[t][1] ? vsc[t][1] : 0.f;
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * v0, p1 * v0));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * v1, p3 * v1));
+      }
+      l[ng][0] = l[ng][0] * alpha[0] + ls0;
+      l[ng][1] = l[ng][1] * alpha[1] + ls1;
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          o[ng][mt2][0] *= alpha[0];
+          o[ng][mt2][1] *= alpha[1];
+          o[ng][mt2][2] *= alpha[0];
+          o[ng][mt2][3] *= alpha[1];
+        }
+      }
+    }
+    // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one
+    // 4-byte load per row covering both 16-token fragments
+#pragma unroll
+    for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+      const uint32_t va = ptx::lds32(aV + ((mt2 * 16 + r8) * 4 + q4) * 4);
+      const uint32_t vb = ptx::lds32(aV + ((mt2 * 16 + r8 + 8) * 4 + q4) * 4);
+      uint32_t a0[4], a1[4];
+      ptx::u4x8_to_f16x2(va, a0[0], a0[2], a1[0], a1[2]);
+      ptx::u4x8_to_f16x2(vb, a0[1], a0[3], a1[1], a1[3]);
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        ptx::mma16816<DT_F16>(o[ng][mt2], a0, pb[ng][0][0], pb[ng][0][1]);
+        ptx::mma16816<DT_F16>(o[ng][mt2], a1, pb[ng][1][0], pb[ng][1][1]);
+      }
+    }
+    __syncwarp();
+    --inflight;
+    const bool last = mt.w == cur.ntiles - 1;
+    if (!exhausted && issue(stage)) ++inflight;
+    if (++stage == q4::kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (!last) continue;
+
+    const int slot_idx = cur.grp * geo.umax + cur.u;
+    const uint32_t hmask = tb.mask[slot_idx];
+    const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float lt = l[ng][i];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int r = ng * 8 + 2 * q4 + i;
+        if (r >= geo.g || !((hmask >> r) & 1u)) continue;
+        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
+        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        float* dst = plan.po + slot * D + r8;
+#pragma unroll
+        for (int mt2 = 0; mt2 < D / 16; ++mt2) {
+          dst[mt2 * 16] = o[ng][mt2][i];
+          dst[mt2 * 16 + 8] = o[ng][mt2][i + 2];
+        }
+        if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- merge
 // One CTA per (b, q-head): its (topk + 1) * C partial slots, in (span rank,
 // chunk) order, split into 8 contiguous runs, one per warp; empty slots
@@ -984,6 +1346,22 @@ cudaError_t attend_q8(const Problem& pr, const void* Q, const int8_t* Kq, const 
                     lse);
 }
 
+template <int DT>
+cudaError_t attend_q4(const Problem& pr, const void* Q, const uint32_t* Kq4, const float* Ks, const uint32_t* Vq4,
+                      const float* Vs, void* O, float* lse, const Plan& plan, const Geo& geo, uint32_t* err,
+                      cudaStream_t st) {
+  constexpr int D = 128;
+  auto attend = pr.g <= 8 ? decode_attend_q4_kernel<DT, 1> : decode_attend_q4_kernel<DT, 2>;
+  static bool attr_done[2][kMaxDevices] = {};
+  cudaError_t e = ensure_smem_attr(attend, q4::kFixed, attr_done[pr.g <= 8 ? 0 : 1]);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attend, dim3(device_sm_count()), dim3(q4::kThreads), q4::kFixed, st, Kq4, Vq4, Ks, Vs, pr.L_cap,
+                 Q, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<DT, D>, dim3(pr.B * pr.Hq), dim3(kMergeWarps * 32), 0, st, plan, geo, O,
+                    lse);
+}
+
 template <int DT, int D>
 cudaError_t attend_16(const Problem& pr, const void* Q, const void* K, const void* V, void* O, float* lse,
                       const Plan& plan, const Geo& geo, uint32_t* err, cudaStream_t st) {
@@ -1016,6 +1394,27 @@ cudaError_t launch_attend_decode_q8(const Problem& pr, const void* Q, int64_t po
   if (e != cudaSuccess) return e;
   if (pr.dtype == DT_BF16) return attend_q8<DT_BF16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
   return attend_q8<DT_F16>(pr, Q, Kq, Ks, Vq, Vs, O, lse, plan, geo, err, st);
+}
+
+cudaError_t launch_attend_decode_q4(const Problem& pr, const void* Q, int64_t pos, const uint32_t* Kq4,
+                                    const float* Ks, const uint32_t* Vq4, const float* Vs, const int32_t* sel,
+                                    void* O, float* lse, void* ws, cudaStream_t st) {
+  Plan plan;
+  Geo geo;
+  plan_geo(pr, pos, ws, plan, geo);
+  uint32_t* err = ws_error(ws);
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(geo.n_grp), dim3(kPlanThreads), 0, st, sel, plan, geo, err);
+  if (e != cudaSuccess) return e;
+  if (pr.dtype == DT_BF16) return attend_q4<DT_BF16>(pr, Q, Kq4, Ks, Vq4, Vs, O, lse, plan, geo, err, st);
+  return attend_q4<DT_F16>(pr, Q, Kq4, Ks, Vq4, Vs, O, lse, plan, geo, err, st);
+}
+
+cudaError_t launch_attend_decode_q4_planned(const Problem& pr, const void* Q, const uint32_t* Kq4, const float* Ks,
+                                            const uint32_t* Vq4, const float* Vs, void* O, float* lse,
+                                            const dplan::Plan& plan, const dplan::Geo& geo, uint32_t* err,
+                                            cudaStream_t st) {
+  if (pr.dtype == DT_BF16) return attend_q4<DT_BF16>(pr, Q, Kq4, Ks, Vq4, Vs, O, lse, plan, geo, err, st);
+  return attend_q4<DT_F16>(pr, Q, Kq4, Ks, Vq4, Vs, O, lse, plan, geo, err, st);
 }
 
 bool decode_fast_supported(const Problem& pr) {

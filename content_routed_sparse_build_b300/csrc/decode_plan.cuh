@@ -210,6 +210,10 @@ void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* pla
 cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,
                                          float* lse, const dplan::Plan& plan, const dplan::Geo& geo,
                                          uint32_t* err, cudaStream_t st);
+cudaError_t launch_attend_decode_q4_planned(const Problem& pr, const void* Q, const uint32_t* Kq4, const float* Ks,
+                                            const uint32_t* Vq4, const float* Vs, void* O, float* lse,
+                                            const dplan::Plan& plan, const dplan::Geo& geo, uint32_t* err,
+                                            cudaStream_t st);
 cudaError_t launch_attend_decode_q8_planned(const Problem& pr, const void* Q, const int8_t* Kq, const float* Ks,
                                             const int8_t* Vq, const float* Vs, void* O, float* lse,
                                             const dplan::Plan& plan, const dplan::Geo& geo, uint32_t* err,

@@ -121,6 +121,16 @@ cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, co
 cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos, const float* summ,
                                   const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
                                   int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_quantize_kv4(const Problem& pr, const void* K, const void* V, int64_t t0, int64_t t1,
+                                uint32_t* Kq4, float* Ks, uint32_t* Vq4, float* Vs, cudaStream_t st);
+cudaError_t launch_summaries_q4(const Problem& pr, const uint32_t* Kq4, const float* Ks, int64_t j0, int64_t j1,
+                                float* summ, cudaStream_t st);
+cudaError_t launch_attend_decode_q4(const Problem& pr, const void* Q, int64_t pos, const uint32_t* Kq4,
+                                    const float* Ks, const uint32_t* Vq4, const float* Vs, const int32_t* sel,
+                                    void* O, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_decode_step_q4(const Problem& pr, const void* Q, int64_t pos, const float* summ,
+                                  const uint32_t* Kq4, const float* Ks, const uint32_t* Vq4, const float* Vs,
+                                  int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t st);
 
 // Prefill attention fast path (16-bit types): dispatch, span tiles, merge.

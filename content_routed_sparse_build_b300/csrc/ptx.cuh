@@ -111,6 +111,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // 8-byte shared-memory load.
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -128,6 +133,22 @@ __device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
   const uint32_t bias = 0x64806480u;
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+// Eight 4-bit fields of w, each a signed code c stored as c + 8, at bits
+// 4 i (element 2 i) and 16 + 4 i (element 2 i + 1) -> four fp16 pairs
+// p_i = (element 2 i, element 2 i + 1), exactly: the field becomes the low
+// mantissa bits of the fp16 1024 + n (0x64nn), and subtracting 1032 leaves c.
+__device__ __forceinline__ void u4x8_to_f16x2(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  p0 = (w & 0x000F000Fu) | 0x64006400u;
+  p1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
+  p2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
+  p3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t bias = 0x64086408u;
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p0) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p1) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p2) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p3) : "r"(bias));
 }
 
 // L2 eviction-priority policies (hints only: lines can always be evicted).

@@ -140,6 +140,130 @@ cudaError_t launch_q(const Problem& pr, const void* K, const void* V, int64_t t0
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- 4-bit
+// The same scheme with 15 levels (SubQ release post, quantisation plan, its
+// 4-bit half): s = max_i |x_i| / 7, q_i = clamp(rint(x_i / s), -7, 7), each
+// code stored as the nibble q + 8.  d = 128 only.  A 32-token tile of K and
+// of V is one 2 KB block of 32-bit words, laid out for the decode kernel's
+// fragment loads (each thread of a warp reads one word per row, the warp's
+// 32 words consecutive):
+//   Kq4 word [J][tok][c]  (J < d / 32, tok < 32, c < 4): token tok's
+//        dimensions d = 32 J + 8 c + e, e < 8
+//   Vq4 word [d][c]       (c < 4): dimension d of tokens
+//        2c + f(e), f = 0, 1, 8, 9, 16, 17, 24, 25 for e = 0..7
+// and inside a word element e sits at bit 4 (e / 2) + 16 (e % 2), so that
+// (w >> 4 i) & 0x000F000F holds elements 2i and 2i + 1 in the low bits of
+// its two halves: one fp16 pair each.
+constexpr int kQ4Tile = 32;
+constexpr int kQ4Words = 512;   // words per 32-token tile of K or of V (d = 128)
+
+__device__ __forceinline__ uint32_t q4_shift(int e) { return 4u * (uint32_t)(e >> 1) + 16u * (uint32_t)(e & 1); }
+
+// The V element slot of token tok (0..31) of a tile: word column c and e.
+__device__ __forceinline__ void q4_vslot(int tok, int& c, int& e) {
+  const int w = tok & 15;
+  c = (w & 7) >> 1;
+  e = (w & 1) + 2 * ((w >> 3) + 2 * (tok >> 4));
+}
+
+// One CTA of 256 threads per (b*kv-head, 32-token tile) overlapping
+// [t0, t1): warp w quantises the tile's tokens w, w + 8, ...  K words belong
+// to one token and are written whole; V words gather eight tokens, so the
+// tile's V block is rebuilt in shared memory from its old contents (tokens
+// outside [t0, t1) keep theirs) and written back whole.
+template <int DT>
+__global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__ K, const void* __restrict__ V,
+                                                         int64_t L_cap, int64_t t0, int64_t t1, int64_t tile0,
+                                                         uint32_t* __restrict__ Kq4, float* __restrict__ Ks,
+                                                         uint32_t* __restrict__ Vq4, float* __restrict__ Vs) {
+  constexpr int D = 128;
+  __shared__ uint32_t vw[kQ4Words];
+  const int64_t bh = blockIdx.y;
+  const int64_t tile = tile0 + blockIdx.x;
+  const int64_t tb = tile * kQ4Tile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* vg = Vq4 + (bh * (L_cap / kQ4Tile) + tile) * kQ4Words;
+  uint32_t* kg = Kq4 + (bh * (L_cap / kQ4Tile) + tile) * kQ4Words;
+  for (int x = threadIdx.x; x < kQ4Words; x += 256) vw[x] = vg[x];
+  __syncthreads();
+  for (int tok = warp; tok < kQ4Tile; tok += 8) {
+    const int64_t t = tb + tok;
+    if (t < t0 || t >= t1) continue;
+    for (int isv = 0; isv < 2; ++isv) {
+      const void* X = isv ? V : K;
+      const int64_t src = (bh * L_cap + t) * D + lane * 4;
+      float x[4];
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[e] = load_elem<DT>(X, src + e);
+        amax = fmaxf(amax, fabsf(x[e]));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float sc = __fdiv_rn(amax, 7.0f);
+      uint32_t nib[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int v = 0;
+        if (sc != 0.f) v = min(7, max(-7, __float2int_rn(__fdiv_rn(x[e], sc))));
+        nib[e] = (uint32_t)(v + 8);
+      }
+      if (!isv) {
+        // lanes 2m and 2m + 1 hold dimensions 8m .. 8m + 7: one word
+        const int half = lane & 1;
+        uint32_t part = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part |= nib[e] << q4_shift(4 * half + e);
+        const uint32_t word = part | __shfl_xor_sync(0xffffffffu, part, 1);
+        if (half == 0) {
+          const int m = lane >> 1, J = m >> 2, c = m & 3;
+          kg[(J * kQ4Tile + tok) * 4 + c] = word;
+        }
+        if (lane == 0) Ks[bh * L_cap + t] = sc;
+      } else {
+        int c, e;
+        q4_vslot(tok, c, e);
+        const uint32_t sh = q4_shift(e);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t* wp = &vw[(lane * 4 + k) * 4 + c];
+          atomicAnd(wp, ~(0xFu << sh));
+          atomicOr(wp, nib[k] << sh);
+        }
+        if (lane == 0) Vs[bh * L_cap + t] = sc;
+      }
+    }
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < kQ4Words; x += 256) vg[x] = vw[x];
+}
+
+// Summaries of the 4-bit keys: one CTA per (b*kv-head, span), thread = d
+// column, the span's tokens added in order.
+__global__ void __launch_bounds__(128) summaries_q4_kernel(const uint32_t* __restrict__ Kq4,
+                                                           const float* __restrict__ Ks, float* __restrict__ summ,
+                                                           int64_t L_cap, int64_t L, int S, int64_t span_begin,
+                                                           int64_t ns_cap) {
+  constexpr int D = 128;
+  const int64_t bh = blockIdx.y;
+  const int64_t j = span_begin + blockIdx.x;
+  const int64_t t0 = j * S;
+  const int64_t t1 = t0 + S < L ? t0 + S : L;
+  const int d = threadIdx.x;
+  const int J = d >> 5, c = (d & 31) >> 3;
+  const uint32_t sh = q4_shift(d & 7);
+  const uint32_t* kb = Kq4 + bh * (L_cap / kQ4Tile) * kQ4Words;
+  const float* sc = Ks + bh * L_cap;
+  float acc = 0.f;
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint32_t w = __ldg(kb + (t / kQ4Tile) * kQ4Words + (J * kQ4Tile + (t % kQ4Tile)) * 4 + c);
+    const int q = (int)((w >> sh) & 0xFu) - 8;
+    acc += (float)q * __ldg(sc + t);
+  }
+  summ[(bh * ns_cap + j) * D + d] = acc / (float)(t1 - t0);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_kv(const Problem& pr, const void* K, const void* V, int64_t t0, int64_t t1,
@@ -168,6 +292,34 @@ cudaError_t launch_summaries_q8(const Problem& pr, const int8_t* Kq, const float
     summaries_q8_kernel<128><<<grid, 256, 0, st>>>(Kq, Ks, summ, pr.L_cap, pr.L, pr.S, j0, pr.ns_cap);
   else
     summaries_q8_kernel<64><<<grid, 256, 0, st>>>(Kq, Ks, summ, pr.L_cap, pr.L, pr.S, j0, pr.ns_cap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_kv4(const Problem& pr, const void* K, const void* V, int64_t t0, int64_t t1,
+                                uint32_t* Kq4, float* Ks, uint32_t* Vq4, float* Vs, cudaStream_t st) {
+  if (t1 <= t0) return cudaSuccess;
+  const int64_t tile0 = t0 / kQ4Tile, tile1 = (t1 + kQ4Tile - 1) / kQ4Tile;
+  if (tile1 - tile0 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)(tile1 - tile0), (unsigned)(pr.B * pr.Hkv));
+  switch (pr.dtype) {
+    case DT_F32:
+      quantize4_kernel<DT_F32><<<grid, 256, 0, st>>>(K, V, pr.L_cap, t0, t1, tile0, Kq4, Ks, Vq4, Vs);
+      break;
+    case DT_BF16:
+      quantize4_kernel<DT_BF16><<<grid, 256, 0, st>>>(K, V, pr.L_cap, t0, t1, tile0, Kq4, Ks, Vq4, Vs);
+      break;
+    default:
+      quantize4_kernel<DT_F16><<<grid, 256, 0, st>>>(K, V, pr.L_cap, t0, t1, tile0, Kq4, Ks, Vq4, Vs);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_summaries_q4(const Problem& pr, const uint32_t* Kq4, const float* Ks, int64_t j0, int64_t j1,
+                                float* summ, cudaStream_t st) {
+  if (j1 <= j0) return cudaSuccess;
+  if (j1 - j0 > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)(j1 - j0), (unsigned)(pr.B * pr.Hkv));
+  summaries_q4_kernel<<<grid, 128, 0, st>>>(Kq4, Ks, summ, pr.L_cap, pr.L, pr.S, j0, pr.ns_cap);
   return cudaGetLastError();
 }
 

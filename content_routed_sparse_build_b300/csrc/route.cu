@@ -563,6 +563,19 @@ cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos,
   return launch_attend_decode_q8_planned(pr, plan.q, Kq, Ks, Vq, Vs, O, lse, plan, geo, ws_error(ws), st);
 }
 
+cudaError_t launch_decode_step_q4(const Problem& pr, const void* Q, int64_t pos, const float* summ,
+                                  const uint32_t* Kq4, const float* Ks, const uint32_t* Vq4, const float* Vs,
+                                  int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
+  dplan::Plan plan;
+  dplan::Geo geo;
+  decode_plan_args(pr, pos, ws, &plan, &geo);
+  const cudaError_t e = pr.dtype == DT_BF16
+                            ? decode_route_g<DT_BF16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
+                            : decode_route_g<DT_F16, 128, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
+  if (e != cudaSuccess) return e;
+  return launch_attend_decode_q4_planned(pr, plan.q, Kq4, Ks, Vq4, Vs, O, lse, plan, geo, ws_error(ws), st);
+}
+
 cudaError_t launch_route(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0,
                          const float* summ, int32_t* sel, float* sel_score, cudaStream_t st) {
   if (n_q == 0) return cudaSuccess;

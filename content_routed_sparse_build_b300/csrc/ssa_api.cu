@@ -284,6 +284,78 @@ int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, const fl
                                            static_cast<cudaStream_t>(stream)));
 }
 
+// The 4-bit cache: d = 128, bf16 / fp16 queries, L_cap a multiple of 32.
+bool q4_supported(const Problem& pr) {
+  return pr.d == 128 && pr.L_cap % 32 == 0 && (pr.dtype == SSA_BF16 || pr.dtype == SSA_F16) &&
+         decode_fast_supported(pr);
+}
+
+int ssa_quantize_kv4(const ssa_params* p, const void* K, const void* V, int64_t t_begin, int64_t t_end,
+                     void* Kq4, float* Ks, void* Vq4, float* Vs, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.d != 128 || pr.L_cap % 32 != 0) return SSA_ERR_UNSUPPORTED;
+  if (t_begin < 0 || t_end < t_begin || t_end > pr.L) return SSA_ERR_INVALID_ARG;
+  if (!K || !V || !Kq4 || !Ks || !Vq4 || !Vs) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(Kq4) || !aligned16(Ks) || !aligned16(Vq4) || !aligned16(Vs))
+    return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_kv4(pr, K, V, t_begin, t_end, static_cast<uint32_t*>(Kq4), Ks,
+                                         static_cast<uint32_t*>(Vq4), Vs, static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_build_summaries_q4(const ssa_params* p, const void* Kq4, const float* Ks, int64_t span_begin,
+                           int64_t span_end, float* summ, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (pr.d != 128 || pr.L_cap % 32 != 0) return SSA_ERR_UNSUPPORTED;
+  if (!Kq4 || !Ks || !summ || !aligned16(Kq4) || !aligned16(Ks) || !aligned16(summ)) return SSA_ERR_INVALID_ARG;
+  const int64_t ns_valid = (pr.L + pr.S - 1) / pr.S;
+  if (span_begin < 0 || span_end < span_begin || span_end > ns_valid) return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_summaries_q4(pr, static_cast<const uint32_t*>(Kq4), Ks, span_begin, span_end, summ,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_attend_decode_q4(const ssa_params* p, const void* Q, int64_t pos, const void* Kq4, const float* Ks,
+                         const void* Vq4, const float* Vs, const int32_t* sel, void* O, float* lse, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (!q4_supported(pr)) return SSA_ERR_UNSUPPORTED;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !Kq4 || !Ks || !Vq4 || !Vs || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(Kq4) || !aligned16(Ks) || !aligned16(Vq4) || !aligned16(Vs) || !aligned16(O))
+    return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  return cuda_status(launch_attend_decode_q4(pr, Q, pos, static_cast<const uint32_t*>(Kq4), Ks,
+                                             static_cast<const uint32_t*>(Vq4), Vs, sel, O, lse, ws,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int ssa_decode_step_q4(const ssa_params* p, const void* Q, int64_t pos, const float* summ, const void* Kq4,
+                       const float* Ks, const void* Vq4, const float* Vs, int32_t* sel, void* O, float* lse,
+                       void* ws, size_t ws_bytes, void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (!q4_supported(pr)) return SSA_ERR_UNSUPPORTED;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !summ || !Kq4 || !Ks || !Vq4 || !Vs || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(summ) || !aligned16(Kq4) || !aligned16(Ks) || !aligned16(Vq4) ||
+      !aligned16(Vs) || !aligned16(O))
+    return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  if (!device_accessible(Q) || !device_accessible(sel) || !device_accessible(O) || !device_accessible(lse))
+    return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_decode_step_q4(pr, Q, pos, summ, static_cast<const uint32_t*>(Kq4), Ks,
+                                           static_cast<const uint32_t*>(Vq4), Vs, sel, O, lse, ws,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 int ssa_selftest_wait_timeout(uint64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
   if (limit_ns > 1000000000ull) return SSA_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kWsHeader) return SSA_ERR_WORKSPACE;

@@ -297,6 +297,58 @@ SSA_API int ssa_decode_step_q8(const ssa_params* p, const void* Q, int64_t pos, 
                                int32_t* sel, void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The 4-bit cache (SubQ release post, geeks.co.kr/post/2077, quantisation
+ * plan: its 4-bit half).  Symmetric rows, one fp32 scale per (b, kv-head,
+ * token): s = max_i |x_i| / 7, q_i = clamp(rint(x_i / s), -7, 7) in fp32
+ * (IEEE division, round to nearest even; q = 0 when s == 0), each code
+ * stored as the 4-bit field q + 8.  d = 128 and L_cap a multiple of 32.
+ * Layouts (32-bit words, little-endian; a 32-token tile of K or of V is one
+ * contiguous block of 512 words):
+ *   Kq4 [B, Hkv, L_cap / 32][J < 4][tok < 32][c < 4] words: token tok of the
+ *       tile, dimensions d = 32 J + 8 c + e, e < 8
+ *   Vq4 [B, Hkv, L_cap / 32][d < 128][c < 4] words: dimension d of the tile's
+ *       tokens 2 c + (0, 1, 8, 9, 16, 17, 24, 25)[e], e < 8
+ *   element e of a word at bits 4 (e / 2) + 16 (e % 2)
+ *   Ks, Vs [B, Hkv, L_cap] fp32 scales
+ * Kq4 and Vq4 are B * Hkv * L_cap * 64 bytes each.
+ */
+
+/*
+ * Quantises rows [t_begin, t_end) of K and V into the 4-bit cache.  Tiles
+ * the range only partly covers keep their other tokens' codes; calls that
+ * touch the same 32-token tile must not overlap in time.
+ */
+SSA_API int ssa_quantize_kv4(const ssa_params* p, const void* K, const void* V, int64_t t_begin, int64_t t_end,
+                             void* Kq4, float* Ks, void* Vq4, float* Vs, void* stream);
+
+/*
+ * ssa_build_summaries over the 4-bit keys: summ[b, kvh, j, :] = mean over
+ * span j's valid tokens of q * s (fp32), for spans [span_begin, span_end).
+ */
+SSA_API int ssa_build_summaries_q4(const ssa_params* p, const void* Kq4, const float* Ks, int64_t span_begin,
+                                   int64_t span_end, float* summ, void* stream);
+
+/*
+ * ssa_attend_decode over the 4-bit cache: the same selections, work split
+ * and merge, with K[t] = q_K[t] * Ks[t] and V[t] = q_V[t] * Vs[t].  Q and O
+ * are bf16 or fp16, d = 128; the products run in fp16 (4-bit codes convert
+ * exactly; Q is rounded to fp16, so |q| must stay below 65504) with fp32
+ * accumulation.  ws as for ssa_attend_decode.  Requires 0 <= pos < L.
+ */
+SSA_API int ssa_attend_decode_q4(const ssa_params* p, const void* Q, int64_t pos, const void* Kq4, const float* Ks,
+                                 const void* Vq4, const float* Vs, const int32_t* sel, void* O, float* lse,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One whole decode step over the 4-bit cache, as ssa_decode_step_q8 is for
+ * the 8-bit one (three launches; Q, sel, O and lse may be mapped page-locked
+ * host memory).  summ are the fp32 summaries (ssa_build_summaries_q4).
+ */
+SSA_API int ssa_decode_step_q4(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
+                               const void* Kq4, const float* Ks, const void* Vq4, const float* Vs, int32_t* sel,
+                               void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Cache snapshots (superlinear release post, geeks.co.kr/post/2077, "why
  * this matters": the cache is kept instead of re-processing the context, in
  * memory for instant replies and saved to / restored from disk per session).

@@ -152,6 +152,50 @@ def test_q8_validation():
 
 
 @needs_no_gpu
+def test_q4_validation():
+    L = ssa.lib()
+    P, I8, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    pp = ctypes.POINTER(ssa.ssa_params)
+    L.ssa_quantize_kv4.argtypes = [pp, P, P, I8, I8, P, P, P, P, P]
+    L.ssa_build_summaries_q4.argtypes = [pp, P, P, I8, I8, P, P]
+    L.ssa_attend_decode_q4.argtypes = [pp, P, I8, P, P, P, P, P, P, P, P, SZ, P]
+    L.ssa_decode_step_q4.argtypes = [pp, P, I8, P, P, P, P, P, P, P, P, P, SZ, P]
+    p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
+    p_d64 = ssa.params(1, 8, 2, 64, 4096, 64, 8, torch.bfloat16)
+    p_ragged = ssa.params(1, 8, 2, 128, 4001, 64, 8, torch.bfloat16)
+    q = lambda p, t0, t1, **kw: L.ssa_quantize_kv4(ctypes.byref(p), FAKE, kw.get("V", FAKE), t0, t1, FAKE, FAKE,
+                                                   FAKE, FAKE, None)
+    assert q(p, 0, 4097) == ssa.SSA_ERR_INVALID_ARG             # past L
+    assert q(p, 10, 5) == ssa.SSA_ERR_INVALID_ARG
+    assert q(p, -1, 5) == ssa.SSA_ERR_INVALID_ARG
+    assert q(p, 0, 10, V=None) == ssa.SSA_ERR_INVALID_ARG
+    assert q(p, 0, 10, V=ctypes.c_void_p(4104)) == ssa.SSA_ERR_INVALID_ARG   # not 16-byte aligned
+    assert q(p_ragged, 0, 10) == ssa.SSA_ERR_UNSUPPORTED        # L_cap % 32
+    assert q(p_d64, 0, 10) == ssa.SSA_ERR_UNSUPPORTED
+    s = lambda p, j0, j1: L.ssa_build_summaries_q4(ctypes.byref(p), FAKE, FAKE, j0, j1, FAKE, None)
+    assert s(p, 0, 65) == ssa.SSA_ERR_INVALID_ARG               # past the last span
+    assert s(p, 3, 2) == ssa.SSA_ERR_INVALID_ARG
+    assert s(p_d64, 0, 1) == ssa.SSA_ERR_UNSUPPORTED
+    need = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE)
+    d = lambda p, pos, ws, n: L.ssa_attend_decode_q4(ctypes.byref(p), FAKE, pos, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                     FAKE, None, ws, n, None)
+    assert d(p, 4096, FAKE, need) == ssa.SSA_ERR_INVALID_ARG          # pos == L
+    assert d(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
+    assert d(p, 10, FAKE, need - 1) == ssa.SSA_ERR_WORKSPACE
+    assert d(p_d64, 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    assert d(p_ragged, 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    assert d(ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.float32), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    st = lambda p, pos, ws, n, **kw: L.ssa_decode_step_q4(
+        ctypes.byref(p), FAKE, pos, kw.get("summ", FAKE), FAKE, FAKE, FAKE, FAKE, kw.get("sel", FAKE), FAKE, None,
+        ws, n, None)
+    assert st(p, 4096, FAKE, need) == ssa.SSA_ERR_INVALID_ARG
+    assert st(p, 10, FAKE, need, summ=None) == ssa.SSA_ERR_INVALID_ARG
+    assert st(p, 10, FAKE, need, sel=None) == ssa.SSA_ERR_INVALID_ARG
+    assert st(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
+    assert st(p_d64, 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+
+
+@needs_no_gpu
 def test_decode_step_validation():
     p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
     L = ssa.lib()
