@@ -1050,6 +1050,8 @@ def main():
     ap.add_argument("--prefill-chunk", type=int, default=None,
                     help="queries of the prefill chunk (profiling runs on a smaller case)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-main-decode", action="store_true",
+                    help="skip the 16-bit per-head decode line only (the decode variant lines still run)")
     ap.add_argument("--no-dense", action="store_true",
                     help="skip the dense-attention comparison (PyTorch SDPA on the same shapes)")
     ap.add_argument("--no-group", action="store_true",
@@ -1085,7 +1087,7 @@ def main():
     w = W.DECODE_1M
     if args.decode_L:
         w = w.with_(name="decode_%d" % args.decode_L, L=args.decode_L, q_pos0=args.decode_L - w.n_q)
-    if args.no_decode:
+    if args.no_decode or args.no_main_decode:
         dec = {"tok_s": None, "ms_per_step": None, "roofline": None, "e2e": None, "clocks": None,
                "attend_ms_per_step": None, "route_plus_gaps_ms_per_step": None,
                "attend_bytes_per_step": None, "route_bytes_per_step": None,
@@ -1106,7 +1108,7 @@ def main():
         "roofline": dec["roofline"],
         "e2e": dec["e2e"],
         "clocks": dec["clocks"],
-        "gpu_launches": steps * launches_per_decode_step(w) if not args.no_decode else 0,
+        "gpu_launches": steps * launches_per_decode_step(w) if dec["tok_s"] is not None else 0,
         "decode_detail": {k: dec[k] for k in ("attend_ms_per_step", "route_plus_gaps_ms_per_step",
                                                "attend_bytes_per_step", "route_bytes_per_step",
                                                "summaries", "device_error_bits", "timing")},
@@ -1143,7 +1145,7 @@ def main():
     if not args.no_tiny and not small:
         line["tiny_prefill"] = bench_tiny(dev, args.prefill_steps, ws_n, cpu_leg)
         torch.cuda.empty_cache()
-    if (not args.no_dense and not args.no_decode and pre is not None and ws_n == 1 and not small):
+    if (not args.no_dense and dec["ms_per_step"] is not None and pre is not None and ws_n == 1 and not small):
         torch.cuda.empty_cache()
         line["dense_comparison"] = bench_dense_comparison(dev, flush, dec["ms_per_step"], pre["ms_per_step"])
     if rank == 0:

@@ -852,31 +852,48 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
 
 // ---------------------------------------------------------------- attend, 4-bit cache
 // The same work items, plan and merge over the 4-bit cache of quant.cu
-// (d = 128).  A ring stage holds one 32-token tile: the 2 KB K block and the
-// 2 KB V block, both laid out for the fragments (quant.cu), and the tile's K
-// and V scales, all by bulk copies.  A thread reads one 32-bit word per
-// fragment row and turns its eight nibbles into four fp16 pairs exactly
-// (each nibble, the code + 8, becomes the low mantissa bits of the fp16
-// 1024 + n; subtracting 1032 leaves the code).  The dimension and token
-// orders of the words are those of the 8-bit kernel's fragments, so Q's
-// fragments, the scaling and the softmax are the 8-bit kernel's.
+// (d = 128).  A ring stage holds 64 tokens: two consecutive 32-token blocks
+// of K (4 KB) and of V (4 KB), both laid out for the fragments (quant.cu),
+// and their K and V scales, all by bulk copies; four independent 16-token
+// fragments per stage give each warp four S chains and amortise the
+// per-stage wait, issue and max reduction over 64 tokens.  A thread reads one 32-bit word per
+// fragment row and masks its eight nibbles n = code + 8 into four fp16 pairs
+// of subnormals, n * 2^-24 or (second and fourth pair) 16 n * 2^-24, with no
+// arithmetic; the MMAs then see exact values and the rest is folded:
+//   K: Q's dimensions that meet a 16 n field are taken at Q / 16, so every
+//      product is q' n 2^-24 with q' the Q value the MMA used; the score is
+//      2^24 acc - 8 sum_d q'_d, the sum taken once per item and head;
+//   V: the tokens stored as 16 n fields (those with bit 3 of the tile index
+//      set) carry P * vs / 16, and one more MMA against a constant fragment
+//      of 1s at the same scales accumulates sum_t (P vs)' 2^-24 per head, so
+//      the output is 2^24 (acc - 8 * that), all of it in the same rounded
+//      products the MMA summed.
+// The dimension and token orders of the words are those of the 8-bit
+// kernel's fragments, so Q's fragments and the softmax are the 8-bit kernel's.
 namespace q4 {
 constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
-constexpr int kKBytes = 2048;          // 32 tokens x 128 nibbles
-constexpr int kVBytes = 2048;          // 128 d-rows x 32 nibbles
-constexpr int kSBytes = 2 * kTile * 4; // ks then vs
+constexpr int kT = 64;                 // tokens per ring stage
+constexpr int kSubT = kT / 16;         // m16 fragments per stage
+constexpr int kBlk = 32;               // tokens per stored block
+constexpr int kBlkBytes = 2048;        // 32 tokens x 128 nibbles, of K or of V
+constexpr int kKBytes = 2 * kBlkBytes;
+constexpr int kVBytes = 2 * kBlkBytes;
+constexpr int kSBytes = 2 * kT * 4;    // ks then vs
 constexpr size_t kRingK = (size_t)kWarps * kStages * kKBytes;
 constexpr size_t kRingV = (size_t)kWarps * kStages * kVBytes;
 constexpr size_t kRingS = (size_t)kWarps * kStages * kSBytes;
 constexpr size_t kBars = (size_t)kWarps * kStages * 8;
-constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
-constexpr size_t kFixed = 1024 + kRingK + kRingV + kRingS + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+constexpr size_t kMeta = (size_t)kWarps * kStages * 16;   // (grp, u, c, tile) per stage
+constexpr size_t kMetaT = (size_t)kWarps * kStages * 16;  // the item's (t0, t1) per stage
+constexpr size_t kFixed =
+    1024 + kRingK + kRingV + kRingS + kBars + kMeta + kMetaT + (size_t)(2 * kMaxGroups + 1) * 4;
+static_assert(kFixed <= (size_t)kSmemLimit, "4-bit ring does not fit in shared memory");
 
-__device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kTile - 1); }
+__device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kT - 1); }
 __device__ __forceinline__ int tiles(int64_t t0, int64_t t1) {
-  return (int)((t1 - tile_base(t0) + kTile - 1) / kTile);
+  return (int)((t1 - tile_base(t0) + kT - 1) / kT);
 }
 }  // namespace q4
 
@@ -894,7 +911,9 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
   uint8_t* ringS = ringV + q4::kRingV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ringS + q4::kRingS);
   int4* metas = reinterpret_cast<int4*>(bars + q4::kWarps * q4::kStages);
-  int* s_gpref = reinterpret_cast<int*>(metas + q4::kWarps * q4::kStages);
+  int64_t* metats = reinterpret_cast<int64_t*>(metas + q4::kWarps * q4::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metats + 2 * q4::kWarps * q4::kStages);
+  int* s_nunion = s_gpref + kMaxGroups + 1;   // the groups' union sizes, read once here
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -906,7 +925,7 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
   ptx::pdl_launch_dependents();
   Tables tb;
   tb.gpref = s_gpref;
-  tb.n_union = plan.n_union;
+  tb.n_union = s_nunion;
   tb.span = plan.span;
   tb.mask = plan.mask;
   tb.rank = plan.rank;
@@ -917,6 +936,7 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
     for (int base = 0; base < geo.n_grp; base += 32) {
       const int gi = base + lane;
       int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+      if (gi < geo.n_grp) s_nunion[gi] = plan.n_union[gi];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, v, off);
@@ -935,16 +955,19 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
   uint8_t* wS = ringS + (size_t)warp * q4::kStages * q4::kSBytes;
   uint64_t* fb = bars + warp * q4::kStages;
   int4* meta = metas + warp * q4::kStages;
-  const int64_t tiles_per_head = L_cap / kTile;
+  int64_t* metat = metats + 2 * warp * q4::kStages;
+  const int64_t blocks_per_head = L_cap / q4::kBlk;
 
   Item iss;
   iss.ntiles = 0;
   iss.grp = iss.u = iss.c = 0;
   iss.t0 = iss.t1 = 0;
   int iss_tile = 0;
-  // the first item of every warp is fixed; later ones come from the counter
+  // the first item of every warp is fixed; later ones come from the counter,
+  // which is not touched at all when the fixed items cover the step
   const int n_static = (int)gridDim.x * (int)(blockDim.x >> 5);
-  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = 0;
+  const bool may_claim = total > n_static;
+  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = total;
   bool have_next = true, claim_issued = false;
   bool exhausted = false;
 
@@ -963,40 +986,106 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
     }
     if (lane == 0) {
       meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      metat[2 * stage] = iss.t0;
+      metat[2 * stage + 1] = iss.t1;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ptx::mbar_arrive_expect_tx(&fb[stage], q4::kKBytes + q4::kVBytes + q4::kSBytes);
-      const int64_t y = q4::tile_base(iss.t0) + (int64_t)iss_tile * kTile;
+      const int64_t y = q4::tile_base(iss.t0) + (int64_t)iss_tile * q4::kT;
+      // the head's last 32-token block may stand alone (L_cap is a multiple
+      // of 32, not of 64); the stage's other half is then never unmasked
+      const uint32_t nb = y + q4::kT <= L_cap ? 2u : 1u;
+      ptx::mbar_arrive_expect_tx(&fb[stage], nb * (2 * q4::kBlkBytes + 2 * q4::kBlk * 4));
       uint8_t* dS = wS + stage * q4::kSBytes;
-      const int64_t blk = ((int64_t)iss.grp * tiles_per_head + y / kTile) * 512;
-      ptx::bulk_load(wK + stage * q4::kKBytes, Kq4 + blk, q4::kKBytes, &fb[stage]);
-      ptx::bulk_load(wV + stage * q4::kVBytes, Vq4 + blk, q4::kVBytes, &fb[stage]);
-      ptx::bulk_load(dS, Ks + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
-      ptx::bulk_load(dS + kTile * 4, Vs + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
+      const int64_t blk = ((int64_t)iss.grp * blocks_per_head + y / q4::kBlk) * 512;
+      ptx::bulk_load(wK + stage * q4::kKBytes, Kq4 + blk, nb * q4::kBlkBytes, &fb[stage]);
+      ptx::bulk_load(wV + stage * q4::kVBytes, Vq4 + blk, nb * q4::kBlkBytes, &fb[stage]);
+      ptx::bulk_load(dS, Ks + (int64_t)iss.grp * L_cap + y, nb * q4::kBlk * 4, &fb[stage]);
+      ptx::bulk_load(dS + q4::kT * 4, Vs + (int64_t)iss.grp * L_cap + y, nb * q4::kBlk * 4, &fb[stage]);
     }
     ++iss_tile;
-    if (!claim_issued && iss.ntiles - iss_tile <= 2) {
+    if (may_claim && !claim_issued && iss.ntiles - iss_tile <= 2) {
       if (lane == 0) it_claim = atomicAdd(plan.counter, 1) + n_static;
       claim_issued = true;
     }
     return true;
   };
 
-  int inflight = 0;
+  int inflight = 0, first_grp = -1;
 #pragma unroll 1
   for (int s = 0; s < q4::kStages; ++s) {
     if (exhausted || !issue(s)) break;
+    if (s == 0) first_grp = iss.grp;
     ++inflight;
   }
 
   const int q4 = lane & 3, r8 = lane >> 2;
-  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+  // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs; pairs 1 and 3
+  // (d + 2, 3 and d + 6, 7) divided by 16.  They depend on the kv group
+  // only: loaded for the first item while its tiles are in flight, and
+  // again only when an item of another group starts.
+  uint32_t qf[NG][D / 32][4];
+  float qs8[NG][2];             // 8 sum_d q'_d of heads 2 q4 and 2 q4 + 1
+  int q_grp = -1;
+  auto load_q = [&](int grp) {
+    const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int h = ng * 8 + r8;
+      const bool ok = h < geo.g;
+      const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
+      // a thread's dimensions 32 J + 8 q4 .. + 7 are 16 contiguous bytes:
+      // four 16-byte loads, all in flight at once
+      uint4 qv[D / 32];
+#pragma unroll
+      for (int J = 0; J < D / 32; ++J)
+        qv[J] = ok ? *reinterpret_cast<const uint4*>(qr + 32 * J + 8 * q4) : make_uint4(0u, 0u, 0u, 0u);
+      float qsum = 0.f;
+#pragma unroll
+      for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          uint32_t v = 0u;
+          if (ok) {
+            const uint32_t w = pr == 0 ? qv[J].x : pr == 1 ? qv[J].y : pr == 2 ? qv[J].z : qv[J].w;
+            float lo, hi;
+            if constexpr (DT == DT_BF16) {
+              lo = __uint_as_float(w << 16);
+              hi = __uint_as_float(w & 0xffff0000u);
+            } else {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+              lo = f.x;
+              hi = f.y;
+            }
+            const float sc = (pr & 1) ? 0.0625f : 1.f;
+            v = ptx::pack2<DT_F16>(lo * sc, hi * sc);
+            // q' as the MMA sees it: the rounded fp16 value, times 16 back
+            const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&v));
+            qsum += (r.x + r.y) * ((pr & 1) ? 16.f : 1.f);
+          }
+          qf[ng][J][pr] = v;
+        }
+      }
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+      // lanes 4 h .. 4 h + 3 hold head h's sum; this thread's columns are
+      // heads 2 q4 and 2 q4 + 1
+      qs8[ng][0] = 8.f * __shfl_sync(0xffffffffu, qsum, 8 * q4);
+      qs8[ng][1] = 8.f * __shfl_sync(0xffffffffu, qsum, 8 * q4 + 4);
+    }
+    q_grp = grp;
+  };
+  if (first_grp >= 0) load_q(first_grp);
+
   float o[NG][D / 16][4];
+  float oc[NG][4];              // sum_t (P vs)'_t 2^-24 of heads 2 q4, 2 q4 + 1
   float m[NG][2], l[NG][2];
+  uint32_t hmask = 0u;          // the item's heads, and this thread's heads' ranks
+  int rk[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
   int stage = 0;
   uint32_t phase = 0;
+  constexpr float kTwo24 = 16777216.f;
 #pragma unroll 1
   while (inflight > 0) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
@@ -1008,43 +1097,25 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
-      {
-        const int nu = tb.n_union[cur.grp];
-        if (cur.u < nu - 1) {
-          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
-          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
-        } else {
-          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
+      cur.t0 = metat[2 * stage];
+      cur.t1 = metat[2 * stage + 1];
+      cur.ntiles = q4::tiles(cur.t0, cur.t1);
+      // the end-of-item tables, read now so that their latency overlaps
+      const int slot_idx = cur.grp * geo.umax + cur.u;
+      hmask = tb.mask[slot_idx];
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = ng * 8 + 2 * q4 + i;
+          rk[ng][i] = r < geo.g ? tb.rank[(size_t)slot_idx * 16 + r] : 0;
         }
-        cur.ntiles = q4::tiles(cur.t0, cur.t1);
-      }
-      const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+      if (cur.grp != q_grp) load_q(cur.grp);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
-        const int h = ng * 8 + r8;
-        const bool ok = h < geo.g;
-        const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
-#pragma unroll
-        for (int J = 0; J < D / 32; ++J) {
-#pragma unroll
-          for (int pr = 0; pr < 4; ++pr) {
-            uint32_t v = 0u;
-            if (ok) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(qr + 32 * J + 8 * q4 + 2 * pr);
-              if constexpr (DT == DT_BF16) {
-                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-                v = ptx::pack2<DT_F16>(lo, hi);
-              } else {
-                v = w;
-              }
-            }
-            qf[ng][J][pr] = v;
-          }
-        }
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) o[ng][mt2][0] = o[ng][mt2][1] = o[ng][mt2][2] = o[ng][mt2][3] = 0.f;
+        oc[ng][0] = oc[ng][1] = oc[ng][2] = oc[ng][3] = 0.f;
         m[ng][0] = m[ng][1] = -INFINITY;
         l[ng][0] = l[ng][1] = 0.f;
       }
@@ -1052,65 +1123,69 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
     const uint32_t aK = ptx::smem_u32(wK + stage * q4::kKBytes);
     const uint32_t aV = ptx::smem_u32(wV + stage * q4::kVBytes);
     const float* sks = reinterpret_cast<const float*>(wS + stage * q4::kSBytes);
-    const float* svs = sks + kTile;
+    const float* svs = sks + q4::kT;
 
-    // S^T = Kq Q^T per 16-token fragment t
-    float s[NG][kSub][4], s2[NG][kSub][4];
+    // S^T = Kq Q^T per 16-token fragment t (block t / 2, rows 16 (t % 2) ..)
+    float s[NG][q4::kSubT][4];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
-      for (int t = 0; t < kSub; ++t)
+      for (int t = 0; t < q4::kSubT; ++t)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[ng][t][i] = s2[ng][t][i] = 0.f;
+        for (int i = 0; i < 4; ++i) s[ng][t][i] = 0.f;
 #pragma unroll
     for (int J = 0; J < D / 32; ++J) {
 #pragma unroll
-      for (int t = 0; t < kSub; ++t) {
-        const int ra = t * 16 + r8, rb = ra + 8;
-        const uint32_t wa = ptx::lds32(aK + ((J * kTile + ra) * 4 + q4) * 4);
-        const uint32_t wb = ptx::lds32(aK + ((J * kTile + rb) * 4 + q4) * 4);
+      for (int t = 0; t < q4::kSubT; ++t) {
+        const uint32_t aB = aK + (t >> 1) * q4::kBlkBytes;
+        const int ra = (t & 1) * 16 + r8, rb = ra + 8;
+        const uint32_t wa = ptx::lds32(aB + ((J * q4::kBlk + ra) * 4 + q4) * 4);
+        const uint32_t wb = ptx::lds32(aB + ((J * q4::kBlk + rb) * 4 + q4) * 4);
         uint32_t a0[4], a1[4];
-        ptx::u4x8_to_f16x2(wa, a0[0], a0[2], a1[0], a1[2]);
-        ptx::u4x8_to_f16x2(wb, a0[1], a0[3], a1[1], a1[3]);
+        ptx::u4x8_to_f16x2_sub(wa, a0[0], a0[2], a1[0], a1[2]);
+        ptx::u4x8_to_f16x2_sub(wb, a0[1], a0[3], a1[1], a1[3]);
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
           ptx::mma16816<DT_F16>(s[ng][t], a0, qf[ng][J][0], qf[ng][J][1]);
-          ptx::mma16816<DT_F16>(s2[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
+          ptx::mma16816<DT_F16>(s[ng][t], a1, qf[ng][J][2], qf[ng][J][3]);
         }
       }
     }
-    // the odd k-steps accumulated apart (two independent MMA chains per fragment)
+    // rows (tokens) r8 and r8 + 8 of each fragment: the K scale, and the V
+    // scale with the 1/16 of the rows stored as 16 n fields (row + 8)
+    float vsc[q4::kSubT][2];
 #pragma unroll
-    for (int ng = 0; ng < NG; ++ng)
+    for (int t = 0; t < q4::kSubT; ++t) {
+      const float k0 = sks[t * 16 + r8], k1 = sks[t * 16 + r8 + 8];
+      vsc[t][0] = svs[t * 16 + r8];
+      vsc[t][1] = svs[t * 16 + r8 + 8] * 0.0625f;
 #pragma unroll
-      for (int t = 0; t < kSub; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[ng][t][i] += s2[ng][t][i];
-    // rows (tokens) r8 and r8 + 8 of each fragment: K / V scales, validity
-    const int64_t tbase = q4::tile_base(cur.t0) + (int64_t)mt.w * kTile;
-    float ksc[kSub][2], vsc[kSub][2];
-    bool valid[kSub][2];
-#pragma unroll
-    for (int t = 0; t < kSub; ++t)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int row = t * 16 + r8 + 8 * i;
-        const int64_t tok = tbase + row;
-        valid[t][i] = tok >= cur.t0 && tok < cur.t1;
-        ksc[t][i] = sks[row];
-        vsc[t][i] = svs[row];
+      for (int ng = 0; ng < NG; ++ng) {
+        s[ng][t][0] = fmaf(s[ng][t][0], kTwo24, -qs8[ng][0]) * k0;
+        s[ng][t][1] = fmaf(s[ng][t][1], kTwo24, -qs8[ng][1]) * k0;
+        s[ng][t][2] = fmaf(s[ng][t][2], kTwo24, -qs8[ng][0]) * k1;
+        s[ng][t][3] = fmaf(s[ng][t][3], kTwo24, -qs8[ng][1]) * k1;
       }
+    }
+    // a tile the item covers only in part: its other tokens get no weight
+    // (their scale slots may hold anything)
+    const int64_t tbase = q4::tile_base(cur.t0) + (int64_t)mt.w * q4::kT;
+    if (tbase < cur.t0 || tbase + q4::kT > cur.t1) {
+      const int lo = (int)(cur.t0 > tbase ? cur.t0 - tbase : 0);
+      const int hi = (int)(cur.t1 - tbase < q4::kT ? cur.t1 - tbase : q4::kT);
 #pragma unroll
-    for (int ng = 0; ng < NG; ++ng)
+      for (int t = 0; t < q4::kSubT; ++t)
 #pragma unroll
-      for (int t = 0; t < kSub; ++t) {
-        s[ng][t][0] = valid[t][0] ? s[ng][t][0] * ksc[t][0] : -INFINITY;
-        s[ng][t][1] = valid[t][0] ? s[ng][t][1] * ksc[t][0] : -INFINITY;
-        s[ng][t][2] = valid[t][1] ? s[ng][t][2] * ksc[t][1] : -INFINITY;
-        s[ng][t][3] = valid[t][1] ? s[ng][t][3] * ksc[t][1] : -INFINITY;
-      }
+        for (int i = 0; i < 2; ++i) {
+          const int row = t * 16 + r8 + 8 * i;
+          if (row >= lo && row < hi) continue;
+          vsc[t][i] = 0.f;
+#pragma unroll
+          for (int ng = 0; ng < NG; ++ng) s[ng][t][2 * i] = s[ng][t][2 * i + 1] = -INFINITY;
+        }
+    }
     const float c = geo.scale_log2e;
-    uint32_t pb[NG][kSub][2];
+    uint32_t pb[NG][q4::kSubT][2];
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
       float mx[2];
@@ -1118,7 +1193,7 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
       for (int i = 0; i < 2; ++i) {
         float v = fmaxf(s[ng][0][i], s[ng][0][i + 2]);
 #pragma unroll
-        for (int t = 1; t < kSub; ++t) v = fmaxf(v, fmaxf(s[ng][t][i], s[ng][t][i + 2]));
+        for (int t = 1; t < q4::kSubT; ++t) v = fmaxf(v, fmaxf(s[ng][t][i], s[ng][t][i + 2]));
         v *= c;
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
         v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
@@ -1135,18 +1210,16 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
       }
       float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-      for (int t = 0; t < kSub; ++t) {
+      for (int t = 0; t < q4::kSubT; ++t) {
         const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
         const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
         const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
         const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
         ls0 += p0 + p2;
         ls1 += p1 + p3;
-        // the V scale of each token weights its P (0 for masked tokens,
-        // whose scale slot may hold anything)
-        const float v0 = valid[t][0] ? vsc[t][0] : 0.f, v1 = valid[t][1] ? vsc[t][1] : 0.f;
-        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * v0, p1 * v0));
-        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * v1, p3 * v1));
+        // the V scale of each token weights its P (0 for masked tokens)
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * vsc[t][0], p1 * vsc[t][0]));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * vsc[t][1], p3 * vsc[t][1]));
       }
       l[ng][0] = l[ng][0] * alpha[0] + ls0;
       l[ng][1] = l[ng][1] * alpha[1] + ls1;
@@ -1158,22 +1231,39 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
           o[ng][mt2][2] *= alpha[0];
           o[ng][mt2][3] *= alpha[1];
         }
+        oc[ng][0] *= alpha[0];
+        oc[ng][1] *= alpha[1];
+        oc[ng][2] *= alpha[0];
+        oc[ng][3] *= alpha[1];
       }
     }
     // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one
     // 4-byte load per row covering both 16-token fragments
 #pragma unroll
     for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-      const uint32_t va = ptx::lds32(aV + ((mt2 * 16 + r8) * 4 + q4) * 4);
-      const uint32_t vb = ptx::lds32(aV + ((mt2 * 16 + r8 + 8) * 4 + q4) * 4);
-      uint32_t a0[4], a1[4];
-      ptx::u4x8_to_f16x2(va, a0[0], a0[2], a1[0], a1[2]);
-      ptx::u4x8_to_f16x2(vb, a0[1], a0[3], a1[1], a1[3]);
 #pragma unroll
-      for (int ng = 0; ng < NG; ++ng) {
-        ptx::mma16816<DT_F16>(o[ng][mt2], a0, pb[ng][0][0], pb[ng][0][1]);
-        ptx::mma16816<DT_F16>(o[ng][mt2], a1, pb[ng][1][0], pb[ng][1][1]);
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t aB = aV + b * q4::kBlkBytes;
+        const uint32_t va = ptx::lds32(aB + ((mt2 * 16 + r8) * 4 + q4) * 4);
+        const uint32_t vb = ptx::lds32(aB + ((mt2 * 16 + r8 + 8) * 4 + q4) * 4);
+        uint32_t a0[4], a1[4];
+        ptx::u4x8_to_f16x2_sub(va, a0[0], a0[2], a1[0], a1[2]);
+        ptx::u4x8_to_f16x2_sub(vb, a0[1], a0[3], a1[1], a1[3]);
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng) {
+          ptx::mma16816<DT_F16>(o[ng][mt2], a0, pb[ng][2 * b][0], pb[ng][2 * b][1]);
+          ptx::mma16816<DT_F16>(o[ng][mt2], a1, pb[ng][2 * b + 1][0], pb[ng][2 * b + 1][1]);
+        }
       }
+    }
+    {
+      // rows of 1s at the scales of the fields: 2^-24 for tokens 2 q4 (+1)
+      // of each 16-token fragment, 16 * 2^-24 for tokens 2 q4 + 8 (+9)
+      const uint32_t one[4] = {0x00010001u, 0x00010001u, 0x00100010u, 0x00100010u};
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+        for (int t = 0; t < q4::kSubT; ++t) ptx::mma16816<DT_F16>(oc[ng], one, pb[ng][t][0], pb[ng][t][1]);
     }
     __syncwarp();
     --inflight;
@@ -1185,8 +1275,6 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
     }
     if (!last) continue;
 
-    const int slot_idx = cur.grp * geo.umax + cur.u;
-    const uint32_t hmask = tb.mask[slot_idx];
     const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
@@ -1198,13 +1286,14 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
         lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const int r = ng * 8 + 2 * q4 + i;
         if (r >= geo.g || !((hmask >> r) & 1u)) continue;
-        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
-        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        const int64_t slot =
+            ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk[ng][i]) * geo.C + cur.c;
         float* dst = plan.po + slot * D + r8;
+        const float corr = -8.f * kTwo24 * oc[ng][i];
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-          dst[mt2 * 16] = o[ng][mt2][i];
-          dst[mt2 * 16 + 8] = o[ng][mt2][i + 2];
+          dst[mt2 * 16] = fmaf(o[ng][mt2][i], kTwo24, corr);
+          dst[mt2 * 16 + 8] = fmaf(o[ng][mt2][i + 2], kTwo24, corr);
         }
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }

@@ -110,7 +110,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 8-byte shared-memory load.
+// 4-byte and 8-byte shared-memory loads.
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -135,20 +135,20 @@ __device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
 }
 
-// Eight 4-bit fields of w, each a signed code c stored as c + 8, at bits
-// 4 i (element 2 i) and 16 + 4 i (element 2 i + 1) -> four fp16 pairs
-// p_i = (element 2 i, element 2 i + 1), exactly: the field becomes the low
-// mantissa bits of the fp16 1024 + n (0x64nn), and subtracting 1032 leaves c.
-__device__ __forceinline__ void u4x8_to_f16x2(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
-  p0 = (w & 0x000F000Fu) | 0x64006400u;
-  p1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;
-  p2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
-  p3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;
-  const uint32_t bias = 0x64086408u;
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p0) : "r"(bias));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p1) : "r"(bias));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p2) : "r"(bias));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(p3) : "r"(bias));
+// Eight 4-bit fields n of w (element 2 i at bits 4 i, element 2 i + 1 at
+// bits 16 + 4 i) -> four fp16 pairs by masking alone: a field left in the low
+// mantissa bits of a half with a zero exponent is the fp16 subnormal
+// n * 2^-24 (pairs 0 and 2: elements 0, 1 and 4, 5), a field at bits 4..7 of
+// the half is 16 n * 2^-24 (pairs 1 and 3: elements 2, 3 and 6, 7).  Every
+// value is exact; the caller folds 2^24, the factor 16 and any offset of
+// the code into its other operand and its epilogue.
+__device__ __forceinline__ void u4x8_to_f16x2_sub(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2,
+                                                  uint32_t& p3) {
+  const uint32_t h = w >> 8;
+  p0 = w & 0x000F000Fu;
+  p1 = w & 0x00F000F0u;
+  p2 = h & 0x000F000Fu;
+  p3 = h & 0x00F000F0u;
 }
 
 // L2 eviction-priority policies (hints only: lines can always be evicted).
