@@ -56,7 +56,8 @@ struct Cfg {
   static constexpr size_t kRing = (size_t)kWarps * kStages * kStage;
   static constexpr size_t kBars = (size_t)kWarps * kStages * 8;
   static constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
-  static constexpr size_t kFixed = 1024 + kRing + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+  static constexpr size_t kMetaT = (size_t)kWarps * kStages * 16;  // the item's (t0, t1) per stage
+  static constexpr size_t kFixed = 1024 + kRing + kBars + kMeta + kMetaT + (size_t)(2 * kMaxGroups + 1) * 4;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -180,7 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRing);
   int4* metas = reinterpret_cast<int4*>(bars + kWarps * C::kStages);
-  int* s_gpref = reinterpret_cast<int*>(metas + kWarps * C::kStages);
+  int64_t* metats = reinterpret_cast<int64_t*>(metas + kWarps * C::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metats + 2 * kWarps * C::kStages);
+  int* s_nunion = s_gpref + kMaxGroups + 1;   // the groups' union sizes, read once here
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::pdl_launch_dependents();
   Tables tb;
   tb.gpref = s_gpref;
-  tb.n_union = plan.n_union;
+  tb.n_union = s_nunion;
   tb.span = plan.span;
   tb.mask = plan.mask;
   tb.rank = plan.rank;
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int base = 0; base < geo.n_grp; base += 32) {
       const int gi = base + lane;
       int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+      if (gi < geo.n_grp) s_nunion[gi] = plan.n_union[gi];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, v, off);
@@ -223,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* wring = ring + (size_t)warp * C::kStages * C::kStage;
   uint64_t* fb = bars + warp * C::kStages;
   int4* meta = metas + warp * C::kStages;
+  int64_t* metat = metats + 2 * warp * C::kStages;
 
   // issue side (lane 0 drives, state kept warp-uniform)
   Item iss;
@@ -256,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      metat[2 * stage] = iss.t0;
+      metat[2 * stage + 1] = iss.t1;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       ptx::mbar_arrive_expect_tx(&fb[stage], C::kStage);
       uint8_t* dK = wring + (size_t)stage * C::kStage;
@@ -290,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t qb[NG][D / 16][2];
   float o[NG][D / 16][4];
   float m[NG][2], l[NG][2];
+  uint32_t hmask = 0u;          // the item's heads, and this thread's heads' ranks
+  int rk[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
@@ -306,17 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
+      cur.t0 = metat[2 * stage];
+      cur.t1 = metat[2 * stage + 1];
+      cur.ntiles = (int)((cur.t1 - cur.t0 + kTile - 1) / kTile);
       {
-        const int nu = tb.n_union[cur.grp];
-        if (cur.u < nu - 1) {
-          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
-          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
-        } else {
-          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
-        }
-        cur.ntiles = (int)((cur.t1 - cur.t0 + kTile - 1) / kTile);
+        // the end-of-item tables, read now so that their latency overlaps
+        const int slot_idx = cur.grp * geo.umax + cur.u;
+        hmask = tb.mask[slot_idx];
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int r = ng * 8 + 2 * q4 + i;
+            rk[ng][i] = r < geo.g ? tb.rank[(size_t)slot_idx * 16 + r] : 0;
+          }
       }
       // B operand of S^T = K Q^T: thread holds Q[head r8][d pair] per k-step
       const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
@@ -447,8 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!last) continue;
 
     // ---- item epilogue: one partial per head that attends this span
-    const int slot_idx = cur.grp * geo.umax + cur.u;
-    const uint32_t hmask = tb.mask[slot_idx];
     const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
@@ -460,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const int r = ng * 8 + 2 * q4 + i;  // head within the group
         if (r >= geo.g || !((hmask >> r) & 1u)) continue;
-        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
-        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        const int64_t slot =
+            ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk[ng][i]) * geo.C + cur.c;
         float* dst = plan.po + slot * D + r8;
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
@@ -502,7 +512,10 @@ constexpr size_t kRingV = (size_t)kWarps * kStages * kVBytes;
 constexpr size_t kRingS = (size_t)kWarps * kStages * kSBytes;
 constexpr size_t kBars = (size_t)kWarps * kStages * 8;
 constexpr size_t kMeta = (size_t)kWarps * kStages * 16;
-constexpr size_t kFixed = 1024 + kRingK + kRingV + kRingS + kBars + kMeta + (size_t)(kMaxGroups + 1) * 4;
+constexpr size_t kMetaT = (size_t)kWarps * kStages * 16;
+constexpr size_t kFixed =
+    1024 + kRingK + kRingV + kRingS + kBars + kMeta + kMetaT + (size_t)(2 * kMaxGroups + 1) * 4;
+static_assert(kFixed <= (size_t)kSmemLimit, "8-bit ring does not fit in shared memory");
 
 // First 32-aligned tile start and tile count of tokens [t0, t1).
 __device__ __forceinline__ int64_t tile_base(int64_t t0) { return t0 & ~(int64_t)(kTile - 1); }
@@ -525,7 +538,9 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   uint8_t* ringS = ringV + q8::kRingV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ringS + q8::kRingS);
   int4* metas = reinterpret_cast<int4*>(bars + q8::kWarps * q8::kStages);
-  int* s_gpref = reinterpret_cast<int*>(metas + q8::kWarps * q8::kStages);
+  int64_t* metats = reinterpret_cast<int64_t*>(metas + q8::kWarps * q8::kStages);
+  int* s_gpref = reinterpret_cast<int*>(metats + 2 * q8::kWarps * q8::kStages);
+  int* s_nunion = s_gpref + kMaxGroups + 1;   // the groups' union sizes, read once here
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -538,7 +553,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   ptx::pdl_launch_dependents();
   Tables tb;
   tb.gpref = s_gpref;
-  tb.n_union = plan.n_union;
+  tb.n_union = s_nunion;
   tb.span = plan.span;
   tb.mask = plan.mask;
   tb.rank = plan.rank;
@@ -549,6 +564,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
     for (int base = 0; base < geo.n_grp; base += 32) {
       const int gi = base + lane;
       int v = gi < geo.n_grp ? plan.n_items[gi] : 0;
+      if (gi < geo.n_grp) s_nunion[gi] = plan.n_union[gi];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, v, off);
@@ -567,6 +583,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   uint8_t* wS = ringS + (size_t)warp * q8::kStages * q8::kSBytes;
   uint64_t* fb = bars + warp * q8::kStages;
   int4* meta = metas + warp * q8::kStages;
+  int64_t* metat = metats + 2 * warp * q8::kStages;
   const int64_t tiles_per_head = L_cap / kTile;
 
   Item iss;
@@ -596,6 +613,8 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
     }
     if (lane == 0) {
       meta[stage] = make_int4(iss.grp, iss.u, iss.c, iss_tile);
+      metat[2 * stage] = iss.t0;
+      metat[2 * stage + 1] = iss.t1;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       ptx::mbar_arrive_expect_tx(&fb[stage], q8::kKBytes + q8::kVBytes + q8::kSBytes);
       const int64_t y = q8::tile_base(iss.t0) + (int64_t)iss_tile * kTile;
@@ -625,6 +644,8 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
   float o[NG][D / 16][4];
   float m[NG][2], l[NG][2];
+  uint32_t hmask = 0u;          // the item's heads, and this thread's heads' ranks
+  int rk[NG][2];
   Item cur;
   cur.grp = cur.u = cur.c = cur.ntiles = 0;
   cur.t0 = cur.t1 = 0;
@@ -641,17 +662,20 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       cur.grp = mt.x;
       cur.u = mt.y;
       cur.c = mt.z;
+      cur.t0 = metat[2 * stage];
+      cur.t1 = metat[2 * stage + 1];
+      cur.ntiles = q8::tiles(cur.t0, cur.t1);
       {
-        const int nu = tb.n_union[cur.grp];
-        if (cur.u < nu - 1) {
-          const int64_t j = tb.span[cur.grp * geo.umax + cur.u];
-          cur.t0 = j * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, (j + 1) * geo.S);
-        } else {
-          cur.t0 = geo.ell * geo.S + (int64_t)cur.c * geo.CH;
-          cur.t1 = min(cur.t0 + geo.CH, geo.pos + 1);
-        }
-        cur.ntiles = q8::tiles(cur.t0, cur.t1);
+        // the end-of-item tables, read now so that their latency overlaps
+        const int slot_idx = cur.grp * geo.umax + cur.u;
+        hmask = tb.mask[slot_idx];
+#pragma unroll
+        for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int r = ng * 8 + 2 * q4 + i;
+            rk[ng][i] = r < geo.g ? tb.rank[(size_t)slot_idx * 16 + r] : 0;
+          }
       }
       const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
 #pragma unroll
@@ -823,8 +847,6 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
     }
     if (!last) continue;
 
-    const int slot_idx = cur.grp * geo.umax + cur.u;
-    const uint32_t hmask = tb.mask[slot_idx];
     const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng) {
@@ -836,8 +858,8 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         lt += __shfl_xor_sync(0xffffffffu, lt, 16);
         const int r = ng * 8 + 2 * q4 + i;
         if (r >= geo.g || !((hmask >> r) & 1u)) continue;
-        const int rk = tb.rank[(size_t)slot_idx * 16 + r];
-        const int64_t slot = ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk) * geo.C + cur.c;
+        const int64_t slot =
+            ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk[ng][i]) * geo.C + cur.c;
         float* dst = plan.po + slot * D + r8;
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
