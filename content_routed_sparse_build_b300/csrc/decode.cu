@@ -489,10 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // cache of quant.cu (d = 128).  Each ring stage holds one 32-token tile: the
 // K rows (TMA, 128-byte swizzle), the d-major V tile and the tile's K and V
 // scales (bulk copies).  Tiles are 32-token aligned; tokens of a tile
-// outside the item are masked.  The MMAs run in fp16: 8-bit values convert
-// to fp16 exactly, and Q is rounded to fp16 once per item.
-//   S^T = ks * (Kq Q^T)                       (tokens x heads)
-//   O^T += Vq^T (vs * P)^T,  l += sum of P    (d x heads)
+// outside the item are masked.  The MMAs run in fp16 on exact values: each
+// code q enters as the fp16 subnormal (q + 128) 2^-24 (an XOR and a byte
+// permute, no conversion arithmetic), and Q is rounded to fp16 once per kv
+// group.  The factor and the offset are folded out:
+//   S^T = ks * (2^24 (Kq' Q^T) - 128 sum_d Q)         (tokens x heads)
+//   O^T += 2^24 (Vq'^T (vs P)^T - 128 * 1^T (vs P)^T), l += sum of P
+// where the last term is one more MMA against a fragment of 2^-24s, so it
+// sums the same rounded (vs P) values the main MMA used.
 // The k order of the K fragments is permuted: thread quad c reads 8
 // consecutive bytes d = 32 J + 8 c .. + 7 of a row, bytes 0-3 feeding k-step
 // 2 J and bytes 4-7 k-step 2 J + 1; Q's fragments are built with the same
@@ -593,7 +597,10 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   int iss_tile = 0;
   // the first item of every warp is fixed; later ones come from the counter
   const int n_static = (int)gridDim.x * (int)(blockDim.x >> 5);
-  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = 0;
+  // the first item of every warp is fixed; later ones come from the counter,
+  // which is not touched at all when the fixed items cover the step
+  const bool may_claim = total > n_static;
+  int it_next = (int)blockIdx.x * (int)(blockDim.x >> 5) + warp, it_claim = total;
   bool have_next = true, claim_issued = false;
   bool exhausted = false;
   const uint64_t pol_stream = ptx::policy_evict_first();  // K rows are read once per step
@@ -626,24 +633,72 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       ptx::bulk_load(dS + kTile * 4, Vs + (int64_t)iss.grp * L_cap + y, kTile * 4, &fb[stage]);
     }
     ++iss_tile;
-    if (!claim_issued && iss.ntiles - iss_tile <= 2) {
+    if (may_claim && !claim_issued && iss.ntiles - iss_tile <= 2) {
       if (lane == 0) it_claim = atomicAdd(plan.counter, 1) + n_static;
       claim_issued = true;
     }
     return true;
   };
 
-  int inflight = 0;
+  int inflight = 0, first_grp = -1;
 #pragma unroll 1
   for (int s = 0; s < q8::kStages; ++s) {
     if (exhausted || !issue(s)) break;
+    if (s == 0) first_grp = iss.grp;
     ++inflight;
   }
 
   const int q4 = lane & 3, r8 = lane >> 2;
-  uint32_t qf[NG][D / 32][4];   // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs
+  // Q of head r8 (+8 ng), d = 32 J + 8 q4 .. + 7, fp16 pairs, and 128 times
+  // the sum of each of this thread's two heads' rounded Q.  They depend on
+  // the kv group only: loaded for the first item while its tiles are in
+  // flight, and again only when an item of another group starts.
+  uint32_t qf[NG][D / 32][4];
+  float qs128[NG][2];
+  int q_grp = -1;
+  auto load_q = [&](int grp) {
+    const int b = grp / geo.Hkv, kvh = grp - b * geo.Hkv;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) {
+      const int h = ng * 8 + r8;
+      const bool ok = h < geo.g;
+      const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
+      // a thread's dimensions 32 J + 8 q4 .. + 7 are 16 contiguous bytes
+      uint4 qv[D / 32];
+#pragma unroll
+      for (int J = 0; J < D / 32; ++J)
+        qv[J] = ok ? *reinterpret_cast<const uint4*>(qr + 32 * J + 8 * q4) : make_uint4(0u, 0u, 0u, 0u);
+      float qsum = 0.f;
+#pragma unroll
+      for (int J = 0; J < D / 32; ++J) {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const uint32_t w = pr == 0 ? qv[J].x : pr == 1 ? qv[J].y : pr == 2 ? qv[J].z : qv[J].w;
+          uint32_t v = w;
+          if constexpr (DT == DT_BF16) {
+            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+            v = ptx::pack2<DT_F16>(lo, hi);
+          }
+          const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&v));
+          qsum += r.x + r.y;
+          qf[ng][J][pr] = v;
+        }
+      }
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+      // lanes 4 h .. 4 h + 3 hold head h's sum; this thread's columns are
+      // heads 2 q4 and 2 q4 + 1
+      qs128[ng][0] = 128.f * __shfl_sync(0xffffffffu, qsum, 8 * q4);
+      qs128[ng][1] = 128.f * __shfl_sync(0xffffffffu, qsum, 8 * q4 + 4);
+    }
+    q_grp = grp;
+  };
+  if (first_grp >= 0) load_q(first_grp);
+
   float o[NG][D / 16][4];
+  float oc[NG][4];              // sum_t (P vs)'_t 2^-24 of heads 2 q4, 2 q4 + 1
   float m[NG][2], l[NG][2];
+  constexpr float kTwo24 = 16777216.f;
   uint32_t hmask = 0u;          // the item's heads, and this thread's heads' ranks
   int rk[NG][2];
   Item cur;
@@ -677,31 +732,12 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
             rk[ng][i] = r < geo.g ? tb.rank[(size_t)slot_idx * 16 + r] : 0;
           }
       }
-      const int b = cur.grp / geo.Hkv, kvh = cur.grp - b * geo.Hkv;
+      if (cur.grp != q_grp) load_q(cur.grp);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
-        const int h = ng * 8 + r8;
-        const bool ok = h < geo.g;
-        const uint16_t* qr = tb.q + (int64_t)(b * geo.Hq + kvh * geo.g + h) * tb.q_stride;
-#pragma unroll
-        for (int J = 0; J < D / 32; ++J) {
-#pragma unroll
-          for (int pr = 0; pr < 4; ++pr) {
-            uint32_t v = 0u;
-            if (ok) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(qr + 32 * J + 8 * q4 + 2 * pr);
-              if constexpr (DT == DT_BF16) {
-                const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-                v = ptx::pack2<DT_F16>(lo, hi);
-              } else {
-                v = w;
-              }
-            }
-            qf[ng][J][pr] = v;
-          }
-        }
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) o[ng][mt2][0] = o[ng][mt2][1] = o[ng][mt2][2] = o[ng][mt2][3] = 0.f;
+        oc[ng][0] = oc[ng][1] = oc[ng][2] = oc[ng][3] = 0.f;
         m[ng][0] = m[ng][1] = -INFINITY;
         l[ng][0] = l[ng][1] = 0.f;
       }
@@ -728,10 +764,10 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         const uint2 wa = ptx::lds64(aK + ptx::sw128(ra, chunk) + 8 * (q4 & 1));
         const uint2 wb = ptx::lds64(aK + ptx::sw128(rb, chunk) + 8 * (q4 & 1));
         uint32_t a0[4], a1[4];
-        ptx::s8x4_to_f16x2(wa.x, a0[0], a0[2]);
-        ptx::s8x4_to_f16x2(wb.x, a0[1], a0[3]);
-        ptx::s8x4_to_f16x2(wa.y, a1[0], a1[2]);
-        ptx::s8x4_to_f16x2(wb.y, a1[1], a1[3]);
+        ptx::s8x4_to_f16x2_sub(wa.x, a0[0], a0[2]);
+        ptx::s8x4_to_f16x2_sub(wb.x, a0[1], a0[3]);
+        ptx::s8x4_to_f16x2_sub(wa.y, a1[0], a1[2]);
+        ptx::s8x4_to_f16x2_sub(wb.y, a1[1], a1[3]);
 #pragma unroll
         for (int ng = 0; ng < NG; ++ng) {
           ptx::mma16816<DT_F16>(s[ng][t], a0, qf[ng][J][0], qf[ng][J][1]);
@@ -760,14 +796,16 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         ksc[t][i] = sks[row];
         vsc[t][i] = svs[row];
       }
+    // the MMA summed q'_d (q_d + 128) 2^-24 over d: the score is
+    // 2^24 acc - 128 sum_d q'_d, times the token's K scale
 #pragma unroll
     for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
       for (int t = 0; t < kSub; ++t) {
-        s[ng][t][0] = valid[t][0] ? s[ng][t][0] * ksc[t][0] : -INFINITY;
-        s[ng][t][1] = valid[t][0] ? s[ng][t][1] * ksc[t][0] : -INFINITY;
-        s[ng][t][2] = valid[t][1] ? s[ng][t][2] * ksc[t][1] : -INFINITY;
-        s[ng][t][3] = valid[t][1] ? s[ng][t][3] * ksc[t][1] : -INFINITY;
+        s[ng][t][0] = valid[t][0] ? fmaf(s[ng][t][0], kTwo24, -qs128[ng][0]) * ksc[t][0] : -INFINITY;
+        s[ng][t][1] = valid[t][0] ? fmaf(s[ng][t][1], kTwo24, -qs128[ng][1]) * ksc[t][0] : -INFINITY;
+        s[ng][t][2] = valid[t][1] ? fmaf(s[ng][t][2], kTwo24, -qs128[ng][0]) * ksc[t][1] : -INFINITY;
+        s[ng][t][3] = valid[t][1] ? fmaf(s[ng][t][3], kTwo24, -qs128[ng][1]) * ksc[t][1] : -INFINITY;
       }
     const float c = geo.scale_log2e;
     uint32_t pb[NG][kSub][2];
@@ -818,6 +856,10 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
           o[ng][mt2][2] *= alpha[0];
           o[ng][mt2][3] *= alpha[1];
         }
+        oc[ng][0] *= alpha[0];
+        oc[ng][1] *= alpha[1];
+        oc[ng][2] *= alpha[0];
+        oc[ng][3] *= alpha[1];
       }
     }
     // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one
@@ -827,14 +869,23 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
       const uint2 va = ptx::lds64(aV + (mt2 * 16 + r8) * 32 + 8 * q4);
       const uint2 vb = ptx::lds64(aV + (mt2 * 16 + r8 + 8) * 32 + 8 * q4);
       uint32_t a0[4], a1[4];
-      ptx::s8x4_to_f16x2(va.x, a0[0], a0[2]);
-      ptx::s8x4_to_f16x2(vb.x, a0[1], a0[3]);
-      ptx::s8x4_to_f16x2(va.y, a1[0], a1[2]);
-      ptx::s8x4_to_f16x2(vb.y, a1[1], a1[3]);
+      ptx::s8x4_to_f16x2_sub(va.x, a0[0], a0[2]);
+      ptx::s8x4_to_f16x2_sub(vb.x, a0[1], a0[3]);
+      ptx::s8x4_to_f16x2_sub(va.y, a1[0], a1[2]);
+      ptx::s8x4_to_f16x2_sub(vb.y, a1[1], a1[3]);
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
         ptx::mma16816<DT_F16>(o[ng][mt2], a0, pb[ng][0][0], pb[ng][0][1]);
         ptx::mma16816<DT_F16>(o[ng][mt2], a1, pb[ng][1][0], pb[ng][1][1]);
+      }
+    }
+    {
+      // a row of 1s at the fields' scale 2^-24: sum_t (P vs)'_t 2^-24 per head
+      const uint32_t one[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};
+#pragma unroll
+      for (int ng = 0; ng < NG; ++ng) {
+        ptx::mma16816<DT_F16>(oc[ng], one, pb[ng][0][0], pb[ng][0][1]);
+        ptx::mma16816<DT_F16>(oc[ng], one, pb[ng][1][0], pb[ng][1][1]);
       }
     }
     __syncwarp();
@@ -861,10 +912,12 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         const int64_t slot =
             ((int64_t)(b * geo.Hq + kvh * geo.g + r) * (geo.topk + 1) + rk[ng][i]) * geo.C + cur.c;
         float* dst = plan.po + slot * D + r8;
+        // 2^24 (acc - 128 * sum_t (P vs)' 2^-24): the codes' offset removed
+        const float corr = -128.f * kTwo24 * oc[ng][i];
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-          dst[mt2 * 16] = o[ng][mt2][i];
-          dst[mt2 * 16 + 8] = o[ng][mt2][i + 2];
+          dst[mt2 * 16] = fmaf(o[ng][mt2][i], kTwo24, corr);
+          dst[mt2 * 16 + 8] = fmaf(o[ng][mt2][i + 2], kTwo24, corr);
         }
         if (r8 == 0) *reinterpret_cast<float2*>(plan.ml + slot * 2) = make_float2(m[ng][i], lt);
       }

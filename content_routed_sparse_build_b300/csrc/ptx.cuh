@@ -135,6 +135,16 @@ __device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
 }
 
+// Four signed 8-bit integers q (the bytes of w) -> two fp16 pairs of
+// subnormals (q + 128) * 2^-24: lo = (b0, b1), hi = (b2, b3).  The offset's
+// XOR and two byte permutes, no arithmetic; every value is exact, and the
+// caller folds 2^24 and the offset into its other operand and its epilogue.
+__device__ __forceinline__ void s8x4_to_f16x2_sub(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0u, 0x4140);
+  hi = __byte_perm(u, 0u, 0x4342);
+}
+
 // Eight 4-bit fields n of w (element 2 i at bits 4 i, element 2 i + 1 at
 // bits 16 + 4 i) -> four fp16 pairs by masking alone: a field left in the low
 // mantissa bits of a half with a zero exponent is the fp16 subnormal
