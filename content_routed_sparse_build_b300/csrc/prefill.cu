@@ -817,16 +817,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 }
 
 // ---------------------------------------------------------------- merge
-// One warp per row of Q: its used spans (sel order) then its local span.
-// The partials of a row are read in batches of kMergeBatch slots with all of
-// a batch's loads in flight at once (one memory round trip per batch; one
-// batch covers topk <= 16).
-constexpr int kMergeBatch = 17;
+// One warp per row of Q, rows in a grid-stride loop.  A row's k + 1 partials
+// are one contiguous block of (k + 1) * d 16-bit values: a bulk copy brings
+// the next row's block into the warp's other shared-memory stage while the
+// warp combines the current one, and its (m, l) and sel entries are read one
+// row ahead into registers.  The combine is two-pass: M = the max of the
+// used slots' m, w_s = 2^(m_s - M) l_s (one exp2 per slot, lane-parallel),
+// O = sum_s w_s o_s / sum_s w_s, lse = M ln 2 + ln sum_s w_s.  Slots are the
+// sel row's used prefix (ranks 0 .. used - 1) and the local span (rank k).
+constexpr int kMergeWarpsMax = 8;
+constexpr size_t kMergeSmemBudget = 96 * 1024;
 
 template <int DT, int E>
-__device__ __forceinline__ void widen_partial(const uint16_t* src, float (&v)[E]) {
+__device__ __forceinline__ void widen_partial(uint32_t saddr, float (&v)[E]) {
   if constexpr (E == 4) {
-    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    const uint2 w = ptx::lds64(saddr);
     const uint32_t ww[2] = {w.x, w.y};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -840,7 +845,7 @@ __device__ __forceinline__ void widen_partial(const uint16_t* src, float (&v)[E]
       }
     }
   } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    const uint32_t w = ptx::lds32(saddr);
     if constexpr (DT == DT_BF16) {
       v[0] = bf16_bits_to_f32(w & 0xffffu);
       v[1] = __uint_as_float(w & 0xffff0000u);
@@ -852,74 +857,134 @@ __device__ __forceinline__ void widen_partial(const uint16_t* src, float (&v)[E]
   }
 }
 
-template <int DT, int D>
-__device__ __forceinline__ void merge_row(const int32_t* __restrict__ sel, const PrefArgs& a, void* __restrict__ O,
-                                          float* __restrict__ lse, int64_t row, int lane) {
-  constexpr int E = D / 32;
-  const int64_t i = row % a.n_q;
-  const int64_t ell = (a.q_pos0 + i) / a.S;
-  const int32_t* srow = sel + row * a.topk;
-  // the sel row and the partials are loaded together: every slot of the row
-  // (ranks 0 .. topk, the local span last) is read whether used or not, and
-  // only the used ones (the sel row's valid prefix, then the local span) are
-  // combined, in rank order
-  const int j0 = lane < a.topk ? srow[lane] : -1;
-  const int j1 = lane + 32 < a.topk ? srow[lane + 32] : -1;
+// A row's per-lane look-ahead: (m, l) of slots lane, lane + 32, lane + 64
+// and its sel entries lane, lane + 32.
+struct MergeAhead {
+  float2 ml[3];
+  int j0, j1;
+};
+
+__device__ __forceinline__ void merge_ahead(const int32_t* __restrict__ sel, const PrefArgs& a, int64_t row,
+                                            int lane, MergeAhead& x) {
   const int nslot = a.topk + 1;
-  const int64_t base = row * (a.topk + 1);
-  float M = -INFINITY, Ls = 0.f, acc[E];
+  const int64_t base = row * nslot;
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  int used = -1;
-  for (int s0 = 0; s0 < nslot; s0 += kMergeBatch) {
-    float2 ml[kMergeBatch];
-    uint2 raw[kMergeBatch];
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + u;
-      if (s < nslot) {
-        ml[u] = a.pml[base + s];
-        const uint16_t* src = a.po + (base + s) * D + lane * E;
-        if constexpr (E == 4) {
-          raw[u] = *reinterpret_cast<const uint2*>(src);
-        } else {
-          raw[u] = make_uint2(*reinterpret_cast<const uint32_t*>(src), 0u);
-        }
-      }
-    }
-    if (used < 0) {
-      bool bad;
-      used = warp_sel_prefix(j0, j1, lane, a.topk, ell, &bad);
-    }
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + u;
-      if (s >= nslot || (s < a.topk && s >= used)) continue;
-      float v[E];
-      widen_partial<DT, E>(reinterpret_cast<const uint16_t*>(&raw[u]), v);
-      const float Mn = fmaxf(M, ml[u].x);
-      const float fa = exp2f(M - Mn), fb = exp2f(ml[u].x - Mn) * ml[u].y;
-      Ls = Ls * fa + fb;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * fa + v[e] * fb;
-      M = Mn;
-    }
+  for (int u = 0; u < 3; ++u) {
+    const int s = lane + 32 * u;
+    x.ml[u] = s < nslot ? a.pml[base + s] : make_float2(-INFINITY, 0.f);
   }
-  const float inv = 1.f / Ls;
-#pragma unroll
-  for (int e = 0; e < E; ++e) store_elem<DT>(O, row * D + lane * E + e, acc[e] * inv);
-  if (lse && lane == 0) lse[row] = M * kLn2 + logf(Ls);
+  const int32_t* srow = sel + row * a.topk;
+  x.j0 = lane < a.topk ? srow[lane] : -1;
+  x.j1 = lane + 32 < a.topk ? srow[lane + 32] : -1;
 }
 
 template <int DT, int D>
-__global__ void __launch_bounds__(256, 2) prefill_merge_kernel(const int32_t* __restrict__ sel, PrefArgs a,
-                                                            void* __restrict__ O, float* __restrict__ lse) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kMergeWarpsMax * 32) prefill_merge_kernel(const int32_t* __restrict__ sel,
+                                                                           PrefArgs a, void* __restrict__ O,
+                                                                           float* __restrict__ lse,
+                                                                           uint32_t* __restrict__ err) {
+  constexpr int E = D / 32;
+  extern __shared__ __align__(128) uint8_t msm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const int nslot = a.topk + 1;
+  const uint32_t row_bytes = (uint32_t)nslot * D * 2;   // a multiple of 16
+  uint8_t* ring = msm + (size_t)warp * 2 * row_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(msm + (size_t)nw * 2 * row_bytes) + 2 * warp;
+  if (lane == 0) {
+    ptx::mbar_init(&bars[0], 1);
+    ptx::mbar_init(&bars[1], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
   const int64_t n_rows = (int64_t)a.B * a.Hq * a.n_q;
-  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < n_rows; row += (int64_t)gridDim.x * 8)
-    merge_row<DT, D>(sel, a, O, lse, row, lane);
+  const int64_t stride = (int64_t)gridDim.x * nw;
+  int64_t row = (int64_t)blockIdx.x * nw + warp;
+  auto issue = [&](int64_t r, int st) {
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ptx::mbar_arrive_expect_tx(&bars[st], row_bytes);
+      ptx::bulk_load(ring + (size_t)st * row_bytes, a.po + r * nslot * D, row_bytes, &bars[st]);
+    }
+  };
+  MergeAhead cur, nxt;
+  if (row < n_rows) {
+    issue(row, 0);
+    merge_ahead(sel, a, row, lane, cur);
+  }
+  int st = 0;
+  uint32_t phb = 0u;            // bit st: the phase stage st waits for next
+  bool pending_other = false;   // a copy in flight in stage st ^ 1
+  for (; row < n_rows; row += stride) {
+    const int64_t rn = row + stride;
+    pending_other = rn < n_rows;
+    if (pending_other) {
+      issue(rn, st ^ 1);
+      merge_ahead(sel, a, rn, lane, nxt);
+    }
+    // the used slots and their weights
+    const int64_t i = row % a.n_q;
+    const int64_t ell = (a.q_pos0 + i) / a.S;
+    bool bad;
+    const int used = warp_sel_prefix(cur.j0, cur.j1, lane, a.topk, ell, &bad);
+    float w[3];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      const int s = lane + 32 * u;
+      const bool ok = s < nslot && (s < used || s == a.topk);
+      w[u] = ok ? cur.ml[u].x : -INFINITY;
+      mx = fmaxf(mx, w[u]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float lsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      w[u] = w[u] == -INFINITY ? 0.f : exp2f(w[u] - mx) * cur.ml[u].y;
+      lsum += w[u];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (!ptx::mbar_wait(&bars[st], (phb >> st) & 1u)) {
+      if (lane == 0) flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+      break;
+    }
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const uint32_t sbase = ptx::smem_u32(ring + (size_t)st * row_bytes) + lane * E * 2;
+    for (int s = 0; s < nslot; ++s) {
+      if (s >= used && s != a.topk) continue;   // warp-uniform
+      const float ws = __shfl_sync(0xffffffffu, s < 32 ? w[0] : s < 64 ? w[1] : w[2], s & 31);
+      float v[E];
+      widen_partial<DT, E>(sbase + (uint32_t)s * D * 2, v);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(ws, v[e], acc[e]);
+    }
+    const float inv = 1.f / lsum;
+#pragma unroll
+    for (int e = 0; e < E; ++e) store_elem<DT>(O, row * D + lane * E + e, acc[e] * inv);
+    if (lse && lane == 0) lse[row] = mx * kLn2 + logf(lsum);
+    phb ^= 1u << st;
+    st ^= 1;
+    cur = nxt;
+    pending_other = false;
+    __syncwarp();   // every lane is done with this stage before it is refilled
+  }
+  // after a timeout: let this warp's own copy in flight land before exiting
+  if (pending_other && !ptx::mbar_wait(&bars[st ^ 1], (phb >> (st ^ 1)) & 1u) && lane == 0)
+    flag_error(err, SSA_DEVERR_WAIT_TIMEOUT);
+}
+
+// Warps per merge CTA: as many as two stages of a row's partials fit in the
+// per-CTA shared-memory budget, at most 8.
+int merge_warps(const Problem& pr) {
+  const size_t row_bytes = (size_t)(pr.topk + 1) * pr.d * 2;
+  const size_t w = kMergeSmemBudget / (2 * row_bytes + 16);
+  return (int)(w < 1 ? 1 : w > (size_t)kMergeWarpsMax ? kMergeWarpsMax : w);
 }
 
 PrefArgs make_args(const Problem& pr, int64_t n_q, int64_t q_pos0, void* ws, const PrefLayout& lay) {
@@ -977,8 +1042,14 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t 
                  tmK, tmV, Q, a, err);
   if (e != cudaSuccess) return e;
   const int64_t n_rows = (int64_t)pr.B * pr.Hq * n_q;
-  const int64_t merge_ctas = min((n_rows + 7) / 8, (int64_t)device_sm_count() * 8);
-  return launch_pdl(prefill_merge_kernel<DT, D>, dim3((unsigned)merge_ctas), dim3(256), 0, st, sel, a, O, lse);
+  const int mw = merge_warps(pr);
+  const size_t msmem = (size_t)mw * (2 * (size_t)(pr.topk + 1) * D * 2 + 16);
+  static bool mattr_done[kMaxDevices] = {};
+  e = ensure_smem_attr(prefill_merge_kernel<DT, D>, kMergeSmemBudget + kMergeWarpsMax * 16, mattr_done);
+  if (e != cudaSuccess) return e;
+  const int64_t merge_ctas = min((n_rows + mw - 1) / mw, (int64_t)device_sm_count() * 3);
+  return launch_pdl(prefill_merge_kernel<DT, D>, dim3((unsigned)merge_ctas), dim3(mw * 32), msmem, st, sel, a, O,
+                    lse, err);
 }
 
 }  // namespace
