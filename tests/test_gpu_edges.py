@@ -155,8 +155,8 @@ def test_empty_chunk_is_a_no_op():
     assert bool((sel == 7).all()) and bool((O == 3.0).all())
 
 
-@pytest.mark.parametrize("q8", [False, True])
-def test_decode_step_with_mapped_host_buffers(q8):
+@pytest.mark.parametrize("cache", ["16", "q8", "q4"])
+def test_decode_step_with_mapped_host_buffers(cache):
     """The one-call steps take page-locked host Q, sel, O and lse directly
     (the route reads Q once over the link, the merge writes O in place) and
     give the same bits as with device buffers; pageable host memory is
@@ -169,13 +169,20 @@ def test_decode_step_with_mapped_host_buffers(q8):
     p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, w.dtype)
     summ = torch.zeros((w.B, w.Hkv, w.n_spans, w.d), dtype=torch.float32, device=dev)
     ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE, dev)
-    if q8:
+    if cache == "q8":
         Kq, Ks, Vq, Vs = ssa.q8_cache(p, dev)
         ssa.ssa_quantize_kv(p, K, V, 0, w.L, Kq, Ks, Vq, Vs)
         ssa.ssa_build_summaries_q8(p, Kq, Ks, 0, w.n_spans, summ)
 
         def step(q, pos, sel, O, lse):
             ssa.ssa_decode_step_q8(p, q, pos, summ, Kq, Ks, Vq, Vs, sel, O, lse, ws)
+    elif cache == "q4":
+        Kq, Ks, Vq, Vs = ssa.q4_cache(p, dev)
+        ssa.ssa_quantize_kv4(p, K, V, 0, w.L, Kq, Ks, Vq, Vs)
+        ssa.ssa_build_summaries_q4(p, Kq, Ks, 0, w.n_spans, summ)
+
+        def step(q, pos, sel, O, lse):
+            ssa.ssa_decode_step_q4(p, q, pos, summ, Kq, Ks, Vq, Vs, sel, O, lse, ws)
     else:
         ssa.ssa_build_summaries(p, K, 0, w.n_spans, summ)
 
