@@ -259,12 +259,12 @@ class DecodeBench:
             ssa.ssa_decode_step_q4(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.Kq, self.Ks, self.Vq,
                                    self.Vs, self.sels[i], self.O, self.lse, self.ws)
             return
-        if not self.group:
-            ssa.ssa_decode_step(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.K, self.V, self.sels[i],
-                                self.O, self.lse, self.ws)
+        if self.group:
+            ssa.ssa_decode_step_group(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.K, self.V,
+                                      self.sels[i], self.O, self.lse, self.ws)
             return
-        self.route(i)
-        self.attend(i)
+        ssa.ssa_decode_step(self.p, self.qs[i], self.w.q_pos0 + i, self.summ, self.K, self.V, self.sels[i],
+                            self.O, self.lse, self.ws)
 
     def graph(self, fn, n):
         """A CUDA graph of fn(0 .. n-1) (query index modulo the 256 queries)."""
@@ -489,7 +489,8 @@ def bench_decode_group(w, dev, steps, ws_n):
     kv-head group): each group's heads attend the same k spans, so a step
     streams k spans plus the local span per kv-head."""
     db = DecodeBench(w, dev, group=True)
-    return variant_line(db, steps, ws_n, {"routing": "group-shared (one top-k per kv-head group)"})
+    return variant_line(db, steps, ws_n, {"routing": "group-shared (one top-k per kv-head group), "
+                                                     "ssa_decode_step_group"})
 
 
 def bench_decode_10m(dev, steps, ws_n, cpu_leg):

@@ -203,6 +203,17 @@ def ssa_decode_step(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor
     _check(rc, "ssa_decode_step")
 
 
+def ssa_decode_step_group(p: ssa_params, Q: torch.Tensor, pos: int, summ: torch.Tensor, K: torch.Tensor,
+                          V: torch.Tensor, sel: torch.Tensor, O: torch.Tensor, lse: torch.Tensor | None,
+                          ws: torch.Tensor | None, stream=None) -> None:
+    f = lib().ssa_decode_step_group
+    f.argtypes = [ctypes.POINTER(ssa_params), _P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    f.restype = ctypes.c_int
+    wp, wn = _ws_args(ws)
+    _check(f(ctypes.byref(p), _ptr(Q), int(pos), _ptr(summ), _ptr(K), _ptr(V), _ptr(sel), _ptr(O), _ptr(lse), wp,
+             wn, _stream(stream)), "ssa_decode_step_group")
+
+
 def ssa_attend_prefill(p: ssa_params, Q: torch.Tensor, n_q: int, q_pos0: int, K: torch.Tensor,
                        V: torch.Tensor, sel: torch.Tensor, O: torch.Tensor,
                        lse: torch.Tensor | None, ws: torch.Tensor | None, stream=None) -> None:

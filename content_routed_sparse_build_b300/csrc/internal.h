@@ -114,10 +114,14 @@ cudaError_t launch_attend_decode(const Problem& pr, const void* Q, int64_t pos, 
                                  cudaStream_t st);
 
 // A whole decode step (16-bit types, the fast decode path): route with the
-// plan built in the route kernel's cluster, then attend with the merges in
-// the attend kernel's tail -- two launches.
+// plan built in the route kernel's cluster, then the attention and the
+// merge -- three launches.  The group variant selects one top-k per kv-head
+// group from the summed queries.
 cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, const float* summ, const void* K,
                                const void* V, int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_decode_step_group(const Problem& pr, const void* Q, int64_t pos, const float* summ,
+                                     const void* K, const void* V, int32_t* sel, void* O, float* lse, void* ws,
+                                     cudaStream_t st);
 cudaError_t launch_decode_step_q8(const Problem& pr, const void* Q, int64_t pos, const float* summ,
                                   const int8_t* Kq, const float* Ks, const int8_t* Vq, const float* Vs,
                                   int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st);

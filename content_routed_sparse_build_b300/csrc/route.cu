@@ -131,6 +131,10 @@ __device__ __forceinline__ void merge_best_desc(uint64_t (&L)[E], const uint64_t
 // With PLAN (a whole decode step) the winners also go to CTA 0, which after
 // a second cluster barrier builds the group's decode plan (decode_plan.cuh)
 // for the attend kernel that follows.
+// With GRP (group-shared selection) the CTAs score one query per kv-head,
+// the sum of the group's g queries, each element summed over the heads in
+// order in fp32 (the group router's own sum, so the selections are its
+// bits), and the winners are every head's selection.
 constexpr int kBlk = 64;
 
 template <int G, int D, int E>
@@ -142,7 +146,7 @@ struct DecodeRouteSmem {
   dplan::PlanSmem ps;                    // winners in span order and plan scratch (CTA 0)
 };
 
-template <int DT, int D, int G, int E, bool PLAN>
+template <int DT, int D, int G, int E, bool PLAN, bool GRP>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
     route_decode_kernel(const void* __restrict__ Q, const float* __restrict__ summ,
                         int32_t* __restrict__ sel, float* __restrict__ sel_score, int Hq, int Hkv,
@@ -158,6 +162,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int g = Hq / Hkv;
+  const int gs = GRP ? 1 : g;   // query rows scored: each head, or the group's sum
   const int64_t ell = pos / S;
   const int64_t chunk = (ell + kCluster - 1) / kCluster;
   const int64_t lo = min(ell, (int64_t)rank * chunk);
@@ -203,17 +208,31 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
           if (tid + 256 * u < nvec) qdst[tid + 256 * u] = raw[u];
       }
     }
+    if constexpr (GRP) {
+      // the group's summed query, four dimensions per thread
+      if (tid < D / 4) {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int h = 0; h < g; ++h) {
+          const int64_t base = (int64_t)(b * Hq + kvh * g + h) * D + 4 * tid;
 #pragma unroll
-    for (int u = 0; u < (G * D / V + 255) / 256; ++u) {
-      const int x = tid + 256 * u;
-      if (x < nvec) {
-        float f[8];
-        unpack16<DT>(raw[u], f);
+          for (int c = 0; c < 4; ++c) s4[c] += load_elem<DT>(Q, base + c);
+        }
+        *reinterpret_cast<float4*>(&sm.q[0][(tid & 3) * kQS + 4 * (tid >> 2)]) =
+            make_float4(s4[0], s4[1], s4[2], s4[3]);
+      }
+    } else {
 #pragma unroll
-        for (int c = 0; c < V; c += 4) {
-          const int e = x * V + c, hl = e / D, d = e - hl * D, ff = d >> 2;
-          *reinterpret_cast<float4*>(&sm.q[hl][(ff & 3) * kQS + 4 * (ff >> 2)]) =
-              make_float4(f[c], f[c + 1], f[c + 2], f[c + 3]);
+      for (int u = 0; u < (G * D / V + 255) / 256; ++u) {
+        const int x = tid + 256 * u;
+        if (x < nvec) {
+          float f[8];
+          unpack16<DT>(raw[u], f);
+#pragma unroll
+          for (int c = 0; c < V; c += 4) {
+            const int e = x * V + c, hl = e / D, d = e - hl * D, ff = d >> 2;
+            *reinterpret_cast<float4*>(&sm.q[hl][(ff & 3) * kQS + 4 * (ff >> 2)]) =
+                make_float4(f[c], f[c + 1], f[c + 2], f[c + 3]);
+          }
         }
       }
     }
@@ -237,7 +256,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
         for (int i = 0; i < NL; ++i) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            if (h < g) {
+            if (h < gs) {
               const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][qq * kQS + 4 * i]);
               acc[h] = fmaf(qv.x, sv[i].x, acc[h]);
               acc[h] = fmaf(qv.y, sv[i].y, acc[h]);
@@ -249,7 +268,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        if (h < g) {
+        if (h < gs) {
           float a = acc[h];
           a += __shfl_xor_sync(0xffffffffu, a, 1);
           a += __shfl_xor_sync(0xffffffffu, a, 2);
@@ -262,7 +281,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
 #pragma unroll
     for (int hh = 0; hh < HPW; ++hh) {
       const int h = warp + 8 * hh;
-      if (h < g) {
+      if (h < gs) {
         uint64_t blk[2] = {sm.sc[h][lane], sm.sc[h][lane + 32]};
         bitonic_sort_desc<2>(blk, lane);
         if constexpr (E == 1) {
@@ -279,14 +298,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
 #pragma unroll
   for (int hh = 0; hh < HPW; ++hh) {
     const int h = warp + 8 * hh;
-    if (h < g) {
+    if (h < gs) {
       uint64_t* dst = cluster.map_shared_rank(&sm.recv[rank][0], h);
 #pragma unroll
       for (int i = 0; i < E; ++i) dst[i * 32 + lane] = L[hh][i];
     }
   }
   cluster.sync();
-  if (rank < g) {
+  if (rank < gs) {
     const int h = rank;
     for (int lev = 0; lev < 4; ++lev) {
       const int a = warp << (lev + 1), c = a + (1 << lev);
@@ -312,10 +331,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
         const int x = lane + 32 * i;
         n += __popc(__ballot_sync(0xffffffffu, x < topk && w[x] != 0ull));
       }
-      const int64_t row = (int64_t)b * Hq + kvh * g + h;
-      int32_t* out = sel + row * topk;
-      float* osc = sel_score ? sel_score + row * topk : nullptr;
-      int* pj = PLAN ? cluster.map_shared_rank(&sm.ps.sj[h][0], 0) : nullptr;
+      // the heads this selection belongs to: head h, or every head of the group
+      const int h0 = GRP ? 0 : h, h1 = GRP ? g : h + 1;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int x = lane + 32 * i;
@@ -323,16 +340,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(256, 1)
           const int jx = entry_span(w[x]);
           int p = 0;
           for (int y = 0; y < n; ++y) p += entry_span(w[y]) < jx;
-          out[p] = jx;
-          if (osc) osc[p] = entry_score(w[x]);
-          if constexpr (PLAN) pj[p] = jx;
+          for (int ht = h0; ht < h1; ++ht) {
+            const int64_t row = (int64_t)b * Hq + kvh * g + ht;
+            sel[row * topk + p] = jx;
+            if (sel_score) sel_score[row * topk + p] = entry_score(w[x]);
+            if constexpr (PLAN) *cluster.map_shared_rank(&sm.ps.sj[ht][p], 0) = jx;
+          }
         } else if (x < topk) {
-          out[x] = -1;
-          if (osc) osc[x] = __int_as_float(0x7fc00000);
+          for (int ht = h0; ht < h1; ++ht) {
+            const int64_t row = (int64_t)b * Hq + kvh * g + ht;
+            sel[row * topk + x] = -1;
+            if (sel_score) sel_score[row * topk + x] = __int_as_float(0x7fc00000);
+          }
         }
       }
       if constexpr (PLAN) {
-        if (lane == 0) *cluster.map_shared_rank(&sm.ps.nv[h], 0) = n;
+        if (lane < h1 - h0) *cluster.map_shared_rank(&sm.ps.nv[h0 + lane], 0) = n;
       }
     }
   }
@@ -480,7 +503,7 @@ __global__ void __launch_bounds__(256) route_prefill_kernel(
   }
 }
 
-template <int DT, int D, int G, int E, bool PLAN>
+template <int DT, int D, int G, int E, bool PLAN, bool GRP>
 cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ,
                                 int32_t* sel, float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo,
                                 cudaStream_t st) {
@@ -491,29 +514,30 @@ cudaError_t launch_decode_route(const Problem& pr, const void* Q, int64_t q_pos0
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, E, PLAN>,
+    e = cudaFuncSetAttribute(route_decode_kernel<DT, D, G, E, PLAN, GRP>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  return launch_pdl(route_decode_kernel<DT, D, G, E, PLAN>, grid, dim3(256), 0, st, Q, summ, sel, sel_score,
+  return launch_pdl(route_decode_kernel<DT, D, G, E, PLAN, GRP>, grid, dim3(256), 0, st, Q, summ, sel, sel_score,
                     pr.Hq, pr.Hkv, q_pos0, pr.S, pr.topk, pr.ns_cap, plan, geo);
 }
 
-template <int DT, int D, int G, bool PLAN>
+template <int DT, int D, int G, bool PLAN, bool GRP>
 cudaError_t decode_route_e(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ, int32_t* sel,
                            float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo, cudaStream_t st) {
   // level-1 lists of 32 entries hold the best k for k <= 32, else 64
-  if (pr.topk <= 32) return launch_decode_route<DT, D, G, 1, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  return launch_decode_route<DT, D, G, 2, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.topk <= 32)
+    return launch_decode_route<DT, D, G, 1, PLAN, GRP>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return launch_decode_route<DT, D, G, 2, PLAN, GRP>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
 }
 
-template <int DT, int D, bool PLAN>
+template <int DT, int D, bool PLAN, bool GRP = false>
 cudaError_t decode_route_g(const Problem& pr, const void* Q, int64_t q_pos0, const float* summ, int32_t* sel,
                            float* sel_score, const dplan::Plan& plan, const dplan::Geo& geo, cudaStream_t st) {
-  if (pr.g <= 4) return decode_route_e<DT, D, 4, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  if (pr.g <= 8) return decode_route_e<DT, D, 8, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
-  return decode_route_e<DT, D, 16, PLAN>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.g <= 4) return decode_route_e<DT, D, 4, PLAN, GRP>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  if (pr.g <= 8) return decode_route_e<DT, D, 8, PLAN, GRP>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
+  return decode_route_e<DT, D, 16, PLAN, GRP>(pr, Q, q_pos0, summ, sel, sel_score, plan, geo, st);
 }
 
 template <int DT, int D>
@@ -546,6 +570,23 @@ cudaError_t launch_decode_step(const Problem& pr, const void* Q, int64_t pos, co
   else
     e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
                             : decode_route_g<DT_F16, 64, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
+  if (e != cudaSuccess) return e;
+  return launch_attend_decode_planned(pr, plan.q, K, V, O, lse, plan, geo, ws_error(ws), st);
+}
+
+cudaError_t launch_decode_step_group(const Problem& pr, const void* Q, int64_t pos, const float* summ,
+                                     const void* K, const void* V, int32_t* sel, void* O, float* lse, void* ws,
+                                     cudaStream_t st) {
+  dplan::Plan plan;
+  dplan::Geo geo;
+  decode_plan_args(pr, pos, ws, &plan, &geo);
+  cudaError_t e;
+  if (pr.d == 128)
+    e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 128, true, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
+                            : decode_route_g<DT_F16, 128, true, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
+  else
+    e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 64, true, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)
+                            : decode_route_g<DT_F16, 64, true, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st);
   if (e != cudaSuccess) return e;
   return launch_attend_decode_planned(pr, plan.q, K, V, O, lse, plan, geo, ws_error(ws), st);
 }

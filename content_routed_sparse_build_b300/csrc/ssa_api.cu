@@ -198,6 +198,25 @@ int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, const float
   return cuda_status(launch_attend_rows(pr, Q, 1, pos, K, V, sel, O, lse, ws_error(ws), st));
 }
 
+int ssa_decode_step_group(const ssa_params* p, const void* Q, int64_t pos, const float* summ, const void* K,
+                          const void* V, int32_t* sel, void* O, float* lse, void* ws, size_t ws_bytes,
+                          void* stream) {
+  Problem pr;
+  int rc = check_params(p, &pr);
+  if (rc != SSA_OK) return rc;
+  if (!decode_fast_supported(pr)) return SSA_ERR_UNSUPPORTED;
+  if (pos < 0 || pos >= pr.L) return SSA_ERR_INVALID_ARG;
+  if (!Q || !summ || !K || !V || !sel || !O) return SSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(summ) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    return SSA_ERR_INVALID_ARG;
+  rc = check_ws(pr, 1, SSA_OP_DECODE, ws, ws_bytes);
+  if (rc != SSA_OK) return rc;
+  if (!device_accessible(Q) || !device_accessible(sel) || !device_accessible(O) || !device_accessible(lse))
+    return SSA_ERR_INVALID_ARG;
+  return cuda_status(launch_decode_step_group(pr, Q, pos, summ, K, V, sel, O, lse, ws,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int ssa_attend_prefill(const ssa_params* p, const void* Q, int64_t n_q, int64_t q_pos0,
                        const void* K, const void* V, const int32_t* sel, void* O, float* lse,
                        void* ws, size_t ws_bytes, void* stream) {

@@ -186,6 +186,23 @@ SSA_API int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, con
                             void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * One whole decode step with group-shared selection: ssa_route_group
+ * (n_q = 1) followed by ssa_attend_decode, in three launches (the router
+ * sums each group's queries in fp32 in head order, as ssa_route_group does,
+ * scores the sum, writes the group's selection to all g heads' sel rows and
+ * builds the attend plan in its cluster; then the attention and the merge).
+ * Selections, O and lse are bit-identical to the two calls.  Arguments as for
+ * ssa_decode_step; ws as for ssa_attend_decode (ssa_workspace_size(p, 1,
+ * SSA_OP_DECODE) bytes; no group-routing workspace is needed).  Q, sel, O
+ * and lse may be mapped page-locked host memory.  16-bit types and the
+ * shapes of the fast decode path only (ssa_attend_path(p, 1, SSA_OP_DECODE)
+ * == SSA_PATH_FAST); otherwise SSA_ERR_UNSUPPORTED.
+ */
+SSA_API int ssa_decode_step_group(const ssa_params* p, const void* Q, int64_t pos, const float* summ,
+                                  const void* K, const void* V, int32_t* sel, void* O, float* lse,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Chunked-prefill attention for n_q queries at positions q_pos0 .. q_pos0 +
  * n_q - 1 (superlinear post: chunked prefill against the kept cache; the
  * attention itself as for ssa_attend_decode).  Work is dispatched span-major:

@@ -196,6 +196,28 @@ def test_q4_validation():
 
 
 @needs_no_gpu
+def test_decode_step_group_validation():
+    p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
+    L = ssa.lib()
+    L.ssa_decode_step_group.argtypes = [ctypes.POINTER(ssa.ssa_params), ctypes.c_void_p, ctypes.c_int64] + \
+        [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p]
+    need = ssa.ssa_workspace_size(p, 1, ssa.SSA_OP_DECODE)
+    step = lambda p, pos, ws, n, **kw: L.ssa_decode_step_group(
+        ctypes.byref(p), kw.get("Q", FAKE), pos, kw.get("summ", FAKE), FAKE, FAKE, kw.get("sel", FAKE), FAKE,
+        None, ws, n, None)
+    assert step(p, 4096, FAKE, need) == ssa.SSA_ERR_INVALID_ARG        # pos == L
+    assert step(p, -1, FAKE, need) == ssa.SSA_ERR_INVALID_ARG
+    assert step(p, 10, FAKE, need, summ=None) == ssa.SSA_ERR_INVALID_ARG
+    assert step(p, 10, FAKE, need, sel=None) == ssa.SSA_ERR_INVALID_ARG
+    assert step(p, 10, FAKE, need, Q=ctypes.c_void_p(4098)) == ssa.SSA_ERR_INVALID_ARG
+    assert step(p, 10, None, 0) == ssa.SSA_ERR_WORKSPACE
+    assert step(p, 10, FAKE, need - 1) == ssa.SSA_ERR_WORKSPACE
+    # only the fast decode path: fp32 and d = 96 are refused
+    assert step(ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.float32), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+    assert step(ssa.params(1, 8, 2, 96, 4096, 64, 8, 1), 10, FAKE, need) == ssa.SSA_ERR_UNSUPPORTED
+
+
+@needs_no_gpu
 def test_decode_step_validation():
     p = ssa.params(1, 8, 2, 128, 4096, 64, 8, torch.bfloat16)
     L = ssa.lib()

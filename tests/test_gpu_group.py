@@ -72,11 +72,14 @@ PREFILL_CASES = [
 
 
 def _decode_run(w, Q, K, V):
+    """route_group + attend per step; where the fast decode path applies, the
+    one-call group step runs beside them and must give the same bits."""
     run = GpuRun(w, Q, K, V)
     run.summaries()
     p = run.p_full
     ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE)
     wsg = ssa.workspace(p, 1, ssa.SSA_OP_ROUTE_GROUP)
+    fused = ssa.ssa_attend_path(p, 1, ssa.SSA_OP_DECODE) == ssa.SSA_PATH_FAST
     sels, outs, lses = [], [], []
     for s in range(w.n_q):
         q = run.Q[s].contiguous()
@@ -85,6 +88,10 @@ def _decode_run(w, Q, K, V):
         lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
         ssa.ssa_route_group(p, q, 1, w.q_pos0 + s, run.summ, sel, None, wsg)
         ssa.ssa_attend_decode(p, q, w.q_pos0 + s, run.K, run.V, sel, O, lse, ws)
+        if fused:
+            sel2, O2, lse2 = torch.full_like(sel, 7), torch.empty_like(O), torch.empty_like(lse)
+            ssa.ssa_decode_step_group(p, q, w.q_pos0 + s, run.summ, run.K, run.V, sel2, O2, lse2, ws)
+            assert torch.equal(sel2, sel) and torch.equal(O2, O) and torch.equal(lse2, lse), s
         sels.append(sel.reshape(-1, w.topk))
         outs.append(O.reshape(-1, w.d))
         lses.append(lse.reshape(-1))
