@@ -62,12 +62,20 @@ struct Cfg {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Tokens per work item: aim at about two items per warp of the GPU for the
-// largest possible union, between 64 and 1024 tokens (a power of two).
-int chunk_tokens(const Problem& pr, int n_warps_total) {
-  const double work = (double)pr.B * pr.Hkv * (pr.g * pr.topk + 1) * (double)pr.S;
-  double ch = work / (2.0 * n_warps_total);
+// Tokens per work item, a power of two from 64 to 1024.  Per-head
+// selection: about two items per warp of the GPU for the largest possible
+// union (g k + 1 spans per group).  Group-shared selection, whose union is
+// always k + 1 spans: the smallest size that gives at most one item per
+// warp.
+int chunk_tokens(const Problem& pr, int n_warps_total, bool group) {
   int c = 64;
+  if (group) {
+    const double work = (double)pr.B * pr.Hkv * (pr.topk + 1) * (double)pr.S;
+    while (c < 1024 && (double)c * n_warps_total < work) c *= 2;
+    return c;
+  }
+  const double work = (double)pr.B * pr.Hkv * (pr.g * pr.topk + 1) * (double)pr.S;
+  const double ch = work / (2.0 * n_warps_total);
   while (c < 1024 && 2.0 * c <= ch) c *= 2;
   return c;
 }
@@ -77,13 +85,20 @@ struct Layout {
   int C, CH;
 };
 
-Layout layout(const Problem& pr) {
+// The decode workspace holds the partial slots of either kind of step: the
+// regions are sized for the smaller item size (more chunks per span), and a
+// step's slots use its own C as the stride.
+Layout layout(const Problem& pr, bool group = false) {
   Layout l;
-  l.CH = chunk_tokens(pr, device_sm_count() * kWarps);
+  const int ch_head = chunk_tokens(pr, device_sm_count() * kWarps, false);
+  const int ch_group = chunk_tokens(pr, device_sm_count() * kWarps, true);
+  l.CH = group ? ch_group : ch_head;
   l.C = (pr.S + l.CH - 1) / l.CH;
+  const int ch_min = ch_head < ch_group ? ch_head : ch_group;
+  const size_t c_alloc = (size_t)((pr.S + ch_min - 1) / ch_min);
   const size_t n_grp = (size_t)pr.B * pr.Hkv;
   const size_t umax = (size_t)pr.g * pr.topk + 1;
-  const size_t parts = (size_t)pr.B * pr.Hq * (pr.topk + 1) * l.C;
+  const size_t parts = (size_t)pr.B * pr.Hq * (pr.topk + 1) * c_alloc;
   size_t off = kWsHeader;
   l.n_union = off; off = align256(off + n_grp * 4);
   l.n_items = off; off = align256(off + n_grp * 4);
@@ -1465,8 +1480,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 
 
 // The plan's workspace pointers and the geometry of a decode step.
-void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo) {
-  const Layout lay = layout(pr);
+void plan_geo(const Problem& pr, int64_t pos, void* ws, Plan& plan, Geo& geo, bool group = false) {
+  const Layout lay = layout(pr, group);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   plan.n_union = reinterpret_cast<int*>(w8 + lay.n_union);
   plan.n_items = reinterpret_cast<int*>(w8 + lay.n_items);
@@ -1588,8 +1603,8 @@ bool decode_fast_supported(const Problem& pr) {
 
 size_t decode_ws_bytes(const Problem& pr) { return layout(pr).total - kWsHeader; }
 
-void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo) {
-  plan_geo(pr, pos, ws, *plan, *geo);
+void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo, bool group) {
+  plan_geo(pr, pos, ws, *plan, *geo, group);
 }
 
 cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,

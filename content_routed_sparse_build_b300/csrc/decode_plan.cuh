@@ -206,7 +206,9 @@ namespace ssa {
 // decode.cu: the plan pointers and geometry of a decode step at `pos` in the
 // decode workspace ws, and the attend + merge launches (16-bit or 8-bit
 // cache) of a step whose plan an earlier kernel on the stream has built.
-void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo);
+// group: the plan of a group-shared step (its own item size).
+void decode_plan_args(const Problem& pr, int64_t pos, void* ws, dplan::Plan* plan, dplan::Geo* geo,
+                      bool group = false);
 cudaError_t launch_attend_decode_planned(const Problem& pr, const void* Q, const void* K, const void* V, void* O,
                                          float* lse, const dplan::Plan& plan, const dplan::Geo& geo,
                                          uint32_t* err, cudaStream_t st);

@@ -579,7 +579,7 @@ cudaError_t launch_decode_step_group(const Problem& pr, const void* Q, int64_t p
                                      cudaStream_t st) {
   dplan::Plan plan;
   dplan::Geo geo;
-  decode_plan_args(pr, pos, ws, &plan, &geo);
+  decode_plan_args(pr, pos, ws, &plan, &geo, true);
   cudaError_t e;
   if (pr.d == 128)
     e = pr.dtype == DT_BF16 ? decode_route_g<DT_BF16, 128, true, true>(pr, Q, pos, summ, sel, nullptr, plan, geo, st)

@@ -191,7 +191,9 @@ SSA_API int ssa_decode_step(const ssa_params* p, const void* Q, int64_t pos, con
  * sums each group's queries in fp32 in head order, as ssa_route_group does,
  * scores the sum, writes the group's selection to all g heads' sel rows and
  * builds the attend plan in its cluster; then the attention and the merge).
- * Selections, O and lse are bit-identical to the two calls.  Arguments as for
+ * The selections are bit-identical to the two calls; O and lse agree to
+ * rounding, since the step splits the group's spans into smaller work items
+ * (a group-shared union is k + 1 spans, not up to g k + 1).  Arguments as for
  * ssa_decode_step; ws as for ssa_attend_decode (ssa_workspace_size(p, 1,
  * SSA_OP_DECODE) bytes; no group-routing workspace is needed).  Q, sel, O
  * and lse may be mapped page-locked host memory.  16-bit types and the
