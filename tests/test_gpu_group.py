@@ -62,6 +62,12 @@ DECODE_CASES = [
                n_q=6, q_pos0=65536 + 94, chunk=1, needles=8, seed=71),
     W.Workload("group_decode_f32_d64", "decode", 2, 8, 2, 64, 6000, 128, 6, F32,
                n_q=3, q_pos0=5997, chunk=1, needles=2, seed=72),
+    # the one-call group step with g = 16 and k = 40 (two-word router lists), B = 2, d = 64
+    W.Workload("group_decode_f16_d64_g16_k40", "decode", 2, 16, 1, 64, 9000, 128, 40, F16,
+               n_q=3, q_pos0=8997, chunk=1, needles=2, seed=75),
+    # g = 4 and S = 300: items start inside 32-token tiles
+    W.Workload("group_decode_bf16_g4_s300", "decode", 1, 16, 4, 128, 20000, 300, 8, BF16,
+               n_q=3, q_pos0=19990, chunk=1, seed=76),
 ]
 PREFILL_CASES = [
     W.Workload("group_prefill_bf16", "prefill", 1, 8, 2, 128, 3000, 128, 4, BF16,
