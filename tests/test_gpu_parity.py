@@ -30,6 +30,10 @@ PREFILL_CASES = [
     # k above the tensor-core router's 16 and above one merge batch of slots
     W.Workload("case_prefill_bf16_k20", "prefill", 1, 8, 2, 128, 4096, 64, 20, BF16,
                n_q=1024, q_pos0=3072, chunk=512, needles=2, seed=14),
+    # k = 64 at d = 128: 65 partial slots per row, more than two merge lanes'
+    # worth, and a merge row of 16,640 bytes (two rows in flight per warp)
+    W.Workload("case_prefill_bf16_d128_k64", "prefill", 1, 8, 2, 128, 80 * 64 + 17, 64, 64, BF16,
+               n_q=1024, q_pos0=80 * 64 + 17 - 1024, chunk=512, needles=2, seed=15),
 ]
 
 DECODE_CASES = [

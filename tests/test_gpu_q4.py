@@ -131,6 +131,9 @@ DCASES = [
                n_q=2, q_pos0=19990, chunk=1, needles=2, seed=92),
     W.Workload("q4_bf16_g16", "decode", 1, 32, 2, 128, 8192, 100, 12, torch.bfloat16,
                n_q=2, q_pos0=8000, chunk=1, seed=93),
+    # k above 32: the router's 64-entry lists, up to 65 spans per row
+    W.Workload("q4_bf16_k64", "decode", 1, 16, 2, 128, 300 * 256 + 50, 256, 64, torch.bfloat16,
+               n_q=2, q_pos0=300 * 256 + 47, chunk=1, needles=4, seed=94),
 ]
 
 

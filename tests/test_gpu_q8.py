@@ -116,6 +116,9 @@ DCASES = [
     # g = 16: two head groups per warp
     W.Workload("q8_bf16_g16", "decode", 1, 32, 2, 128, 8192, 100, 12, torch.bfloat16,
                n_q=2, q_pos0=8000, chunk=1, seed=83),
+    # k above 32: the router's 64-entry lists, up to 65 spans per row
+    W.Workload("q8_bf16_k64", "decode", 1, 16, 2, 128, 300 * 256 + 50, 256, 64, torch.bfloat16,
+               n_q=2, q_pos0=300 * 256 + 47, chunk=1, needles=4, seed=84),
 ]
 
 
