@@ -714,6 +714,7 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
   float oc[NG][4];              // sum_t (P vs)'_t 2^-24 of heads 2 q4, 2 q4 + 1
   float m[NG][2], l[NG][2];
   constexpr float kTwo24 = 16777216.f;
+  const float2 kTwo24x2 = make_float2(kTwo24, kTwo24);
   uint32_t hmask = 0u;          // the item's heads, and this thread's heads' ranks
   int rk[NG][2];
   Item cur;
@@ -817,10 +818,15 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
     for (int ng = 0; ng < NG; ++ng)
 #pragma unroll
       for (int t = 0; t < kSub; ++t) {
-        s[ng][t][0] = valid[t][0] ? fmaf(s[ng][t][0], kTwo24, -qs128[ng][0]) * ksc[t][0] : -INFINITY;
-        s[ng][t][1] = valid[t][0] ? fmaf(s[ng][t][1], kTwo24, -qs128[ng][1]) * ksc[t][0] : -INFINITY;
-        s[ng][t][2] = valid[t][1] ? fmaf(s[ng][t][2], kTwo24, -qs128[ng][0]) * ksc[t][1] : -INFINITY;
-        s[ng][t][3] = valid[t][1] ? fmaf(s[ng][t][3], kTwo24, -qs128[ng][1]) * ksc[t][1] : -INFINITY;
+        const float2 nq = make_float2(-qs128[ng][0], -qs128[ng][1]);
+        const float2 a = __fmul2_rn(__ffma2_rn(make_float2(s[ng][t][0], s[ng][t][1]), kTwo24x2, nq),
+                                    make_float2(ksc[t][0], ksc[t][0]));
+        const float2 b = __fmul2_rn(__ffma2_rn(make_float2(s[ng][t][2], s[ng][t][3]), kTwo24x2, nq),
+                                    make_float2(ksc[t][1], ksc[t][1]));
+        s[ng][t][0] = valid[t][0] ? a.x : -INFINITY;
+        s[ng][t][1] = valid[t][0] ? a.y : -INFINITY;
+        s[ng][t][2] = valid[t][1] ? b.x : -INFINITY;
+        s[ng][t][3] = valid[t][1] ? b.y : -INFINITY;
       }
     const float c = geo.scale_log2e;
     uint32_t pb[NG][kSub][2];
@@ -846,35 +852,44 @@ __global__ void __launch_bounds__(q8::kThreads, 1)
         alpha[i] = exp2f(m[ng][i] - bse);
         m[ng][i] = mx[i];
       }
-      float ls0 = 0.f, ls1 = 0.f;
+      // the two rows of a fragment (heads 2 c and 2 c + 1) side by side in
+      // packed fp32 operations, each lane rounded as its scalar form
+      const float2 c2 = make_float2(c, c), nb2 = make_float2(nb[0], nb[1]);
+      float2 ls = make_float2(0.f, 0.f);
 #pragma unroll
       for (int t = 0; t < kSub; ++t) {
-        const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
-        const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
-        const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
-        const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
-        ls0 += p0 + p2;
-        ls1 += p1 + p3;
+        const float2 e01 = __ffma2_rn(make_float2(s[ng][t][0], s[ng][t][1]), c2, nb2);
+        const float2 e23 = __ffma2_rn(make_float2(s[ng][t][2], s[ng][t][3]), c2, nb2);
+        const float2 p01 = make_float2(ptx::ex2(e01.x), ptx::ex2(e01.y));
+        const float2 p23 = make_float2(ptx::ex2(e23.x), ptx::ex2(e23.y));
+        ls = __fadd2_rn(ls, __fadd2_rn(p01, p23));
         // the V scale of each token weights its P (0 for masked tokens,
         // whose scale slot may hold anything)
         const float v0 = valid[t][0] ? vsc[t][0] : 0.f, v1 = valid[t][1] ? vsc[t][1] : 0.f;
-        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * v0, p1 * v0));
-        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * v1, p3 * v1));
+        const float2 w01 = __fmul2_rn(p01, make_float2(v0, v0));
+        const float2 w23 = __fmul2_rn(p23, make_float2(v1, v1));
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(w01.x, w01.y));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(w23.x, w23.y));
       }
-      l[ng][0] = l[ng][0] * alpha[0] + ls0;
-      l[ng][1] = l[ng][1] * alpha[1] + ls1;
+      l[ng][0] = l[ng][0] * alpha[0] + ls.x;
+      l[ng][1] = l[ng][1] * alpha[1] + ls.y;
       if (alpha[0] != 1.f || alpha[1] != 1.f) {
+        const float2 al = make_float2(alpha[0], alpha[1]);
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-          o[ng][mt2][0] *= alpha[0];
-          o[ng][mt2][1] *= alpha[1];
-          o[ng][mt2][2] *= alpha[0];
-          o[ng][mt2][3] *= alpha[1];
+          const float2 x = __fmul2_rn(make_float2(o[ng][mt2][0], o[ng][mt2][1]), al);
+          const float2 y = __fmul2_rn(make_float2(o[ng][mt2][2], o[ng][mt2][3]), al);
+          o[ng][mt2][0] = x.x;
+          o[ng][mt2][1] = x.y;
+          o[ng][mt2][2] = y.x;
+          o[ng][mt2][3] = y.y;
         }
-        oc[ng][0] *= alpha[0];
-        oc[ng][1] *= alpha[1];
-        oc[ng][2] *= alpha[0];
-        oc[ng][3] *= alpha[1];
+        const float2 x = __fmul2_rn(make_float2(oc[ng][0], oc[ng][1]), al);
+        const float2 y = __fmul2_rn(make_float2(oc[ng][2], oc[ng][3]), al);
+        oc[ng][0] = x.x;
+        oc[ng][1] = x.y;
+        oc[ng][2] = y.x;
+        oc[ng][3] = y.y;
       }
     }
     // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one
@@ -1176,6 +1191,7 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
   constexpr float kTwo24 = 16777216.f;
+  const float2 kTwo24x2 = make_float2(kTwo24, kTwo24);
 #pragma unroll 1
   while (inflight > 0) {
     if (!ptx::mbar_wait(&fb[stage], phase)) {
@@ -1251,10 +1267,15 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
       vsc[t][1] = svs[t * 16 + r8 + 8] * 0.0625f;
 #pragma unroll
       for (int ng = 0; ng < NG; ++ng) {
-        s[ng][t][0] = fmaf(s[ng][t][0], kTwo24, -qs8[ng][0]) * k0;
-        s[ng][t][1] = fmaf(s[ng][t][1], kTwo24, -qs8[ng][1]) * k0;
-        s[ng][t][2] = fmaf(s[ng][t][2], kTwo24, -qs8[ng][0]) * k1;
-        s[ng][t][3] = fmaf(s[ng][t][3], kTwo24, -qs8[ng][1]) * k1;
+        const float2 nq = make_float2(-qs8[ng][0], -qs8[ng][1]);
+        const float2 a = __fmul2_rn(__ffma2_rn(make_float2(s[ng][t][0], s[ng][t][1]), kTwo24x2, nq),
+                                    make_float2(k0, k0));
+        const float2 b = __fmul2_rn(__ffma2_rn(make_float2(s[ng][t][2], s[ng][t][3]), kTwo24x2, nq),
+                                    make_float2(k1, k1));
+        s[ng][t][0] = a.x;
+        s[ng][t][1] = a.y;
+        s[ng][t][2] = b.x;
+        s[ng][t][3] = b.y;
       }
     }
     // a tile the item covers only in part: its other tokens get no weight
@@ -1298,33 +1319,41 @@ __global__ void __launch_bounds__(q4::kThreads, 1)
         alpha[i] = exp2f(m[ng][i] - bse);
         m[ng][i] = mx[i];
       }
-      float ls0 = 0.f, ls1 = 0.f;
+      // the two rows of a fragment side by side in packed fp32 operations
+      const float2 c2 = make_float2(c, c), nb2 = make_float2(nb[0], nb[1]);
+      float2 ls = make_float2(0.f, 0.f);
 #pragma unroll
       for (int t = 0; t < q4::kSubT; ++t) {
-        const float p0 = ptx::ex2(fmaf(s[ng][t][0], c, nb[0]));
-        const float p1 = ptx::ex2(fmaf(s[ng][t][1], c, nb[1]));
-        const float p2 = ptx::ex2(fmaf(s[ng][t][2], c, nb[0]));
-        const float p3 = ptx::ex2(fmaf(s[ng][t][3], c, nb[1]));
-        ls0 += p0 + p2;
-        ls1 += p1 + p3;
+        const float2 e01 = __ffma2_rn(make_float2(s[ng][t][0], s[ng][t][1]), c2, nb2);
+        const float2 e23 = __ffma2_rn(make_float2(s[ng][t][2], s[ng][t][3]), c2, nb2);
+        const float2 p01 = make_float2(ptx::ex2(e01.x), ptx::ex2(e01.y));
+        const float2 p23 = make_float2(ptx::ex2(e23.x), ptx::ex2(e23.y));
+        ls = __fadd2_rn(ls, __fadd2_rn(p01, p23));
         // the V scale of each token weights its P (0 for masked tokens)
-        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p0 * vsc[t][0], p1 * vsc[t][0]));
-        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(p2 * vsc[t][1], p3 * vsc[t][1]));
+        const float2 w01 = __fmul2_rn(p01, make_float2(vsc[t][0], vsc[t][0]));
+        const float2 w23 = __fmul2_rn(p23, make_float2(vsc[t][1], vsc[t][1]));
+        pb[ng][t][0] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(w01.x, w01.y));
+        pb[ng][t][1] = ptx::movmatrix_trans(ptx::pack2<DT_F16>(w23.x, w23.y));
       }
-      l[ng][0] = l[ng][0] * alpha[0] + ls0;
-      l[ng][1] = l[ng][1] * alpha[1] + ls1;
+      l[ng][0] = l[ng][0] * alpha[0] + ls.x;
+      l[ng][1] = l[ng][1] * alpha[1] + ls.y;
       if (alpha[0] != 1.f || alpha[1] != 1.f) {
+        const float2 al = make_float2(alpha[0], alpha[1]);
 #pragma unroll
         for (int mt2 = 0; mt2 < D / 16; ++mt2) {
-          o[ng][mt2][0] *= alpha[0];
-          o[ng][mt2][1] *= alpha[1];
-          o[ng][mt2][2] *= alpha[0];
-          o[ng][mt2][3] *= alpha[1];
+          const float2 x = __fmul2_rn(make_float2(o[ng][mt2][0], o[ng][mt2][1]), al);
+          const float2 y = __fmul2_rn(make_float2(o[ng][mt2][2], o[ng][mt2][3]), al);
+          o[ng][mt2][0] = x.x;
+          o[ng][mt2][1] = x.y;
+          o[ng][mt2][2] = y.x;
+          o[ng][mt2][3] = y.y;
         }
-        oc[ng][0] *= alpha[0];
-        oc[ng][1] *= alpha[1];
-        oc[ng][2] *= alpha[0];
-        oc[ng][3] *= alpha[1];
+        const float2 x = __fmul2_rn(make_float2(oc[ng][0], oc[ng][1]), al);
+        const float2 y = __fmul2_rn(make_float2(oc[ng][2], oc[ng][3]), al);
+        oc[ng][0] = x.x;
+        oc[ng][1] = x.y;
+        oc[ng][2] = y.x;
+        oc[ng][3] = y.y;
       }
     }
     // O^T += Vq^T (vs P)^T: d-rows r8 and r8 + 8 of each m16 slice, one

@@ -694,13 +694,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       if (lane == 0) ptx::mbar_arrive_relaxed(&o_free[tx]);
       if (pslot >= 0) {
         const float inv = 1.f / pl;
+        const float2 inv2 = make_float2(inv, inv);
         uint16_t* dst = a.po + pslot * D;  // 32-byte aligned: a slot is D * 2 bytes
 #pragma unroll
         for (int q = 0; q < D / 16; ++q) {
           uint32_t pk[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pk[j] = ptx::pack2<DT>(__uint_as_float(o[16 * q + 2 * j]) * inv, __uint_as_float(o[16 * q + 2 * j + 1]) * inv);
+          for (int j = 0; j < 8; ++j) {
+            const float2 y = __fmul2_rn(
+                make_float2(__uint_as_float(o[16 * q + 2 * j]), __uint_as_float(o[16 * q + 2 * j + 1])), inv2);
+            pk[j] = ptx::pack2<DT>(y.x, y.y);
+          }
           ptx::st_global_v8(dst + 16 * q, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
         }
         a.pml[pslot] = make_float2(pm, pl);
@@ -756,16 +760,21 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const bool need = kb > 0 && m_new != m;
         const float nb = m_new == -INFINITY ? 0.f : -m_new;
         // P = 2^(s c - m) as 16-bit pairs over the S columns just read, in two
-        // halves of 64 keys (two partial sums keep the adds off one chain)
+        // halves of 64 keys (two partial sums keep the adds off one chain);
+        // s c - m of two keys in one packed fp32 FMA (each lane rounded as
+        // fmaf would)
         float lsum = 0.f;
+        const float2 c2 = make_float2(c, c), nb2 = make_float2(nb, nb);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[32];
           float la = 0.f, lb = 0.f;
 #pragma unroll
           for (int j = 0; j < 64; j += 2) {
-            const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[64 * hf + j]), c, nb));
-            const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[64 * hf + j + 1]), c, nb));
+            const float2 e = __ffma2_rn(
+                make_float2(__uint_as_float(sr[64 * hf + j]), __uint_as_float(sr[64 * hf + j + 1])), c2, nb2);
+            const float p0 = ptx::ex2(e.x);
+            const float p1 = ptx::ex2(e.y);
             la += p0;
             lb += p1;
             pk[j / 2] = ptx::pack2<DT>(p0, p1);
@@ -787,8 +796,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int q = 0; q < D / 32; ++q) {
             uint32_t rr[32];
             tc::ld32(tO + q * 32, rr);
+            const float2 f2 = make_float2(f, f);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
+            for (int j = 0; j < 32; j += 2) {
+              const float2 y = __fmul2_rn(make_float2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), f2);
+              rr[j] = __float_as_uint(y.x);
+              rr[j + 1] = __float_as_uint(y.y);
+            }
             tc::st32(tO + q * 32, rr);
           }
           l *= f;
