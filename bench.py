@@ -170,9 +170,9 @@ def job_throughput(units_per_rank: float, seconds: float, ws: int) -> float:
 NCU_TRAFFIC = {
     "decode_1m": (2.214e8, "profiles/decode_1m_launches.md: route + attend + merge of one step, "
                            "256K capture scaled to 1M"),
-    "decode_1m_q8": (1.156e8, "profiles/decode_1m_launches.md: route + 8-bit attend + merge, 256K capture "
+    "decode_1m_q8": (1.155e8, "profiles/decode_1m_launches.md: route + 8-bit attend + merge, 256K capture "
                               "scaled to 1M"),
-    "decode_1m_q4": (6.109e7, "profiles/decode_attend_q4_256k.md: route + 4-bit attend + merge, 256K capture "
+    "decode_1m_q4": (6.108e7, "profiles/decode_attend_q4_256k.md: route + 4-bit attend + merge, 256K capture "
                               "scaled to 1M"),
 }
 
