@@ -93,8 +93,11 @@ struct PrefArgs {
 };
 
 // The used entries of a sel row (the leading strictly ascending run of
-// candidate spans; anything else but -1 after it is an error), one thread.
-__device__ __forceinline__ int row_used(const int32_t* row, int topk, int64_t ell, int* js, bool* bad) {
+// candidate spans; anything else but -1 after it is an error), one thread:
+// f(rank, span) for each, in order.  Returns their count; the rank of a used
+// entry is its index in the row.
+template <class F>
+__device__ __forceinline__ int row_used(const int32_t* row, int topk, int64_t ell, bool* bad, F&& f) {
   int n = 0;
   int64_t prev = -1;
   bool stop = false;
@@ -102,7 +105,7 @@ __device__ __forceinline__ int row_used(const int32_t* row, int topk, int64_t el
   for (int r = 0; r < topk; ++r) {
     const int j = row[r];
     if (!stop && j >= 0 && j < ell && j > prev) {
-      js[n++] = j;
+      f(n++, j);
       prev = j;
     } else {
       stop = true;
@@ -132,14 +135,12 @@ __global__ void __launch_bounds__(256) prefill_count_kernel(const int32_t* __res
   if (i < a.n_q) {
     const int64_t row = (int64_t)bhq * a.n_q + i;
     const int64_t ell = (a.q_pos0 + i) / a.S;
-    int js[kMaxK];
     bool bad;
-    const int n = row_used(sel + row * a.topk, a.topk, ell, js, &bad);
+    row_used(sel + row * a.topk, a.topk, ell, &bad, [&](int, int j) {
+      if (use_hist) atomicAdd(&hist[j], 1);
+      else atomicAdd(&gcount[j], 1);
+    });
     if (bad) flag_error(err, SSA_DEVERR_BAD_SELECTION);
-    for (int r = 0; r < n; ++r) {
-      if (use_hist) atomicAdd(&hist[js[r]], 1);
-      else atomicAdd(&gcount[js[r]], 1);
-    }
   }
   __syncthreads();
   if (use_hist)
@@ -260,14 +261,14 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
     for (int x = threadIdx.x; x < ns; x += 256) hist[x] = 0;
   __syncthreads();
   const int64_t bkt0 = (int64_t)(b * a.Hkv + kvh) * ns;
-  int js[kMaxK];
   int n = 0;
   const int64_t row = (int64_t)bhq * a.n_q + i;
+  const int32_t* srow = sel + (i < a.n_q ? row : 0) * a.topk;
   if (i < a.n_q) {
     bool bad;
-    n = row_used(sel + row * a.topk, a.topk, (a.q_pos0 + i) / a.S, js, &bad);
-    if (use_hist)
-      for (int r = 0; r < n; ++r) atomicAdd(&hist[js[r]], 1);
+    n = row_used(srow, a.topk, (a.q_pos0 + i) / a.S, &bad, [&](int, int j) {
+      if (use_hist) atomicAdd(&hist[j], 1);
+    });
   }
   __syncthreads();
   if (use_hist) {
@@ -278,8 +279,9 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
     }
   }
   __syncthreads();
+  // the used entries are the row's first n
   for (int r = 0; r < n; ++r) {
-    const int j = js[r];
+    const int j = srow[r];
     const int pos = use_hist ? base[j] + atomicAdd(&hist[j], 1) : atomicAdd(&a.cursors[bkt0 + j], 1);
     a.rows[pos] = (int)((row << 6) | r);
   }
@@ -313,7 +315,8 @@ struct Pair {
   int kind_bh;          // bucket (>= 0) or -1 - bh
   int bh;
   int row0;             // span pairs: bucket row of tile A's first row (tile B: 128 rows on)
-  int n[2];             // rows of tiles A and B (0: no tile B)
+  int n0, n1;           // rows of tiles A and B (0: no tile B)
+  __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
   int64_t i0;           // local pairs: tile A's first query (tile B: 128 / g queries on)
   int64_t key0, key_end;  // keys [key0, key_end)
   int nkb;
@@ -327,8 +330,8 @@ __device__ __forceinline__ Pair decode_pair(const PrefArgs& a, int4 v) {
     x.bh = (int)(bk / a.ns_cap);
     const int64_t j = bk - (int64_t)x.bh * a.ns_cap;
     x.row0 = v.y;
-    x.n[0] = v.z;
-    x.n[1] = v.w;
+    x.n0 = v.z;
+    x.n1 = v.w;
     x.key0 = j * a.S;
     x.key_end = x.key0 + a.S;
     x.i0 = 0;
@@ -336,8 +339,8 @@ __device__ __forceinline__ Pair decode_pair(const PrefArgs& a, int4 v) {
     x.bh = -1 - v.x;
     x.i0 = v.y;
     x.row0 = 0;
-    x.n[0] = v.z * a.g;
-    x.n[1] = v.w * a.g;
+    x.n0 = v.z * a.g;
+    x.n1 = v.w * a.g;
     const int64_t t0 = a.q_pos0 + v.y;
     x.key0 = (t0 / a.S) * a.S;
     const int64_t mq = kTileRows / a.g;
@@ -355,7 +358,7 @@ __device__ __forceinline__ int64_t pair_row(const PrefArgs& a, const Pair& x, in
                                             int64_t* tpos, uint32_t* err) {
   *rank = a.topk;
   *tpos = x.key_end - 1;
-  if (r >= x.n[t]) return -1;
+  if (r >= x.n(t)) return -1;
   if (x.kind_bh >= 0) {
     const int e = a.rows[(int64_t)a.offsets[x.kind_bh] + x.row0 + t * kTileRows + r];
     const int64_t row = (int64_t)(e >> 6);
@@ -503,13 +506,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
         for (int i = 0; i < kTileRows / 32; ++i) {
           const int r = i * 32 + lane;
-          e[i] = r < x.n[tt] ? __ldg(a.rows + off + r) : -1;
+          e[i] = r < x.n(tt) ? __ldg(a.rows + off + r) : -1;
         }
 #pragma unroll
         for (int i = 0; i < kTileRows / 32; ++i) {
           const int64_t row = (int64_t)(e[i] >> 6);
           qrow[i] = -1;
-          if (i * 32 + lane < x.n[tt]) {
+          if (i * 32 + lane < x.n(tt)) {
             if (e[i] < 0 || row >= (int64_t)a.B * a.Hq * a.n_q || (e[i] & 63) >= a.topk)
               flag_error(err, SSA_DEVERR_OVERFLOW);
             else
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         break;
       }
       if (tt == 0 && lane == 0) tinfo[qb] = v;
-      if (x.n[tt] > 0) {
+      if (x.n(tt) > 0) {
         uint8_t* qt = tt == 0 ? sQA + qb * C::kQTile : sQB;
 #pragma unroll
         for (int i = 0; i < kTileRows / 32; ++i) {
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         tc::fence_after();
         const Pair x = decode_pair(a, tinfo[qb]);
-        const bool hb = x.n[1] > 0;
+        const bool hb = x.n1 > 0;
         npx[0] += 1;
         npx[1] += hb ? 1 : 0;
         const uint32_t aQA = aQA0 + qb * C::kQTile;
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&q_empty[qb]);
       const Pair x = decode_pair(a, v);
-      if (x.n[tx] == 0) {
+      if (x.n(tx) == 0) {
         // no tile B in this pair: the pending epilogue cannot wait for it
         if (pend && !(ok = epilogue())) break;
         continue;
