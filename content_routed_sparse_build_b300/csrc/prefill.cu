@@ -21,10 +21,11 @@
 //  attend   persistent, one CTA per SM, twelve warps, one pair at a time.
 //           Two loader warps gather the pair's query rows into 128-byte
 //           swizzled K-major Q buffers ahead of use (tile A's double
-//           buffered); a TMA warp streams the shared key / value blocks of
-//           128 tokens through a four-slot ring; one thread issues
-//           tcgen05.mma, alternating the tiles: S = Q K^T into tensor
-//           memory, then O += P V with P read from tensor memory.  Eight
+//           buffered, tile B's too for spans of 512 tokens or more); a TMA
+//           warp streams the shared key / value blocks of 128 tokens
+//           through a four-slot ring (three with tile B's two); one thread
+//           issues tcgen05.mma, alternating the tiles: S = Q K^T into
+//           tensor memory, then O += P V with P read from tensor memory.  Eight
 //           softmax warps (four per tile, one row per thread) turn S into
 //           P = 2^(S c - m) (16-bit, written over S), rescale O only when
 //           the running maximum grows by more than 2^8, and end each tile
@@ -288,17 +289,23 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 }
 
 // ---------------------------------------------------------------- attend
-template <int D>
+// QB: tile B's Q buffers.  Seven 128-row operand buffers fit in shared
+// memory: tile A's two Q buffers, then either one for tile B and a four-slot
+// K / V ring (QB = 1), or two for tile B and a three-slot ring (QB = 2).
+// Long spans (many key blocks per pair) gain from tile B's next rows loading
+// during the pair; short ones from the deeper ring, which reaches into the
+// next pair's blocks.
+template <int D, int QB>
 struct ACfg {
   static constexpr int kRegion = kTileRows * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = (D / 64) * kRegion;      // one 128-row Q tile
   static constexpr int kKV = (D / 64) * kRegion;         // one K or V block of 128 tokens
   // one ring for both: K(0), V(0), K(1), V(1), ...  A K slot is free once
-  // both tiles' S of its block are done, a V slot once both P V are.  Four
-  // slots hold the block in use and the next one: tile A's Q is double
-  // buffered, tile B's single (its next rows load once its last S is done).
-  static constexpr int kSlots = 4;
-  static constexpr size_t kOperands = 3 * (size_t)kQTile + (size_t)kSlots * kKV;
+  // both tiles' S of its block are done, a V slot once both P V are.  Tile
+  // A's Q is double buffered; with one buffer, tile B's next rows load once
+  // its last S of the pair is done.
+  static constexpr int kSlots = QB == 2 ? 3 : 4;
+  static constexpr size_t kOperands = (2 + QB) * (size_t)kQTile + (size_t)kSlots * kKV;
   static constexpr int kSmallBytes = 512;                // barriers and the two pair entries
   static constexpr size_t kSmem = 1024 + kOperands + kSmallBytes;
   // tensor memory: S_A [0, 128), S_B [128, 256) (the P of a block is written
@@ -390,17 +397,17 @@ __device__ __forceinline__ int64_t pair_row(const PrefArgs& a, const Pair& x, in
 // running maximum grows by more than 2^8.  A tile's epilogue (one partial
 // (m, l, normalised o) per row) runs after the next pair's first P is out,
 // so that waiting for its last P V overlaps that softmax.
-template <int DT, int D>
+template <int DT, int D, int QB>
 __global__ void __launch_bounds__(kAttThreads, 1)
     prefill_attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const void* __restrict__ Q, PrefArgs a, uint32_t* __restrict__ err) {
-  using C = ACfg<D>;
+  using C = ACfg<D, QB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQA = base;                               // [2 buffers] tile A's Q
-  uint8_t* sQB = sQA + 2 * C::kQTile;                // tile B's Q
-  uint8_t* sKV = sQB + C::kQTile;                    // [kSlots]
+  uint8_t* sQB = sQA + 2 * C::kQTile;                // [QB] tile B's Q
+  uint8_t* sKV = sQB + QB * C::kQTile;               // [kSlots]
   uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + C::kSlots * C::kKV);
   uint64_t* q_full = bar + 0;     // [2] tile A's Q of a pair and the pair entry loaded
   uint64_t* q_empty = bar + 2;    // [2] last S of the pair done + every softmax warp read the entry
@@ -411,11 +418,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint64_t* pv_done = bar + 16;   // [2 tiles] O += P V of the tile's block done
   uint64_t* o_free = bar + 18;    // [2 tiles] O read out by the tile's epilogue (4 warps)
   uint64_t* drain = bar + 20;     // every MMA issued has completed
-  uint64_t* qb_full = bar + 21;   // tile B's Q of the pair loaded (every pair)
-  uint64_t* qb_empty = bar + 22;  // last S of the pair done: tile B's buffer is free (every pair)
-  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 23);
-  volatile int* abort = reinterpret_cast<volatile int*>(bar + 24);
-  int4* tinfo = reinterpret_cast<int4*>(bar + 26);  // [2] pair entries
+  uint64_t* qb_full = bar + 21;   // [QB] tile B's Q of the pair loaded (every pair)
+  uint64_t* qb_empty = bar + 23;  // [QB] last S of the pair done: tile B's buffer is free (every pair)
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(bar + 25);
+  volatile int* abort = reinterpret_cast<volatile int*>(bar + 26);
+  int4* tinfo = reinterpret_cast<int4*>(bar + 28);  // [2] pair entries
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -432,8 +439,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       ptx::mbar_init(&kv_empty[s], 1);
     }
     ptx::mbar_init(drain, 1);
-    ptx::mbar_init(qb_full, 1);
-    ptx::mbar_init(qb_empty, 1);
+    for (int s = 0; s < QB; ++s) {
+      ptx::mbar_init(&qb_full[s], 1);
+      ptx::mbar_init(&qb_empty[s], 1);
+    }
     *abort = 0;
     ptx::fence_mbar_init();
   }
@@ -490,13 +499,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // ------------------------------------------------ Q loaders
     // Warp kQWarp + t gathers the 128 query rows of tile t of the pair into
     // the swizzled K-major Q buffer; the tile-A warp publishes the pair
-    // entry.  Tile A's buffer is double buffered; tile B's is single, so
-    // its warp loads the pair's row entries first and starts the copies as
-    // soon as the previous pair's last S has read the buffer.
+    // entry.  Tile A's buffer is double buffered; tile B's has QB buffers
+    // (with one, its warp loads the pair's row entries first and starts the
+    // copies as soon as the previous pair's last S has read the buffer).
     const int tt = warp - kQWarp;
     int pc = 0;
     for (int t = blockIdx.x; t < npairs && !*abort; t += gridDim.x, ++pc) {
       const int qb = pc & 1;
+      const int qbB = QB == 2 ? qb : 0;  // tile B's buffer
       const int4 v = a.tiles[t];
       const Pair x = decode_pair(a, v);
       int64_t qrow[kTileRows / 32];
@@ -528,14 +538,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
       }
       const bool free_buf = tt == 0 ? (pc < 2 || ptx::mbar_wait(&q_empty[qb], (uint32_t)(((pc - 2) >> 1) & 1)))
-                                    : (pc < 1 || ptx::mbar_wait(qb_empty, (uint32_t)((pc - 1) & 1)));
+                                    : (pc < QB || ptx::mbar_wait(&qb_empty[qbB], (uint32_t)(((pc - QB) / QB) & 1)));
       if (!free_buf) {
         fail(SSA_DEVERR_WAIT_TIMEOUT);
         break;
       }
       if (tt == 0 && lane == 0) tinfo[qb] = v;
       if (x.n(tt) > 0) {
-        uint8_t* qt = tt == 0 ? sQA + qb * C::kQTile : sQB;
+        uint8_t* qt = tt == 0 ? sQA + qb * C::kQTile : sQB + qbB * C::kQTile;
 #pragma unroll
         for (int i = 0; i < kTileRows / 32; ++i) {
           const int r = i * 32 + lane;
@@ -554,7 +564,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tt == 0 ? &q_full[qb] : qb_full);
+      if (lane == 0) ptx::mbar_arrive(tt == 0 ? &q_full[qb] : &qb_full[qbB]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp) {
@@ -607,6 +617,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       int pc = 0;
       for (int t = blockIdx.x; t < npairs && ok && !*abort; t += gridDim.x, ++pc) {
         const int qb = pc & 1;
+        const int qbB = QB == 2 ? qb : 0;  // tile B's buffer
         if (!ptx::mbar_wait(&q_full[qb], (uint32_t)((pc >> 1) & 1))) {
           ok = false;
           break;
@@ -630,14 +641,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
           if (hb) {
             // tile B's Q of this pair (its single buffer) must be in
-            if (kb == 0 && !(ok = ptx::mbar_wait(qb_full, (uint32_t)(pc & 1)))) break;
+            if (kb == 0 && !(ok = ptx::mbar_wait(&qb_full[qbB], (uint32_t)((pc / QB) & 1)))) break;
             tc::fence_after();
-            issue_s(1, aQB, ks);
+            issue_s(1, aQB + qbB * C::kQTile, ks);
           }
           tc::commit(&kv_empty[ks]);           // K(b) read by both tiles
           if (kb == x.nkb - 1) {
             tc::commit(&q_empty[qb]);
-            tc::commit(qb_empty);
+            tc::commit(&qb_empty[qbB]);
           }
           ++u;
           pend = true;
@@ -1030,10 +1041,23 @@ PrefArgs make_args(const Problem& pr, int64_t n_q, int64_t q_pos0, void* ws, con
   return a;
 }
 
+// The attend kernel's launch: tile B's Q double buffered for spans of four
+// key blocks or more (A/B on one B300: a 1M chunk with S = 1024 3.097 ->
+// 3.048 ms, the 128K prefill with S = 256 21.37 -> 22.03 ms).
+template <int DT, int D, int QB>
+cudaError_t launch_attend(const PrefArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, const void* Q,
+                          uint32_t* err, cudaStream_t st) {
+  using C = ACfg<D, QB>;
+  static bool attr_done[kMaxDevices] = {};
+  cudaError_t e = ensure_smem_attr(prefill_attend_kernel<DT, D, QB>, C::kSmem, attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(prefill_attend_kernel<DT, D, QB>, dim3(device_sm_count()), dim3(kAttThreads), C::kSmem, st,
+                    tmK, tmV, Q, a, err);
+}
+
 template <int DT, int D>
 cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t q_pos0, const void* K,
                          const void* V, const int32_t* sel, void* O, float* lse, void* ws, cudaStream_t st) {
-  using C = ACfg<D>;
   const PrefLayout lay = pref_layout(pr, n_q);
   const PrefArgs a = make_args(pr, n_q, q_pos0, ws, lay);
   uint32_t* err = ws_error(ws);
@@ -1052,11 +1076,8 @@ cudaError_t launch_typed(const Problem& pr, const void* Q, int64_t n_q, int64_t 
   if (e != cudaSuccess) return e;
   e = launch_pdl(prefill_scatter_kernel, grid_rows, dim3(256), 2 * hist_bytes, st, sel, a);
   if (e != cudaSuccess) return e;
-  static bool attr_done[kMaxDevices] = {};
-  e = ensure_smem_attr(prefill_attend_kernel<DT, D>, C::kSmem, attr_done);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(prefill_attend_kernel<DT, D>, dim3(device_sm_count()), dim3(kAttThreads), C::kSmem, st,
-                 tmK, tmV, Q, a, err);
+  e = pr.S >= 4 * kKeyBlk ? launch_attend<DT, D, 2>(a, tmK, tmV, Q, err, st)
+                          : launch_attend<DT, D, 1>(a, tmK, tmV, Q, err, st);
   if (e != cudaSuccess) return e;
   const int64_t n_rows = (int64_t)pr.B * pr.Hq * n_q;
   const int mw = merge_warps(pr);

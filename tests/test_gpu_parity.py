@@ -34,6 +34,12 @@ PREFILL_CASES = [
     # worth, and a merge row of 16,640 bytes (two rows in flight per warp)
     W.Workload("case_prefill_bf16_d128_k64", "prefill", 1, 8, 2, 128, 80 * 64 + 17, 64, 64, BF16,
                n_q=1024, q_pos0=80 * 64 + 17 - 1024, chunk=512, needles=2, seed=15),
+    # spans of 512 tokens or more: the attend kernel's layout with two Q
+    # buffers for tile B and a three-slot K / V ring
+    W.Workload("case_prefill_bf16_s1024", "prefill", 1, 8, 2, 128, 10 * 1024 + 300, 1024, 4, BF16,
+               n_q=1024, q_pos0=10 * 1024 + 300 - 1024, chunk=1024, needles=2, seed=16),
+    W.Workload("case_prefill_f16_d64_s512", "prefill", 1, 4, 4, 64, 14 * 512 + 77, 512, 6, F16,
+               n_q=700, q_pos0=14 * 512 + 77 - 700, chunk=700, seed=17),
 ]
 
 DECODE_CASES = [
