@@ -105,7 +105,7 @@ def _bad_rows(w: W.Workload, margin: np.ndarray) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ CUDA side
-class GpuRun:
+class DeviceRun:
     """Runs the CUDA path of a workload through the C ABI."""
 
     def __init__(self, w: W.Workload, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,

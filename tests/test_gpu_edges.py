@@ -17,7 +17,7 @@ import content_routed_sparse_build_b300 as ssa
 import oracle
 from synth import workloads as W
 
-from harness import LSE_TOL, TOL, GpuRun, max_abs
+from harness import LSE_TOL, TOL, DeviceRun, max_abs
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def test_decode_periodic_cache_ties(topk):
     summ = oracle.summaries(K, L, S)
     sel_o = np.stack([oracle.route(Q[s].reshape(B, Hq, 1, d).contiguous(), w.q_pos0 + s, summ, Hkv, S, topk)[0]
                       for s in range(n)])
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     for fused in (False, True):
         sel_g, O_g, lse_g, err = run.decode(fused=fused)
@@ -72,7 +72,7 @@ def test_prefill_periodic_cache_ties():
     w = W.Workload("ties_prefill", "prefill", B, Hq, Hkv, d, L, S, topk, BF16, n_q=n, q_pos0=L - n, chunk=n)
     summ = oracle.summaries(K, L, S)
     sel_o, _ = oracle.route(Q, L - n, summ, Hkv, S, topk)
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill()
     assert err == 0
     assert np.array_equal(sel_g, sel_o)
@@ -91,7 +91,7 @@ def test_zero_queries_take_the_lowest_spans():
     n = 3
     Qd = torch.zeros((n, B, Hq, d), dtype=BF16)
     wd = W.Workload("zero_q_decode", "decode", B, Hq, Hkv, d, L, S, topk, BF16, n_q=n, q_pos0=L - n, chunk=1)
-    run = GpuRun(wd, Qd, K, V)
+    run = DeviceRun(wd, Qd, K, V)
     run.summaries()
     want = np.broadcast_to(np.arange(topk, dtype=np.int32), (n, B * Hq, topk))
     for fused in (False, True):
@@ -104,7 +104,7 @@ def test_zero_queries_take_the_lowest_spans():
     m = 256
     Qp = torch.zeros((B, Hq, m, d), dtype=BF16)
     wp = W.Workload("zero_q_prefill", "prefill", B, Hq, Hkv, d, L, S, topk, BF16, n_q=m, q_pos0=L - m, chunk=m)
-    sel_p, O_p, lse_p, err = GpuRun(wp, Qp, K, V).prefill()
+    sel_p, O_p, lse_p, err = DeviceRun(wp, Qp, K, V).prefill()
     assert err == 0
     assert np.array_equal(sel_p, np.broadcast_to(np.arange(topk, dtype=np.int32), sel_p.shape))
 
@@ -124,7 +124,7 @@ def test_first_positions(pos):
     q4 = Q[0].reshape(B, Hq, 1, d).contiguous()
     sel_o, _ = oracle.route(q4, pos, summ, Hkv, S, topk)
     O_o, lse_o, _ = oracle.attend(q4, K, V, pos, S, sel_o)
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     for fused in (False, True):
         sel_g, O_g, lse_g, err = run.decode(fused=fused)

@@ -32,7 +32,7 @@ import oracle
 from oracle import streamed
 from synth import workloads as W
 
-from harness import (LSE_TOL, MARGIN, TOL, GpuRun, margin_checked_inputs, max_abs, oracle_outputs_decode,
+from harness import (LSE_TOL, MARGIN, TOL, DeviceRun, margin_checked_inputs, max_abs, oracle_outputs_decode,
                      params_of, report_margins)
 
 pytestmark = pytest.mark.gpu
@@ -88,7 +88,7 @@ def test_decode_1m_all_steps():
     w = W.DECODE_1M
     inp, Q, K, orc, sel_o, margin, _ = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     sel_g, O_g, lse_g, err = run.decode()
     assert err == 0
@@ -116,7 +116,7 @@ def test_prefill_chunk_vs_1m_all_rows():
     w = W.PREFILL_1M
     inp, Q, K, orc, sel_o, margin, _ = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill()
     assert err == 0
     assert np.array_equal(sel_g, sel_o), "selection mismatch in %d rows" % int(
@@ -183,7 +183,7 @@ def test_prefill_128k_sampled_rows():
         raise RuntimeError("margin not reached")
     report_margins(w.name, margin, redrawn)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill()
     assert err == 0
     assert np.array_equal(sel_g[rows], sel_o)
@@ -222,7 +222,7 @@ def test_decode_10m_all_steps():
     report_margins(w.name, margin, redrawn)
     dev = torch.device("cuda")
     Kd, Vd = inp.k(dev), inp.v(dev)
-    run = GpuRun(w, Q, Kd, Vd)
+    run = DeviceRun(w, Q, Kd, Vd)
     run.summaries()
     sel_g, O_g, lse_g, err = run.decode()
     assert err == 0

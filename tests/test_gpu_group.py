@@ -12,7 +12,7 @@ import content_routed_sparse_build_b300 as ssa
 import oracle
 from synth import workloads as W
 
-from harness import LSE_TOL, MARGIN, TOL, GpuRun, max_abs, params_of
+from harness import LSE_TOL, MARGIN, TOL, DeviceRun, max_abs, params_of
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,7 @@ def _decode_run(w, Q, K, V):
     one-call group step runs beside them: the same selections bit for bit,
     and its own outputs (its work items are smaller, so its partials split
     the spans differently), which the tests hold to the oracle as well."""
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     p = run.p_full
     ws = ssa.workspace(p, 1, ssa.SSA_OP_DECODE)
@@ -131,7 +131,7 @@ def test_group_decode_parity(w):
 def test_group_prefill_parity(w):
     inp, Q, K, summ, sel_o, margin = group_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel = torch.empty((w.B, w.Hq, w.n_q, w.topk), dtype=torch.int32, device="cuda")
     O = torch.empty((w.B, w.Hq, w.n_q, w.d), dtype=w.dtype, device="cuda")
     lse = torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device="cuda")

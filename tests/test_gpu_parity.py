@@ -11,7 +11,7 @@ import content_routed_sparse_build_b300 as ssa
 import oracle
 from synth import workloads as W
 
-from harness import (LSE_TOL, TOL, GpuRun, OracleRun, margin_checked_inputs, max_abs,
+from harness import (LSE_TOL, TOL, DeviceRun, OracleRun, margin_checked_inputs, max_abs,
                      oracle_outputs_decode, oracle_outputs_prefill)
 
 pytestmark = pytest.mark.gpu
@@ -67,7 +67,7 @@ DECODE_CASES = [
 def test_prefill_parity(w):
     inp, Q, K, orc, sel_o, margin, redrawn = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill()
     assert err == 0
     assert np.array_equal(sel_g, sel_o), "selection mismatch in %d rows" % int(
@@ -81,7 +81,7 @@ def test_prefill_parity(w):
 def test_decode_parity(w):
     inp, Q, K, orc, sel_o, margin, redrawn = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     sel_g, O_g, lse_g, err = run.decode()
     assert err == 0
@@ -98,7 +98,7 @@ def test_decode_step_parity(w):
     calls."""
     inp, Q, K, orc, sel_o, margin, redrawn = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     run.summaries()
     sel_g, O_g, lse_g, err = run.decode(fused=True)
     assert err == 0
@@ -118,7 +118,7 @@ def test_summaries_parity_fp32_exactish():
                    chunk=1, seed=31)
     inp = W.Inputs(w)
     K = inp.k()
-    run = GpuRun(w, inp.q(), K, K)
+    run = DeviceRun(w, inp.q(), K, K)
     run.summaries()
     ref = oracle.summaries(K, w.L, w.S)
     got = run.summ.cpu().double().numpy()
@@ -140,7 +140,7 @@ def test_exact_arithmetic_ties_match():
     summ = oracle.summaries(K, L, S)
     sel_o, margin = oracle.route(Q, 0, summ, Hkv, S, topk)
     assert (margin == 0).sum() > 100
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill(chunked=False)
     assert err == 0
     assert np.array_equal(sel_g, sel_o)
@@ -159,7 +159,7 @@ def test_decode_matches_prefill_rows():
                    n_q=512, q_pos0=3584, chunk=512, needles=2, seed=41)
     inp, Q, K, orc, sel_o, margin, _ = margin_checked_inputs(w)
     V = inp.v()
-    run = GpuRun(w, Q, K, V)
+    run = DeviceRun(w, Q, K, V)
     sel_g, O_g, lse_g, err = run.prefill()
     assert np.array_equal(sel_g, sel_o)
     p = ssa.params(w.B, w.Hq, w.Hkv, w.d, w.L, w.S, w.topk, BF16)
