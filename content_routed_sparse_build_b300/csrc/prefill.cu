@@ -314,6 +314,13 @@ struct ACfg {
   static constexpr uint32_t kColO = 256;
 };
 
+// Every layout fits the 227 KB of shared memory a CTA may use, and the small
+// block holds the barriers (words 0-24), the tensor-memory address (25), the
+// abort flag (26) and the two pair entries (words 28-31).
+static_assert(ACfg<128, 1>::kSmem <= 227 * 1024 && ACfg<128, 2>::kSmem <= 227 * 1024, "attend layout too large");
+static_assert(ACfg<64, 1>::kSmem <= 227 * 1024 && ACfg<64, 2>::kSmem <= 227 * 1024, "attend layout too large");
+static_assert(32 * 8 <= ACfg<128, 1>::kSmallBytes, "attend barrier block too small");
+
 constexpr int kSoftWarps = 8;      // warps 0-3: tile A, 4-7: tile B (one lane quarter each)
 constexpr int kTmaWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1, kQWarp = kSoftWarps + 2;  // Q loaders: 10, 11
 constexpr int kAttThreads = (kSoftWarps + 4) * 32;
